@@ -1,0 +1,418 @@
+/*
+ * gq_oracle.c -- CPU oracle for the Global-QSGD compress / aggregate / decompress path.
+ *
+ * TEST INFRASTRUCTURE ONLY.  This is the plain, slow, single-threaded definition that the CUDA
+ * library is checked against.  Only the test suite, the smoke check and the CPU-baseline leg of
+ * bench.py load it; the product path never does.  It shares no code, header, table or constant
+ * generator with the CUDA sources, and it includes none of them.
+ *
+ * Method: "Global-QSGD: Practical Floatless Quantization for Distributed Learning with Theoretical
+ * Guarantees" (Xin, Canini, Richtarik, Horvath; arXiv 2305.18627), cited below as "Global-QSGD".
+ * Random numbers: Philox4x32-10 from Salmon, Moraes, Dror, Shaw, "Parallel Random Numbers: As
+ * Easy as 1, 2, 3" (SC'11), cited as "Philox (SC'11)".
+ *
+ * Precision.  The norm, the rounding probabilities and the dequantised mean are computed in fp64
+ * (all exactly, except the norm's sum and square root and the final division of the mean).  The
+ * one step carried in fp32 is the normalisation v = |x| / N: the quantiser works on fp32
+ * gradients and an fp32 norm, and v is the correctly rounded fp32 quotient.
+ *
+ * Parity status (each function's pins live in tests/test_oracle_*.py):
+ *   gqo_philox4x32_10      pinned: published known-answer vectors (tests/golden/)
+ *   gqo_global_norm        pinned: closed forms, numpy.linalg.norm per axis, exact fsum
+ *   gqo_level_split        pinned: exact expectation E[Q]=x, closed-form variance, fixed levels
+ *   gqo_quantize           pinned: level split + Philox word, Monte-Carlo unbiasedness
+ *   gqo_reduce_codes       pinned: hand-decoded codes, exact level values
+ *   gqo_dequantize         pinned: hand examples, Monte-Carlo mean
+ *
+ * Build: gcc -std=c99 -O2 -ffp-contract=off -fPIC -shared gq_oracle.c -lm
+ * (-ffp-contract=off keeps every float operation a separately rounded IEEE operation on both
+ * x86-64 and aarch64.)
+ */
+#include <math.h>
+#include <stdint.h>
+#include <string.h>
+
+/* Return codes (same meanings as the library's status values; defined here independently). */
+#define GQO_OK 0
+#define GQO_ERR_INVALID 1
+#define GQO_ERR_UNSUPPORTED 2
+#define GQO_ERR_NONFINITE 4
+
+/* Element types of the gradient matrix. */
+#define GQO_F32 0
+#define GQO_BF16 1
+
+/* Level grids: standard (linear) dithering Global-L_s and exponential dithering Global-E_s. */
+#define GQO_LINEAR 0
+#define GQO_EXP 1
+
+/* Norm orders: 2 is the l2 norm, 0 stands for the l-infinity norm. */
+#define GQO_INF 0
+
+int gqo_abi_version(void) { return 1; }
+
+/* ------------------------------------------------------------------------------------------ */
+/* Philox4x32-10 (Philox (SC'11), the Philox-4x32 bijection with 10 rounds)                    */
+/* ------------------------------------------------------------------------------------------ */
+
+/* Full 64-bit product of two 32-bit words, split into high and low halves. */
+static void mul_hi_lo(uint32_t a, uint32_t b, uint32_t *hi, uint32_t *lo)
+{
+    uint64_t prod = (uint64_t)a * (uint64_t)b;
+    *hi = (uint32_t)(prod >> 32);
+    *lo = (uint32_t)prod;
+}
+
+/*
+ * One call of the Philox4x32-10 counter-based generator: four 32-bit counter words and two
+ * 32-bit key words in, four 32-bit random words out.  Each round multiplies counter words 0 and
+ * 2 by the two round multipliers, then forms the new counter from the high halves xor-ed with
+ * the other two counter words and the round key, and the low halves.  The key advances by the
+ * two Weyl increments between rounds.  The multipliers and increments are the ones the SC'11
+ * paper gives for Philox-4x32 (the increments are the golden ratio and sqrt(3)-1 in 0.32 fixed
+ * point).
+ */
+void gqo_philox4x32_10(const uint32_t ctr_in[4], const uint32_t key_in[2], uint32_t out[4])
+{
+    const uint32_t mult0 = 0xD2511F53u, mult1 = 0xCD9E8D57u;
+    const uint32_t weyl0 = 0x9E3779B9u, weyl1 = 0xBB67AE85u;
+    uint32_t c0 = ctr_in[0], c1 = ctr_in[1], c2 = ctr_in[2], c3 = ctr_in[3];
+    uint32_t k0 = key_in[0], k1 = key_in[1];
+    int round;
+    for (round = 0; round < 10; ++round) {
+        uint32_t hi0, lo0, hi1, lo1;
+        if (round > 0) {
+            k0 += weyl0;
+            k1 += weyl1;
+        }
+        mul_hi_lo(mult0, c0, &hi0, &lo0);
+        mul_hi_lo(mult1, c2, &hi1, &lo1);
+        {
+            uint32_t n0 = hi1 ^ c1 ^ k0;
+            uint32_t n1 = lo1;
+            uint32_t n2 = hi0 ^ c3 ^ k1;
+            uint32_t n3 = lo0;
+            c0 = n0;
+            c1 = n1;
+            c2 = n2;
+            c3 = n3;
+        }
+    }
+    out[0] = c0;
+    out[1] = c1;
+    out[2] = c2;
+    out[3] = c3;
+}
+
+/*
+ * The uniform 32-bit word that decides the rounding of element (worker i, coordinate j) at
+ * training step `step` under seed `seed`.  Global-QSGD leaves the source of randomness open; this
+ * project fixes it as: key = (low 32 bits of seed, high 32 bits of seed), counter =
+ * (j / 4, i, low 32 bits of step, high 32 bits of step), and the word used is word (j mod 4) of
+ * the call's output.  So the four coordinates 4t..4t+3 of one worker share one Philox call.
+ */
+uint32_t gqo_philox_word(uint64_t seed, uint64_t step, int64_t i, int64_t j)
+{
+    uint32_t ctr[4], key[2], out[4];
+    ctr[0] = (uint32_t)((uint64_t)j >> 2);
+    ctr[1] = (uint32_t)i;
+    ctr[2] = (uint32_t)step;
+    ctr[3] = (uint32_t)(step >> 32);
+    key[0] = (uint32_t)seed;
+    key[1] = (uint32_t)(seed >> 32);
+    gqo_philox4x32_10(ctr, key, out);
+    return out[j & 3];
+}
+
+/* ------------------------------------------------------------------------------------------ */
+/* Input element access                                                                       */
+/* ------------------------------------------------------------------------------------------ */
+
+/* Element idx of the gradient buffer as an fp32 value.  bf16 is the high half of a binary32
+ * word, so widening it is a 16-bit left shift of its bits. */
+static float load_x(const void *x, int dtype, int64_t idx)
+{
+    if (dtype == GQO_F32)
+        return ((const float *)x)[idx];
+    {
+        uint32_t bits = (uint32_t)((const uint16_t *)x)[idx] << 16;
+        float f;
+        memcpy(&f, &bits, sizeof f);
+        return f;
+    }
+}
+
+/* ------------------------------------------------------------------------------------------ */
+/* Global norm ||x||_{q,p}                                                                     */
+/* ------------------------------------------------------------------------------------------ */
+
+/*
+ * ||x||_{q,p} of the concatenated vector x = [x_1, ..., x_n] in R^{nd} (Global-QSGD, notation
+ * paragraph of the preliminaries: the (sum over coordinates of ||.||_q^p)^(1/p) norm).  The
+ * page's index ranges are garbled; the reading taken is: for every coordinate j, the q-norm over
+ * the n workers of (x_1j, ..., x_nj); then the p-norm over j of those d numbers.  q and p are 2
+ * or GQO_INF (0).  x is worker-major: element (i, j) is at i*d + j.
+ *
+ * Computed literally in fp64: the per-coordinate q-norm (sqrt of a sum of squares, or a max of
+ * magnitudes), then the p-norm of those values.  Returns NaN if any element is NaN, +Inf if
+ * any is infinite (and none is NaN), -1 for invalid arguments.
+ */
+double gqo_global_norm(const void *x, int dtype, int64_t n, int64_t d, int q, int p)
+{
+    int64_t i, j;
+    int has_nan = 0, has_inf = 0;
+    double outer = 0.0;
+    if (x == NULL || n < 1 || d < 1 || (dtype != GQO_F32 && dtype != GQO_BF16))
+        return -1.0;
+    if ((q != 2 && q != GQO_INF) || (p != 2 && p != GQO_INF))
+        return -1.0;
+    for (j = 0; j < d; ++j) {
+        double inner = 0.0; /* ||(x_1j, ..., x_nj)||_q */
+        for (i = 0; i < n; ++i) {
+            double v = (double)load_x(x, dtype, i * d + j);
+            if (isnan(v)) {
+                has_nan = 1;
+                continue;
+            }
+            if (isinf(v)) {
+                has_inf = 1;
+                continue;
+            }
+            if (q == 2)
+                inner += v * v;
+            else if (fabs(v) > inner)
+                inner = fabs(v);
+        }
+        if (q == 2)
+            inner = sqrt(inner);
+        if (p == 2)
+            outer += inner * inner;
+        else if (inner > outer)
+            outer = inner;
+    }
+    if (has_nan)
+        return NAN;
+    if (has_inf)
+        return INFINITY;
+    return p == 2 ? sqrt(outer) : outer;
+}
+
+/* ------------------------------------------------------------------------------------------ */
+/* Stochastic rounding onto the level grid                                                     */
+/* ------------------------------------------------------------------------------------------ */
+
+/*
+ * Where |x| sits on the level grid.  Global-QSGD (Global-Q operator, formal definition) scales
+ * each worker's vector by the global norm N and rounds v = |x|/N in [0, 1] at random to one of
+ * the two adjacent levels lo <= v <= hi, up with probability (v - lo)/(hi - lo), which keeps the
+ * result unbiased.  The grids (Global-QSGD, paragraph introducing the two forms of the
+ * operator):
+ *   Global-L_s (standard dithering):    levels m/s, m = 0..s (the page writes l_i = (s-i)/s);
+ *   Global-E_s (exponential dithering): levels 0 and 2^-(s-k), k = 1..s.  The page writes
+ *     "l_s = 0 and l_i = 2^-(s-i) for i in 1..s", which names l_s twice; the reading taken is
+ *     the set {0, 2^-(s-1), ..., 1/2, 1} with level index k = 0 for the value 0.
+ *
+ * Output: *lo = index of the lower level (L: m with value m/s; E: k with value 0 for k = 0 and
+ * 2^-(s-k) otherwise), *T = floor(P(up) * 2^32), so that "round up iff r < T" for a uniform
+ * 32-bit word r rounds up with probability T / 2^32.  P(up) is computed exactly from v (every
+ * step below is exact in fp64), so T is floor(P(up) * 2^32) exactly.
+ *
+ * v = fp32(|x| / N), clamped to 1: a norm handed in from outside that is smaller than |x|
+ * saturates the element at the top level.  norm must be finite and > 0.
+ */
+int gqo_level_split(float absx, float norm, int scheme, int s, int32_t *lo, uint32_t *T)
+{
+    float v;
+    double f;
+    if (!(norm > 0.0f) || isinf(norm) || s < 1 || lo == NULL || T == NULL)
+        return GQO_ERR_INVALID;
+    if (scheme == GQO_LINEAR) {
+        if (s > 127)
+            return GQO_ERR_UNSUPPORTED;
+    } else if (scheme == GQO_EXP) {
+        if (s > 62)
+            return GQO_ERR_UNSUPPORTED;
+    } else {
+        return GQO_ERR_INVALID;
+    }
+    v = fabsf(absx) / norm; /* the one fp32 rounding */
+    if (v > 1.0f)
+        v = 1.0f;
+    if (scheme == GQO_LINEAR) {
+        double t = (double)v * (double)s; /* exact: 24-bit significand times a 7-bit integer */
+        double m = floor(t);
+        f = t - m; /* exact */
+        *lo = (int32_t)m;
+    } else {
+        double smallest = ldexp(1.0, -(s - 1)); /* the lowest non-zero level 2^-(s-1) */
+        if (v == 0.0f) {
+            *lo = 0;
+            f = 0.0;
+        } else if ((double)v < smallest) {
+            /* between the levels 0 and 2^-(s-1) */
+            *lo = 0;
+            f = (double)v / smallest; /* exact: division by a power of two */
+        } else {
+            /* between 2^e and 2^(e+1) with e = floor(log2 v), -(s-1) <= e <= 0 */
+            int ex;
+            frexp((double)v, &ex); /* v = mant * 2^ex with mant in [0.5, 1) */
+            {
+                int e = ex - 1;
+                *lo = s + e; /* 2^e = 2^-(s - lo) */
+                f = ldexp((double)v, -e) - 1.0; /* (v - 2^e) / (2^(e+1) - 2^e), exact */
+            }
+        }
+    }
+    *T = (uint32_t)floor(f * 4294967296.0); /* f * 2^32 is exact; f < 1 keeps T < 2^32 */
+    return GQO_OK;
+}
+
+/*
+ * Quantise the coordinate window [j0, j1) of all n workers to signed integer codes.
+ * Code c_ij = sign(x_ij) * k_ij where k_ij = lo + (r_ij < T_ij) is the level index chosen by
+ * the stochastic rounding and r_ij = gqo_philox_word(seed, step, i, j).  The stored code is
+ * the signed level index (Global-QSGD, theta example: one bit of sign and the remaining bits for
+ * the level).  codes is n x (j1 - j0), worker-major, one int8 per element.
+ *
+ * norm is the fp32 global norm.  norm == 0 (all-zero input) gives all-zero codes and GQO_OK; a
+ * non-finite norm gives all-zero codes and GQO_ERR_NONFINITE.
+ */
+int gqo_quantize(const void *x, int dtype, int64_t n, int64_t d, int64_t j0, int64_t j1,
+                 float norm, int scheme, int s, uint64_t seed, uint64_t step, int8_t *codes)
+{
+    int64_t i, j, w = j1 - j0;
+    if (x == NULL || codes == NULL || n < 1 || d < 1 || j0 < 0 || j1 > d || j0 > j1)
+        return GQO_ERR_INVALID;
+    if (dtype != GQO_F32 && dtype != GQO_BF16)
+        return GQO_ERR_INVALID;
+    if (scheme != GQO_LINEAR && scheme != GQO_EXP)
+        return GQO_ERR_INVALID;
+    if (s < 1 || s > (scheme == GQO_LINEAR ? 127 : 62))
+        return GQO_ERR_UNSUPPORTED;
+    if (isnan(norm) || isinf(norm) || norm < 0.0f) {
+        memset(codes, 0, (size_t)(n * w));
+        return GQO_ERR_NONFINITE;
+    }
+    if (norm == 0.0f) {
+        memset(codes, 0, (size_t)(n * w));
+        return GQO_OK;
+    }
+    for (i = 0; i < n; ++i) {
+        for (j = j0; j < j1; ++j) {
+            float xv = load_x(x, dtype, i * d + j);
+            int32_t lo;
+            uint32_t T, r;
+            int32_t k;
+            int rc = gqo_level_split(xv, norm, scheme, s, &lo, &T);
+            if (rc != GQO_OK)
+                return rc;
+            r = gqo_philox_word(seed, step, i, j);
+            k = lo + (r < T ? 1 : 0);
+            codes[i * w + (j - j0)] = (int8_t)(xv < 0.0f ? -k : k);
+        }
+    }
+    return GQO_OK;
+}
+
+/*
+ * Sum the codes over the n workers: the reduction the allreduce performs.  For Global-L_s the
+ * code is summed as it is (Global-QSGD, performance model: standard dithering reduces by the
+ * native arithmetic sum).  For Global-E_s a code of level index k stands for the value
+ * 2^-(s-k) = 2^(k-1) units of 2^-(s-1), so the sum adds sign * 2^(k-1) (0 for k = 0), which
+ * keeps it an exact integer.  codes is n x w, worker-major; sums has w entries.
+ */
+int gqo_reduce_codes(const int8_t *codes, int scheme, int s, int64_t n, int64_t w,
+                     int64_t *sums)
+{
+    int64_t i, j;
+    if (codes == NULL || sums == NULL || n < 1 || w < 0)
+        return GQO_ERR_INVALID;
+    if (scheme != GQO_LINEAR && scheme != GQO_EXP)
+        return GQO_ERR_INVALID;
+    if (s < 1 || s > (scheme == GQO_LINEAR ? 127 : 62))
+        return GQO_ERR_UNSUPPORTED;
+    for (j = 0; j < w; ++j) {
+        int64_t acc = 0;
+        for (i = 0; i < n; ++i) {
+            int c = codes[i * w + j];
+            if (scheme == GQO_LINEAR) {
+                acc += c;
+            } else if (c != 0) {
+                int k = c < 0 ? -c : c;
+                int64_t units = (int64_t)1 << (k - 1);
+                acc += c < 0 ? -units : units;
+            }
+        }
+        sums[j] = acc;
+    }
+    return GQO_OK;
+}
+
+/*
+ * Dequantise the code sums to the estimate of the mean gradient (1/n) sum_i Q(x_i), with
+ * Q(x_i) = N * sign(x_i) * level (Global-QSGD, Global-Q operator; third step of the
+ * communication hook).  One code unit is 1/s for Global-L_s and 2^-(s-1) for Global-E_s, so
+ * out_j = N * S_j / (n * s) or N * S_j * 2^-(s-1) / n.  In fp64, N * S_j is exact while
+ * |S_j| < 2^29 (a 24-bit significand times a 29-bit integer), the power-of-two scaling is exact,
+ * and the division by n (or n * s) is the one rounding.
+ */
+int gqo_dequantize(const int64_t *sums, float norm, int scheme, int s, int64_t n, int64_t w,
+                   double *out)
+{
+    int64_t j;
+    if (sums == NULL || out == NULL || n < 1 || w < 0)
+        return GQO_ERR_INVALID;
+    if (scheme != GQO_LINEAR && scheme != GQO_EXP)
+        return GQO_ERR_INVALID;
+    if (s < 1 || s > (scheme == GQO_LINEAR ? 127 : 62))
+        return GQO_ERR_UNSUPPORTED;
+    if (isnan(norm) || isinf(norm)) {
+        for (j = 0; j < w; ++j)
+            out[j] = 0.0;
+        return GQO_ERR_NONFINITE;
+    }
+    for (j = 0; j < w; ++j) {
+        double num = (double)norm * (double)sums[j];
+        if (scheme == GQO_LINEAR)
+            out[j] = num / ((double)n * (double)s);
+        else
+            out[j] = ldexp(num, -(s - 1)) / (double)n;
+    }
+    return GQO_OK;
+}
+
+/*
+ * The whole pipeline on the coordinate window [j0, j1): global norm over all d coordinates
+ * (fp64), rounded once to the fp32 norm N that the quantiser uses; codes, code sums and the
+ * dequantised mean for the window.  *norm64 receives the fp64 norm and *norm32 the fp32 one.
+ * codes (n x w int8), sums (w int64) and out (w fp64) are written for the window.
+ */
+int gqo_allreduce_mean(const void *x, int dtype, int64_t n, int64_t d, int q, int p, int scheme,
+                       int s, uint64_t seed, uint64_t step, int64_t j0, int64_t j1,
+                       double *norm64, float *norm32, int8_t *codes, int64_t *sums, double *out)
+{
+    double nrm;
+    float n32;
+    int rc;
+    int64_t w = j1 - j0;
+    if (norm64 == NULL || norm32 == NULL || codes == NULL || sums == NULL || out == NULL)
+        return GQO_ERR_INVALID;
+    nrm = gqo_global_norm(x, dtype, n, d, q, p);
+    if (nrm < 0.0)
+        return GQO_ERR_INVALID;
+    n32 = (float)nrm;
+    *norm64 = nrm;
+    *norm32 = n32;
+    rc = gqo_quantize(x, dtype, n, d, j0, j1, n32, scheme, s, seed, step, codes);
+    if (rc != GQO_OK && rc != GQO_ERR_NONFINITE)
+        return rc;
+    {
+        int rc2 = gqo_reduce_codes(codes, scheme, s, n, w, sums);
+        if (rc2 != GQO_OK)
+            return rc2;
+        rc2 = gqo_dequantize(sums, n32, scheme, s, n, w, out);
+        if (rc2 != GQO_OK)
+            return rc2;
+    }
+    return rc;
+}
