@@ -46,7 +46,9 @@ def build(force: bool = False) -> str:
 def lib() -> ctypes.CDLL:
     global _lib
     if _lib is None:
-        path = build()
+        # GQ_ORACLE_LIB points the pin tests at a deliberately broken copy of the oracle
+        # (tests/test_oracle_mutants.py), to show that the pins catch planted mistakes.
+        path = os.environ.get("GQ_ORACLE_LIB") or build()
         L = ctypes.CDLL(path)
         i64, u64, u32, i32 = ctypes.c_int64, ctypes.c_uint64, ctypes.c_uint32, ctypes.c_int32
         vp = ctypes.c_void_p

@@ -1,0 +1,56 @@
+"""The oracle's pins are sensitive: each plausible mistake planted in a copy of the oracle makes
+the pin suite fail (CPU only).
+
+Each mutant is the oracle source with one edit (a dropped term, a wrong sign, index or
+comparison, a transposed operand), compiled to a temporary library; the pin tests run against it
+in a subprocess (GQ_ORACLE_LIB) and must fail.
+"""
+import os
+import subprocess
+import sys
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+SRC = os.path.join(ROOT, "oracle", "gq_oracle.c")
+
+# (name, text in the oracle, replacement)
+MUTANTS = [
+    ("round-up compare <=", "k = lo + (r < T ? 1 : 0);", "k = lo + (r <= T ? 1 : 0);"),
+    ("round-up compare inverted", "k = lo + (r < T ? 1 : 0);", "k = lo + (r >= T ? 1 : 0);"),
+    ("worker dropped from counter", "ctr[1] = (uint32_t)i;", "ctr[1] = 0u;"),
+    ("step dropped from counter", "ctr[2] = (uint32_t)step;", "ctr[2] = 0u;"),
+    ("wrong word of the call", "return out[j & 3];", "return out[(j + 1) & 3];"),
+    ("philox key bump dropped", "k1 += weyl1;", "k1 += 0u;"),
+    ("philox halves swapped", "uint32_t n1 = lo1;", "uint32_t n1 = hi1;"),
+    ("E level off by one", "*lo = s + e; /* 2^e = 2^-(s - lo) */", "*lo = s + e + 1;"),
+    ("E first interval scale", "f = (double)v / smallest;", "f = (double)v / (2.0 * smallest);"),
+    ("L fraction dropped", "f = t - m; /* exact */", "f = 0.0;"),
+    ("sign dropped", "codes[i * w + (j - j0)] = (int8_t)(xv < 0.0f ? -k : k);",
+     "codes[i * w + (j - j0)] = (int8_t)k;"),
+    ("E decode 2^k", "int64_t units = (int64_t)1 << (k - 1);", "int64_t units = (int64_t)1 << k;"),
+    ("mean not divided by n", "out[j] = ldexp(num, -(s - 1)) / (double)n;",
+     "out[j] = ldexp(num, -(s - 1));"),
+    ("L scale drops s", "out[j] = num / ((double)n * (double)s);", "out[j] = num / (double)n;"),
+    ("norm transposed", "double v = (double)load_x(x, dtype, i * d + j);",
+     "double v = (double)load_x(x, dtype, (i * d + j) % n * d + (i * d + j) / n);"),
+    ("q=2 inner sqrt dropped", "        if (q == 2)\n            inner = sqrt(inner);", ""),
+    ("bf16 widened wrong", "<< 16;", "<< 8;"),
+]
+
+
+@pytest.mark.parametrize("name,old,new", MUTANTS, ids=[m[0] for m in MUTANTS])
+def test_pins_catch_mutant(tmp_path, name, old, new):
+    src = open(SRC).read()
+    assert src.count(old) == 1, name
+    mutant_c = tmp_path / "mutant.c"
+    mutant_c.write_text(src.replace(old, new))
+    so = tmp_path / "libmutant.so"
+    subprocess.run(["gcc", "-std=c99", "-O2", "-ffp-contract=off", "-fPIC", "-shared", "-o",
+                    str(so), str(mutant_c), "-lm"], check=True)
+    env = dict(os.environ, GQ_ORACLE_LIB=str(so))
+    pins = [os.path.join(ROOT, "tests", f) for f in
+            ("test_oracle_philox.py", "test_oracle_norm.py", "test_oracle_quantize.py")]
+    r = subprocess.run([sys.executable, "-m", "pytest", "-x", "-q", "-p", "no:cacheprovider",
+                        *pins], cwd=ROOT, env=env, capture_output=True, text=True, timeout=600)
+    assert r.returncode != 0, "pins did not catch mutant %r" % name

@@ -358,3 +358,22 @@ def test_codes_in_range(oracle):
         r = oracle.allreduce_mean(x, INF, 2, scheme, s, 11, 12)
         assert np.abs(r["codes"].astype(int)).max() <= s
         assert ((r["codes"] == 0) | (np.sign(r["codes"]) == np.sign(x))).all()
+
+
+def test_tie_does_not_round_up(oracle):
+    # Round up iff r < T.  Global-E thresholds are the 23-bit fraction of v shifted left by 9,
+    # so a word r with nine low zero bits is a reachable threshold: build v with T == r exactly
+    # (must stay at the lower level) and v with T == r + 512 (must round up).
+    seed, step = 5, 0
+    j = next(j for j in range(1, 50000)
+             if oracle.philox_word(seed, step, 0, j) & 0x1FF == 0
+             and oracle.philox_word(seed, step, 0, j) != 0)
+    r = oracle.philox_word(seed, step, 0, j)
+    for frac, want in [(r >> 9, 6), ((r >> 9) + 1, 7)]:
+        x = np.zeros((1, j + 1), dtype=np.float32)
+        x[0, 0] = 1.0  # max norm N = 1
+        v = (1.0 + frac / 2.0**23) * 0.25  # in [1/4, 1/2): level index 8 - 2 = 6 under E_8
+        x[0, j] = v
+        assert oracle.level_split(v, 1.0, EXP, 8) == (6, frac << 9)
+        codes, rc = oracle.quantize(x, np.float32(1.0), EXP, 8, seed, step)
+        assert codes[0, j] == want
