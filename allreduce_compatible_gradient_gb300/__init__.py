@@ -1,0 +1,13 @@
+"""GB300-native Global-QSGD compress / aggregate / decompress (Xin, Canini, Richtarik, Horvath,
+"Global-QSGD: Practical Floatless Quantization for Distributed Learning with Theoretical
+Guarantees", arXiv 2305.18627).
+
+The compute lives in libgq.so (hand-written CUDA for sm_103a, C ABI in include/gq.h); this
+package is a thin ctypes binding with the same names.  PyTorch supplies device memory and
+streams only.  There is no CPU fallback: importing the package without a built libgq.so raises.
+"""
+from ._binding import (  # noqa: F401
+    BF16, EXP, F32, LINEAR, NORM_INF, NORM_L2, GQError, gq_abi_version, gq_allreduce_mean,
+    gq_allreduce_mean_with_norm, gq_code_bits, gq_code_bytes, gq_code_pitch, gq_dequantize,
+    gq_get_status, gq_global_norm, gq_philox4x32_10, gq_quantize, gq_reduce_codes,
+    gq_status_string, gq_workspace, gq_workspace_bytes, lib, library_path)

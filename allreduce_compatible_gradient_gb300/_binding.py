@@ -1,0 +1,201 @@
+"""ctypes binding over libgq.so (include/gq.h).  Argument marshalling only: every step of the
+pipeline runs in the library's CUDA kernels.  Output tensors that the caller does not pass are
+allocated here with torch (the library itself allocates nothing)."""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+_LIB_PATH = os.path.join(_PKG, "libgq.so")
+
+F32, BF16 = 0, 1
+LINEAR, EXP = 0, 1
+NORM_INF, NORM_L2 = 0, 2
+
+_lib = None
+
+
+def library_path() -> str:
+    return _LIB_PATH
+
+
+def lib() -> ctypes.CDLL:
+    """Load libgq.so (built by ``__graft_entry__.build()``); fail loudly if it is missing."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(_LIB_PATH):
+        raise ImportError("libgq.so is not built (%s): run `python -c \"import __graft_entry__ as g; "
+                          "g.build()\"` first; there is no fallback path" % _LIB_PATH)
+    L = ctypes.CDLL(_LIB_PATH)
+    i64, u64, vp, ci = ctypes.c_int64, ctypes.c_uint64, ctypes.c_void_p, ctypes.c_int
+    sz = ctypes.c_size_t
+    sig = {
+        "gq_abi_version": (ci, []),
+        "gq_workspace_bytes": (sz, [i64, i64]),
+        "gq_workspace_init": (ci, [vp, sz, vp]),
+        "gq_code_bits": (ci, [ci, ci]),
+        "gq_code_pitch": (i64, [i64]),
+        "gq_code_bytes": (sz, [ci, ci, i64, i64]),
+        "gq_global_norm": (ci, [vp, ci, i64, i64, ci, ci, vp, vp, sz, vp]),
+        "gq_quantize": (ci, [vp, ci, i64, i64, vp, ci, ci, u64, u64, vp, vp]),
+        "gq_reduce_codes": (ci, [vp, ci, ci, i64, i64, vp, vp]),
+        "gq_dequantize": (ci, [vp, vp, ci, ci, i64, i64, vp, vp]),
+        "gq_allreduce_mean": (ci, [vp, ci, i64, i64, ci, ci, ci, ci, u64, u64, vp, vp, vp, vp, sz,
+                                   vp]),
+        "gq_allreduce_mean_with_norm": (ci, [vp, ci, i64, i64, vp, ci, ci, u64, u64, vp, vp, vp]),
+        "gq_philox4x32_10": (ci, [vp, vp, i64, vp]),
+        "gq_get_status": (ci, [vp, vp]),
+        "gq_status_string": (ctypes.c_char_p, [ci]),
+    }
+    for name, (res, args) in sig.items():
+        fn = getattr(L, name)
+        fn.restype = res
+        fn.argtypes = args
+    _lib = L
+    return L
+
+
+class GQError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__("%s: %s (status %d)" % (where, gq_status_string(status), status))
+
+
+def gq_status_string(status: int) -> str:
+    return lib().gq_status_string(int(status)).decode()
+
+
+def _check(status: int, where: str) -> None:
+    if status != 0:
+        raise GQError(status, where)
+
+
+def _p(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _dtype_code(t: torch.Tensor) -> int:
+    if t.dtype == torch.float32:
+        return F32
+    if t.dtype == torch.bfloat16:
+        return BF16
+    raise TypeError("gradients must be float32 or bfloat16, got %s" % t.dtype)
+
+
+def _grads(t: torch.Tensor):
+    if t.dim() != 2 or not t.is_cuda or not t.is_contiguous():
+        raise ValueError("gradients must be a contiguous n x d CUDA tensor")
+    return _dtype_code(t), t.shape[0], t.shape[1]
+
+
+# ---- sizes ---------------------------------------------------------------------------------
+
+def gq_abi_version() -> int:
+    return lib().gq_abi_version()
+
+
+def gq_workspace_bytes(n: int = 1, d: int = 1) -> int:
+    return lib().gq_workspace_bytes(n, d)
+
+
+def gq_code_bits(scheme: int, s: int) -> int:
+    return lib().gq_code_bits(scheme, s)
+
+
+def gq_code_pitch(d: int) -> int:
+    return lib().gq_code_pitch(d)
+
+
+def gq_code_bytes(scheme: int, s: int, n: int, d: int) -> int:
+    return lib().gq_code_bytes(scheme, s, n, d)
+
+
+def gq_workspace(device=None, stream=None) -> torch.Tensor:
+    """A zero-initialised workspace tensor (uint8) for the norm step."""
+    nb = gq_workspace_bytes()
+    ws = torch.empty(nb, dtype=torch.uint8, device=device or "cuda")
+    _check(lib().gq_workspace_init(_p(ws), nb, _stream(stream)), "gq_workspace_init")
+    return ws
+
+
+# ---- the pipeline --------------------------------------------------------------------------
+
+def gq_global_norm(grads, q, p, norm=None, ws=None, stream=None) -> torch.Tensor:
+    dt, n, d = _grads(grads)
+    norm = torch.empty(1, dtype=torch.float32, device=grads.device) if norm is None else norm
+    ws = gq_workspace(grads.device, stream) if ws is None else ws
+    _check(lib().gq_global_norm(_p(grads), dt, n, d, q, p, _p(norm), _p(ws), ws.numel(),
+                                _stream(stream)), "gq_global_norm")
+    return norm
+
+
+def gq_quantize(grads, norm, scheme, s, seed, step, codes=None, stream=None) -> torch.Tensor:
+    dt, n, d = _grads(grads)
+    if codes is None:
+        codes = torch.empty(gq_code_bytes(scheme, s, n, d), dtype=torch.uint8, device=grads.device)
+    _check(lib().gq_quantize(_p(grads), dt, n, d, _p(norm), scheme, s, seed, step, _p(codes),
+                             _stream(stream)), "gq_quantize")
+    return codes
+
+
+def gq_reduce_codes(codes, scheme, s, n, d, sums=None, stream=None) -> torch.Tensor:
+    if sums is None:
+        sums = torch.empty(d, dtype=torch.int32, device=codes.device)
+    _check(lib().gq_reduce_codes(_p(codes), scheme, s, n, d, _p(sums), _stream(stream)),
+           "gq_reduce_codes")
+    return sums
+
+
+def gq_dequantize(sums, norm, scheme, s, n, out=None, stream=None) -> torch.Tensor:
+    d = sums.numel()
+    if out is None:
+        out = torch.empty(d, dtype=torch.float32, device=sums.device)
+    _check(lib().gq_dequantize(_p(sums), _p(norm), scheme, s, n, d, _p(out), _stream(stream)),
+           "gq_dequantize")
+    return out
+
+
+def gq_allreduce_mean(grads, q, p, scheme, s, seed, step, out=None, norm=None, codes=None,
+                      ws=None, stream=None) -> torch.Tensor:
+    dt, n, d = _grads(grads)
+    if out is None:
+        out = torch.empty(d, dtype=torch.float32, device=grads.device)
+    ws = gq_workspace(grads.device, stream) if ws is None else ws
+    _check(lib().gq_allreduce_mean(_p(grads), dt, n, d, q, p, scheme, s, seed, step, _p(out),
+                                   _p(norm), _p(codes), _p(ws), ws.numel(), _stream(stream)),
+           "gq_allreduce_mean")
+    return out
+
+
+def gq_allreduce_mean_with_norm(grads, norm, scheme, s, seed, step, out=None, codes=None,
+                                stream=None) -> torch.Tensor:
+    dt, n, d = _grads(grads)
+    if out is None:
+        out = torch.empty(d, dtype=torch.float32, device=grads.device)
+    _check(lib().gq_allreduce_mean_with_norm(_p(grads), dt, n, d, _p(norm), scheme, s, seed, step,
+                                             _p(out), _p(codes), _stream(stream)),
+           "gq_allreduce_mean_with_norm")
+    return out
+
+
+def gq_philox4x32_10(ctr_key, out=None, stream=None) -> torch.Tensor:
+    """ctr_key: count x 6 int32 tensor (counter words 0..3, key words 0..1, as bit patterns)."""
+    count = ctr_key.shape[0]
+    if out is None:
+        out = torch.empty((count, 4), dtype=torch.int32, device=ctr_key.device)
+    _check(lib().gq_philox4x32_10(_p(ctr_key), _p(out), count, _stream(stream)),
+           "gq_philox4x32_10")
+    return out
+
+
+def gq_get_status(ws, stream=None) -> int:
+    return lib().gq_get_status(_p(ws), _stream(stream))

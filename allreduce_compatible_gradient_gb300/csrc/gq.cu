@@ -1,0 +1,352 @@
+// gq.cu -- C ABI (include/gq.h) over the sm_103a kernels in gq_kernels.cuh.
+//
+// Host side only: argument checks (returned synchronously, before anything is enqueued),
+// launch geometry (grid = resident blocks per SM x SM count, capped by the work), and kernel
+// dispatch on (dtype, scheme, code width, norm order).  No memory is allocated here.
+#include "gq.h"
+#include "gq_kernels.cuh"
+
+#include <cuda_runtime.h>
+
+#include <cstdint>
+#include <cstring>
+
+namespace {
+
+using gq::kThreads;
+
+constexpr int64_t kMaxD = int64_t(1) << 34;  // Philox counter word 0 holds j / 4 in 32 bits
+constexpr int kMaxDevices = 64;
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int sm_count() {
+    static int cache[kMaxDevices] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 152;
+    if (cache[dev] == 0) {
+        int v = 0;
+        if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || v <= 0)
+            v = 152;
+        cache[dev] = v;
+    }
+    return cache[dev];
+}
+
+// Resident blocks per SM for a kernel (cached per kernel instantiation and device).
+template <typename K>
+int blocks_per_sm(K kernel) {
+    static int cache[kMaxDevices] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) dev = 0;
+    if (cache[dev] == 0) {
+        int nb = 0;
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, kernel, kThreads, 0) != cudaSuccess ||
+            nb <= 0)
+            nb = 1;
+        cache[dev] = nb;
+    }
+    return cache[dev];
+}
+
+// Grid for a grid-stride kernel over `work` thread-items: one full wave of resident blocks
+// (a multiple of the SM count), fewer when the work is smaller.
+template <typename K>
+unsigned grid_for(K kernel, int64_t work, int64_t cap = INT32_MAX) {
+    const int64_t full = static_cast<int64_t>(blocks_per_sm(kernel)) * sm_count();
+    int64_t need = (work + kThreads - 1) / kThreads;
+    int64_t g = need < full ? need : full;
+    if (g > cap) g = cap;
+    if (g < 1) g = 1;
+    return static_cast<unsigned>(g);
+}
+
+gq_status launch_status() {
+    return cudaGetLastError() == cudaSuccess ? GQ_OK : GQ_ERR_CUDA;
+}
+
+gq_status check_grads(const void* grads, int dtype, int64_t n, int64_t d) {
+    if (!grads || !aligned16(grads)) return GQ_ERR_INVALID;
+    if (dtype != GQ_F32 && dtype != GQ_BF16) return GQ_ERR_INVALID;
+    if (n < 1 || n >= (int64_t(1) << 31) || d < 1 || d >= kMaxD) return GQ_ERR_INVALID;
+    return GQ_OK;
+}
+
+gq_status check_scheme(int scheme, int s, int64_t n) {
+    if (scheme != GQ_LINEAR && scheme != GQ_EXP) return GQ_ERR_INVALID;
+    if (scheme == GQ_LINEAR) {
+        if (s < 1 || s > 127) return GQ_ERR_UNSUPPORTED;
+        if (n * static_cast<int64_t>(s) >= (int64_t(1) << 24)) return GQ_ERR_OVERFLOW;
+    } else {
+        if (s < 1 || s > 24) return GQ_ERR_UNSUPPORTED;
+        if (n * (int64_t(1) << (s - 1)) >= (int64_t(1) << 24)) return GQ_ERR_OVERFLOW;
+    }
+    return GQ_OK;
+}
+
+gq_status check_ws(const void* ws, size_t ws_bytes, int64_t n, int64_t d) {
+    if (!ws || !aligned16(ws)) return GQ_ERR_WORKSPACE;
+    if (ws_bytes < gq_workspace_bytes(n, d)) return GQ_ERR_WORKSPACE;
+    return GQ_OK;
+}
+
+int norm_mode(int q, int p) {
+    if (q == GQ_NORM_INF && p == GQ_NORM_INF) return gq::kMaxMax;
+    if (q == GQ_NORM_L2 && p == GQ_NORM_L2) return gq::kL2L2;
+    if (q == GQ_NORM_L2 && p == GQ_NORM_INF) return gq::kL2Max;
+    if (q == GQ_NORM_INF && p == GQ_NORM_L2) return gq::kMaxL2;
+    return -1;
+}
+
+// ---- norm ---------------------------------------------------------------------------------
+template <typename T, int MODE>
+gq_status run_norm(const T* x, int64_t n, int64_t d, float* norm_user, unsigned char* ws,
+                   cudaStream_t st) {
+    constexpr int C = gq::Elem<T>::kCols;
+    const int64_t groups = (d + C - 1) / C;
+    const bool vec_rows = (d % C) == 0;
+    auto k = gq::norm_kernel<T, MODE>;
+    const unsigned grid = grid_for(k, groups, gq::kMaxPartials);
+    k<<<grid, kThreads, 0, st>>>(x, n, d, groups, vec_rows, norm_user, ws);
+    return launch_status();
+}
+
+template <typename T>
+gq_status dispatch_norm(const void* grads, int mode, int64_t n, int64_t d, float* norm_user,
+                        unsigned char* ws, cudaStream_t st) {
+    const T* x = static_cast<const T*>(grads);
+    switch (mode) {
+        case gq::kMaxMax: return run_norm<T, gq::kMaxMax>(x, n, d, norm_user, ws, st);
+        case gq::kL2L2: return run_norm<T, gq::kL2L2>(x, n, d, norm_user, ws, st);
+        case gq::kL2Max: return run_norm<T, gq::kL2Max>(x, n, d, norm_user, ws, st);
+        default: return run_norm<T, gq::kMaxL2>(x, n, d, norm_user, ws, st);
+    }
+}
+
+gq_status norm_any(const void* grads, int dtype, int mode, int64_t n, int64_t d, float* norm_user,
+                   void* ws, cudaStream_t st) {
+    unsigned char* w = static_cast<unsigned char*>(ws);
+    return dtype == GQ_F32 ? dispatch_norm<float>(grads, mode, n, d, norm_user, w, st)
+                           : dispatch_norm<uint16_t>(grads, mode, n, d, norm_user, w, st);
+}
+
+// ---- quantize (+ sum + dequantize) ----------------------------------------------------------
+template <typename T, int SCHEME, int BITS, bool OUT>
+gq_status run_quant(const void* grads, const gq::QuantArgs& a, void* codes, float* out,
+                    cudaStream_t st) {
+    constexpr int C = gq::Elem<T>::kCols;
+    const int64_t groups = BITS ? a.pitch / C : (a.d + C - 1) / C;
+    auto k = gq::quantize_kernel<T, SCHEME, BITS, OUT>;
+    const unsigned grid = grid_for(k, groups);
+    k<<<grid, kThreads, 0, st>>>(static_cast<const T*>(grads), a, groups,
+                                 static_cast<unsigned char*>(codes), out);
+    return launch_status();
+}
+
+template <typename T, int SCHEME, bool OUT>
+gq_status quant_bits(const void* grads, const gq::QuantArgs& a, int bits, void* codes, float* out,
+                     cudaStream_t st) {
+    if (!codes) return run_quant<T, SCHEME, 0, OUT>(grads, a, nullptr, out, st);
+    if (bits == 4) return run_quant<T, SCHEME, 4, OUT>(grads, a, codes, out, st);
+    return run_quant<T, SCHEME, 8, OUT>(grads, a, codes, out, st);
+}
+
+template <bool OUT>
+gq_status quant_any(const void* grads, int dtype, const gq::QuantArgs& a, int scheme, int bits,
+                    void* codes, float* out, cudaStream_t st) {
+    if (dtype == GQ_F32)
+        return scheme == GQ_LINEAR ? quant_bits<float, gq::kLinear, OUT>(grads, a, bits, codes, out, st)
+                                   : quant_bits<float, gq::kExp, OUT>(grads, a, bits, codes, out, st);
+    return scheme == GQ_LINEAR ? quant_bits<uint16_t, gq::kLinear, OUT>(grads, a, bits, codes, out, st)
+                               : quant_bits<uint16_t, gq::kExp, OUT>(grads, a, bits, codes, out, st);
+}
+
+gq::QuantArgs make_args(const float* norm_ptr, int dtype, int64_t n, int64_t d, int s,
+                        uint64_t seed, uint64_t step) {
+    gq::QuantArgs a;
+    a.norm_ptr = norm_ptr;
+    a.s = static_cast<uint32_t>(s);
+    a.key0 = static_cast<uint32_t>(seed);
+    a.key1 = static_cast<uint32_t>(seed >> 32);
+    a.step_lo = static_cast<uint32_t>(step);
+    a.step_hi = static_cast<uint32_t>(step >> 32);
+    a.n = n;
+    a.d = d;
+    a.pitch = gq_code_pitch(d);
+    a.vec_rows = (d % (dtype == GQ_F32 ? 4 : 8)) == 0;
+    return a;
+}
+
+}  // namespace
+
+extern "C" {
+
+int gq_abi_version(void) { return 1; }
+
+size_t gq_workspace_bytes(int64_t n, int64_t d) {
+    (void)n;
+    (void)d;
+    return static_cast<size_t>(gq::kHeaderBytes) + sizeof(uint64_t) * gq::kMaxPartials;
+}
+
+gq_status gq_workspace_init(void* ws, size_t ws_bytes, void* stream) {
+    if (!ws || !aligned16(ws) || ws_bytes < gq_workspace_bytes(1, 1))
+        return GQ_ERR_WORKSPACE;
+    if (cudaMemsetAsync(ws, 0, gq_workspace_bytes(1, 1), static_cast<cudaStream_t>(stream)) != cudaSuccess)
+        return GQ_ERR_CUDA;
+    return GQ_OK;
+}
+
+int gq_code_bits(int scheme, int s) {
+    if (scheme != GQ_LINEAR && scheme != GQ_EXP) return 0;
+    if (s < 1 || s > (scheme == GQ_LINEAR ? 127 : 24)) return 0;
+    return s <= 7 ? 4 : 8;
+}
+
+int64_t gq_code_pitch(int64_t d) { return d < 1 ? 0 : (d + 31) / 32 * 32; }
+
+size_t gq_code_bytes(int scheme, int s, int64_t n, int64_t d) {
+    const int bits = gq_code_bits(scheme, s);
+    if (!bits || n < 1 || d < 1) return 0;
+    return static_cast<size_t>(n) * static_cast<size_t>(gq_code_pitch(d)) * bits / 8;
+}
+
+gq_status gq_global_norm(const void* grads, int dtype, int64_t n, int64_t d, int q, int p,
+                         float* norm_dev, void* ws, size_t ws_bytes, void* stream) {
+    gq_status st = check_grads(grads, dtype, n, d);
+    if (st != GQ_OK) return st;
+    const int mode = norm_mode(q, p);
+    if (mode < 0 || !norm_dev) return GQ_ERR_INVALID;
+    if ((st = check_ws(ws, ws_bytes, n, d)) != GQ_OK) return st;
+    return norm_any(grads, dtype, mode, n, d, norm_dev, ws, static_cast<cudaStream_t>(stream));
+}
+
+gq_status gq_quantize(const void* grads, int dtype, int64_t n, int64_t d, const float* norm_dev,
+                      int scheme, int s, uint64_t seed, uint64_t step, void* codes,
+                      void* stream) {
+    gq_status st = check_grads(grads, dtype, n, d);
+    if (st != GQ_OK) return st;
+    if ((st = check_scheme(scheme, s, n)) != GQ_OK) return st;
+    if (!norm_dev || !codes || !aligned16(codes)) return GQ_ERR_INVALID;
+    const gq::QuantArgs a = make_args(norm_dev, dtype, n, d, s, seed, step);
+    return quant_any<false>(grads, dtype, a, scheme, gq_code_bits(scheme, s), codes, nullptr,
+                            static_cast<cudaStream_t>(stream));
+}
+
+gq_status gq_reduce_codes(const void* codes, int scheme, int s, int64_t n, int64_t d,
+                          int32_t* sum_dev, void* stream) {
+    if (!codes || !sum_dev || !aligned16(codes) || !aligned16(sum_dev)) return GQ_ERR_INVALID;
+    if (n < 1 || n >= (int64_t(1) << 31) || d < 1 || d >= kMaxD) return GQ_ERR_INVALID;
+    gq_status st = check_scheme(scheme, s, n);
+    if (st != GQ_OK) return st;
+    const int bits = gq_code_bits(scheme, s);
+    const int64_t row_bytes = gq_code_pitch(d) * bits / 8;
+    const int64_t chunks = row_bytes / 16;
+    cudaStream_t cs = static_cast<cudaStream_t>(stream);
+    const unsigned char* c = static_cast<const unsigned char*>(codes);
+#define GQ_REDUCE(BITS, SCH)                                                     \
+    do {                                                                         \
+        auto k = gq::reduce_codes_kernel<BITS, SCH>;                             \
+        k<<<grid_for(k, chunks), kThreads, 0, cs>>>(c, n, d, row_bytes, chunks, sum_dev); \
+    } while (0)
+    if (bits == 8) {
+        if (scheme == GQ_LINEAR) GQ_REDUCE(8, gq::kLinear); else GQ_REDUCE(8, gq::kExp);
+    } else {
+        if (scheme == GQ_LINEAR) GQ_REDUCE(4, gq::kLinear); else GQ_REDUCE(4, gq::kExp);
+    }
+#undef GQ_REDUCE
+    return launch_status();
+}
+
+gq_status gq_dequantize(const int32_t* sum_dev, const float* norm_dev, int scheme, int s,
+                        int64_t n, int64_t d, float* out_dev, void* stream) {
+    if (!sum_dev || !norm_dev || !out_dev || !aligned16(sum_dev) || !aligned16(out_dev))
+        return GQ_ERR_INVALID;
+    if (n < 1 || n >= (int64_t(1) << 31) || d < 1 || d >= kMaxD) return GQ_ERR_INVALID;
+    gq_status st = check_scheme(scheme, s, n);
+    if (st != GQ_OK) return st;
+    cudaStream_t cs = static_cast<cudaStream_t>(stream);
+    const int64_t quads = (d + 3) / 4;
+    if (scheme == GQ_LINEAR) {
+        auto k = gq::dequantize_kernel<gq::kLinear>;
+        k<<<grid_for(k, quads), kThreads, 0, cs>>>(sum_dev, norm_dev, n, static_cast<uint32_t>(s), d, out_dev);
+    } else {
+        auto k = gq::dequantize_kernel<gq::kExp>;
+        k<<<grid_for(k, quads), kThreads, 0, cs>>>(sum_dev, norm_dev, n, static_cast<uint32_t>(s), d, out_dev);
+    }
+    return launch_status();
+}
+
+gq_status gq_allreduce_mean(const void* grads, int dtype, int64_t n, int64_t d, int q, int p,
+                            int scheme, int s, uint64_t seed, uint64_t step, float* out_dev,
+                            float* norm_dev, void* codes, void* ws, size_t ws_bytes,
+                            void* stream) {
+    gq_status st = check_grads(grads, dtype, n, d);
+    if (st != GQ_OK) return st;
+    const int mode = norm_mode(q, p);
+    if (mode < 0) return GQ_ERR_INVALID;
+    if ((st = check_scheme(scheme, s, n)) != GQ_OK) return st;
+    if (!out_dev || !aligned16(out_dev) || (codes && !aligned16(codes))) return GQ_ERR_INVALID;
+    if ((st = check_ws(ws, ws_bytes, n, d)) != GQ_OK) return st;
+    cudaStream_t cs = static_cast<cudaStream_t>(stream);
+    if ((st = norm_any(grads, dtype, mode, n, d, norm_dev, ws, cs)) != GQ_OK) return st;
+    const float* ws_norm = &reinterpret_cast<const gq::WsHeader*>(ws)->norm;
+    const gq::QuantArgs a = make_args(ws_norm, dtype, n, d, s, seed, step);
+    return quant_any<true>(grads, dtype, a, scheme, gq_code_bits(scheme, s), codes, out_dev, cs);
+}
+
+gq_status gq_allreduce_mean_with_norm(const void* grads, int dtype, int64_t n, int64_t d,
+                                      const float* norm_dev, int scheme, int s, uint64_t seed,
+                                      uint64_t step, float* out_dev, void* codes, void* stream) {
+    gq_status st = check_grads(grads, dtype, n, d);
+    if (st != GQ_OK) return st;
+    if ((st = check_scheme(scheme, s, n)) != GQ_OK) return st;
+    if (!norm_dev || !out_dev || !aligned16(out_dev) || (codes && !aligned16(codes)))
+        return GQ_ERR_INVALID;
+    const gq::QuantArgs a = make_args(norm_dev, dtype, n, d, s, seed, step);
+    return quant_any<true>(grads, dtype, a, scheme, gq_code_bits(scheme, s), codes, out_dev,
+                           static_cast<cudaStream_t>(stream));
+}
+
+gq_status gq_philox4x32_10(const uint32_t* ctr_key_dev, uint32_t* out_dev, int64_t count,
+                           void* stream) {
+    if (!ctr_key_dev || !out_dev || count < 0 || count > (int64_t(1) << 40)) return GQ_ERR_INVALID;
+    if (count == 0) return GQ_OK;
+    const int64_t blocks = (count + kThreads - 1) / kThreads;
+    if (blocks > INT32_MAX) return GQ_ERR_INVALID;
+    gq::philox_kernel<<<static_cast<unsigned>(blocks), kThreads, 0,
+                        static_cast<cudaStream_t>(stream)>>>(ctr_key_dev, out_dev, count);
+    return launch_status();
+}
+
+gq_status gq_get_status(void* ws, void* stream) {
+    if (!ws) return GQ_ERR_WORKSPACE;
+    cudaStream_t cs = static_cast<cudaStream_t>(stream);
+    if (cudaStreamSynchronize(cs) != cudaSuccess) return GQ_ERR_CUDA;
+    unsigned int v = 0;
+    gq::WsHeader* hdr = static_cast<gq::WsHeader*>(ws);
+    if (cudaMemcpy(&v, &hdr->status, sizeof v, cudaMemcpyDeviceToHost) != cudaSuccess)
+        return GQ_ERR_CUDA;
+    if (v != 0) {
+        const unsigned int zero = 0;
+        if (cudaMemcpy(&hdr->status, &zero, sizeof zero, cudaMemcpyHostToDevice) != cudaSuccess)
+            return GQ_ERR_CUDA;
+    }
+    return static_cast<gq_status>(v);
+}
+
+const char* gq_status_string(int status) {
+    switch (status) {
+        case GQ_OK: return "ok";
+        case GQ_ERR_INVALID: return "invalid argument";
+        case GQ_ERR_UNSUPPORTED: return "unsupported number of levels";
+        case GQ_ERR_OVERFLOW: return "code sum would overflow the exact fp32 range";
+        case GQ_ERR_NONFINITE: return "non-finite norm";
+        case GQ_ERR_TIMEOUT: return "device wait timed out";
+        case GQ_ERR_CUDA: return "CUDA error";
+        case GQ_ERR_WORKSPACE: return "workspace null, too small or misaligned";
+        default: return "unknown status";
+    }
+}
+
+}  // extern "C"

@@ -1,0 +1,637 @@
+// gq_kernels.cuh -- sm_103a kernels of the Global-QSGD compress / aggregate / decompress path.
+//
+// Method: "Global-QSGD: Practical Floatless Quantization for Distributed Learning with
+// Theoretical Guarantees" (arXiv 2305.18627), cited as "Global-QSGD".  All kernels are
+// HBM-bandwidth kernels (nothing here is a dense contraction): each thread owns one 16-byte
+// column group (4 fp32 or 8 bf16 coordinates) and walks the n worker rows of that group, so a
+// warp reads 512 contiguous bytes of one row per load.  Grids are grid-stride loops sized to
+// the resident capacity of the GPU (a multiple of its SM count).
+//
+// Built with -fmad=false: every fp32 operation is a separately rounded IEEE operation, and the
+// normalisation is the correctly rounded quotient (__fdiv_rn).
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace gq {
+
+constexpr int kThreads = 256;        // threads per block for every kernel
+constexpr int kMaxPartials = 4096;   // upper bound on norm-kernel blocks (workspace size)
+constexpr int kHeaderBytes = 256;    // workspace header, then kMaxPartials 8-byte partials
+
+// Workspace header (device memory owned by the caller).
+struct WsHeader {
+    unsigned int status;  // sticky device-detected status (0 = ok)
+    unsigned int ticket;  // blocks of the running norm kernel that have finished; 0 between calls
+    float norm;           // fp32 norm written by the last norm kernel
+    unsigned int pad[61];
+};
+static_assert(sizeof(WsHeader) == kHeaderBytes, "workspace header is 256 bytes");
+
+enum NormMode { kMaxMax = 0, kL2L2 = 1, kL2Max = 2, kMaxL2 = 3 };  // (q, p) pairs
+enum Scheme { kLinear = 0, kExp = 1 };
+
+// ------------------------------------------------------------------------------------------
+// Philox4x32-10 (Salmon, Moraes, Dror, Shaw, SC'11): ten rounds of the Philox-4x32 bijection.
+// Each round multiplies counter words 0 and 2 by the round multipliers (full 64-bit products),
+// xors the high halves into words 1 and 3 with the round key, and swaps; the key advances by
+// the two Weyl constants between rounds.
+// ------------------------------------------------------------------------------------------
+__device__ __forceinline__ uint4 philox4x32_10(uint4 c, uint32_t k0, uint32_t k1) {
+    const uint32_t kMul0 = 0xD2511F53u, kMul1 = 0xCD9E8D57u;
+    const uint32_t kWeyl0 = 0x9E3779B9u, kWeyl1 = 0xBB67AE85u;
+#pragma unroll
+    for (int round = 0; round < 10; ++round) {
+        const uint32_t hi0 = __umulhi(kMul0, c.x), lo0 = kMul0 * c.x;
+        const uint32_t hi1 = __umulhi(kMul1, c.z), lo1 = kMul1 * c.z;
+        c = make_uint4(hi1 ^ c.y ^ k0, lo1, hi0 ^ c.w ^ k1, lo0);
+        k0 += kWeyl0;
+        k1 += kWeyl1;
+    }
+    return c;
+}
+
+// ------------------------------------------------------------------------------------------
+// Element access: a 16-byte column group of one row, widened to fp32.
+// ------------------------------------------------------------------------------------------
+template <typename T> struct Elem;
+template <> struct Elem<float> {
+    static constexpr int kCols = 4;
+    __device__ __forceinline__ static void load_vec(const float* p, float (&v)[4]) {
+        const float4 t = __ldg(reinterpret_cast<const float4*>(p));
+        v[0] = t.x; v[1] = t.y; v[2] = t.z; v[3] = t.w;
+    }
+    __device__ __forceinline__ static float load_one(const float* p) { return __ldg(p); }
+};
+// bf16 is the high half of a binary32 word: widening is a 16-bit shift of the bits.
+template <> struct Elem<uint16_t> {
+    static constexpr int kCols = 8;
+    __device__ __forceinline__ static void load_vec(const uint16_t* p, float (&v)[8]) {
+        const uint4 t = __ldg(reinterpret_cast<const uint4*>(p));
+        const uint32_t w[4] = {t.x, t.y, t.z, t.w};
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            v[2 * k] = __uint_as_float(w[k] << 16);
+            v[2 * k + 1] = __uint_as_float(w[k] & 0xFFFF0000u);
+        }
+    }
+    __device__ __forceinline__ static float load_one(const uint16_t* p) {
+        return __uint_as_float(static_cast<uint32_t>(__ldg(p)) << 16);
+    }
+};
+
+// Row i, column group g (columns g*C .. g*C+C-1) of the n x d matrix x, zero past column d.
+template <typename T>
+__device__ __forceinline__ void load_group(const T* __restrict__ x, int64_t i, int64_t g,
+                                           int64_t d, bool vec_rows,
+                                           float (&v)[Elem<T>::kCols]) {
+    constexpr int C = Elem<T>::kCols;
+    const int64_t j0 = g * C;
+    const T* row = x + i * d;
+    if (vec_rows && j0 + C <= d) {
+        Elem<T>::load_vec(row + j0, v);
+    } else {
+#pragma unroll
+        for (int c = 0; c < C; ++c) v[c] = (j0 + c < d) ? Elem<T>::load_one(row + j0 + c) : 0.0f;
+    }
+}
+
+// 2^k as fp32 for k in [-149, 127] (exact: normal or subnormal power of two).
+__device__ __forceinline__ float exp2i(int k) {
+    return k >= -126 ? __int_as_float((k + 127) << 23) : __int_as_float(1 << (k + 149));
+}
+
+constexpr uint32_t kInfBits = 0x7F800000u;
+
+// ------------------------------------------------------------------------------------------
+// Sum of squares with a power-of-two scale (for the l2 norms).  Values are multiplied by
+// f = 2^-E before squaring, where 2^(E+1) bounds every magnitude seen so far, so squares
+// neither overflow nor vanish anywhere in the fp32 range; the squares are summed with Kahan
+// compensation.  When a larger magnitude arrives the running sum is rescaled (rare).  NaN and
+// infinite values flow through the arithmetic and leave the sum non-finite.
+// ------------------------------------------------------------------------------------------
+struct ScaledSumSq {
+    float acc, comp;  // Kahan sum of (x * f)^2 and its running compensation
+    float f;          // 2^-E
+    float lim;        // 2^(E+1): magnitudes >= lim need a rescale first
+    int e;            // E
+
+    __device__ __forceinline__ void init() {
+        acc = 0.0f; comp = 0.0f; e = -150; f = 1.0f; lim = exp2i(-149);  // any non-zero rescales
+    }
+    // Make 2^(E+1) bound the finite magnitude m >= lim.
+    __device__ __forceinline__ void rescale(float m) {
+        if (!(m < __uint_as_float(kInfBits))) return;  // Inf / NaN: left to the arithmetic
+        const uint32_t eb = __float_as_uint(m) >> 23;
+        const int ne = eb ? static_cast<int>(eb) - 127 : -127;  // m < 2^(ne+1)
+        if (ne <= e) return;
+        const int half = e - ne;  // the sum scales by 2^(2 half), half < 0
+        if (half < -100) {
+            acc = 0.0f;  // the old sum is below 2^-200 of one new square: negligible
+            comp = 0.0f;
+        } else {
+            const float h = exp2i(half);
+            acc = (acc * h) * h;
+            comp = (comp * h) * h;
+        }
+        e = ne;
+        f = exp2i(-ne);
+        lim = (ne + 1 >= 128) ? __uint_as_float(kInfBits) : exp2i(ne + 1);
+    }
+    __device__ __forceinline__ void kahan_add(float y) {
+        const float yy = y - comp;
+        const float t = acc + yy;
+        comp = (t - acc) - yy;
+        acc = t;
+    }
+    // Add the squares of C values.
+    template <int C>
+    __device__ __forceinline__ void add(const float (&v)[C]) {
+        float m = fabsf(v[0]);
+#pragma unroll
+        for (int c = 1; c < C; ++c) m = fmaxf(m, fabsf(v[c]));
+        if (m >= lim) rescale(m);
+        float sq[C];
+#pragma unroll
+        for (int c = 0; c < C; ++c) { const float t = v[c] * f; sq[c] = t * t; }
+#pragma unroll
+        for (int w = 1; w < C; w *= 2)
+#pragma unroll
+            for (int c = 0; c + w < C; c += 2 * w) sq[c] = sq[c] + sq[c + w];
+        kahan_add(sq[0]);
+    }
+    __device__ __forceinline__ float sum() const { return acc - comp; }
+    // The sum as fp64, scale removed.
+    __device__ __forceinline__ double value() const {
+        return ldexp(static_cast<double>(acc) - static_cast<double>(comp), 2 * e);
+    }
+};
+
+// Order-preserving 64-bit key of c * 4^E for a normal positive fp32 c (maxima of scaled column
+// norms without fp64 arithmetic per column): the exponent field extended past 8 bits.
+__device__ __forceinline__ int64_t scaled_key(float c, int e) {
+    return static_cast<int64_t>(__float_as_uint(c)) + (static_cast<int64_t>(2 * e) << 23);
+}
+// The fp64 value of a key (exact).
+__device__ __forceinline__ double key_value(int64_t key) {
+    const int64_t ex = (key >> 23) - 127;  // unbiased exponent of c * 4^E
+    const uint64_t frac = static_cast<uint64_t>(key & 0x7FFFFF);
+    const uint64_t bits = (static_cast<uint64_t>(ex + 1023) << 52) | (frac << 29);
+    return __longlong_as_double(static_cast<long long>(bits));
+}
+
+// ------------------------------------------------------------------------------------------
+// Block reductions (fixed order: deterministic for a given grid and block size).
+// ------------------------------------------------------------------------------------------
+__device__ __forceinline__ double block_sum(double v, double* sh) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_down_sync(0xFFFFFFFFu, v, o);
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    if (lane == 0) sh[warp] = v;
+    __syncthreads();
+    double r = 0.0;
+    if (threadIdx.x == 0)
+        for (int w = 0; w < kThreads / 32; ++w) r += sh[w];
+    __syncthreads();
+    return r;  // valid in thread 0
+}
+// Max over non-negative fp64 values by their bit patterns: NaN (sign clear) orders above +Inf,
+// so a NaN anywhere wins.
+__device__ __forceinline__ uint64_t block_max_bits(uint64_t v, uint64_t* sh) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        const uint64_t t = __shfl_down_sync(0xFFFFFFFFu, v, o);
+        v = t > v ? t : v;
+    }
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    if (lane == 0) sh[warp] = v;
+    __syncthreads();
+    uint64_t r = 0;
+    if (threadIdx.x == 0)
+        for (int w = 0; w < kThreads / 32; ++w) r = sh[w] > r ? sh[w] : r;
+    __syncthreads();
+    return r;
+}
+
+// ------------------------------------------------------------------------------------------
+// Step 1: global norm ||x||_{q,p} (Global-QSGD, notation paragraph): the q-norm over the
+// workers of every coordinate, then the p-norm over the coordinates.  One pass over x; each
+// block writes one partial; the last block to finish (completion ticket, no waiting) combines
+// the partials in index order and writes the fp32 norm.
+// ------------------------------------------------------------------------------------------
+template <typename T, int MODE>
+__global__ void __launch_bounds__(kThreads)
+norm_kernel(const T* __restrict__ x, int64_t n, int64_t d, int64_t groups, bool vec_rows,
+            float* __restrict__ norm_user, unsigned char* __restrict__ ws) {
+    constexpr int C = Elem<T>::kCols;
+    WsHeader* hdr = reinterpret_cast<WsHeader*>(ws);
+    uint64_t* partials = reinterpret_cast<uint64_t*>(ws + kHeaderBytes);
+    __shared__ double sh_d[kThreads / 32];
+    __shared__ uint64_t sh_u[kThreads / 32];
+    __shared__ bool is_last;
+
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * kThreads;
+    uint32_t maxbits = 0;       // kMaxMax: max |x| bit pattern
+    ScaledSumSq ssq;            // kL2L2, kMaxL2
+    ssq.init();
+    int64_t best_key = INT64_MIN;  // kL2Max
+    uint32_t bad_col = 0;          // kL2Max: a non-finite column norm was seen
+
+    constexpr int U = (C == 4) ? 8 : 4;  // rows in flight per thread
+    for (int64_t g = static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x; g < groups;
+         g += stride) {
+        uint32_t colmax[C];   // kMaxL2
+        ScaledSumSq col[C];   // kL2Max
+#pragma unroll
+        for (int c = 0; c < C; ++c) { colmax[c] = 0; col[c].init(); }
+        for (int64_t i0 = 0; i0 < n; i0 += U) {
+            float v[U][C];
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                if (i0 + u < n) {
+                    load_group<T>(x, i0 + u, g, d, vec_rows, v[u]);
+                } else {
+#pragma unroll
+                    for (int c = 0; c < C; ++c) v[u][c] = 0.0f;  // zero rows add nothing
+                }
+            }
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                if (MODE == kMaxMax) {
+#pragma unroll
+                    for (int c = 0; c < C; ++c) {
+                        const uint32_t b = __float_as_uint(v[u][c]) & 0x7FFFFFFFu;
+                        maxbits = b > maxbits ? b : maxbits;
+                    }
+                } else if (MODE == kL2L2) {
+                    ssq.add<C>(v[u]);
+                } else if (MODE == kMaxL2) {
+#pragma unroll
+                    for (int c = 0; c < C; ++c) {
+                        const uint32_t b = __float_as_uint(v[u][c]) & 0x7FFFFFFFu;
+                        colmax[c] = b > colmax[c] ? b : colmax[c];
+                    }
+                } else {
+#pragma unroll
+                    for (int c = 0; c < C; ++c) {
+                        const float one[1] = {v[u][c]};
+                        col[c].add<1>(one);
+                    }
+                }
+            }
+        }
+        if (MODE == kMaxL2) {
+            float m[C];
+#pragma unroll
+            for (int c = 0; c < C; ++c) m[c] = __uint_as_float(colmax[c]);
+            ssq.add<C>(m);
+        } else if (MODE == kL2Max) {
+#pragma unroll
+            for (int c = 0; c < C; ++c) {
+                const float sum = col[c].sum();
+                if (!(sum < __uint_as_float(kInfBits))) {  // NaN or Inf column
+                    const uint32_t b = __float_as_uint(sum) & 0x7FFFFFFFu;
+                    bad_col = b > bad_col ? b : bad_col;
+                } else if (sum > 0.0f) {
+                    const int64_t key = scaled_key(sum, col[c].e);
+                    best_key = key > best_key ? key : best_key;
+                }
+            }
+        }
+    }
+
+    // Block partial: a non-negative fp64 value, stored by its bits.
+    uint64_t part_bits;
+    if (MODE == kMaxMax) {
+        const double m = static_cast<double>(__uint_as_float(maxbits));
+        part_bits = block_max_bits(static_cast<uint64_t>(__double_as_longlong(m)), sh_u);
+    } else if (MODE == kL2Max) {
+        double m = best_key == INT64_MIN ? 0.0 : key_value(best_key);
+        if (bad_col) m = static_cast<double>(__uint_as_float(bad_col));
+        part_bits = block_max_bits(static_cast<uint64_t>(__double_as_longlong(m)), sh_u);
+    } else {
+        const double s = block_sum(ssq.value(), sh_d);
+        part_bits = static_cast<uint64_t>(__double_as_longlong(s));
+    }
+
+    if (threadIdx.x == 0) {
+        partials[blockIdx.x] = part_bits;
+        __threadfence();
+        const unsigned int t = atomicAdd(&hdr->ticket, 1u);
+        is_last = (t == gridDim.x - 1);
+    }
+    __syncthreads();
+    if (!is_last) return;
+    __threadfence();
+
+    // Last block: combine the gridDim.x partials in a fixed order.
+    const int nb = gridDim.x;
+    double result;
+    if (MODE == kMaxMax || MODE == kL2Max) {
+        uint64_t m = 0;
+        for (int b = threadIdx.x; b < nb; b += kThreads) {
+            const uint64_t v = __ldcg(reinterpret_cast<const unsigned long long*>(partials + b));
+            m = v > m ? v : m;
+        }
+        m = block_max_bits(m, sh_u);
+        result = __longlong_as_double(static_cast<long long>(m));
+    } else {
+        double s = 0.0;
+        for (int b = threadIdx.x; b < nb; b += kThreads)
+            s += __longlong_as_double(
+                static_cast<long long>(__ldcg(reinterpret_cast<const unsigned long long*>(partials + b))));
+        result = block_sum(s, sh_d);
+    }
+    if (threadIdx.x == 0) {
+        double nrm = result;
+        if (MODE != kMaxMax) nrm = sqrt(result);  // (2,2), (inf,2): sqrt of a sum; (2,inf): of a max
+        const float n32 = static_cast<float>(nrm);
+        hdr->norm = n32;
+        if (norm_user) *norm_user = n32;
+        if (!(fabsf(n32) < __uint_as_float(kInfBits))) atomicCAS(&hdr->status, 0u, 4u);
+        hdr->ticket = 0;  // ready for the next call on this workspace
+        __threadfence();
+    }
+}
+
+// ------------------------------------------------------------------------------------------
+// Steps 2-4: stochastic rounding onto the level grid (Global-QSGD, Global-Q operator; grids of
+// Global-L_s and Global-E_s), the integer sum over the workers and the dequantisation.
+// ------------------------------------------------------------------------------------------
+
+// Level index of one element: v = fp32(|x| / N) clamped to [0, 1] (NaN -> 0); the lower level
+// and T = floor(P(up) * 2^32) are read exactly off the bits of v; round up iff r < T.
+template <int SCHEME>
+__device__ __forceinline__ uint32_t level_index(float xv, float nrm, uint32_t s, uint32_t r) {
+    float v = __fdiv_rn(fabsf(xv), nrm);
+    v = (v <= 1.0f) ? v : ((v > 1.0f) ? 1.0f : 0.0f);
+    const uint32_t vb = __float_as_uint(v);
+    const uint32_t eb = vb >> 23;  // biased exponent, 0..127
+    const uint32_t frac = vb & 0x7FFFFFu;
+    const uint32_t mant = frac | (eb ? 0x800000u : 0u);  // v = mant * 2^(max(eb,1) - 150)
+    const uint32_t ee = eb ? eb : 1u;
+    if (SCHEME == kLinear) {
+        // t = v * s = (mant * s) * 2^(ee - 150), exact in 31 bits; its integer part is the
+        // lower level m and its fraction times 2^32 is T: one 64-bit shift gives both.
+        const uint32_t prod = mant * s;
+        const uint32_t sh = min(150u - ee, 63u);
+        const uint64_t w = (static_cast<uint64_t>(prod) << 32) >> sh;
+        const uint32_t m = static_cast<uint32_t>(w >> 32);
+        const uint32_t T = static_cast<uint32_t>(w);
+        return m + (r < T ? 1u : 0u);
+    } else {
+        // v in [2^e, 2^(e+1)) with e >= -(s-1): lower level index s + e, P(up) = fraction of v.
+        // v < 2^-(s-1): between 0 and 2^-(s-1), P(up) = v * 2^(s-1).
+        if (eb + s >= 128u) {
+            const uint32_t lo = s + eb - 127u;
+            const uint32_t T = frac << 9;
+            return lo + (r < T ? 1u : 0u);
+        }
+        const uint32_t sh = min(151u - ee - s, 63u);
+        const uint32_t T = static_cast<uint32_t>((static_cast<uint64_t>(mant) << 32) >> sh);
+        return r < T ? 1u : 0u;
+    }
+}
+
+// Signed contribution of a code to the integer sum: L sums the level index; E sums
+// 2^(k-1) units of 2^-(s-1) for level index k >= 1.
+template <int SCHEME>
+__device__ __forceinline__ int32_t code_units(uint32_t k, bool neg) {
+    const int32_t u = (SCHEME == kLinear) ? static_cast<int32_t>(k)
+                                          : static_cast<int32_t>((1u << k) >> 1);
+    return neg ? -u : u;
+}
+
+struct QuantArgs {
+    const float* norm_ptr;   // fp32 norm in device memory
+    uint32_t s;
+    uint32_t key0, key1;     // Philox key = seed
+    uint32_t step_lo, step_hi;
+    int64_t n, d;
+    int64_t pitch;           // code row pitch in elements
+    bool vec_rows;
+};
+
+// Per-block fp32 dequantisation scale from the fp32 norm, computed in fp64 by one thread:
+// N / (n s) for Global-L_s, N 2^-(s-1) / n for Global-E_s.  0 when the norm is 0 or non-finite.
+template <int SCHEME>
+__device__ __forceinline__ float block_scale(float nrm, int64_t n, uint32_t s, float* sh) {
+    if (threadIdx.x == 0) {
+        float sc = 0.0f;
+        if (nrm > 0.0f && nrm < __uint_as_float(kInfBits)) {
+            const double num = static_cast<double>(nrm);
+            sc = (SCHEME == kLinear)
+                     ? static_cast<float>(num / (static_cast<double>(n) * static_cast<double>(s)))
+                     : static_cast<float>(ldexp(num, -static_cast<int>(s - 1)) / static_cast<double>(n));
+        }
+        *sh = sc;
+    }
+    __syncthreads();
+    return *sh;
+}
+
+// Store C codes of one row (int8 or int4 nibbles) for column group g.
+template <int C, int CODE_BITS>
+__device__ __forceinline__ void store_codes(unsigned char* __restrict__ codes, int64_t i,
+                                            int64_t g, int64_t pitch, const int32_t (&c)[C]) {
+    if (CODE_BITS == 8) {
+        unsigned char* p = codes + i * pitch + g * C;
+        if (C == 4) {
+            uint32_t w = 0;
+#pragma unroll
+            for (int k = 0; k < 4; ++k) w |= (static_cast<uint32_t>(c[k]) & 0xFFu) << (8 * k);
+            *reinterpret_cast<uint32_t*>(p) = w;
+        } else {
+            uint32_t w0 = 0, w1 = 0;
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                w0 |= (static_cast<uint32_t>(c[k]) & 0xFFu) << (8 * k);
+                w1 |= (static_cast<uint32_t>(c[k + 4]) & 0xFFu) << (8 * k);
+            }
+            *reinterpret_cast<uint2*>(p) = make_uint2(w0, w1);
+        }
+    } else {
+        unsigned char* p = codes + i * (pitch / 2) + g * (C / 2);
+        uint32_t w = 0;
+#pragma unroll
+        for (int k = 0; k < C; ++k) w |= (static_cast<uint32_t>(c[k]) & 0xFu) << (4 * k);
+        if (C == 4)
+            *reinterpret_cast<uint16_t*>(p) = static_cast<uint16_t>(w);
+        else
+            *reinterpret_cast<uint32_t*>(p) = w;
+    }
+}
+
+// Quantise column group g of all n rows; accumulate the integer sums; optionally store codes.
+// Returns the per-column sums in S.
+template <typename T, int SCHEME, int CODE_BITS>
+__device__ __forceinline__ void quantize_group(const T* __restrict__ x, const QuantArgs& a,
+                                               float nrm, int64_t g,
+                                               unsigned char* __restrict__ codes,
+                                               int32_t (&S)[Elem<T>::kCols]) {
+    constexpr int C = Elem<T>::kCols;
+    constexpr int U = (C == 4) ? 8 : 4;  // rows in flight per thread
+#pragma unroll
+    for (int c = 0; c < C; ++c) S[c] = 0;
+    for (int64_t i0 = 0; i0 < a.n; i0 += U) {
+        float v[U][C];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            if (i0 + u < a.n) load_group<T>(x, i0 + u, g, a.d, a.vec_rows, v[u]);
+        }
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            if (i0 + u >= a.n) break;
+            const uint32_t row = static_cast<uint32_t>(i0 + u);
+            int32_t code[C];
+#pragma unroll
+            for (int h = 0; h < C / 4; ++h) {
+                // columns g*C + 4h .. +3 share Philox counter ((g*C)/4 + h, row, step)
+                const uint32_t ctr0 = static_cast<uint32_t>((g * C) >> 2) + h;
+                const uint4 r = philox4x32_10(make_uint4(ctr0, row, a.step_lo, a.step_hi),
+                                              a.key0, a.key1);
+                const uint32_t rw[4] = {r.x, r.y, r.z, r.w};
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    const float xv = v[u][4 * h + k];
+                    const uint32_t lvl = level_index<SCHEME>(xv, nrm, a.s, rw[k]);
+                    const bool neg = xv < 0.0f;
+                    code[4 * h + k] = neg ? -static_cast<int32_t>(lvl) : static_cast<int32_t>(lvl);
+                    S[4 * h + k] += code_units<SCHEME>(lvl, neg);
+                }
+            }
+            if (CODE_BITS) store_codes<C, CODE_BITS>(codes, row, g, a.pitch, code);
+        }
+    }
+}
+
+// Quantise (+ sum + dequantise).  CODE_BITS: 0 (no codes), 4 or 8.  WRITE_OUT: dequantise the
+// sums into out.  Groups run over ceil(d/C) columns groups, or pitch/C when codes are written
+// (padding columns get zero codes).
+template <typename T, int SCHEME, int CODE_BITS, bool WRITE_OUT>
+__global__ void __launch_bounds__(kThreads)
+quantize_kernel(const T* __restrict__ x, QuantArgs a, int64_t groups,
+                unsigned char* __restrict__ codes, float* __restrict__ out) {
+    constexpr int C = Elem<T>::kCols;
+    __shared__ float sh_scale;
+    const float nrm = __ldg(a.norm_ptr);
+    const float scale = block_scale<SCHEME>(nrm, a.n, a.s, &sh_scale);
+    const bool live = nrm > 0.0f && nrm < __uint_as_float(kInfBits);
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * kThreads;
+    for (int64_t g = static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x; g < groups;
+         g += stride) {
+        int32_t S[C];
+        if (live) {
+            quantize_group<T, SCHEME, CODE_BITS>(x, a, nrm, g, codes, S);
+        } else {
+#pragma unroll
+            for (int c = 0; c < C; ++c) S[c] = 0;
+            if (CODE_BITS)
+                for (int64_t i = 0; i < a.n; ++i) store_codes<C, CODE_BITS>(codes, i, g, a.pitch, S);
+        }
+        if (WRITE_OUT) {
+            const int64_t j0 = g * C;
+            if (j0 + C <= a.d) {
+#pragma unroll
+                for (int h = 0; h < C / 4; ++h)
+                    reinterpret_cast<float4*>(out + j0)[h] =
+                        make_float4(scale * static_cast<float>(S[4 * h]),
+                                    scale * static_cast<float>(S[4 * h + 1]),
+                                    scale * static_cast<float>(S[4 * h + 2]),
+                                    scale * static_cast<float>(S[4 * h + 3]));
+            } else {
+#pragma unroll
+                for (int c = 0; c < C; ++c)
+                    if (j0 + c < a.d) out[j0 + c] = scale * static_cast<float>(S[c]);
+            }
+        }
+    }
+}
+
+// ------------------------------------------------------------------------------------------
+// Step 3 unfused: integer sum of the code matrix over the workers.  Each thread owns 16 bytes
+// of every code row (16 int8 or 32 int4 codes).
+// ------------------------------------------------------------------------------------------
+template <int CODE_BITS, int SCHEME>
+__global__ void __launch_bounds__(kThreads)
+reduce_codes_kernel(const unsigned char* __restrict__ codes, int64_t n, int64_t d,
+                    int64_t row_bytes, int64_t chunks, int32_t* __restrict__ sums) {
+    constexpr int K = (CODE_BITS == 8) ? 16 : 32;  // codes per 16-byte chunk
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * kThreads;
+    for (int64_t q = static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x; q < chunks;
+         q += stride) {
+        int32_t S[K];
+#pragma unroll
+        for (int k = 0; k < K; ++k) S[k] = 0;
+        const unsigned char* base = codes + q * 16;
+        int64_t i = 0;
+        for (; i < n; i += 4) {
+            uint4 w[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u)
+                if (i + u < n) w[u] = __ldg(reinterpret_cast<const uint4*>(base + (i + u) * row_bytes));
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                if (i + u >= n) break;
+                const uint32_t word[4] = {w[u].x, w[u].y, w[u].z, w[u].w};
+#pragma unroll
+                for (int k = 0; k < K; ++k) {
+                    int32_t c;
+                    if (CODE_BITS == 8)
+                        c = static_cast<int32_t>(word[k >> 2] << (24 - 8 * (k & 3))) >> 24;
+                    else
+                        c = static_cast<int32_t>(word[k >> 3] << (28 - 4 * (k & 7))) >> 28;
+                    const bool neg = c < 0;
+                    const uint32_t lvl = static_cast<uint32_t>(neg ? -c : c);
+                    S[k] += code_units<SCHEME>(lvl, neg);
+                }
+            }
+        }
+        const int64_t j0 = q * K;
+        if (j0 + K <= d) {
+#pragma unroll
+            for (int h = 0; h < K / 4; ++h)
+                reinterpret_cast<int4*>(sums + j0)[h] = make_int4(S[4 * h], S[4 * h + 1], S[4 * h + 2], S[4 * h + 3]);
+        } else {
+#pragma unroll
+            for (int k = 0; k < K; ++k)
+                if (j0 + k < d) sums[j0 + k] = S[k];
+        }
+    }
+}
+
+// Step 4 unfused: out_j = scale * S_j.
+template <int SCHEME>
+__global__ void __launch_bounds__(kThreads)
+dequantize_kernel(const int32_t* __restrict__ sums, const float* __restrict__ norm_ptr,
+                  int64_t n, uint32_t s, int64_t d, float* __restrict__ out) {
+    __shared__ float sh_scale;
+    const float scale = block_scale<SCHEME>(__ldg(norm_ptr), n, s, &sh_scale);
+    const int64_t quads = (d + 3) / 4;
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * kThreads;
+    for (int64_t q = static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x; q < quads;
+         q += stride) {
+        const int64_t j0 = q * 4;
+        if (j0 + 4 <= d) {
+            const int4 t = __ldg(reinterpret_cast<const int4*>(sums + j0));
+            reinterpret_cast<float4*>(out + j0)[0] =
+                make_float4(scale * static_cast<float>(t.x), scale * static_cast<float>(t.y),
+                            scale * static_cast<float>(t.z), scale * static_cast<float>(t.w));
+        } else {
+            for (int64_t j = j0; j < d; ++j) out[j] = scale * static_cast<float>(__ldg(sums + j));
+        }
+    }
+}
+
+// Philox check kernel: one call per thread.
+__global__ void philox_kernel(const uint32_t* __restrict__ ck, uint32_t* __restrict__ out,
+                              int64_t count) {
+    const int64_t t = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+    if (t >= count) return;
+    const uint32_t* p = ck + 6 * t;
+    const uint4 r = philox4x32_10(make_uint4(p[0], p[1], p[2], p[3]), p[4], p[5]);
+    out[4 * t] = r.x; out[4 * t + 1] = r.y; out[4 * t + 2] = r.z; out[4 * t + 3] = r.w;
+}
+
+}  // namespace gq

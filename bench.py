@@ -1,0 +1,375 @@
+"""Benchmark of the fused Global-QSGD allreduce-mean (gq_allreduce_mean) on GB300.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--config NAME] [--impl ours|reference]
+
+One step = one call of the whole hot path (global norm -> stochastic quantisation -> integer sum
+over the n workers -> dequantisation) over one n x d gradient matrix resident in HBM.  The
+metric is GB/s of gradient consumed (n * d * element bytes per step / step time).  Inputs are
+synthetic and seeded (allreduce_compatible_gradient_gb300.workloads); the default workload is
+ResNet-50-sized (n = 8 workers, d = 25,557,032 fp32, Global-L_127, max norm).
+
+Timing: W warm-up steps, then K steps timed one by one with CUDA events on the launching stream;
+L2 is flushed (a 512 MiB write) between timed steps, outside the timed region.  Under torchrun
+every rank runs an independent replica on its own GPU (the path needs no data exchange on one
+GPU per problem); elapsed time is the max over ranks.
+
+--impl reference times the CPU oracle (test infrastructure, as it stands) on a bounded column
+window of the same workload on the host cores, rank 0 only.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "fused Global-QSGD GB/s of fp32 grads (n×d) and % of GB300 HBM roofline"
+UNIT = "GB/s"
+FALLBACK_HBM_GBS = 6800.0
+
+
+def _args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--config", default="resnet50_n8")
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    return ap.parse_args()
+
+
+def _peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            pk = json.load(f)
+        return float(pk["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def _kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for rel in ("allreduce_compatible_gradient_gb300/csrc/gq.cu",
+                "allreduce_compatible_gradient_gb300/csrc/gq_kernels.cuh"):
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def _ncu_traffic(key: str):
+    """DRAM bytes per launch from the committed ncu summary, if taken on this kernel source."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            t = json.load(f)
+    except (OSError, ValueError):
+        return None
+    if t.get("kernel_source_hash") != _kernel_source_hash():
+        return None
+    v = t.get("per_launch_dram_bytes", {}).get(key)
+    return None if v is None else float(v)
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 200 ms during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), "--query-gpu=" + self.FIELDS,
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        if self.thread:
+            self.thread.join(timeout=2)
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[5:9]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def _dist_init(nranks):
+    import torch
+    import torch.distributed as dist
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    if world > 1:
+        local = int(os.environ.get("LOCAL_RANK", "0"))
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+        return dist.get_rank(), world, local
+    return 0, 1, 0
+
+
+def _max_over_ranks(value: float, world: int) -> float:
+    if world == 1:
+        return value
+    import torch
+    import torch.distributed as dist
+
+    t = torch.tensor([value], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def _barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.barrier()
+
+
+def cpu_baseline(cfg: dict, seconds: float, host_x=None) -> dict:
+    """Time the CPU oracle (as it stands, single-threaded) on a column window of the workload."""
+    import numpy as np
+
+    from allreduce_compatible_gradient_gb300 import workloads
+    from oracle import gq_oracle
+
+    n, d = cfg["n"], cfg["d"]
+    elt = 2 if cfg["dtype"] == "bf16" else 4
+    w = min(d, 1 << 14)
+    x = workloads.host_inputs(cfg["dist"], n, w, seed=cfg["input_seed"], dtype=cfg["dtype"])
+    t0 = time.perf_counter()
+    gq_oracle.allreduce_mean(x, cfg["q"], cfg["p"], cfg["scheme"], cfg["s"], cfg["seed"],
+                             cfg["step"])
+    dt = time.perf_counter() - t0
+    # grow the window to fill about `seconds` of CPU work
+    w = int(min(d, max(w, w * seconds / max(dt, 1e-6))))
+    w = max(32, w // 32 * 32) if w < d else d
+    x = workloads.host_inputs(cfg["dist"], n, w, seed=cfg["input_seed"], dtype=cfg["dtype"])
+    t0 = time.perf_counter()
+    gq_oracle.allreduce_mean(x, cfg["q"], cfg["p"], cfg["scheme"], cfg["s"], cfg["seed"],
+                             cfg["step"])
+    dt = time.perf_counter() - t0
+    return {"value": round(n * w * elt / dt / 1e9, 6), "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": "%d x %d columns of %s (same distribution; whole pipeline: norm of the "
+                      "window, quantise, sum, dequantise), %.1f s" % (n, w, cfg["name"], dt),
+            "seconds": round(dt, 3), "window_columns": w}
+
+
+def run_reference(a, cfg):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return 0
+    steps = []
+    for i in range(a.warmup + a.steps):
+        r = cpu_baseline(cfg, seconds=max(1.0, min(a.cpu_seconds, 120.0 / (a.steps + a.warmup))))
+        if i >= a.warmup:
+            steps.append(r)
+    val = statistics.median(r["value"] for r in steps)
+    elt = 2 if cfg["dtype"] == "bf16" else 4
+    ms = 1e3 * cfg["n"] * cfg["d"] * elt / (val * 1e9)
+    line = {"impl": "reference", "metric": METRIC, "value": val, "unit": UNIT,
+            "n_gpus": a.gpus, "steps": a.steps, "warmup": a.warmup, "ms_per_step": round(ms, 4),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+            "data": "synthetic",
+            "config": _config_block(cfg, a.gpus),
+            "cpu_baseline": {"value": val, "unit": UNIT, "cores": 1, "kind": "oracle",
+                             "sample": steps[0]["sample"]},
+            "e2e": {"value": val, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def _config_block(cfg, ngpus):
+    return {"workload": cfg["name"], "n": cfg["n"], "d": cfg["d"], "input_dtype": cfg["dtype"],
+            "distribution": cfg["dist"], "scheme": "Global-L" if cfg["scheme"] == 0 else "Global-E",
+            "s": cfg["s"], "q": "inf" if cfg["q"] == 0 else 2, "p": "inf" if cfg["p"] == 0 else 2,
+            "philox_seed": cfg["seed"], "parallelism": "replica x%d" % ngpus,
+            "l2": "flushed between timed steps (512 MiB write); input %.1f MB > 129 MB L2"
+                  % (cfg["n"] * cfg["d"] * (2 if cfg["dtype"] == "bf16" else 4) / 1e6)}
+
+
+def main():
+    a = _args()
+    from allreduce_compatible_gradient_gb300 import workloads
+
+    cfg = dict(workloads.CONFIGS[a.config], name=a.config)
+    if a.impl == "reference":
+        return run_reference(a, cfg)
+
+    import torch
+
+    import allreduce_compatible_gradient_gb300 as gq
+
+    rank, world, local = _dist_init(a.gpus)
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    n, d = cfg["n"], cfg["d"]
+    elt = 2 if cfg["dtype"] == "bf16" else 4
+    in_bytes = n * d * elt
+    x = workloads.device_inputs(cfg["dist"], n, d, seed=cfg["input_seed"] + rank,
+                                dtype=cfg["dtype"], device=dev)
+    out = torch.empty(d, dtype=torch.float32, device=dev)
+    norm = torch.empty(1, dtype=torch.float32, device=dev)
+    ws = gq.gq_workspace(dev)
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    sc, s, q, p, seed = cfg["scheme"], cfg["s"], cfg["q"], cfg["p"], cfg["seed"]
+
+    def step(k):
+        gq.gq_allreduce_mean(x, q, p, sc, s, seed, k, out=out, norm=norm, ws=ws, stream=stream)
+
+    for k in range(a.warmup):
+        step(k)
+    torch.cuda.synchronize()
+    if gq.gq_get_status(ws) != 0:
+        raise RuntimeError("device status not ok after warm-up")
+
+    # --- timed: the public fused call ---------------------------------------------------------
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(a.steps)]
+    clocks = ClockSampler(local)
+    clocks.start()
+    _barrier(world)
+    torch.cuda.synchronize()
+    for k in range(a.steps):
+        flush.zero_()
+        ev[k][0].record(stream)
+        step(a.warmup + k)
+        ev[k][1].record(stream)
+    torch.cuda.synchronize()
+    _barrier(world)
+    clk = clocks.stop()
+    times = [e0.elapsed_time(e1) for e0, e1 in ev]
+    total_ms = _max_over_ranks(sum(times), world)
+    ms_per_step = total_ms / a.steps
+    value = world * in_bytes / (ms_per_step * 1e-3) / 1e9
+
+    # --- per-kernel durations (same two kernels, launched through the split entry points) -----
+    ev_k = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(a.steps)]
+    for k in range(a.steps):
+        flush.zero_()
+        ev_k[k][0].record(stream)
+        gq.gq_global_norm(x, q, p, norm=norm, ws=ws, stream=stream)
+        ev_k[k][1].record(stream)
+        gq.gq_allreduce_mean_with_norm(x, norm, sc, s, seed, a.warmup + k, out=out, stream=stream)
+        ev_k[k][2].record(stream)
+    torch.cuda.synchronize()
+    t_norm = statistics.mean(e[0].elapsed_time(e[1]) for e in ev_k)
+    t_quant = statistics.mean(e[1].elapsed_time(e[2]) for e in ev_k)
+    peak, peak_kind = _peaks()
+    kernels = {
+        "norm": {"ms": t_norm, "bytes": in_bytes},
+        "quantize_sum_dequantize": {"ms": t_quant, "bytes": in_bytes + 4 * d},
+    }
+    dom_name = max(kernels, key=lambda k: kernels[k]["ms"])
+    dom = kernels[dom_name]
+    achieved = dom["bytes"] / (dom["ms"] * 1e-3) / 1e9
+    traffic = _ncu_traffic("%s@%s" % (dom_name, cfg["name"]))
+    roofline = {"bound": "hbm", "kernel": dom_name, "achieved": round(achieved, 1),
+                "peak": peak, "unit": "GB/s", "frac": round(achieved / peak, 4),
+                "peak_kind": peak_kind, "traffic": traffic,
+                "algorithmic_bytes_per_launch": dom["bytes"],
+                "kernels_ms": {k: round(v["ms"], 4) for k, v in kernels.items()},
+                "whole_step_frac": round(2 * in_bytes / (ms_per_step * 1e-3) / 1e9 / peak, 4),
+                "whole_step_frac_of_8tbs": round(
+                    (2 * in_bytes + 4 * d) / (ms_per_step * 1e-3) / 1e12 / 8.0, 4)}
+
+    # --- end to end through the public API with host buffers ---------------------------------
+    e2e = None
+    if not a.no_e2e:
+        xh = torch.empty((n, d), dtype=x.dtype, pin_memory=True)
+        xh.copy_(x)
+        oh = torch.empty(d, dtype=torch.float32, pin_memory=True)
+        xd = torch.empty_like(x)
+        for k in range(2):
+            xd.copy_(xh, non_blocking=True)
+            gq.gq_allreduce_mean(xd, q, p, sc, s, seed, k, out=out, norm=norm, ws=ws, stream=stream)
+            oh.copy_(out, non_blocking=True)
+        torch.cuda.synchronize()
+        ke = max(3, min(a.steps, 10))
+        _barrier(world)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for k in range(ke):
+            xd.copy_(xh, non_blocking=True)
+            gq.gq_allreduce_mean(xd, q, p, sc, s, seed, k, out=out, norm=norm, ws=ws, stream=stream)
+            oh.copy_(out, non_blocking=True)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        e_ms = _max_over_ranks(e0.elapsed_time(e1) / ke, world)
+        e2e = {"value": round(world * in_bytes / (e_ms * 1e-3) / 1e9, 3), "unit": UNIT,
+               "ms_per_step": round(e_ms, 4), "h2d_bytes_per_step": in_bytes,
+               "d2h_bytes_per_step": 4 * d}
+        del xh, oh, xd
+
+    if gq.gq_get_status(ws) != 0:
+        raise RuntimeError("device status not ok after the timed steps")
+
+    cpu = None
+    if rank == 0 and not a.no_cpu_baseline:
+        cpu = cpu_baseline(cfg, a.cpu_seconds)
+
+    if rank == 0:
+        line = {"metric": METRIC, "value": round(value, 3), "unit": UNIT, "n_gpus": world,
+                "steps": a.steps, "warmup": a.warmup, "ms_per_step": round(ms_per_step, 5),
+                "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+                "dtype": "f32", "data": "synthetic",
+                "config": _config_block(cfg, world), "roofline": roofline,
+                "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": 2 * a.steps,
+                "clocks": clk, "impl": "ours"}
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,176 @@
+/*
+ * gq.h -- C ABI of the GB300 (sm_103a) Global-QSGD compress / aggregate / decompress library.
+ *
+ * The method: "Global-QSGD: Practical Floatless Quantization for Distributed Learning with
+ * Theoretical Guarantees" (Xin, Canini, Richtarik, Horvath; arXiv 2305.18627), cited below as
+ * "Global-QSGD".  n workers' gradients x_1..x_n in R^d are held as one n x d matrix X on one GPU
+ * (row i = worker i, element (i, j) at i*d + j: the concatenated vector x = [x_1, ..., x_n] of
+ * the notation paragraph).  The pipeline:
+ *   1. N = ||x||_{q,p}: the q-norm over the workers of every coordinate, then the p-norm of those
+ *      d values (notation paragraph); q, p in {2, inf}.
+ *   2. every element is normalised, v = |x_ij| / N in fp32, and rounded at random, without bias,
+ *      to one of the two adjacent levels of the grid (Global-Q operator):
+ *        GQ_LINEAR  Global-L_s, standard dithering, levels m/s, m = 0..s;
+ *        GQ_EXP     Global-E_s, exponential dithering, levels 0 and 2^-(s-k), k = 1..s
+ *      (the paragraph introducing the two forms of the operator, with its footnote on base 2).
+ *      The code is the signed level index c = sign(x) * k.
+ *   3. the codes are summed over the workers in integer arithmetic: the allreduce of the
+ *      communication hook, on one GPU.  Global-E codes are summed as fixed-point values:
+ *      level k counts 2^(k-1) units of 2^-(s-1), so the sum stays exact.
+ *   4. the sum is dequantised to the estimate of the mean gradient:
+ *        out_j = N * S_j / (n * s)            (Global-L_s)
+ *        out_j = N * S_j * 2^-(s-1) / n       (Global-E_s)
+ *      (implementation paragraph: quantisation, allreduce, dequantisation).
+ * Round up iff r < T, where r is word (j mod 4) of Philox4x32-10 (Salmon et al., SC'11) at
+ * counter (j / 4, i, low 32 bits of step, high 32 bits of step) and key (low, high 32 bits of
+ * seed), and T = floor(P(up) * 2^32) is computed exactly from v.
+ *
+ * Conventions for every call:
+ *   - All buffers are caller-owned device memory (grads, codes, sums, out, norm, ws), 16-byte
+ *     aligned (cudaMalloc and PyTorch give 256 bytes).  The library allocates no memory.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = the legacy default stream).  Every call
+ *     is asynchronous on that stream; argument errors are returned synchronously before anything
+ *     is enqueued.  Calls on different streams may run concurrently if they use different
+ *     workspaces.
+ *   - Device-detected conditions (a non-finite norm) are recorded in the workspace status word
+ *     and read with gq_get_status.  On a non-finite norm every output is written as zeros.
+ *   - Sizes: n >= 1, 1 <= d < 2^34 (the Philox counter holds j / 4 in 32 bits), n < 2^31.
+ *   - Codes: int8 when the code needs more than 4 bits (s > 7), else int4 (two's-complement
+ *     nibbles, element 2m in the low nibble of byte m).  Code rows have a pitch of
+ *     gq_code_pitch(d) = round_up(d, 32) elements; padding codes are written as 0.
+ */
+#ifndef GQ_H
+#define GQ_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    GQ_OK = 0,
+    GQ_ERR_INVALID = 1,     /* null pointer, bad size, bad enum, misaligned buffer */
+    GQ_ERR_UNSUPPORTED = 2, /* s outside [1, 127] (Global-L) or [1, 24] (Global-E) */
+    GQ_ERR_OVERFLOW = 3,    /* n * s >= 2^24 (L) or n * 2^(s-1) >= 2^24 (E): the code sum
+                               would not convert to fp32 exactly */
+    GQ_ERR_NONFINITE = 4,   /* device: the norm is NaN or infinite */
+    GQ_ERR_TIMEOUT = 5,     /* device: a bounded wait gave up (no kernel waits today) */
+    GQ_ERR_CUDA = 6,        /* a CUDA runtime call or kernel launch failed */
+    GQ_ERR_WORKSPACE = 7    /* workspace null, too small or misaligned */
+} gq_status;
+
+typedef enum { GQ_F32 = 0, GQ_BF16 = 1 } gq_dtype;
+
+typedef enum {
+    GQ_LINEAR = 0, /* Global-L_s, standard dithering */
+    GQ_EXP = 1     /* Global-E_s, exponential dithering */
+} gq_scheme;
+
+/* Norm orders for q and p. */
+#define GQ_NORM_INF 0
+#define GQ_NORM_L2 2
+
+/* Version of this ABI (incremented on incompatible change). */
+int gq_abi_version(void);
+
+/* Bytes of workspace the norm step needs for an n x d problem (a small constant today,
+ * 33,024 bytes).  The workspace holds the device status word, the block partials of the norm,
+ * a completion ticket and the last norm. */
+size_t gq_workspace_bytes(int64_t n, int64_t d);
+
+/* Zero a freshly allocated workspace (enqueued on `stream`).  Required once before its first
+ * use; every later call leaves the ticket at zero and the status word sticky. */
+gq_status gq_workspace_init(void *ws, size_t ws_bytes, void *stream);
+
+/* 4 or 8: bits per stored code for this scheme and s; 0 if s is unsupported. */
+int gq_code_bits(int scheme, int s);
+
+/* Row pitch of the code matrix in elements: round_up(d, 32); 0 if d < 1. */
+int64_t gq_code_pitch(int64_t d);
+
+/* Bytes of the n x pitch code matrix: n * gq_code_pitch(d) * gq_code_bits / 8; 0 if invalid. */
+size_t gq_code_bytes(int scheme, int s, int64_t n, int64_t d);
+
+/*
+ * Step 1: the global norm N = ||x||_{q,p} (Global-QSGD, notation paragraph) of the n x d
+ * gradient matrix `grads` (dtype GQ_F32 or GQ_BF16), written as fp32 to *norm_dev.
+ * q, p: GQ_NORM_L2 or GQ_NORM_INF.  One kernel: a grid-wide pass with a fixed-order block
+ * combine (deterministic on a given GPU).  The l2 forms are accurate to ~1e-7 relative over the
+ * whole fp32 range (sums of squares are carried in fp32 with a per-thread power-of-two scale and
+ * compensation, combined in fp64).  A NaN or infinite element makes the norm non-finite and
+ * sets GQ_ERR_NONFINITE in the workspace status.
+ */
+gq_status gq_global_norm(const void *grads, int dtype, int64_t n, int64_t d, int q, int p,
+                         float *norm_dev, void *ws, size_t ws_bytes, void *stream);
+
+/*
+ * Step 2: quantise every element to its signed level-index code (Global-QSGD, Global-Q
+ * operator and the two level grids), using the fp32 norm at *norm_dev (device memory; a norm
+ * below some |x_ij| saturates that element at level s).  `codes` receives the n x pitch code
+ * matrix (gq_code_bytes bytes).  NaN elements get code 0.  A norm of 0 gives all-zero codes; a
+ * non-finite norm gives all-zero codes (and no status: this call has no workspace).
+ * seed and step key the Philox stream (see the file comment).
+ */
+gq_status gq_quantize(const void *grads, int dtype, int64_t n, int64_t d, const float *norm_dev,
+                      int scheme, int s, uint64_t seed, uint64_t step, void *codes,
+                      void *stream);
+
+/*
+ * Step 3: sum the code matrix over the n workers into int32 sums[d] (the allreduce reduction
+ * of the communication hook: the native integer sum for Global-L; for Global-E each level index
+ * k is summed as 2^(k-1) units of 2^-(s-1)).  Exact.
+ */
+gq_status gq_reduce_codes(const void *codes, int scheme, int s, int64_t n, int64_t d,
+                          int32_t *sum_dev, void *stream);
+
+/*
+ * Step 4: dequantise the sums to the mean-gradient estimate out[d] (fp32):
+ * out_j = fp32(scale * S_j) with scale = fp32(N / (n s)) (L) or fp32(N 2^-(s-1) / n) (E), the
+ * scale computed in fp64 from the fp32 norm at *norm_dev.  |out_j - exact| <= 2^-23 |out_j|.
+ * A non-finite norm gives all zeros.
+ */
+gq_status gq_dequantize(const int32_t *sum_dev, const float *norm_dev, int scheme, int s,
+                        int64_t n, int64_t d, float *out_dev, void *stream);
+
+/*
+ * Steps 1-4 fused: the norm pass, then one pass that quantises, sums over the workers in
+ * registers and dequantises, so codes and sums never touch memory.  Traffic: X is read twice,
+ * out written once.  norm_dev (nullable) receives the fp32 norm; codes (nullable) receives the
+ * code matrix as gq_quantize would write it.  Bit-identical to gq_global_norm + gq_quantize +
+ * gq_reduce_codes + gq_dequantize on the same stream.
+ */
+gq_status gq_allreduce_mean(const void *grads, int dtype, int64_t n, int64_t d, int q, int p,
+                            int scheme, int s, uint64_t seed, uint64_t step, float *out_dev,
+                            float *norm_dev, void *codes, void *ws, size_t ws_bytes,
+                            void *stream);
+
+/*
+ * Steps 2-4 fused with a norm supplied in device memory (*norm_dev), e.g. one agreed on by a
+ * separate scalar collective.  Same outputs as gq_quantize + gq_reduce_codes + gq_dequantize.
+ * codes is nullable.
+ */
+gq_status gq_allreduce_mean_with_norm(const void *grads, int dtype, int64_t n, int64_t d,
+                                      const float *norm_dev, int scheme, int s, uint64_t seed,
+                                      uint64_t step, float *out_dev, void *codes, void *stream);
+
+/*
+ * Philox4x32-10 on the device, for checking the random stream: `count` calls, input
+ * ctr_key[6*c .. 6*c+5] = counter words 0..3 then key words 0..1, output out[4*c .. 4*c+3].
+ */
+gq_status gq_philox4x32_10(const uint32_t *ctr_key_dev, uint32_t *out_dev, int64_t count,
+                           void *stream);
+
+/* Synchronise `stream`, read the workspace status word, clear it, and return it (GQ_OK if no
+ * device-detected condition occurred since the last read). */
+gq_status gq_get_status(void *ws, void *stream);
+
+/* Static string naming a status value. */
+const char *gq_status_string(int status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GQ_H */

@@ -218,7 +218,8 @@ double gqo_global_norm(const void *x, int dtype, int64_t n, int64_t d, int q, in
  * step below is exact in fp64), so T is floor(P(up) * 2^32) exactly.
  *
  * v = fp32(|x| / N), clamped to 1: a norm handed in from outside that is smaller than |x|
- * saturates the element at the top level.  norm must be finite and > 0.
+ * saturates the element at the top level; a NaN element gets v = 0.  norm must be finite and
+ * > 0.
  */
 int gqo_level_split(float absx, float norm, int scheme, int s, int32_t *lo, uint32_t *T)
 {
@@ -238,6 +239,8 @@ int gqo_level_split(float absx, float norm, int scheme, int s, int32_t *lo, uint
     v = fabsf(absx) / norm; /* the one fp32 rounding */
     if (v > 1.0f)
         v = 1.0f;
+    if (isnan(v))
+        v = 0.0f; /* a NaN element under a finite norm contributes nothing */
     if (scheme == GQO_LINEAR) {
         double t = (double)v * (double)s; /* exact: 24-bit significand times a 7-bit integer */
         double m = floor(t);

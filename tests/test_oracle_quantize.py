@@ -377,3 +377,10 @@ def test_tie_does_not_round_up(oracle):
         assert oracle.level_split(v, 1.0, EXP, 8) == (6, frac << 9)
         codes, rc = oracle.quantize(x, np.float32(1.0), EXP, 8, seed, step)
         assert codes[0, j] == want
+
+
+def test_nan_element_under_supplied_norm(oracle):
+    x = np.array([[np.nan, 1.0, np.inf, -2.0]], dtype=np.float32)
+    codes, rc = oracle.quantize(x, np.float32(2.0), LINEAR, 5, 1, 1)
+    assert rc == 0
+    assert codes[0, 0] == 0 and codes[0, 2] == 5 and codes[0, 3] == -5
