@@ -104,24 +104,40 @@ void gqo_philox4x32_10(const uint32_t ctr_in[4], const uint32_t key_in[2], uint3
     out[3] = c3;
 }
 
+/* 16-bit half h (0..7) of a Philox output: the low half of word h/2 for even h, the high half
+ * for odd h. */
+static uint32_t half16(const uint32_t w[4], int h)
+{
+    uint32_t word = w[h >> 1];
+    return (h & 1) ? (word >> 16) : (word & 0xFFFFu);
+}
+
 /*
- * The uniform 32-bit word that decides the rounding of element (worker i, coordinate j) at
+ * The uniform 32-bit word r that decides the rounding of element (worker i, coordinate j) at
  * training step `step` under seed `seed`.  Global-QSGD leaves the source of randomness open; this
- * project fixes it as: key = (low 32 bits of seed, high 32 bits of seed), counter =
- * (j / 4, i, low 32 bits of step, high 32 bits of step), and the word used is word (j mod 4) of
- * the call's output.  So the four coordinates 4t..4t+3 of one worker share one Philox call.
+ * project fixes it as follows.  Key = (low 32 bits of seed, high 32 bits of seed).  The group of
+ * eight coordinates j = 8t..8t+7 of worker i owns two counters,
+ *     A = (t,         i, low 32 bits of step, high 32 bits of step)
+ *     B = (2^31 + t,  i, low 32 bits of step, high 32 bits of step)
+ * (t < 2^31 since d < 2^34).  The high 16 bits of r are half (j mod 8) of Philox(A) and the low
+ * 16 bits are half (j mod 8) of Philox(B).  r is uniform on [0, 2^32) and independent across
+ * elements.  (The split lets a caller decide "r < T" from the high half alone unless it equals
+ * the high half of T, which happens with probability 2^-16.)
  */
 uint32_t gqo_philox_word(uint64_t seed, uint64_t step, int64_t i, int64_t j)
 {
-    uint32_t ctr[4], key[2], out[4];
-    ctr[0] = (uint32_t)((uint64_t)j >> 2);
+    uint32_t ctr[4], key[2], a[4], b[4];
+    int h = (int)(j & 7);
+    ctr[0] = (uint32_t)((uint64_t)j >> 3);
     ctr[1] = (uint32_t)i;
     ctr[2] = (uint32_t)step;
     ctr[3] = (uint32_t)(step >> 32);
     key[0] = (uint32_t)seed;
     key[1] = (uint32_t)(seed >> 32);
-    gqo_philox4x32_10(ctr, key, out);
-    return out[j & 3];
+    gqo_philox4x32_10(ctr, key, a);
+    ctr[0] |= 0x80000000u;
+    gqo_philox4x32_10(ctr, key, b);
+    return (half16(a, h) << 16) | half16(b, h);
 }
 
 /* ------------------------------------------------------------------------------------------ */

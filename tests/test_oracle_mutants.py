@@ -20,7 +20,10 @@ MUTANTS = [
     ("round-up compare inverted", "k = lo + (r < T ? 1 : 0);", "k = lo + (r >= T ? 1 : 0);"),
     ("worker dropped from counter", "ctr[1] = (uint32_t)i;", "ctr[1] = 0u;"),
     ("step dropped from counter", "ctr[2] = (uint32_t)step;", "ctr[2] = 0u;"),
-    ("wrong word of the call", "return out[j & 3];", "return out[(j + 1) & 3];"),
+    ("wrong half of the call", "int h = (int)(j & 7);", "int h = (int)((j + 1) & 7);"),
+    ("halves of r swapped", "return (half16(a, h) << 16) | half16(b, h);",
+     "return (half16(b, h) << 16) | half16(a, h);"),
+    ("second counter space dropped", "ctr[0] |= 0x80000000u;", "ctr[0] |= 0u;"),
     ("philox key bump dropped", "k1 += weyl1;", "k1 += 0u;"),
     ("philox halves swapped", "uint32_t n1 = lo1;", "uint32_t n1 = hi1;"),
     ("E level off by one", "*lo = s + e; /* 2^e = 2^-(s - lo) */", "*lo = s + e + 1;"),
