@@ -131,34 +131,37 @@ gq_status norm_any(const void* grads, int dtype, int mode, int64_t n, int64_t d,
 }
 
 // ---- quantize (+ sum + dequantize) ----------------------------------------------------------
-template <typename T, int SCHEME, int BITS, bool OUT>
+// TRUSTED: the norm comes from norm_kernel on the same gradients (fused path), so a finite norm
+// rules out NaN and infinite elements.
+template <typename T, int SCHEME, int BITS, bool OUT, bool TRUSTED>
 gq_status run_quant(const void* grads, const gq::QuantArgs& a, void* codes, float* out,
                     cudaStream_t st) {
-    constexpr int C = gq::Elem<T>::kCols;
-    const int64_t groups = BITS ? a.pitch / C : (a.d + C - 1) / C;
-    auto k = gq::quantize_kernel<T, SCHEME, BITS, OUT>;
+    const int64_t groups = BITS ? a.pitch / gq::kQCols : (a.d + gq::kQCols - 1) / gq::kQCols;
+    auto k = gq::quantize_kernel<T, SCHEME, BITS, OUT, TRUSTED>;
     const unsigned grid = grid_for(k, groups);
     k<<<grid, kThreads, 0, st>>>(static_cast<const T*>(grads), a, groups,
                                  static_cast<unsigned char*>(codes), out);
     return launch_status();
 }
 
-template <typename T, int SCHEME, bool OUT>
+template <typename T, int SCHEME, bool OUT, bool TRUSTED>
 gq_status quant_bits(const void* grads, const gq::QuantArgs& a, int bits, void* codes, float* out,
                      cudaStream_t st) {
-    if (!codes) return run_quant<T, SCHEME, 0, OUT>(grads, a, nullptr, out, st);
-    if (bits == 4) return run_quant<T, SCHEME, 4, OUT>(grads, a, codes, out, st);
-    return run_quant<T, SCHEME, 8, OUT>(grads, a, codes, out, st);
+    if (!codes) return run_quant<T, SCHEME, 0, OUT, TRUSTED>(grads, a, nullptr, out, st);
+    if (bits == 4) return run_quant<T, SCHEME, 4, OUT, TRUSTED>(grads, a, codes, out, st);
+    return run_quant<T, SCHEME, 8, OUT, TRUSTED>(grads, a, codes, out, st);
 }
 
-template <bool OUT>
+template <bool OUT, bool TRUSTED>
 gq_status quant_any(const void* grads, int dtype, const gq::QuantArgs& a, int scheme, int bits,
                     void* codes, float* out, cudaStream_t st) {
     if (dtype == GQ_F32)
-        return scheme == GQ_LINEAR ? quant_bits<float, gq::kLinear, OUT>(grads, a, bits, codes, out, st)
-                                   : quant_bits<float, gq::kExp, OUT>(grads, a, bits, codes, out, st);
-    return scheme == GQ_LINEAR ? quant_bits<uint16_t, gq::kLinear, OUT>(grads, a, bits, codes, out, st)
-                               : quant_bits<uint16_t, gq::kExp, OUT>(grads, a, bits, codes, out, st);
+        return scheme == GQ_LINEAR
+                   ? quant_bits<float, gq::kLinear, OUT, TRUSTED>(grads, a, bits, codes, out, st)
+                   : quant_bits<float, gq::kExp, OUT, TRUSTED>(grads, a, bits, codes, out, st);
+    return scheme == GQ_LINEAR
+               ? quant_bits<uint16_t, gq::kLinear, OUT, TRUSTED>(grads, a, bits, codes, out, st)
+               : quant_bits<uint16_t, gq::kExp, OUT, TRUSTED>(grads, a, bits, codes, out, st);
 }
 
 gq::QuantArgs make_args(const float* norm_ptr, int dtype, int64_t n, int64_t d, int s,
@@ -229,8 +232,8 @@ gq_status gq_quantize(const void* grads, int dtype, int64_t n, int64_t d, const 
     if ((st = check_scheme(scheme, s, n)) != GQ_OK) return st;
     if (!norm_dev || !codes || !aligned16(codes)) return GQ_ERR_INVALID;
     const gq::QuantArgs a = make_args(norm_dev, dtype, n, d, s, seed, step);
-    return quant_any<false>(grads, dtype, a, scheme, gq_code_bits(scheme, s), codes, nullptr,
-                            static_cast<cudaStream_t>(stream));
+    return quant_any<false, false>(grads, dtype, a, scheme, gq_code_bits(scheme, s), codes,
+                                   nullptr, static_cast<cudaStream_t>(stream));
 }
 
 gq_status gq_reduce_codes(const void* codes, int scheme, int s, int64_t n, int64_t d,
@@ -292,7 +295,8 @@ gq_status gq_allreduce_mean(const void* grads, int dtype, int64_t n, int64_t d, 
     if ((st = norm_any(grads, dtype, mode, n, d, norm_dev, ws, cs)) != GQ_OK) return st;
     const float* ws_norm = &reinterpret_cast<const gq::WsHeader*>(ws)->norm;
     const gq::QuantArgs a = make_args(ws_norm, dtype, n, d, s, seed, step);
-    return quant_any<true>(grads, dtype, a, scheme, gq_code_bits(scheme, s), codes, out_dev, cs);
+    return quant_any<true, true>(grads, dtype, a, scheme, gq_code_bits(scheme, s), codes, out_dev,
+                                 cs);
 }
 
 gq_status gq_allreduce_mean_with_norm(const void* grads, int dtype, int64_t n, int64_t d,
@@ -304,8 +308,8 @@ gq_status gq_allreduce_mean_with_norm(const void* grads, int dtype, int64_t n, i
     if (!norm_dev || !out_dev || !aligned16(out_dev) || (codes && !aligned16(codes)))
         return GQ_ERR_INVALID;
     const gq::QuantArgs a = make_args(norm_dev, dtype, n, d, s, seed, step);
-    return quant_any<true>(grads, dtype, a, scheme, gq_code_bits(scheme, s), codes, out_dev,
-                           static_cast<cudaStream_t>(stream));
+    return quant_any<true, false>(grads, dtype, a, scheme, gq_code_bits(scheme, s), codes,
+                                  out_dev, static_cast<cudaStream_t>(stream));
 }
 
 gq_status gq_philox4x32_10(const uint32_t* ctr_key_dev, uint32_t* out_dev, int64_t count,

@@ -358,49 +358,84 @@ norm_kernel(const T* __restrict__ x, int64_t n, int64_t d, int64_t groups, bool 
 // ------------------------------------------------------------------------------------------
 // Steps 2-4: stochastic rounding onto the level grid (Global-QSGD, Global-Q operator; grids of
 // Global-L_s and Global-E_s), the integer sum over the workers and the dequantisation.
+//
+// Definitions (shared with the CPU oracle by specification only):
+//   v = fp32(|x| / N) clamped to [0, 1] (NaN -> 0);
+//   P(v) = position on the grid in level-index units: v s (L), or for E the level index of the
+//          binade below v plus the fraction of the way to the next level;
+//   T = floor(frac(P) 2^32); k = floor(P) + [r < T];
+//   r = (half (j mod 8) of Philox(j/8, i, step)) << 16 | half (j mod 8) of Philox(2^31 + j/8, i,
+//       step), key = seed.
+// Writing U = floor(P 2^32) as a 64-bit number and ~r = 2^32 - 1 - r, k = (U + ~r) >> 32.
+//
+// The kernel decides k from two cheap approximations and falls back to the exact computation
+// only when they could disagree with it:
+//   * v_c = RN(|x| RN(1/N)) instead of the correctly rounded quotient: |v_c - v| < 3.0001 u v
+//     (u = 2^-24), so |U(v_c) - U(v)| <= M with M = 1024 s (L) or 4096 (E), both bounds with
+//     room to spare (L: slope s 2^32; E: slope 2^(32-e) within binade e, at most 2^34 u v);
+//   * only the high half H of r is known: ~r lies in [~(H << 16) - 0xFFFF, ~(H << 16)].
+// With Z = U(v_c) + ~(H << 16), k is certain when no multiple of 2^32 lies within
+// [Z - M - 0xFFFF, Z + M]; then k = Z >> 32.  Otherwise (probability about (2M + 2^16) / 2^32 per
+// element) the group takes the exact path: __fdiv_rn and the second Philox call.
 // ------------------------------------------------------------------------------------------
 
-// Level index of one element: v = fp32(|x| / N) clamped to [0, 1] (NaN -> 0); the lower level
-// and T = floor(P(up) * 2^32) are read exactly off the bits of v; round up iff r < T.
-template <int SCHEME>
-__device__ __forceinline__ uint32_t level_index(float xv, float nrm, uint32_t s, uint32_t r) {
-    float v = __fdiv_rn(fabsf(xv), nrm);
-    v = (v <= 1.0f) ? v : ((v > 1.0f) ? 1.0f : 0.0f);
-    const uint32_t vb = __float_as_uint(v);
-    const uint32_t eb = vb >> 23;  // biased exponent, 0..127
-    const uint32_t frac = vb & 0x7FFFFFu;
-    const uint32_t mant = frac | (eb ? 0x800000u : 0u);  // v = mant * 2^(max(eb,1) - 150)
-    const uint32_t ee = eb ? eb : 1u;
-    if (SCHEME == kLinear) {
-        // t = v * s = (mant * s) * 2^(ee - 150), exact in 31 bits; its integer part is the
-        // lower level m and its fraction times 2^32 is T: one 64-bit shift gives both.
-        const uint32_t prod = mant * s;
-        const uint32_t sh = min(150u - ee, 63u);
-        const uint64_t w = (static_cast<uint64_t>(prod) << 32) >> sh;
-        const uint32_t m = static_cast<uint32_t>(w >> 32);
-        const uint32_t T = static_cast<uint32_t>(w);
-        return m + (r < T ? 1u : 0u);
-    } else {
-        // v in [2^e, 2^(e+1)) with e >= -(s-1): lower level index s + e, P(up) = fraction of v.
-        // v < 2^-(s-1): between 0 and 2^-(s-1), P(up) = v * 2^(s-1).
-        if (eb + s >= 128u) {
-            const uint32_t lo = s + eb - 127u;
-            const uint32_t T = frac << 9;
-            return lo + (r < T ? 1u : 0u);
+constexpr int kQCols = 8;  // coordinates per thread per row in the quantise kernels
+
+// 64-bit right shift with the PTX rule that shift amounts above 64 give 0.
+__device__ __forceinline__ uint64_t shr64(uint64_t v, uint32_t n) {
+    uint64_t r;
+    asm("shr.b64 %0, %1, %2;" : "=l"(r) : "l"(v), "r"(n));
+    return r;
+}
+
+// Eight coordinates 8g..8g+7 of row i, widened to fp32; zero past column d.
+template <typename T>
+__device__ __forceinline__ void load8(const T* __restrict__ x, int64_t i, int64_t g, int64_t d,
+                                      bool vec_rows, float (&v)[kQCols]) {
+    const int64_t j0 = g * kQCols;
+    const T* row = x + i * d + j0;
+    if (vec_rows && j0 + kQCols <= d) {
+        if (sizeof(T) == 4) {
+            float a[4], b[4];
+            Elem<float>::load_vec(reinterpret_cast<const float*>(row), a);
+            Elem<float>::load_vec(reinterpret_cast<const float*>(row) + 4, b);
+#pragma unroll
+            for (int c = 0; c < 4; ++c) { v[c] = a[c]; v[c + 4] = b[c]; }
+        } else {
+            Elem<uint16_t>::load_vec(reinterpret_cast<const uint16_t*>(row), v);
         }
-        const uint32_t sh = min(151u - ee - s, 63u);
-        const uint32_t T = static_cast<uint32_t>((static_cast<uint64_t>(mant) << 32) >> sh);
-        return r < T ? 1u : 0u;
+    } else {
+#pragma unroll
+        for (int c = 0; c < kQCols; ++c) v[c] = (j0 + c < d) ? Elem<T>::load_one(row + c) : 0.0f;
     }
 }
 
-// Signed contribution of a code to the integer sum: L sums the level index; E sums
-// 2^(k-1) units of 2^-(s-1) for level index k >= 1.
+// U = floor(P(v) 2^32) as (hi, lo) = (lower level index, T), for the bits vb of 0 <= v <= 1.
+// Exact.  (A subnormal v is given the implicit bit; its U is below 1 either way, so 0.)
 template <int SCHEME>
-__device__ __forceinline__ int32_t code_units(uint32_t k, bool neg) {
-    const int32_t u = (SCHEME == kLinear) ? static_cast<int32_t>(k)
-                                          : static_cast<int32_t>((1u << k) >> 1);
-    return neg ? -u : u;
+__device__ __forceinline__ void grid_position(uint32_t vb, uint32_t s, uint32_t& hi,
+                                              uint32_t& lo) {
+    const uint32_t eb = vb >> 23;  // biased exponent, 0..127
+    const uint32_t mant = (vb & 0x7FFFFFu) | 0x800000u;  // v = mant 2^(eb - 150)
+    if (SCHEME == kLinear) {
+        // v s = (mant s) 2^(eb - 150): mant s < 2^31, so U = (mant s) 2^32 >> (150 - eb)
+        const uint64_t w = shr64(static_cast<uint64_t>(mant * s) << 32, 150u - eb);
+        hi = static_cast<uint32_t>(w >> 32);
+        lo = static_cast<uint32_t>(w);
+    } else if (eb + s >= 128u) {
+        // v in [2^e, 2^(e+1)), e = eb - 127 >= -(s-1): level s + e, fraction = mantissa bits
+        hi = eb + s - 127u;
+        lo = vb << 9;
+    } else {
+        // v < 2^-(s-1): between level 0 and 2^-(s-1); U = v 2^(s-1) 2^32 = mant 2^(eb+s-119)
+        hi = 0u;
+        lo = static_cast<uint32_t>(shr64(static_cast<uint64_t>(mant) << 32, 151u - eb - s));
+    }
+}
+
+// 16-bit half c of a Philox output (low half of word c/2 for even c).
+__device__ __forceinline__ uint32_t half16(const uint32_t (&w)[4], int c) {
+    return (c & 1) ? (w[c >> 1] >> 16) : (w[c >> 1] & 0xFFFFu);
 }
 
 struct QuantArgs {
@@ -431,110 +466,155 @@ __device__ __forceinline__ float block_scale(float nrm, int64_t n, uint32_t s, f
     return *sh;
 }
 
-// Store C codes of one row (int8 or int4 nibbles) for column group g.
-template <int C, int CODE_BITS>
+// Store eight codes of one row (int8 bytes or int4 nibbles) for column group g.
+template <int CODE_BITS>
 __device__ __forceinline__ void store_codes(unsigned char* __restrict__ codes, int64_t i,
-                                            int64_t g, int64_t pitch, const int32_t (&c)[C]) {
+                                            int64_t g, int64_t pitch,
+                                            const int32_t (&c)[kQCols]) {
     if (CODE_BITS == 8) {
-        unsigned char* p = codes + i * pitch + g * C;
-        if (C == 4) {
-            uint32_t w = 0;
+        uint32_t w0 = 0, w1 = 0;
 #pragma unroll
-            for (int k = 0; k < 4; ++k) w |= (static_cast<uint32_t>(c[k]) & 0xFFu) << (8 * k);
-            *reinterpret_cast<uint32_t*>(p) = w;
-        } else {
-            uint32_t w0 = 0, w1 = 0;
-#pragma unroll
-            for (int k = 0; k < 4; ++k) {
-                w0 |= (static_cast<uint32_t>(c[k]) & 0xFFu) << (8 * k);
-                w1 |= (static_cast<uint32_t>(c[k + 4]) & 0xFFu) << (8 * k);
-            }
-            *reinterpret_cast<uint2*>(p) = make_uint2(w0, w1);
+        for (int k = 0; k < 4; ++k) {
+            w0 |= (static_cast<uint32_t>(c[k]) & 0xFFu) << (8 * k);
+            w1 |= (static_cast<uint32_t>(c[k + 4]) & 0xFFu) << (8 * k);
         }
+        *reinterpret_cast<uint2*>(codes + i * pitch + g * kQCols) = make_uint2(w0, w1);
     } else {
-        unsigned char* p = codes + i * (pitch / 2) + g * (C / 2);
         uint32_t w = 0;
 #pragma unroll
-        for (int k = 0; k < C; ++k) w |= (static_cast<uint32_t>(c[k]) & 0xFu) << (4 * k);
-        if (C == 4)
-            *reinterpret_cast<uint16_t*>(p) = static_cast<uint16_t>(w);
-        else
-            *reinterpret_cast<uint32_t*>(p) = w;
+        for (int k = 0; k < kQCols; ++k) w |= (static_cast<uint32_t>(c[k]) & 0xFu) << (4 * k);
+        *reinterpret_cast<uint32_t*>(codes + i * (pitch / 2) + g * (kQCols / 2)) = w;
+    }
+}
+
+// Per-kernel constants of the rounding decision.
+struct Decide {
+    float nrm;        // N
+    float rcp;        // RN(1 / N)
+    bool fast;        // the candidate path is valid (N and 1/N normal)
+    uint32_t lowb;    // M + 0xFFFF
+    uint32_t width;   // 2^32 - 2M - 0xFFFF: certain iff (Z mod 2^32) - lowb < width
+};
+
+template <int SCHEME>
+__device__ __forceinline__ Decide make_decide(float nrm, uint32_t s) {
+    Decide dc;
+    dc.nrm = nrm;
+    dc.rcp = __frcp_rn(nrm);
+    dc.fast = nrm >= 0x1p-126f && nrm <= 0x1p126f;
+    const uint32_t M = (SCHEME == kLinear) ? (s << 10) : 4096u;
+    dc.lowb = M + 0xFFFFu;
+    dc.width = 0u - (2u * M + 0xFFFFu);
+    return dc;
+}
+
+// Level indices k of the eight elements of one row-group.
+template <int SCHEME, bool TRUSTED>
+__device__ __forceinline__ void decide_row(const float (&xv)[kQCols], const Decide& dc,
+                                           const QuantArgs& a, uint32_t g32, uint32_t row,
+                                           uint32_t (&k)[kQCols]) {
+    const uint4 ra = philox4x32_10(make_uint4(g32, row, a.step_lo, a.step_hi), a.key0, a.key1);
+    const uint32_t aw[4] = {ra.x, ra.y, ra.z, ra.w};
+    bool unsure = !dc.fast;
+#pragma unroll
+    for (int c = 0; c < kQCols; ++c) {
+        uint32_t vb = __float_as_uint(fabsf(xv[c]) * dc.rcp);
+        if (!TRUSTED) unsure |= vb > kInfBits;  // NaN: decided on the exact path
+        vb = min(vb, 0x3F800000u);
+        uint32_t hi, lo;
+        grid_position<SCHEME>(vb, a.s, hi, lo);
+        const uint32_t hc = ~(half16(aw, c) << 16);
+        uint32_t z, kk;
+        asm("add.cc.u32 %0, %2, %3;\n\taddc.u32 %1, %4, 0;"
+            : "=r"(z), "=r"(kk) : "r"(lo), "r"(hc), "r"(hi));
+        k[c] = kk;
+        unsure |= (z - dc.lowb) >= dc.width;
+    }
+    if (unsure) {  // exact path: the correctly rounded quotient and the full 32-bit word
+        const uint4 rb = philox4x32_10(make_uint4(g32 | 0x80000000u, row, a.step_lo, a.step_hi),
+                                       a.key0, a.key1);
+        const uint32_t bw[4] = {rb.x, rb.y, rb.z, rb.w};
+#pragma unroll
+        for (int c = 0; c < kQCols; ++c) {
+            uint32_t vb = __float_as_uint(__fdiv_rn(fabsf(xv[c]), dc.nrm));
+            vb = (vb > kInfBits) ? 0u : min(vb, 0x3F800000u);
+            uint32_t hi, lo;
+            grid_position<SCHEME>(vb, a.s, hi, lo);
+            const uint32_t r = (half16(aw, c) << 16) | half16(bw, c);
+            k[c] = hi + (r < lo ? 1u : 0u);
+        }
     }
 }
 
 // Quantise column group g of all n rows; accumulate the integer sums; optionally store codes.
-// Returns the per-column sums in S.
-template <typename T, int SCHEME, int CODE_BITS>
+template <typename T, int SCHEME, int CODE_BITS, bool TRUSTED>
 __device__ __forceinline__ void quantize_group(const T* __restrict__ x, const QuantArgs& a,
-                                               float nrm, int64_t g,
+                                               const Decide& dc, int64_t g,
                                                unsigned char* __restrict__ codes,
-                                               int32_t (&S)[Elem<T>::kCols]) {
-    constexpr int C = Elem<T>::kCols;
-    constexpr int U = (C == 4) ? 8 : 4;  // rows in flight per thread
+                                               int32_t (&S)[kQCols]) {
+    // rows in flight per thread: 2 x 32 B (fp32) or 1 x 16 B (bf16); with 4 blocks of 256
+    // threads per SM that keeps ~64 KB (fp32) of loads in flight per SM
+    constexpr int U = (sizeof(T) == 4) ? 2 : 1;
 #pragma unroll
-    for (int c = 0; c < C; ++c) S[c] = 0;
+    for (int c = 0; c < kQCols; ++c) S[c] = 0;
+    const uint32_t g32 = static_cast<uint32_t>(g);
     for (int64_t i0 = 0; i0 < a.n; i0 += U) {
-        float v[U][C];
+        float v[U][kQCols];
 #pragma unroll
-        for (int u = 0; u < U; ++u) {
-            if (i0 + u < a.n) load_group<T>(x, i0 + u, g, a.d, a.vec_rows, v[u]);
-        }
+        for (int u = 0; u < U; ++u)
+            if (i0 + u < a.n) load8<T>(x, i0 + u, g, a.d, a.vec_rows, v[u]);
 #pragma unroll
         for (int u = 0; u < U; ++u) {
             if (i0 + u >= a.n) break;
             const uint32_t row = static_cast<uint32_t>(i0 + u);
-            int32_t code[C];
+            uint32_t k[kQCols];
+            decide_row<SCHEME, TRUSTED>(v[u], dc, a, g32, row, k);
+            int32_t code[kQCols];
 #pragma unroll
-            for (int h = 0; h < C / 4; ++h) {
-                // columns g*C + 4h .. +3 share Philox counter ((g*C)/4 + h, row, step)
-                const uint32_t ctr0 = static_cast<uint32_t>((g * C) >> 2) + h;
-                const uint4 r = philox4x32_10(make_uint4(ctr0, row, a.step_lo, a.step_hi),
-                                              a.key0, a.key1);
-                const uint32_t rw[4] = {r.x, r.y, r.z, r.w};
-#pragma unroll
-                for (int k = 0; k < 4; ++k) {
-                    const float xv = v[u][4 * h + k];
-                    const uint32_t lvl = level_index<SCHEME>(xv, nrm, a.s, rw[k]);
-                    const bool neg = xv < 0.0f;
-                    code[4 * h + k] = neg ? -static_cast<int32_t>(lvl) : static_cast<int32_t>(lvl);
-                    S[4 * h + k] += code_units<SCHEME>(lvl, neg);
-                }
+            for (int c = 0; c < kQCols; ++c) {
+                const int32_t sgn = static_cast<int32_t>(__float_as_uint(v[u][c])) >> 31;
+                const int32_t units = (SCHEME == kLinear) ? static_cast<int32_t>(k[c])
+                                                          : static_cast<int32_t>((1u << k[c]) >> 1);
+                S[c] += (units ^ sgn) - sgn;
+                code[c] = (static_cast<int32_t>(k[c]) ^ sgn) - sgn;
             }
-            if (CODE_BITS) store_codes<C, CODE_BITS>(codes, row, g, a.pitch, code);
+            if (CODE_BITS) store_codes<CODE_BITS>(codes, row, g, a.pitch, code);
         }
     }
 }
 
 // Quantise (+ sum + dequantise).  CODE_BITS: 0 (no codes), 4 or 8.  WRITE_OUT: dequantise the
-// sums into out.  Groups run over ceil(d/C) columns groups, or pitch/C when codes are written
-// (padding columns get zero codes).
-template <typename T, int SCHEME, int CODE_BITS, bool WRITE_OUT>
-__global__ void __launch_bounds__(kThreads)
+// sums into out.  TRUSTED: the norm was computed from these gradients by norm_kernel, so a
+// finite norm means no element is NaN or infinite.  Groups of 8 columns run over ceil(d/8), or
+// pitch/8 when codes are written (padding columns get zero codes), from the last group to the
+// first: the fused path's norm pass ends on the last columns, which are still in L2.
+template <typename T, int SCHEME, int CODE_BITS, bool WRITE_OUT, bool TRUSTED>
+__global__ void __launch_bounds__(kThreads, 4)
 quantize_kernel(const T* __restrict__ x, QuantArgs a, int64_t groups,
                 unsigned char* __restrict__ codes, float* __restrict__ out) {
-    constexpr int C = Elem<T>::kCols;
     __shared__ float sh_scale;
     const float nrm = __ldg(a.norm_ptr);
     const float scale = block_scale<SCHEME>(nrm, a.n, a.s, &sh_scale);
     const bool live = nrm > 0.0f && nrm < __uint_as_float(kInfBits);
+    const Decide dc = make_decide<SCHEME>(nrm, a.s);
     const int64_t stride = static_cast<int64_t>(gridDim.x) * kThreads;
-    for (int64_t g = static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x; g < groups;
-         g += stride) {
-        int32_t S[C];
+    for (int64_t it = static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x; it < groups;
+         it += stride) {
+        const int64_t g = groups - 1 - it;
+        int32_t S[kQCols];
         if (live) {
-            quantize_group<T, SCHEME, CODE_BITS>(x, a, nrm, g, codes, S);
+            quantize_group<T, SCHEME, CODE_BITS, TRUSTED>(x, a, dc, g, codes, S);
         } else {
 #pragma unroll
-            for (int c = 0; c < C; ++c) S[c] = 0;
+            for (int c = 0; c < kQCols; ++c) S[c] = 0;
             if (CODE_BITS)
-                for (int64_t i = 0; i < a.n; ++i) store_codes<C, CODE_BITS>(codes, i, g, a.pitch, S);
+                for (int64_t i = 0; i < a.n; ++i) store_codes<CODE_BITS>(codes, i, g, a.pitch, S);
         }
         if (WRITE_OUT) {
-            const int64_t j0 = g * C;
-            if (j0 + C <= a.d) {
+            const int64_t j0 = g * kQCols;
+            if (j0 + kQCols <= a.d) {
 #pragma unroll
-                for (int h = 0; h < C / 4; ++h)
+                for (int h = 0; h < kQCols / 4; ++h)
                     reinterpret_cast<float4*>(out + j0)[h] =
                         make_float4(scale * static_cast<float>(S[4 * h]),
                                     scale * static_cast<float>(S[4 * h + 1]),
@@ -542,11 +622,20 @@ quantize_kernel(const T* __restrict__ x, QuantArgs a, int64_t groups,
                                     scale * static_cast<float>(S[4 * h + 3]));
             } else {
 #pragma unroll
-                for (int c = 0; c < C; ++c)
+                for (int c = 0; c < kQCols; ++c)
                     if (j0 + c < a.d) out[j0 + c] = scale * static_cast<float>(S[c]);
             }
         }
     }
+}
+
+// Signed contribution of a code to the integer sum: L sums the level index; E sums
+// 2^(k-1) units of 2^-(s-1) for level index k >= 1.
+template <int SCHEME>
+__device__ __forceinline__ int32_t code_units(uint32_t k, bool neg) {
+    const int32_t u = (SCHEME == kLinear) ? static_cast<int32_t>(k)
+                                          : static_cast<int32_t>((1u << k) >> 1);
+    return neg ? -u : u;
 }
 
 // ------------------------------------------------------------------------------------------
