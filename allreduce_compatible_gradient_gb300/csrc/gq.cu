@@ -171,6 +171,10 @@ gq::QuantArgs make_args(const float* norm_ptr, int dtype, int64_t n, int64_t d, 
     a.s = static_cast<uint32_t>(s);
     a.key0 = static_cast<uint32_t>(seed);
     a.key1 = static_cast<uint32_t>(seed >> 32);
+    for (int r = 0; r < 10; ++r) {  // Philox round keys: the key advanced by r Weyl steps
+        a.rk[2 * r] = a.key0 + static_cast<uint32_t>(r) * 0x9E3779B9u;
+        a.rk[2 * r + 1] = a.key1 + static_cast<uint32_t>(r) * 0xBB67AE85u;
+    }
     a.step_lo = static_cast<uint32_t>(step);
     a.step_hi = static_cast<uint32_t>(step >> 32);
     a.n = n;

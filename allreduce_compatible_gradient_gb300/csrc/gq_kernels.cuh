@@ -52,6 +52,19 @@ __device__ __forceinline__ uint4 philox4x32_10(uint4 c, uint32_t k0, uint32_t k1
     return c;
 }
 
+// The same bijection with the ten round keys precomputed (rk[2r], rk[2r+1] = key words of
+// round r); used by the quantise kernels, whose key is fixed for the whole launch.
+__device__ __forceinline__ uint4 philox4x32_10_rk(uint4 c, const uint32_t (&rk)[20]) {
+    const uint32_t kMul0 = 0xD2511F53u, kMul1 = 0xCD9E8D57u;
+#pragma unroll
+    for (int round = 0; round < 10; ++round) {
+        const uint32_t hi0 = __umulhi(kMul0, c.x), lo0 = kMul0 * c.x;
+        const uint32_t hi1 = __umulhi(kMul1, c.z), lo1 = kMul1 * c.z;
+        c = make_uint4(hi1 ^ c.y ^ rk[2 * round], lo1, hi0 ^ c.w ^ rk[2 * round + 1], lo0);
+    }
+    return c;
+}
+
 // ------------------------------------------------------------------------------------------
 // Element access: a 16-byte column group of one row, widened to fp32.
 // ------------------------------------------------------------------------------------------
@@ -363,20 +376,26 @@ norm_kernel(const T* __restrict__ x, int64_t n, int64_t d, int64_t groups, bool 
 //   v = fp32(|x| / N) clamped to [0, 1] (NaN -> 0);
 //   P(v) = position on the grid in level-index units: v s (L), or for E the level index of the
 //          binade below v plus the fraction of the way to the next level;
-//   T = floor(frac(P) 2^32); k = floor(P) + [r < T];
+//   T = floor(frac(P) 2^32); k = floor(P) + [r < T] = floor(P + rho), rho = (2^32 - 1 - r) / 2^32;
 //   r = (half (j mod 8) of Philox(j/8, i, step)) << 16 | half (j mod 8) of Philox(2^31 + j/8, i,
 //       step), key = seed.
-// Writing U = floor(P 2^32) as a 64-bit number and ~r = 2^32 - 1 - r, k = (U + ~r) >> 32.
 //
-// The kernel decides k from two cheap approximations and falls back to the exact computation
-// only when they could disagree with it:
-//   * v_c = RN(|x| RN(1/N)) instead of the correctly rounded quotient: |v_c - v| < 3.0001 u v
-//     (u = 2^-24), so |U(v_c) - U(v)| <= M with M = 1024 s (L) or 4096 (E), both bounds with
-//     room to spare (L: slope s 2^32; E: slope 2^(32-e) within binade e, at most 2^34 u v);
-//   * only the high half H of r is known: ~r lies in [~(H << 16) - 0xFFFF, ~(H << 16)].
-// With Z = U(v_c) + ~(H << 16), k is certain when no multiple of 2^32 lies within
-// [Z - M - 0xFFFF, Z + M]; then k = Z >> 32.  Otherwise (probability about (2M + 2^16) / 2^32 per
-// element) the group takes the exact path: __fdiv_rn and the second Philox call.
+// Fast path (per element, no division, no variable shift): an approximation P_c of P in 16.16
+// fixed point, read off the bits of one fp32 result:
+//   L: fp32(fp32(|x| RN(s/N)) + 128) has unit 2^-16 in [128, 256), so its bits minus those of 128
+//      are P_c 2^16 (P <= s <= 127);
+//   E: v_c = fp32(|x| RN(1/N)); for v_c >= 2^-(s-1) the bits of v_c shifted right by 7 are
+//      (biased exponent, 16 fraction bits), i.e. (P_c + 127 - s) 2^16; below 2^-(s-1),
+//      P = v 2^(s-1) is read off fp32(fp32(|x| 2^(s-1) RN(1/N)) + 128) as for L.
+// |P_c 2^16 - P 2^16| < 2 in all cases (relative error below 3.0001 u of the products, u = 2^-24,
+// times P <= 127, plus the 2^-16 rounding or truncation).  With H the high half of r,
+// Y = P_c 2^16 + (0xFFFF - H) - 2 and the true P 2^16 + rho 2^16 in [Y, Y + 5), k = Y >> 16 is
+// certain when (Y & 0xFFFF) <= 0xFFFB.  Otherwise (probability about 5/65536 per element) the
+// eight elements of the row-group take the exact path: __fdiv_rn, integer grid position, and the
+// second Philox call for the low half of r.
+//
+// The integer sum over the workers is accumulated in fp32: every partial sum is an integer of
+// magnitude below 2^24 (the library rejects larger n s and n 2^(s-1)), so it is exact.
 // ------------------------------------------------------------------------------------------
 
 constexpr int kQCols = 8;  // coordinates per thread per row in the quantise kernels
@@ -442,6 +461,7 @@ struct QuantArgs {
     const float* norm_ptr;   // fp32 norm in device memory
     uint32_t s;
     uint32_t key0, key1;     // Philox key = seed
+    uint32_t rk[20];         // Philox round keys of that key
     uint32_t step_lo, step_hi;
     int64_t n, d;
     int64_t pitch;           // code row pitch in elements
@@ -491,9 +511,11 @@ __device__ __forceinline__ void store_codes(unsigned char* __restrict__ codes, i
 struct Decide {
     float nrm;        // N
     float rcp;        // RN(1 / N)
-    bool fast;        // the candidate path is valid (N and 1/N normal)
-    uint32_t lowb;    // M + 0xFFFF
-    uint32_t width;   // 2^32 - 2M - 0xFFFF: certain iff (Z mod 2^32) - lowb < width
+    float c1;         // L: RN(s / N); E: 2^(s-1) RN(1 / N)
+    bool fast;        // 2^-100 <= N <= 2^100: the fast path's products stay normal and finite
+    uint32_t clampb;  // L: bits of s + 128 (P <= s)
+    uint32_t bigmin;  // E: bits of 2^-(s-1)
+    uint32_t cbig;    // E: ((s - 127) << 16) + bits of 128
 };
 
 template <int SCHEME>
@@ -501,38 +523,50 @@ __device__ __forceinline__ Decide make_decide(float nrm, uint32_t s) {
     Decide dc;
     dc.nrm = nrm;
     dc.rcp = __frcp_rn(nrm);
-    dc.fast = nrm >= 0x1p-126f && nrm <= 0x1p126f;
-    const uint32_t M = (SCHEME == kLinear) ? (s << 10) : 4096u;
-    dc.lowb = M + 0xFFFFu;
-    dc.width = 0u - (2u * M + 0xFFFFu);
+    dc.fast = nrm >= 0x1p-100f && nrm <= 0x1p100f;
+    if (SCHEME == kLinear) {
+        dc.c1 = __fdiv_rn(static_cast<float>(s), nrm);
+        dc.clampb = __float_as_uint(static_cast<float>(s) + 128.0f);
+        dc.bigmin = 0u;
+        dc.cbig = 0u;
+    } else {
+        dc.c1 = dc.rcp * exp2i(static_cast<int>(s) - 1);
+        dc.clampb = 0x3F800000u;
+        dc.bigmin = (128u - s) << 23;
+        dc.cbig = ((s - 127u) << 16) + 0x43000000u;
+    }
     return dc;
 }
 
-// Level indices k of the eight elements of one row-group.
+// Level indices k of the eight elements of one row-group (see the fast-path comment above).
 template <int SCHEME, bool TRUSTED>
 __device__ __forceinline__ void decide_row(const float (&xv)[kQCols], const Decide& dc,
                                            const QuantArgs& a, uint32_t g32, uint32_t row,
                                            uint32_t (&k)[kQCols]) {
-    const uint4 ra = philox4x32_10(make_uint4(g32, row, a.step_lo, a.step_hi), a.key0, a.key1);
+    const uint4 ra = philox4x32_10_rk(make_uint4(g32, row, a.step_lo, a.step_hi), a.rk);
     const uint32_t aw[4] = {ra.x, ra.y, ra.z, ra.w};
-    bool unsure = !dc.fast;
+    uint32_t worst = dc.fast ? 0u : 0xFFFFu;  // largest (Y & 0xFFFF) of the row-group
 #pragma unroll
     for (int c = 0; c < kQCols; ++c) {
-        uint32_t vb = __float_as_uint(fabsf(xv[c]) * dc.rcp);
-        if (!TRUSTED) unsure |= vb > kInfBits;  // NaN: decided on the exact path
-        vb = min(vb, 0x3F800000u);
-        uint32_t hi, lo;
-        grid_position<SCHEME>(vb, a.s, hi, lo);
-        const uint32_t hc = ~(half16(aw, c) << 16);
-        uint32_t z, kk;
-        asm("add.cc.u32 %0, %2, %3;\n\taddc.u32 %1, %4, 0;"
-            : "=r"(z), "=r"(kk) : "r"(lo), "r"(hc), "r"(hi));
-        k[c] = kk;
-        unsure |= (z - dc.lowb) >= dc.width;
+        const float ax = fabsf(xv[c]);
+        uint32_t pb;
+        if (SCHEME == kLinear) {
+            pb = min(__float_as_uint(ax * dc.c1 + 128.0f), dc.clampb);
+        } else {
+            const uint32_t vb = min(__float_as_uint(ax * dc.rcp), 0x3F800000u);
+            const uint32_t pbig = (vb >> 7) + dc.cbig;
+            const uint32_t psmall = __float_as_uint(ax * dc.c1 + 128.0f);
+            pb = (vb >= dc.bigmin) ? pbig : psmall;
+        }
+        if (!TRUSTED && !(ax == ax)) worst = 0xFFFFu;  // NaN: decided on the exact path
+        const uint32_t hbar = 0xFFFFu - half16(aw, c);
+        const uint32_t y = pb + hbar - (0x43000000u + 2u);
+        k[c] = y >> 16;
+        worst = max(worst, y & 0xFFFFu);
     }
-    if (unsure) {  // exact path: the correctly rounded quotient and the full 32-bit word
-        const uint4 rb = philox4x32_10(make_uint4(g32 | 0x80000000u, row, a.step_lo, a.step_hi),
-                                       a.key0, a.key1);
+    if (worst > 0xFFFBu) {  // exact path: the correctly rounded quotient and the full word
+        const uint4 rb = philox4x32_10_rk(make_uint4(g32 | 0x80000000u, row, a.step_lo, a.step_hi),
+                                          a.rk);
         const uint32_t bw[4] = {rb.x, rb.y, rb.z, rb.w};
 #pragma unroll
         for (int c = 0; c < kQCols; ++c) {
@@ -546,17 +580,18 @@ __device__ __forceinline__ void decide_row(const float (&xv)[kQCols], const Deci
     }
 }
 
-// Quantise column group g of all n rows; accumulate the integer sums; optionally store codes.
+// Quantise column group g of all n rows; accumulate the sums (fp32, exact); optionally store
+// codes.
 template <typename T, int SCHEME, int CODE_BITS, bool TRUSTED>
 __device__ __forceinline__ void quantize_group(const T* __restrict__ x, const QuantArgs& a,
                                                const Decide& dc, int64_t g,
                                                unsigned char* __restrict__ codes,
-                                               int32_t (&S)[kQCols]) {
-    // rows in flight per thread: 2 x 32 B (fp32) or 1 x 16 B (bf16); with 4 blocks of 256
-    // threads per SM that keeps ~64 KB (fp32) of loads in flight per SM
+                                               float (&S)[kQCols]) {
+    // rows in flight per thread: 2 x 32 B (fp32) or 1 x 16 B (bf16); with 3 blocks of 256
+    // threads per SM that keeps ~48 KB (fp32) of loads in flight per SM
     constexpr int U = (sizeof(T) == 4) ? 2 : 1;
 #pragma unroll
-    for (int c = 0; c < kQCols; ++c) S[c] = 0;
+    for (int c = 0; c < kQCols; ++c) S[c] = 0.0f;
     const uint32_t g32 = static_cast<uint32_t>(g);
     for (int64_t i0 = 0; i0 < a.n; i0 += U) {
         float v[U][kQCols];
@@ -572,11 +607,19 @@ __device__ __forceinline__ void quantize_group(const T* __restrict__ x, const Qu
             int32_t code[kQCols];
 #pragma unroll
             for (int c = 0; c < kQCols; ++c) {
-                const int32_t sgn = static_cast<int32_t>(__float_as_uint(v[u][c])) >> 31;
-                const int32_t units = (SCHEME == kLinear) ? static_cast<int32_t>(k[c])
-                                                          : static_cast<int32_t>((1u << k[c]) >> 1);
-                S[c] += (units ^ sgn) - sgn;
-                code[c] = (static_cast<int32_t>(k[c]) ^ sgn) - sgn;
+                const uint32_t xb = __float_as_uint(v[u][c]);
+                // +-1 with the sign of x, and the summed value of the code as an exact fp32
+                const float sgn = __uint_as_float((xb & 0x80000000u) | 0x3F800000u);
+                float units;
+                if (SCHEME == kLinear)
+                    units = __uint_as_float(k[c] | 0x4B000000u) - 8388608.0f;  // k < 2^23
+                else  // 2^(k-1), and 0 for k = 0 (0.5 + 2^23 rounds to the even 2^23)
+                    units = (__uint_as_float((k[c] + 126u) << 23) + 8388608.0f) - 8388608.0f;
+                S[c] = __fmaf_rn(sgn, units, S[c]);
+                if (CODE_BITS) {
+                    const int32_t sg = static_cast<int32_t>(xb) >> 31;
+                    code[c] = (static_cast<int32_t>(k[c]) ^ sg) - sg;
+                }
             }
             if (CODE_BITS) store_codes<CODE_BITS>(codes, row, g, a.pitch, code);
         }
@@ -589,7 +632,7 @@ __device__ __forceinline__ void quantize_group(const T* __restrict__ x, const Qu
 // pitch/8 when codes are written (padding columns get zero codes), from the last group to the
 // first: the fused path's norm pass ends on the last columns, which are still in L2.
 template <typename T, int SCHEME, int CODE_BITS, bool WRITE_OUT, bool TRUSTED>
-__global__ void __launch_bounds__(kThreads, 4)
+__global__ void __launch_bounds__(kThreads, 3)
 quantize_kernel(const T* __restrict__ x, QuantArgs a, int64_t groups,
                 unsigned char* __restrict__ codes, float* __restrict__ out) {
     __shared__ float sh_scale;
@@ -601,14 +644,16 @@ quantize_kernel(const T* __restrict__ x, QuantArgs a, int64_t groups,
     for (int64_t it = static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x; it < groups;
          it += stride) {
         const int64_t g = groups - 1 - it;
-        int32_t S[kQCols];
+        float S[kQCols];
         if (live) {
             quantize_group<T, SCHEME, CODE_BITS, TRUSTED>(x, a, dc, g, codes, S);
         } else {
 #pragma unroll
-            for (int c = 0; c < kQCols; ++c) S[c] = 0;
-            if (CODE_BITS)
-                for (int64_t i = 0; i < a.n; ++i) store_codes<CODE_BITS>(codes, i, g, a.pitch, S);
+            for (int c = 0; c < kQCols; ++c) S[c] = 0.0f;
+            if (CODE_BITS) {
+                const int32_t zero[kQCols] = {0, 0, 0, 0, 0, 0, 0, 0};
+                for (int64_t i = 0; i < a.n; ++i) store_codes<CODE_BITS>(codes, i, g, a.pitch, zero);
+            }
         }
         if (WRITE_OUT) {
             const int64_t j0 = g * kQCols;
@@ -616,14 +661,12 @@ quantize_kernel(const T* __restrict__ x, QuantArgs a, int64_t groups,
 #pragma unroll
                 for (int h = 0; h < kQCols / 4; ++h)
                     reinterpret_cast<float4*>(out + j0)[h] =
-                        make_float4(scale * static_cast<float>(S[4 * h]),
-                                    scale * static_cast<float>(S[4 * h + 1]),
-                                    scale * static_cast<float>(S[4 * h + 2]),
-                                    scale * static_cast<float>(S[4 * h + 3]));
+                        make_float4(scale * S[4 * h], scale * S[4 * h + 1], scale * S[4 * h + 2],
+                                    scale * S[4 * h + 3]);
             } else {
 #pragma unroll
                 for (int c = 0; c < kQCols; ++c)
-                    if (j0 + c < a.d) out[j0 + c] = scale * static_cast<float>(S[c]);
+                    if (j0 + c < a.d) out[j0 + c] = scale * S[c];
             }
         }
     }
