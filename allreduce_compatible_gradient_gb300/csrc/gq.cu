@@ -10,6 +10,7 @@
 
 #include <cstdint>
 #include <cstring>
+#include <mutex>
 
 namespace {
 
@@ -33,27 +34,40 @@ int sm_count() {
     return cache[dev];
 }
 
-// Resident blocks per SM for a kernel (cached per kernel instantiation and device).
+// Resident blocks per SM for a kernel with `smem` bytes of dynamic shared memory, cached per
+// (kernel, device).  The first query for a kernel on a device also raises that kernel's
+// dynamic shared-memory limit to `smem`.
 template <typename K>
-int blocks_per_sm(K kernel) {
-    static int cache[kMaxDevices] = {0};
+int blocks_per_sm(K kernel, int smem = 0) {
+    struct Entry {
+        const void* fn;
+        int dev;
+        int nb;
+    };
+    static Entry table[512];
+    static int used = 0;
+    static std::mutex mu;
+    const void* fn = reinterpret_cast<const void*>(kernel);
     int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) dev = 0;
-    if (cache[dev] == 0) {
-        int nb = 0;
-        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, kernel, kThreads, 0) != cudaSuccess ||
-            nb <= 0)
-            nb = 1;
-        cache[dev] = nb;
-    }
-    return cache[dev];
+    if (cudaGetDevice(&dev) != cudaSuccess) dev = 0;
+    std::lock_guard<std::mutex> lock(mu);
+    for (int e = 0; e < used; ++e)
+        if (table[e].fn == fn && table[e].dev == dev) return table[e].nb;
+    if (smem > 0)  // dynamic + static shared memory may pass the default 48 KB
+        cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    int nb = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, kernel, kThreads, smem) != cudaSuccess ||
+        nb <= 0)
+        nb = 1;
+    if (used < 512) table[used++] = Entry{fn, dev, nb};
+    return nb;
 }
 
 // Grid for a grid-stride kernel over `work` thread-items: one full wave of resident blocks
 // (a multiple of the SM count), fewer when the work is smaller.
 template <typename K>
-unsigned grid_for(K kernel, int64_t work, int64_t cap = INT32_MAX) {
-    const int64_t full = static_cast<int64_t>(blocks_per_sm(kernel)) * sm_count();
+unsigned grid_for(K kernel, int64_t work, int64_t cap = INT32_MAX, int smem = 0) {
+    const int64_t full = static_cast<int64_t>(blocks_per_sm(kernel, smem)) * sm_count();
     int64_t need = (work + kThreads - 1) / kThreads;
     int64_t g = need < full ? need : full;
     if (g > cap) g = cap;
@@ -138,9 +152,10 @@ gq_status run_quant(const void* grads, const gq::QuantArgs& a, void* codes, floa
                     cudaStream_t st) {
     const int64_t groups = BITS ? a.pitch / gq::kQCols : (a.d + gq::kQCols - 1) / gq::kQCols;
     auto k = gq::quantize_kernel<T, SCHEME, BITS, OUT, TRUSTED>;
-    const unsigned grid = grid_for(k, groups);
-    k<<<grid, kThreads, 0, st>>>(static_cast<const T*>(grads), a, groups,
-                                 static_cast<unsigned char*>(codes), out);
+    constexpr int smem = gq::Staging<T>::kBytes;
+    const unsigned grid = grid_for(k, groups, INT32_MAX, smem);
+    k<<<grid, kThreads, smem, st>>>(static_cast<const T*>(grads), a, groups,
+                                    static_cast<unsigned char*>(codes), out);
     return launch_status();
 }
 

@@ -538,92 +538,269 @@ __device__ __forceinline__ Decide make_decide(float nrm, uint32_t s) {
     return dc;
 }
 
-// Level indices k of the eight elements of one row-group (see the fast-path comment above).
-template <int SCHEME, bool TRUSTED>
-__device__ __forceinline__ void decide_row(const float (&xv)[kQCols], const Decide& dc,
-                                           const QuantArgs& a, uint32_t g32, uint32_t row,
-                                           uint32_t (&k)[kQCols]) {
-    const uint4 ra = philox4x32_10_rk(make_uint4(g32, row, a.step_lo, a.step_hi), a.rk);
-    const uint32_t aw[4] = {ra.x, ra.y, ra.z, ra.w};
-    uint32_t worst = dc.fast ? 0u : 0xFFFFu;  // largest (Y & 0xFFFF) of the row-group
+// Philox words of R row-groups: call (g, row0 + u, step) for u < R.
+template <int R>
+__device__ __forceinline__ void philox_rows(const QuantArgs& a, uint32_t g32, uint32_t row0,
+                                            uint32_t (&aw)[R][4]) {
 #pragma unroll
-    for (int c = 0; c < kQCols; ++c) {
-        const float ax = fabsf(xv[c]);
-        uint32_t pb;
-        if (SCHEME == kLinear) {
-            pb = min(__float_as_uint(ax * dc.c1 + 128.0f), dc.clampb);
-        } else {
-            const uint32_t vb = min(__float_as_uint(ax * dc.rcp), 0x3F800000u);
-            const uint32_t pbig = (vb >> 7) + dc.cbig;
-            const uint32_t psmall = __float_as_uint(ax * dc.c1 + 128.0f);
-            pb = (vb >= dc.bigmin) ? pbig : psmall;
-        }
-        if (!TRUSTED && !(ax == ax)) worst = 0xFFFFu;  // NaN: decided on the exact path
-        const uint32_t hbar = 0xFFFFu - half16(aw, c);
-        const uint32_t y = pb + hbar - (0x43000000u + 2u);
-        k[c] = y >> 16;
-        worst = max(worst, y & 0xFFFFu);
+    for (int u = 0; u < R; ++u) {
+        const uint4 ra = philox4x32_10_rk(make_uint4(g32, row0 + u, a.step_lo, a.step_hi), a.rk);
+        aw[u][0] = ra.x; aw[u][1] = ra.y; aw[u][2] = ra.z; aw[u][3] = ra.w;
     }
-    if (worst > 0xFFFBu) {  // exact path: the correctly rounded quotient and the full word
-        const uint4 rb = philox4x32_10_rk(make_uint4(g32 | 0x80000000u, row, a.step_lo, a.step_hi),
-                                          a.rk);
-        const uint32_t bw[4] = {rb.x, rb.y, rb.z, rb.w};
+}
+
+// Level indices k of the eight elements of R row-groups (rows row0 .. row0+R-1), given the
+// high-half Philox words aw of those rows; the rare exact path runs once for the batch if any
+// of its elements needs it.
+template <int SCHEME, bool TRUSTED, int R>
+__device__ __forceinline__ void decide_rows(const float (&xv)[R][kQCols], const Decide& dc,
+                                            const QuantArgs& a, uint32_t g32, uint32_t row0,
+                                            const uint32_t (&aw)[R][4],
+                                            uint32_t (&k)[R][kQCols]) {
+    // Y = P_c 2^16 + (0xFFFF - H) - 2, with the bias of 128's bits folded in
+    constexpr uint32_t kBias = 0xFFFFu - 0x43000000u - 2u;
+    uint32_t worst = dc.fast ? 0u : 0xFFFFu;  // largest (Y & 0xFFFF) of the batch
+#pragma unroll
+    for (int u = 0; u < R; ++u) {
 #pragma unroll
         for (int c = 0; c < kQCols; ++c) {
-            uint32_t vb = __float_as_uint(__fdiv_rn(fabsf(xv[c]), dc.nrm));
-            vb = (vb > kInfBits) ? 0u : min(vb, 0x3F800000u);
-            uint32_t hi, lo;
-            grid_position<SCHEME>(vb, a.s, hi, lo);
-            const uint32_t r = (half16(aw, c) << 16) | half16(bw, c);
-            k[c] = hi + (r < lo ? 1u : 0u);
+            const float ax = fabsf(xv[u][c]);
+            uint32_t pb;
+            if (SCHEME == kLinear) {
+                pb = min(__float_as_uint(ax * dc.c1 + 128.0f), dc.clampb);
+            } else {
+                const uint32_t vb = min(__float_as_uint(ax * dc.rcp), 0x3F800000u);
+                const uint32_t pbig = (vb >> 7) + dc.cbig;
+                const uint32_t psmall = __float_as_uint(ax * dc.c1 + 128.0f);
+                pb = (vb >= dc.bigmin) ? pbig : psmall;
+            }
+            if (!TRUSTED && !(ax == ax)) worst = 0xFFFFu;  // NaN: decided on the exact path
+            const uint32_t y = pb - half16(aw[u], c) + kBias;
+            k[u][c] = y >> 16;
+            worst = max(worst, y & 0xFFFFu);
+        }
+    }
+    if (worst > 0xFFFBu) {  // exact path: the correctly rounded quotient and the full word
+#pragma unroll
+        for (int u = 0; u < R; ++u) {
+            const uint4 rb = philox4x32_10_rk(
+                make_uint4(g32 | 0x80000000u, row0 + u, a.step_lo, a.step_hi), a.rk);
+            const uint32_t bw[4] = {rb.x, rb.y, rb.z, rb.w};
+#pragma unroll
+            for (int c = 0; c < kQCols; ++c) {
+                uint32_t vb = __float_as_uint(__fdiv_rn(fabsf(xv[u][c]), dc.nrm));
+                vb = (vb > kInfBits) ? 0u : min(vb, 0x3F800000u);
+                uint32_t hi, lo;
+                grid_position<SCHEME>(vb, a.s, hi, lo);
+                const uint32_t r = (half16(aw[u], c) << 16) | half16(bw, c);
+                k[u][c] = hi + (r < lo ? 1u : 0u);
+            }
         }
     }
 }
 
-// Quantise column group g of all n rows; accumulate the sums (fp32, exact); optionally store
-// codes.
+// Accumulate one row-group's codes into the sums (fp32, exact: integers below 2^24) and return
+// the signed codes.
+template <int SCHEME>
+__device__ __forceinline__ void accumulate_row(const float (&xv)[kQCols],
+                                               const uint32_t (&k)[kQCols], float (&S)[kQCols],
+                                               int32_t (&code)[kQCols]) {
+#pragma unroll
+    for (int c = 0; c < kQCols; ++c) {
+        const uint32_t xb = __float_as_uint(xv[c]);
+        // +-1 with the sign of x, and the summed value of the code as an exact fp32
+        const float sgn = __uint_as_float((xb & 0x80000000u) | 0x3F800000u);
+        float units;
+        if (SCHEME == kLinear)
+            units = __uint_as_float(k[c] | 0x4B000000u) - 8388608.0f;  // k < 2^23
+        else  // 2^(k-1), and 0 for k = 0 (0.5 + 2^23 rounds to the even 2^23)
+            units = (__uint_as_float((k[c] + 126u) << 23) + 8388608.0f) - 8388608.0f;
+        S[c] = __fmaf_rn(sgn, units, S[c]);
+        const int32_t sg = static_cast<int32_t>(xb) >> 31;
+        code[c] = (static_cast<int32_t>(k[c]) ^ sg) - sg;
+    }
+}
+
+// Quantise column group g of all n rows with direct loads; accumulate the sums; optionally
+// store codes.  Two rows are loaded at a time; each row is decided on its own.
 template <typename T, int SCHEME, int CODE_BITS, bool TRUSTED>
 __device__ __forceinline__ void quantize_group(const T* __restrict__ x, const QuantArgs& a,
                                                const Decide& dc, int64_t g,
                                                unsigned char* __restrict__ codes,
                                                float (&S)[kQCols]) {
-    // rows in flight per thread: 2 x 32 B (fp32) or 1 x 16 B (bf16); with 3 blocks of 256
-    // threads per SM that keeps ~48 KB (fp32) of loads in flight per SM
-    constexpr int U = (sizeof(T) == 4) ? 2 : 1;
+    constexpr int U = 2;  // rows loaded per batch
 #pragma unroll
     for (int c = 0; c < kQCols; ++c) S[c] = 0.0f;
     const uint32_t g32 = static_cast<uint32_t>(g);
     for (int64_t i0 = 0; i0 < a.n; i0 += U) {
-        float v[U][kQCols];
+        float v[U][1][kQCols];
 #pragma unroll
         for (int u = 0; u < U; ++u)
-            if (i0 + u < a.n) load8<T>(x, i0 + u, g, a.d, a.vec_rows, v[u]);
+            if (i0 + u < a.n) load8<T>(x, i0 + u, g, a.d, a.vec_rows, v[u][0]);
 #pragma unroll
         for (int u = 0; u < U; ++u) {
             if (i0 + u >= a.n) break;
             const uint32_t row = static_cast<uint32_t>(i0 + u);
-            uint32_t k[kQCols];
-            decide_row<SCHEME, TRUSTED>(v[u], dc, a, g32, row, k);
+            uint32_t aw[1][4];
+            philox_rows<1>(a, g32, row, aw);
+            uint32_t k[1][kQCols];
+            decide_rows<SCHEME, TRUSTED, 1>(v[u], dc, a, g32, row, aw, k);
             int32_t code[kQCols];
-#pragma unroll
-            for (int c = 0; c < kQCols; ++c) {
-                const uint32_t xb = __float_as_uint(v[u][c]);
-                // +-1 with the sign of x, and the summed value of the code as an exact fp32
-                const float sgn = __uint_as_float((xb & 0x80000000u) | 0x3F800000u);
-                float units;
-                if (SCHEME == kLinear)
-                    units = __uint_as_float(k[c] | 0x4B000000u) - 8388608.0f;  // k < 2^23
-                else  // 2^(k-1), and 0 for k = 0 (0.5 + 2^23 rounds to the even 2^23)
-                    units = (__uint_as_float((k[c] + 126u) << 23) + 8388608.0f) - 8388608.0f;
-                S[c] = __fmaf_rn(sgn, units, S[c]);
-                if (CODE_BITS) {
-                    const int32_t sg = static_cast<int32_t>(xb) >> 31;
-                    code[c] = (static_cast<int32_t>(k[c]) ^ sg) - sg;
-                }
-            }
+            accumulate_row<SCHEME>(v[u][0], k[0], S, code);
             if (CODE_BITS) store_codes<CODE_BITS>(codes, row, g, a.pitch, code);
         }
     }
+}
+
+// ------------------------------------------------------------------------------------------
+// Asynchronous staging of the gradient rows.  Each thread copies its own 16-byte pieces of the
+// next rows into its own shared-memory slots (cp.async, L1 bypassed) and reads them back when
+// they are needed, so loads stay in flight without holding registers.  A thread only ever
+// reads what it copied itself, so the only synchronisation is cp.async.wait_group (a hardware
+// wait on the thread's own copies).
+// ------------------------------------------------------------------------------------------
+__device__ __forceinline__ void cp_async16(void* smem, const void* gmem) {
+    const uint32_t sa = static_cast<uint32_t>(__cvta_generic_to_shared(smem));
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(sa), "l"(gmem) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() {
+    asm volatile("cp.async.commit_group;" ::: "memory");
+}
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
+template <typename T>
+struct Staging {
+    // Measured on the quantise pass: staging pays for bf16 (twice the elements per byte, so a
+    // thread spends longer per loaded byte) and not for fp32, where the direct loads of two
+    // rows per batch already keep enough bytes in flight.
+    static constexpr bool kEnabled = sizeof(T) == 2;
+    static constexpr int kPieces = sizeof(T) == 4 ? 2 : 1;  // 16-byte pieces per row-group
+    static constexpr int kRows = 2;                         // rows per batch
+    static constexpr int kStages = 4;                       // batches in the ring
+    static constexpr int kBytes = kEnabled ? kStages * kRows * kPieces * kThreads * 16 : 0;
+};
+
+// Widen one staged row-group (kPieces x 16 bytes) to eight fp32 values.
+template <typename T>
+__device__ __forceinline__ void unstage(const uint4* piece0, const uint4* piece1,
+                                        float (&v)[kQCols]) {
+    if (sizeof(T) == 4) {
+        const uint4 p = *piece0, q = *piece1;
+        v[0] = __uint_as_float(p.x); v[1] = __uint_as_float(p.y);
+        v[2] = __uint_as_float(p.z); v[3] = __uint_as_float(p.w);
+        v[4] = __uint_as_float(q.x); v[5] = __uint_as_float(q.y);
+        v[6] = __uint_as_float(q.z); v[7] = __uint_as_float(q.w);
+    } else {
+        const uint4 p = *piece0;
+        const uint32_t w[4] = {p.x, p.y, p.z, p.w};
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            v[2 * k] = __uint_as_float(w[k] << 16);
+            v[2 * k + 1] = __uint_as_float(w[k] & 0xFFFF0000u);
+        }
+    }
+}
+
+// Output of one finished column group: dequantise the sums into out.
+__device__ __forceinline__ void store_out(float* __restrict__ out, int64_t g, int64_t d,
+                                          float scale, const float (&S)[kQCols]) {
+    const int64_t j0 = g * kQCols;
+    if (j0 + kQCols <= d) {
+#pragma unroll
+        for (int h = 0; h < kQCols / 4; ++h)
+            reinterpret_cast<float4*>(out + j0)[h] =
+                make_float4(scale * S[4 * h], scale * S[4 * h + 1], scale * S[4 * h + 2],
+                            scale * S[4 * h + 3]);
+    } else {
+#pragma unroll
+        for (int c = 0; c < kQCols; ++c)
+            if (j0 + c < d) out[j0 + c] = scale * S[c];
+    }
+}
+
+// The column groups 0 .. full-1 (every row of them vector-aligned and inside d), visited from
+// the last to the first in grid-stride order, with the rows staged through shared memory.
+template <typename T, int SCHEME, int CODE_BITS, bool WRITE_OUT, bool TRUSTED>
+__device__ __forceinline__ void staged_groups(const T* __restrict__ x, const QuantArgs& a,
+                                              const Decide& dc, int64_t full, float scale,
+                                              unsigned char* __restrict__ codes,
+                                              float* __restrict__ out, uint4* stage) {
+    using St = Staging<T>;
+    constexpr int R = St::kRows, P = St::kPieces, NS = St::kStages;
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * kThreads;
+    const int64_t it0 = static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x;
+    const int64_t ngroups = it0 < full ? (full - 1 - it0) / stride + 1 : 0;
+    const int64_t nb = (a.n + R - 1) / R;  // batches per group
+    const int64_t total = ngroups * nb;
+    auto slot = [&](int st, int u, int p) -> uint4* {
+        return stage + ((st * R + u) * P + p) * kThreads + threadIdx.x;
+    };
+    // issue cursor: batch ib = (group iq, batch ir)
+    int64_t ib = 0, iq = 0, ir = 0;
+    auto issue = [&]() {
+        if (ib < total) {
+            const int64_t g = full - 1 - (it0 + iq * stride);
+            const int st = static_cast<int>(ib % NS);
+#pragma unroll
+            for (int u = 0; u < R; ++u) {
+                const int64_t row = ir * R + u;
+                if (row < a.n) {
+                    const T* src = x + row * a.d + g * kQCols;
+#pragma unroll
+                    for (int p = 0; p < P; ++p) cp_async16(slot(st, u, p), src + p * (16 / sizeof(T)));
+                }
+            }
+            if (++ir == nb) { ir = 0; ++iq; }
+        }
+        ++ib;
+        cp_async_commit();
+    };
+#pragma unroll
+    for (int k = 0; k < NS - 1; ++k) issue();
+    float S[kQCols];
+    int64_t q = 0, r = 0;
+    for (int64_t b = 0; b < total; ++b) {
+        issue();
+        cp_async_wait<NS - 1>();
+        const int st = static_cast<int>(b % NS);
+        const int64_t g = full - 1 - (it0 + q * stride);
+        const uint32_t g32 = static_cast<uint32_t>(g);
+        if (r == 0) {
+#pragma unroll
+            for (int c = 0; c < kQCols; ++c) S[c] = 0.0f;
+        }
+        float v[R][kQCols];
+#pragma unroll
+        for (int u = 0; u < R; ++u) {
+            if (r * R + u < a.n) {
+                unstage<T>(slot(st, u, 0), slot(st, u, P - 1), v[u]);
+            } else {
+#pragma unroll
+                for (int c = 0; c < kQCols; ++c) v[u][c] = 0.0f;
+            }
+        }
+        uint32_t aw[R][4];
+        philox_rows<R>(a, g32, static_cast<uint32_t>(r * R), aw);
+        uint32_t k[R][kQCols];
+        decide_rows<SCHEME, TRUSTED, R>(v, dc, a, g32, static_cast<uint32_t>(r * R), aw, k);
+#pragma unroll
+        for (int u = 0; u < R; ++u) {
+            const int64_t row64 = r * R + u;
+            if (row64 >= a.n) break;
+            int32_t code[kQCols];
+            accumulate_row<SCHEME>(v[u], k[u], S, code);
+            if (CODE_BITS) store_codes<CODE_BITS>(codes, row64, g, a.pitch, code);
+        }
+        if (++r == nb) {
+            r = 0;
+            ++q;
+            if (WRITE_OUT) store_out(out, g, a.d, scale, S);
+        }
+    }
+    cp_async_wait<0>();
 }
 
 // Quantise (+ sum + dequantise).  CODE_BITS: 0 (no codes), 4 or 8.  WRITE_OUT: dequantise the
@@ -632,16 +809,27 @@ __device__ __forceinline__ void quantize_group(const T* __restrict__ x, const Qu
 // pitch/8 when codes are written (padding columns get zero codes), from the last group to the
 // first: the fused path's norm pass ends on the last columns, which are still in L2.
 template <typename T, int SCHEME, int CODE_BITS, bool WRITE_OUT, bool TRUSTED>
-__global__ void __launch_bounds__(kThreads, 3)
+__global__ void __launch_bounds__(kThreads, sizeof(T) == 4 ? 3 : 2)
 quantize_kernel(const T* __restrict__ x, QuantArgs a, int64_t groups,
                 unsigned char* __restrict__ codes, float* __restrict__ out) {
+    extern __shared__ uint4 stage[];
     __shared__ float sh_scale;
     const float nrm = __ldg(a.norm_ptr);
     const float scale = block_scale<SCHEME>(nrm, a.n, a.s, &sh_scale);
     const bool live = nrm > 0.0f && nrm < __uint_as_float(kInfBits);
     const Decide dc = make_decide<SCHEME>(nrm, a.s);
+    // groups [0, full) are staged through shared memory; the rest (the ragged last group, code
+    // padding, or everything when rows are not 16-byte aligned) use direct loads
+    int64_t full = 0;
+    if constexpr (Staging<T>::kEnabled) {
+        full = (live && a.vec_rows) ? a.d / kQCols : 0;
+        if (full > 0)
+            staged_groups<T, SCHEME, CODE_BITS, WRITE_OUT, TRUSTED>(x, a, dc, full, scale, codes,
+                                                                    out, stage);
+    }
     const int64_t stride = static_cast<int64_t>(gridDim.x) * kThreads;
-    for (int64_t it = static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x; it < groups;
+    const int64_t rest = groups - full;
+    for (int64_t it = static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x; it < rest;
          it += stride) {
         const int64_t g = groups - 1 - it;
         float S[kQCols];
@@ -655,20 +843,7 @@ quantize_kernel(const T* __restrict__ x, QuantArgs a, int64_t groups,
                 for (int64_t i = 0; i < a.n; ++i) store_codes<CODE_BITS>(codes, i, g, a.pitch, zero);
             }
         }
-        if (WRITE_OUT) {
-            const int64_t j0 = g * kQCols;
-            if (j0 + kQCols <= a.d) {
-#pragma unroll
-                for (int h = 0; h < kQCols / 4; ++h)
-                    reinterpret_cast<float4*>(out + j0)[h] =
-                        make_float4(scale * S[4 * h], scale * S[4 * h + 1], scale * S[4 * h + 2],
-                                    scale * S[4 * h + 3]);
-            } else {
-#pragma unroll
-                for (int c = 0; c < kQCols; ++c)
-                    if (j0 + c < a.d) out[j0 + c] = scale * S[c];
-            }
-        }
+        if (WRITE_OUT) store_out(out, g, a.d, scale, S);
     }
 }
 

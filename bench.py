@@ -9,7 +9,7 @@ synthetic and seeded (allreduce_compatible_gradient_gb300.workloads); the defaul
 ResNet-50-sized (n = 8 workers, d = 25,557,032 fp32, Global-L_127, max norm).
 
 Timing: W warm-up steps, then K steps timed one by one with CUDA events on the launching stream;
-L2 is flushed (a 512 MiB write) between timed steps, outside the timed region.  Under torchrun
+L2 is flushed (a 512 MiB write, then a 256 MiB read) between timed steps, outside the timed region.  Under torchrun
 every rank runs an independent replica on its own GPU (the path needs no data exchange on one
 GPU per problem); elapsed time is the max over ranks.
 
