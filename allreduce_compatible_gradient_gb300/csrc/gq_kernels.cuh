@@ -94,6 +94,27 @@ template <> struct Elem<uint16_t> {
     }
 };
 
+// Raw 16-byte column group g of row i (vector rows only; no bounds check) and its widening.
+__device__ __forceinline__ uint4 load_raw16(const void* __restrict__ x, int64_t i, int64_t g,
+                                            int64_t row_bytes) {
+    return __ldg(reinterpret_cast<const uint4*>(static_cast<const unsigned char*>(x) +
+                                                i * row_bytes) + g);
+}
+template <typename T>
+__device__ __forceinline__ void widen16(const uint4& t, float (&v)[Elem<T>::kCols]) {
+    if (sizeof(T) == 4) {
+        v[0] = __uint_as_float(t.x); v[1] = __uint_as_float(t.y);
+        v[2] = __uint_as_float(t.z); v[3] = __uint_as_float(t.w);
+    } else {
+        const uint32_t w[4] = {t.x, t.y, t.z, t.w};
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            v[2 * k] = __uint_as_float(w[k] << 16);
+            v[2 * k + 1] = __uint_as_float(w[k] & 0xFFFF0000u);
+        }
+    }
+}
+
 // Row i, column group g (columns g*C .. g*C+C-1) of the n x d matrix x, zero past column d.
 template <typename T>
 __device__ __forceinline__ void load_group(const T* __restrict__ x, int64_t i, int64_t g,
@@ -234,7 +255,7 @@ __device__ __forceinline__ uint64_t block_max_bits(uint64_t v, uint64_t* sh) {
 // the partials in index order and writes the fp32 norm.
 // ------------------------------------------------------------------------------------------
 template <typename T, int MODE>
-__global__ void __launch_bounds__(kThreads)
+__global__ void __launch_bounds__(kThreads, 4)
 norm_kernel(const T* __restrict__ x, int64_t n, int64_t d, int64_t groups, bool vec_rows,
             float* __restrict__ norm_user, unsigned char* __restrict__ ws) {
     constexpr int C = Elem<T>::kCols;
@@ -251,44 +272,54 @@ norm_kernel(const T* __restrict__ x, int64_t n, int64_t d, int64_t groups, bool 
     int64_t best_key = INT64_MIN;  // kL2Max
     uint32_t bad_col = 0;          // kL2Max: a non-finite column norm was seen
 
-    constexpr int U = (C == 4) ? 8 : 4;  // rows in flight per thread
+    // rows in flight per thread: 8 raw 16-byte loads (widened when used); fewer for the
+    // (2, inf) form, whose per-column scaled sums take C x 5 registers
+    constexpr int U = (MODE == kL2Max) ? (C == 8 ? 2 : 4) : 8;
+    const int64_t row_bytes = d * static_cast<int64_t>(sizeof(T));
     for (int64_t g = static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x; g < groups;
          g += stride) {
         uint32_t colmax[C];   // kMaxL2
         ScaledSumSq col[C];   // kL2Max
 #pragma unroll
         for (int c = 0; c < C; ++c) { colmax[c] = 0; col[c].init(); }
+        const bool vec = vec_rows && (g + 1) * C <= d;
         for (int64_t i0 = 0; i0 < n; i0 += U) {
-            float v[U][C];
+            uint4 raw[U];
+            if (vec) {
 #pragma unroll
-            for (int u = 0; u < U; ++u) {
-                if (i0 + u < n) {
-                    load_group<T>(x, i0 + u, g, d, vec_rows, v[u]);
-                } else {
-#pragma unroll
-                    for (int c = 0; c < C; ++c) v[u][c] = 0.0f;  // zero rows add nothing
-                }
+                for (int u = 0; u < U; ++u)
+                    raw[u] = (i0 + u < n) ? load_raw16(x, i0 + u, g, row_bytes)
+                                          : make_uint4(0u, 0u, 0u, 0u);  // zero rows add nothing
             }
 #pragma unroll
             for (int u = 0; u < U; ++u) {
+                float v[C];
+                if (vec) {
+                    widen16<T>(raw[u], v);
+                } else if (i0 + u < n) {
+                    load_group<T>(x, i0 + u, g, d, false, v);
+                } else {
+#pragma unroll
+                    for (int c = 0; c < C; ++c) v[c] = 0.0f;
+                }
                 if (MODE == kMaxMax) {
 #pragma unroll
                     for (int c = 0; c < C; ++c) {
-                        const uint32_t b = __float_as_uint(v[u][c]) & 0x7FFFFFFFu;
+                        const uint32_t b = __float_as_uint(v[c]) & 0x7FFFFFFFu;
                         maxbits = b > maxbits ? b : maxbits;
                     }
                 } else if (MODE == kL2L2) {
-                    ssq.add<C>(v[u]);
+                    ssq.add<C>(v);
                 } else if (MODE == kMaxL2) {
 #pragma unroll
                     for (int c = 0; c < C; ++c) {
-                        const uint32_t b = __float_as_uint(v[u][c]) & 0x7FFFFFFFu;
+                        const uint32_t b = __float_as_uint(v[c]) & 0x7FFFFFFFu;
                         colmax[c] = b > colmax[c] ? b : colmax[c];
                     }
                 } else {
 #pragma unroll
                     for (int c = 0; c < C; ++c) {
-                        const float one[1] = {v[u][c]};
+                        const float one[1] = {v[c]};
                         col[c].add<1>(one);
                     }
                 }
@@ -560,6 +591,8 @@ __device__ __forceinline__ void decide_rows(const float (&xv)[R][kQCols], const 
     // Y = P_c 2^16 + (0xFFFF - H) - 2, with the bias of 128's bits folded in
     constexpr uint32_t kBias = 0xFFFFu - 0x43000000u - 2u;
     uint32_t worst = dc.fast ? 0u : 0xFFFFu;  // largest (Y & 0xFFFF) of the batch
+    bool anybig = false;
+    uint32_t pbs[R][kQCols];
 #pragma unroll
     for (int u = 0; u < R; ++u) {
 #pragma unroll
@@ -569,13 +602,30 @@ __device__ __forceinline__ void decide_rows(const float (&xv)[R][kQCols], const 
             if (SCHEME == kLinear) {
                 pb = min(__float_as_uint(ax * dc.c1 + 128.0f), dc.clampb);
             } else {
-                const uint32_t vb = min(__float_as_uint(ax * dc.rcp), 0x3F800000u);
-                const uint32_t pbig = (vb >> 7) + dc.cbig;
-                const uint32_t psmall = __float_as_uint(ax * dc.c1 + 128.0f);
-                pb = (vb >= dc.bigmin) ? pbig : psmall;
+                // below 2^-(s-1) (P < 1, the common case under l2 norms): P read as for L;
+                // at or above it the binade form is computed for the row (see below)
+                pb = __float_as_uint(ax * dc.c1 + 128.0f);
+                anybig |= pb >= 0x43010000u;  // P_c >= 1
             }
             if (!TRUSTED && !(ax == ax)) worst = 0xFFFFu;  // NaN: decided on the exact path
-            const uint32_t y = pb - half16(aw[u], c) + kBias;
+            pbs[u][c] = pb;
+        }
+    }
+    if (SCHEME == kExp && anybig) {
+        // v_c >= 2^-(s-1): (bits of v_c) >> 7 is (biased exponent, 16 fraction bits)
+#pragma unroll
+        for (int u = 0; u < R; ++u)
+#pragma unroll
+            for (int c = 0; c < kQCols; ++c) {
+                const uint32_t vb = min(__float_as_uint(fabsf(xv[u][c]) * dc.rcp), 0x3F800000u);
+                if (vb >= dc.bigmin) pbs[u][c] = (vb >> 7) + dc.cbig;
+            }
+    }
+#pragma unroll
+    for (int u = 0; u < R; ++u) {
+#pragma unroll
+        for (int c = 0; c < kQCols; ++c) {
+            const uint32_t y = pbs[u][c] - half16(aw[u], c) + kBias;
             k[u][c] = y >> 16;
             worst = max(worst, y & 0xFFFFu);
         }
