@@ -8,6 +8,6 @@ streams only.  There is no CPU fallback: importing the package without a built l
 """
 from ._binding import (  # noqa: F401
     BF16, EXP, F32, LINEAR, NORM_INF, NORM_L2, GQError, gq_abi_version, gq_allreduce_mean,
-    gq_allreduce_mean_with_norm, gq_code_bits, gq_code_bytes, gq_code_pitch, gq_dequantize,
+    gq_allreduce_mean_noalloc, gq_allreduce_mean_with_norm, gq_code_bits, gq_code_bytes, gq_code_pitch, gq_dequantize,
     gq_get_status, gq_global_norm, gq_philox4x32_10, gq_quantize, gq_reduce_codes,
     gq_status_string, gq_workspace, gq_workspace_bytes, lib, library_path)

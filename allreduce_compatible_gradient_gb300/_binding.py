@@ -47,6 +47,8 @@ def lib() -> ctypes.CDLL:
         "gq_allreduce_mean": (ci, [vp, ci, i64, i64, ci, ci, ci, ci, u64, u64, vp, vp, vp, vp, sz,
                                    vp]),
         "gq_allreduce_mean_with_norm": (ci, [vp, ci, i64, i64, vp, ci, ci, u64, u64, vp, vp, vp]),
+        "gq_allreduce_mean_noalloc": (ci, [vp, ci, i64, i64, ci, ci, ci, ci, u64, u64, vp, vp, vp,
+                                           vp]),
         "gq_philox4x32_10": (ci, [vp, vp, i64, vp]),
         "gq_get_status": (ci, [vp, vp]),
         "gq_status_string": (ctypes.c_char_p, [ci]),
@@ -184,6 +186,17 @@ def gq_allreduce_mean_with_norm(grads, norm, scheme, s, seed, step, out=None, co
     _check(lib().gq_allreduce_mean_with_norm(_p(grads), dt, n, d, _p(norm), scheme, s, seed, step,
                                              _p(out), _p(codes), _stream(stream)),
            "gq_allreduce_mean_with_norm")
+    return out
+
+
+def gq_allreduce_mean_noalloc(grads, q, p, scheme, s, seed, step, out, norm=None, codes=None,
+                              stream=None) -> torch.Tensor:
+    """gq_allreduce_mean for callers that cannot allocate: the library uses its own fixed device
+    scratch instead of a workspace, so `out` (and `norm` / `codes` when wanted) must be passed in."""
+    dt, n, d = _grads(grads)
+    _check(lib().gq_allreduce_mean_noalloc(_p(grads), dt, n, d, q, p, scheme, s, seed, step,
+                                           _p(out), _p(norm), _p(codes), _stream(stream)),
+           "gq_allreduce_mean_noalloc")
     return out
 
 

@@ -373,3 +373,88 @@ const char* gq_status_string(int status) {
 }
 
 }  // extern "C"
+
+// ---- allocation-free variant of gq_allreduce_mean ------------------------------------------
+// Some callers cannot allocate device memory at the point where they need the allreduce: code
+// that runs inside a framework's caching allocator or communication hook (where re-entering
+// the allocator is not allowed), or a process whose device memory is fully planned ahead.
+// This entry point takes the norm step's scratch (status word, completion ticket, norm and the
+// per-block partials) from a fixed array in the library's own device memory instead of a
+// caller-provided workspace.
+namespace {
+
+constexpr int kNoAllocPartials = 1024;  // block partials the fixed scratch holds
+constexpr size_t kNoAllocScratchBytes =
+    static_cast<size_t>(gq::kHeaderBytes) + sizeof(uint64_t) * kNoAllocPartials;  // 8,448 B
+
+// Every GPU that loads the library holds this array until the process exits.  In host code the
+// name is only a host-side stand-in: its device address comes from cudaGetSymbolAddress.
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+
+// Device address of the fixed scratch on the current device, looked up once per device.
+gq_status noalloc_scratch(unsigned char** out) {
+    static void* addr[kMaxDevices] = {nullptr};
+    static std::mutex mu;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return GQ_ERR_CUDA;
+    std::lock_guard<std::mutex> lock(mu);
+    if (addr[dev] == nullptr) {
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr)
+            return GQ_ERR_CUDA;
+        addr[dev] = p;
+    }
+    *out = static_cast<unsigned char*>(addr[dev]);
+    return GQ_OK;
+}
+
+// Blocks the norm step launches for this problem (the same rule as gq_global_norm).
+template <typename T, int MODE>
+int64_t norm_blocks(int64_t d) {
+    constexpr int C = gq::Elem<T>::kCols;
+    return grid_for(gq::norm_kernel<T, MODE>, (d + C - 1) / C, gq::kMaxPartials);
+}
+
+int64_t norm_blocks_any(int dtype, int mode, int64_t d) {
+    if (dtype == GQ_F32) {
+        switch (mode) {
+            case gq::kMaxMax: return norm_blocks<float, gq::kMaxMax>(d);
+            case gq::kL2L2: return norm_blocks<float, gq::kL2L2>(d);
+            case gq::kL2Max: return norm_blocks<float, gq::kL2Max>(d);
+            default: return norm_blocks<float, gq::kMaxL2>(d);
+        }
+    }
+    switch (mode) {
+        case gq::kMaxMax: return norm_blocks<uint16_t, gq::kMaxMax>(d);
+        case gq::kL2L2: return norm_blocks<uint16_t, gq::kL2L2>(d);
+        case gq::kL2Max: return norm_blocks<uint16_t, gq::kL2Max>(d);
+        default: return norm_blocks<uint16_t, gq::kMaxL2>(d);
+    }
+}
+
+}  // namespace
+
+extern "C" gq_status gq_allreduce_mean_noalloc(const void* grads, int dtype, int64_t n, int64_t d,
+                                               int q, int p, int scheme, int s, uint64_t seed,
+                                               uint64_t step, float* out_dev, float* norm_dev,
+                                               void* codes, void* stream) {
+    gq_status st = check_grads(grads, dtype, n, d);
+    if (st != GQ_OK) return st;
+    const int mode = norm_mode(q, p);
+    if (mode < 0) return GQ_ERR_INVALID;
+    if ((st = check_scheme(scheme, s, n)) != GQ_OK) return st;
+    if (!out_dev || !aligned16(out_dev) || (codes && !aligned16(codes))) return GQ_ERR_INVALID;
+    // the fixed scratch holds kNoAllocPartials block partials: refuse a launch that needs more
+    if (norm_blocks_any(dtype, mode, d) > kNoAllocPartials) return GQ_ERR_WORKSPACE;
+    unsigned char* ws = nullptr;
+    if ((st = noalloc_scratch(&ws)) != GQ_OK) return st;
+    cudaStream_t cs = static_cast<cudaStream_t>(stream);
+    // the array keeps the previous call's contents: the status word and the completion ticket
+    // must start at zero
+    if (cudaMemsetAsync(ws, 0, gq::kHeaderBytes, cs) != cudaSuccess) return GQ_ERR_CUDA;
+    if ((st = norm_any(grads, dtype, mode, n, d, norm_dev, ws, cs)) != GQ_OK) return st;
+    const float* ws_norm = &reinterpret_cast<const gq::WsHeader*>(ws)->norm;
+    const gq::QuantArgs a = make_args(ws_norm, dtype, n, d, s, seed, step);
+    return quant_any<true, true>(grads, dtype, a, scheme, gq_code_bits(scheme, s), codes, out_dev,
+                                 cs);
+}

@@ -156,6 +156,29 @@ gq_status gq_allreduce_mean_with_norm(const void *grads, int dtype, int64_t n, i
                                       uint64_t step, float *out_dev, void *codes, void *stream);
 
 /*
+ * gq_allreduce_mean without a workspace argument, for callers that cannot allocate device
+ * memory where they need the allreduce (for example code running inside a framework's caching
+ * allocator or communication hook, which may not call back into the allocator, or a process
+ * whose device memory is planned in full ahead of time).  The paper has no counterpart to this
+ * call; it exists for those callers only.
+ *
+ * Same arguments and results as gq_allreduce_mean minus ws / ws_bytes.  The norm step's scratch
+ * (status word, completion ticket, norm and up to 1,024 per-block partials: 8,448 bytes) lives
+ * in a fixed array in the library's device memory, which every GPU that loads the library holds
+ * until the process exits.  Nothing is allocated: no cudaMalloc, cudaFree or allocating library
+ * call.  The first call on a device looks up that array's device address (cudaGetSymbolAddress)
+ * with the device current; make that first call before any stream capture.  A problem whose norm
+ * step would launch more than 1,024 blocks is refused with GQ_ERR_WORKSPACE (on GB300 the norm
+ * step launches at most 608).  Every call shares the one array: each call clears its status word
+ * and ticket first, and calls that overlap on the GPU (other streams, other host threads) race,
+ * so serialise them.  A non-finite norm gives all-zero outputs; there is no status word to read,
+ * so test the norm written to norm_dev (nullable) instead.
+ */
+gq_status gq_allreduce_mean_noalloc(const void *grads, int dtype, int64_t n, int64_t d, int q,
+                                    int p, int scheme, int s, uint64_t seed, uint64_t step,
+                                    float *out_dev, float *norm_dev, void *codes, void *stream);
+
+/*
  * Philox4x32-10 on the device, for checking the random stream: `count` calls, input
  * ctr_key[6*c .. 6*c+5] = counter words 0..3 then key words 0..1, output out[4*c .. 4*c+3].
  */
