@@ -16,7 +16,7 @@ namespace {
 
 using gq::kThreads;
 
-constexpr int64_t kMaxD = int64_t(1) << 34;  // Philox counter word 0 holds j / 4 in 32 bits
+constexpr int64_t kMaxD = int64_t(1) << 34;  // Philox counter word 0 holds j / 8 in 31 bits
 constexpr int kMaxDevices = 64;
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }

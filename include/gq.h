@@ -21,9 +21,11 @@
  *        out_j = N * S_j / (n * s)            (Global-L_s)
  *        out_j = N * S_j * 2^-(s-1) / n       (Global-E_s)
  *      (implementation paragraph: quantisation, allreduce, dequantisation).
- * Round up iff r < T, where r is word (j mod 4) of Philox4x32-10 (Salmon et al., SC'11) at
- * counter (j / 4, i, low 32 bits of step, high 32 bits of step) and key (low, high 32 bits of
- * seed), and T = floor(P(up) * 2^32) is computed exactly from v.
+ * Round up iff r < T, where T = floor(P(up) * 2^32) is computed exactly from v and r is a
+ * uniform 32-bit word from Philox4x32-10 (Salmon et al., SC'11) with key (low, high 32 bits of
+ * seed): its high 16 bits are half (j mod 8) of the call at counter (j / 8, i, low 32 bits of
+ * step, high 32 bits of step), its low 16 bits half (j mod 8) of the call at counter
+ * (2^31 + j / 8, i, step); half h is the low half of word h/2 for even h, the high half for odd h.
  *
  * Conventions for every call:
  *   - All buffers are caller-owned device memory (grads, codes, sums, out, norm, ws), 16-byte
@@ -34,7 +36,7 @@
  *     workspaces.
  *   - Device-detected conditions (a non-finite norm) are recorded in the workspace status word
  *     and read with gq_get_status.  On a non-finite norm every output is written as zeros.
- *   - Sizes: n >= 1, 1 <= d < 2^34 (the Philox counter holds j / 4 in 32 bits), n < 2^31.
+ *   - Sizes: n >= 1, 1 <= d < 2^34 (the Philox counter holds j / 8 in 31 bits), n < 2^31.
  *   - Codes: int8 when the code needs more than 4 bits (s > 7), else int4 (two's-complement
  *     nibbles, element 2m in the low nibble of byte m).  Code rows have a pitch of
  *     gq_code_pitch(d) = round_up(d, 32) elements; padding codes are written as 0.
