@@ -40,8 +40,8 @@ FALLBACK_HBM_GBS = 6800.0
 def _args():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
-    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--config", default="resnet50_n8")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-e2e", action="store_true")
@@ -84,9 +84,10 @@ def _ncu_traffic(key: str):
 
 
 class ClockSampler:
-    """nvidia-smi clocks and throttle reasons sampled every 200 ms during the timed region."""
+    """nvidia-smi clocks and throttle reasons, sampled every 50 ms; only the samples whose
+    timestamps fall inside the timed window are reported."""
 
-    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
@@ -95,26 +96,32 @@ class ClockSampler:
         self.proc = None
         self.lines = []
         self.thread = None
+        self.t0 = self.t1 = None
 
     def start(self):
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.gpu), "--query-gpu=" + self.FIELDS,
-                 "--format=csv,noheader,nounits", "-lms", "200"],
+                 "--format=csv,noheader,nounits", "-lms", "50"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except OSError:
             self.proc = None
             return
         self.thread = threading.Thread(target=self._read, daemon=True)
         self.thread.start()
+        time.sleep(0.5)  # let the first samples arrive before the timed window opens
 
     def _read(self):
         for line in self.proc.stdout:
-            self.lines.append(line.strip())
+            self.lines.append((time.time(), line.strip()))
+
+    def window(self, t0, t1):
+        self.t0, self.t1 = t0, t1
 
     def stop(self):
         if self.proc is None:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.2)
         self.proc.terminate()
         try:
             self.proc.wait(timeout=5)
@@ -122,22 +129,27 @@ class ClockSampler:
             self.proc.kill()
         if self.thread:
             self.thread.join(timeout=2)
-        sm, smax, reasons = [], [], set()
+        sm, smax, power, reasons = [], [], [], set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for ln in self.lines:
+        # a sample read at host time t describes the GPU up to ~50 ms before t
+        for t, ln in self.lines:
+            if self.t0 is not None and not (self.t0 <= t <= self.t1 + 0.06):
+                continue
             parts = [p.strip() for p in ln.split(",")]
-            if len(parts) < 9:
+            if len(parts) < 10:
                 continue
             try:
-                sm.append(float(parts[1]))
-                smax.append(float(parts[2]))
+                sm.append(float(parts[2]))
+                smax.append(float(parts[3]))
+                power.append(float(parts[4]))
             except ValueError:
                 continue
-            for name, val in zip(names, parts[5:9]):
+            for name, val in zip(names, parts[6:10]):
                 if val.lower() == "active":
                     reasons.add(name)
         return {"sm_mhz": statistics.median(sm) if sm else None,
                 "sm_max_mhz": max(smax) if smax else None,
+                "power_w_max": max(power) if power else None,
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
@@ -271,6 +283,8 @@ def main():
     def step(k):
         gq.gq_allreduce_mean(x, q, p, sc, s, seed, k, out=out, norm=norm, ws=ws, stream=stream)
 
+    clocks = ClockSampler(local)
+    clocks.start()
     for k in range(a.warmup):
         step(k)
     torch.cuda.synchronize()
@@ -280,17 +294,18 @@ def main():
     # --- timed: the public fused call ---------------------------------------------------------
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
           for _ in range(a.steps)]
-    clocks = ClockSampler(local)
-    clocks.start()
     _barrier(world)
     torch.cuda.synchronize()
+    t_open = time.time()
     for k in range(a.steps):
         flush_l2()
         ev[k][0].record(stream)
         step(a.warmup + k)
         ev[k][1].record(stream)
     torch.cuda.synchronize()
+    t_close = time.time()
     _barrier(world)
+    clocks.window(t_open, t_close)
     clk = clocks.stop()
     times = [e0.elapsed_time(e1) for e0, e1 in ev]
     total_ms = _max_over_ranks(sum(times), world)
@@ -308,7 +323,10 @@ def main():
         ev_k[k][2].record(stream)
     torch.cuda.synchronize()
     t_norm = statistics.mean(e[0].elapsed_time(e[1]) for e in ev_k)
-    t_quant = statistics.mean(e[1].elapsed_time(e[2]) for e in ev_k)
+    t_quant_split = statistics.mean(e[1].elapsed_time(e[2]) for e in ev_k)
+    # the fused call launches the same norm kernel and then its own quantise pass: that pass
+    # takes the step time minus the norm time (both measured above with events on the stream)
+    t_quant = max(ms_per_step - t_norm, 1e-6)
     peak, peak_kind = _peaks()
     kernels = {
         "norm": {"ms": t_norm, "bytes": in_bytes},
@@ -323,6 +341,7 @@ def main():
                 "peak_kind": peak_kind, "traffic": traffic,
                 "algorithmic_bytes_per_launch": dom["bytes"],
                 "kernels_ms": {k: round(v["ms"], 4) for k, v in kernels.items()},
+                "quantize_with_norm_entry_ms": round(t_quant_split, 4),
                 "whole_step_frac": round(2 * in_bytes / (ms_per_step * 1e-3) / 1e9 / peak, 4),
                 "whole_step_frac_of_8tbs": round(
                     (2 * in_bytes + 4 * d) / (ms_per_step * 1e-3) / 1e12 / 8.0, 4)}
