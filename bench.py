@@ -167,14 +167,23 @@ def _dist_init(nranks):
 
 
 def _max_over_ranks(value: float, world: int) -> float:
+    """The max of `value` over all ranks (a scalar collective on the timing, not on data)."""
     if world == 1:
         return value
     import torch
     import torch.distributed as dist
 
-    t = torch.tensor([value], dtype=torch.float64, device="cuda")
+    dev = "cpu" if dist.get_backend() == "gloo" else "cuda"
+    t = torch.tensor([value], dtype=torch.float64, device=dev)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
+
+
+def aggregate(per_rank_ms: float, bytes_per_rank: int, world: int) -> tuple:
+    """Whole-job throughput: every rank processed `bytes_per_rank`; the job took the slowest
+    rank's time.  Returns (ms per step, GB/s)."""
+    ms = _max_over_ranks(per_rank_ms, world)
+    return ms, world * bytes_per_rank / (ms * 1e-3) / 1e9
 
 
 def _barrier(world):
@@ -308,9 +317,7 @@ def main():
     clocks.window(t_open, t_close)
     clk = clocks.stop()
     times = [e0.elapsed_time(e1) for e0, e1 in ev]
-    total_ms = _max_over_ranks(sum(times), world)
-    ms_per_step = total_ms / a.steps
-    value = world * in_bytes / (ms_per_step * 1e-3) / 1e9
+    ms_per_step, value = aggregate(sum(times) / a.steps, in_bytes, world)
 
     # --- per-kernel durations (same two kernels, launched through the split entry points) -----
     ev_k = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(a.steps)]
