@@ -65,6 +65,61 @@ __device__ __forceinline__ uint4 philox4x32_10_rk(uint4 c, const uint32_t (&rk)[
     return c;
 }
 
+// The same call for counter (g, row, step_lo, step_hi) split into the part that depends on the
+// column group g only (computed once per group) and the rest (computed per row).  Rounds 1-3
+// partly depend on g or on row alone: round 1's products are M0 g and M1 step_lo; round 2's are
+// M0 (f(row)) and M1 (f(g)); round 3's first is M0 (f(g)).  Same outputs as philox4x32_10_rk.
+struct PhiloxGroup {
+    uint32_t lo0_1;   // round 1: low half of M0 g          (counter word 3 after round 1)
+    uint32_t y2;      // round 2: low half of M1 z1         (counter word 1 after round 2)
+    uint32_t z3k;     // round 3: high half of M0 x2, xor round-3 key word 1
+    uint32_t lo0_3;   // round 3: low half of M0 x2         (counter word 3 after round 3)
+};
+
+__device__ __forceinline__ void mulhilo(uint32_t m, uint32_t a, uint32_t& hi, uint32_t& lo) {
+    const uint64_t p = static_cast<uint64_t>(m) * a;
+    hi = static_cast<uint32_t>(p >> 32);
+    lo = static_cast<uint32_t>(p);
+}
+
+__device__ __forceinline__ PhiloxGroup philox_group(uint32_t g, uint32_t step_lo, uint32_t step_hi,
+                                                    const uint32_t (&rk)[20]) {
+    const uint32_t kMul0 = 0xD2511F53u, kMul1 = 0xCD9E8D57u;
+    PhiloxGroup pg;
+    uint32_t hi0, hi1s, lo1s, h, l;
+    mulhilo(kMul0, g, hi0, pg.lo0_1);           // round 1, word 0 = g
+    mulhilo(kMul1, step_lo, hi1s, lo1s);        // round 1, word 2 = step_lo
+    const uint32_t z1 = hi0 ^ step_hi ^ rk[1];  // round 1 output word 2
+    mulhilo(kMul1, z1, h, l);                   // round 2, word 2
+    pg.y2 = l;
+    const uint32_t x2 = h ^ lo1s ^ rk[2];       // round 2 output word 0 (round 1 word 1 = lo1s)
+    mulhilo(kMul0, x2, h, l);                   // round 3, word 0
+    pg.z3k = h ^ rk[5];
+    pg.lo0_3 = l;
+    return pg;
+}
+
+__device__ __forceinline__ uint4 philox_row(const PhiloxGroup& pg, uint32_t row, uint32_t step_lo,
+                                            const uint32_t (&rk)[20]) {
+    const uint32_t kMul0 = 0xD2511F53u, kMul1 = 0xCD9E8D57u;
+    uint32_t hi1s, lo1s;
+    mulhilo(kMul1, step_lo, hi1s, lo1s);        // round 1, word 2 (loop-invariant)
+    const uint32_t x1 = hi1s ^ row ^ rk[0];     // round 1 output word 0
+    uint32_t hi0, lo0;
+    mulhilo(kMul0, x1, hi0, lo0);               // round 2, word 0
+    const uint32_t z2 = hi0 ^ pg.lo0_1 ^ rk[3]; // round 2 output word 2 (round 1 word 3)
+    uint32_t hi1, lo1;
+    mulhilo(kMul1, z2, hi1, lo1);               // round 3, word 2
+    uint4 c = make_uint4(hi1 ^ pg.y2 ^ rk[4], lo1, pg.z3k ^ lo0, pg.lo0_3);  // round 3 output
+#pragma unroll
+    for (int round = 3; round < 10; ++round) {
+        mulhilo(kMul0, c.x, hi0, lo0);
+        mulhilo(kMul1, c.z, hi1, lo1);
+        c = make_uint4(hi1 ^ c.y ^ rk[2 * round], lo1, hi0 ^ c.w ^ rk[2 * round + 1], lo0);
+    }
+    return c;
+}
+
 // ------------------------------------------------------------------------------------------
 // Element access: a 16-byte column group of one row, widened to fp32.
 // ------------------------------------------------------------------------------------------
@@ -569,17 +624,6 @@ __device__ __forceinline__ Decide make_decide(float nrm, uint32_t s) {
     return dc;
 }
 
-// Philox words of R row-groups: call (g, row0 + u, step) for u < R.
-template <int R>
-__device__ __forceinline__ void philox_rows(const QuantArgs& a, uint32_t g32, uint32_t row0,
-                                            uint32_t (&aw)[R][4]) {
-#pragma unroll
-    for (int u = 0; u < R; ++u) {
-        const uint4 ra = philox4x32_10_rk(make_uint4(g32, row0 + u, a.step_lo, a.step_hi), a.rk);
-        aw[u][0] = ra.x; aw[u][1] = ra.y; aw[u][2] = ra.z; aw[u][3] = ra.w;
-    }
-}
-
 // Level indices k of the eight elements of R row-groups (rows row0 .. row0+R-1), given the
 // high-half Philox words aw of those rows; the rare exact path runs once for the batch if any
 // of its elements needs it.
@@ -600,11 +644,11 @@ __device__ __forceinline__ void decide_rows(const float (&xv)[R][kQCols], const 
             const float ax = fabsf(xv[u][c]);
             uint32_t pb;
             if (SCHEME == kLinear) {
-                pb = min(__float_as_uint(ax * dc.c1 + 128.0f), dc.clampb);
+                pb = min(__float_as_uint(__fmaf_rn(ax, dc.c1, 128.0f)), dc.clampb);
             } else {
                 // below 2^-(s-1) (P < 1, the common case under l2 norms): P read as for L;
                 // at or above it the binade form is computed for the row (see below)
-                pb = __float_as_uint(ax * dc.c1 + 128.0f);
+                pb = __float_as_uint(__fmaf_rn(ax, dc.c1, 128.0f));
                 anybig |= pb >= 0x43010000u;  // P_c >= 1
             }
             if (!TRUSTED && !(ax == ax)) worst = 0xFFFFu;  // NaN: decided on the exact path
@@ -672,16 +716,17 @@ __device__ __forceinline__ void accumulate_row(const float (&xv)[kQCols],
 }
 
 // Quantise column group g of all n rows with direct loads; accumulate the sums; optionally
-// store codes.  Two rows are loaded at a time; each row is decided on its own.
+// store codes.  Four rows are loaded at a time; each row is decided on its own.
 template <typename T, int SCHEME, int CODE_BITS, bool TRUSTED>
 __device__ __forceinline__ void quantize_group(const T* __restrict__ x, const QuantArgs& a,
                                                const Decide& dc, int64_t g,
                                                unsigned char* __restrict__ codes,
                                                float (&S)[kQCols]) {
-    constexpr int U = 2;  // rows loaded per batch
+    constexpr int U = 4;  // rows loaded per batch
 #pragma unroll
     for (int c = 0; c < kQCols; ++c) S[c] = 0.0f;
     const uint32_t g32 = static_cast<uint32_t>(g);
+    const PhiloxGroup pg = philox_group(g32, a.step_lo, a.step_hi, a.rk);
     for (int64_t i0 = 0; i0 < a.n; i0 += U) {
         float v[U][1][kQCols];
 #pragma unroll
@@ -691,8 +736,8 @@ __device__ __forceinline__ void quantize_group(const T* __restrict__ x, const Qu
         for (int u = 0; u < U; ++u) {
             if (i0 + u >= a.n) break;
             const uint32_t row = static_cast<uint32_t>(i0 + u);
-            uint32_t aw[1][4];
-            philox_rows<1>(a, g32, row, aw);
+            const uint4 ra = philox_row(pg, row, a.step_lo, a.rk);
+            const uint32_t aw[1][4] = {{ra.x, ra.y, ra.z, ra.w}};
             uint32_t k[1][kQCols];
             decide_rows<SCHEME, TRUSTED, 1>(v[u], dc, a, g32, row, aw, k);
             int32_t code[kQCols];
@@ -833,7 +878,14 @@ __device__ __forceinline__ void staged_groups(const T* __restrict__ x, const Qua
             }
         }
         uint32_t aw[R][4];
-        philox_rows<R>(a, g32, static_cast<uint32_t>(r * R), aw);
+        {
+            const PhiloxGroup pg = philox_group(g32, a.step_lo, a.step_hi, a.rk);
+#pragma unroll
+            for (int u = 0; u < R; ++u) {
+                const uint4 ra = philox_row(pg, static_cast<uint32_t>(r * R + u), a.step_lo, a.rk);
+                aw[u][0] = ra.x; aw[u][1] = ra.y; aw[u][2] = ra.z; aw[u][3] = ra.w;
+            }
+        }
         uint32_t k[R][kQCols];
         decide_rows<SCHEME, TRUSTED, R>(v, dc, a, g32, static_cast<uint32_t>(r * R), aw, k);
 #pragma unroll
@@ -859,7 +911,7 @@ __device__ __forceinline__ void staged_groups(const T* __restrict__ x, const Qua
 // pitch/8 when codes are written (padding columns get zero codes), from the last group to the
 // first: the fused path's norm pass ends on the last columns, which are still in L2.
 template <typename T, int SCHEME, int CODE_BITS, bool WRITE_OUT, bool TRUSTED>
-__global__ void __launch_bounds__(kThreads, sizeof(T) == 4 ? 3 : 2)
+__global__ void __launch_bounds__(kThreads, 2)
 quantize_kernel(const T* __restrict__ x, QuantArgs a, int64_t groups,
                 unsigned char* __restrict__ codes, float* __restrict__ out) {
     extern __shared__ uint4 stage[];
