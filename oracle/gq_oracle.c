@@ -30,6 +30,7 @@
  */
 #include <math.h>
 #include <stdint.h>
+#include <stdlib.h>
 #include <string.h>
 
 /* Return codes (same meanings as the library's status values; defined here independently). */
@@ -434,4 +435,169 @@ int gqo_allreduce_mean(const void *x, int dtype, int64_t n, int64_t d, int q, in
             return rc2;
     }
     return rc;
+}
+
+/* ------------------------------------------------------------------------------------------ */
+/* Global-E allreduce with re-rounding at every hop                                           */
+/* ------------------------------------------------------------------------------------------ */
+
+/*
+ * Global-QSGD's exponential dithering keeps the communicated data in the exponential code inside
+ * the allreduce: every reduction step decodes two partial sums, adds them and rounds the result
+ * at random back onto the grid, which adds variance ("extra variance due to stochastic rounding
+ * during AllReduce", the theta worked example; the implementation paragraph's custom reduction
+ * for exponential dithering; the performance model prefers the tree allreduce because it has
+ * fewer such steps).  The pages do not spell the step out.  Reading taken: a partial sum is
+ * kept in the same code, extended above level s (level index k stands for 2^(k-1) units of
+ * 2^-(s-1), k = 0 for 0, any k up to 127); the sum t of two decoded values is an exact integer
+ * number of units, and |t| > 0 is rounded between 2^e and 2^(e+1), e = floor(log2 |t|), up with
+ * probability (|t| - 2^e) / 2^e (exact, so the step is unbiased); the sign of t is kept.
+ */
+
+/* Value of an extended Global-E code in units of 2^-(s-1). */
+static int64_t exp_units(int c)
+{
+    int k = c < 0 ? -c : c;
+    int64_t u;
+    if (k == 0)
+        return 0;
+    u = (int64_t)1 << (k - 1);
+    return c < 0 ? -u : u;
+}
+
+/* Where |t| units sit on the extended exponential grid: *lo = level index of 2^e (e + 1),
+ * *T = floor(P(up) 2^32) with P(up) = (|t| - 2^e) / 2^e.  t = 0 gives lo = 0, T = 0. */
+int gqo_exp_split_units(int64_t t, int32_t *lo, uint32_t *T)
+{
+    int e = 0;
+    uint64_t a, frac;
+    if (lo == NULL || T == NULL)
+        return GQO_ERR_INVALID;
+    a = (uint64_t)(t < 0 ? -t : t);
+    if (a == 0) {
+        *lo = 0;
+        *T = 0;
+        return GQO_OK;
+    }
+    while (e < 63 && (a >> (e + 1)) != 0)
+        ++e;
+    frac = a - ((uint64_t)1 << e); /* the distance above the lower level, < 2^e */
+    *lo = e + 1;
+    if (e <= 32)
+        *T = (uint32_t)(frac << (32 - e)); /* exact: frac 2^(32 - e) < 2^32 */
+    else
+        *T = (uint32_t)(frac >> (e - 32));
+    return GQO_OK;
+}
+
+/* Re-round t units with the random word of (seed, step, stream, j): the signed code. */
+static int exp_reround(int64_t t, uint64_t seed, uint64_t step, int64_t stream_id, int64_t j)
+{
+    int32_t lo;
+    uint32_t T;
+    int k;
+    gqo_exp_split_units(t, &lo, &T);
+    k = lo + (gqo_philox_word(seed, step, stream_id, j) < T ? 1 : 0);
+    return t < 0 ? -k : k;
+}
+
+/* Random-stream identifiers of the reduction steps (counter word 1; worker indices are below
+ * 2^31): tree level l (1-based) combining into node m: 2^31 + l 2^24 + m; ring step h (1-based)
+ * of chunk c: 2^31 + 2^30 + h 2^12 + c. */
+int64_t gqo_exp_tree_stream(int l, int64_t m) { return (int64_t)0x80000000LL + ((int64_t)l << 24) + m; }
+int64_t gqo_exp_ring_stream(int64_t h, int64_t c) { return (int64_t)0xC0000000LL + (h << 12) + c; }
+
+/*
+ * One reduction step on w coordinates (the custom reduction of the pages' Global-E allreduce):
+ * out[j] = re-round(decode(a[j]) + decode(b[j])) with the random words of stream `stream_id` at
+ * coordinates j0 + j.  Codes are signed level indices (|k| <= 127).
+ */
+int gqo_exp_combine(const int8_t *a, const int8_t *b, int64_t w, int64_t j0, uint64_t seed,
+                    uint64_t step, int64_t stream_id, int8_t *out)
+{
+    int64_t j;
+    if (a == NULL || b == NULL || out == NULL || w < 0 || j0 < 0)
+        return GQO_ERR_INVALID;
+    for (j = 0; j < w; ++j) {
+        int64_t t = exp_units(a[j]) + exp_units(b[j]);
+        int c = exp_reround(t, seed, step, stream_id, j0 + j);
+        if (c > 127 || c < -127)
+            return GQO_ERR_UNSUPPORTED;
+        out[j] = (int8_t)c;
+    }
+    return GQO_OK;
+}
+
+/*
+ * Tree allreduce of n code rows (n x w, worker-major) with a re-rounding at every step (the
+ * pages' tree: reduce recursively, then a recursive-doubling allgather that only copies).
+ * Level l = 1, 2, ...: row i (a multiple of 2^l) takes re-round(row i + row i + 2^(l-1)) when
+ * that partner exists, else it is kept.  root receives row 0 (w codes).  1 <= n <= 4096.
+ */
+int gqo_exp_tree_allreduce(const int8_t *codes, int64_t n, int64_t w, int64_t j0, uint64_t seed,
+                           uint64_t step, int8_t *root)
+{
+    int64_t i, j;
+    int l;
+    int64_t *u;
+    if (codes == NULL || root == NULL || n < 1 || n > 4096 || w < 0 || j0 < 0)
+        return GQO_ERR_INVALID;
+    u = (int64_t *)malloc(sizeof(int64_t) * (size_t)n);
+    if (u == NULL)
+        return GQO_ERR_INVALID;
+    for (j = 0; j < w; ++j) {
+        int8_t c0 = codes[j];
+        for (i = 0; i < n; ++i)
+            u[i] = exp_units(codes[i * w + j]);
+        for (l = 1; ((int64_t)1 << (l - 1)) < n; ++l) {
+            int64_t half = (int64_t)1 << (l - 1), stride = (int64_t)1 << l;
+            for (i = 0; i + half < n; i += stride) {
+                int c = exp_reround(u[i] + u[i + half], seed, step,
+                                    gqo_exp_tree_stream(l, i >> l), j0 + j);
+                u[i] = exp_units(c);
+                if (c > 127 || c < -127) {
+                    free(u);
+                    return GQO_ERR_UNSUPPORTED;
+                }
+            }
+        }
+        /* the root's code: u[0] is a single level (or the untouched code when n = 1) */
+        if (n == 1) {
+            root[j] = c0;
+        } else {
+            int32_t lo;
+            uint32_t T;
+            gqo_exp_split_units(u[0], &lo, &T); /* exact level: T = 0 */
+            root[j] = (int8_t)(u[0] < 0 ? -lo : lo);
+        }
+    }
+    free(u);
+    return GQO_OK;
+}
+
+/*
+ * Ring allreduce of n code rows over d coordinates (the window [j0, j0 + w)): the coordinates
+ * are split into n chunks of ceil(d / n); chunk c is accumulated starting from worker c + 1 and
+ * visits workers c + 2, ..., c (indices mod n), re-rounding after every step h = 1..n-1 (the
+ * reduce-scatter; the allgather only copies).  root receives the reduced codes.
+ */
+int gqo_exp_ring_allreduce(const int8_t *codes, int64_t n, int64_t d, int64_t w, int64_t j0,
+                           uint64_t seed, uint64_t step, int8_t *root)
+{
+    int64_t j, h, chunk;
+    if (codes == NULL || root == NULL || n < 1 || n > 4096 || w < 0 || j0 < 0 || j0 + w > d)
+        return GQO_ERR_INVALID;
+    chunk = (d + n - 1) / n;
+    for (j = 0; j < w; ++j) {
+        int64_t c = (j0 + j) / chunk;
+        int code = codes[((c + 1) % n) * w + j];
+        for (h = 1; h < n; ++h) {
+            int64_t t = exp_units(code) + exp_units(codes[((c + 1 + h) % n) * w + j]);
+            code = exp_reround(t, seed, step, gqo_exp_ring_stream(h, c), j0 + j);
+            if (code > 127 || code < -127)
+                return GQO_ERR_UNSUPPORTED;
+        }
+        root[j] = (int8_t)code;
+    }
+    return GQO_OK;
 }

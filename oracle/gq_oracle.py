@@ -74,6 +74,18 @@ def lib() -> ctypes.CDLL:
                                          ctypes.POINTER(ctypes.c_double),
                                          ctypes.POINTER(ctypes.c_float), vp, vp, vp]
         L.gqo_allreduce_mean.restype = ctypes.c_int
+        L.gqo_exp_split_units.argtypes = [i64, ctypes.POINTER(i32), ctypes.POINTER(u32)]
+        L.gqo_exp_split_units.restype = ctypes.c_int
+        L.gqo_exp_tree_stream.argtypes = [ctypes.c_int, i64]
+        L.gqo_exp_tree_stream.restype = i64
+        L.gqo_exp_ring_stream.argtypes = [i64, i64]
+        L.gqo_exp_ring_stream.restype = i64
+        L.gqo_exp_combine.argtypes = [vp, vp, i64, i64, u64, u64, i64, vp]
+        L.gqo_exp_combine.restype = ctypes.c_int
+        L.gqo_exp_tree_allreduce.argtypes = [vp, i64, i64, i64, u64, u64, vp]
+        L.gqo_exp_tree_allreduce.restype = ctypes.c_int
+        L.gqo_exp_ring_allreduce.argtypes = [vp, i64, i64, i64, i64, u64, u64, vp]
+        L.gqo_exp_ring_allreduce.restype = ctypes.c_int
         _lib = L
     return _lib
 
@@ -168,3 +180,60 @@ def allreduce_mean(x: np.ndarray, q: int, p: int, scheme: int, s: int, seed: int
                                   sums.ctypes.data, out.ctypes.data)
     return {"norm64": n64.value, "norm32": np.float32(n32.value), "codes": codes, "sums": sums,
             "out": out, "rc": rc}
+
+
+# ---- Global-E allreduce with re-rounding at every hop ------------------------------------------
+
+def exp_units(codes) -> np.ndarray:
+    """Value of extended Global-E codes in units of 2^-(s-1): sign * 2^(|k|-1), 0 for k = 0."""
+    c = np.asarray(codes, dtype=np.int64)
+    k = np.abs(c)
+    u = np.where(k > 0, np.left_shift(np.int64(1), np.maximum(k - 1, 0)), 0)
+    return np.sign(c) * u
+
+
+def exp_split_units(t: int):
+    lo = ctypes.c_int32()
+    T = ctypes.c_uint32()
+    lib().gqo_exp_split_units(int(t), ctypes.byref(lo), ctypes.byref(T))
+    return int(lo.value), int(T.value)
+
+
+def exp_tree_stream(level: int, m: int) -> int:
+    return int(lib().gqo_exp_tree_stream(level, m))
+
+
+def exp_ring_stream(h: int, c: int) -> int:
+    return int(lib().gqo_exp_ring_stream(h, c))
+
+
+def exp_combine(a, b, seed: int, step: int, stream_id: int, j0: int = 0) -> np.ndarray:
+    a = np.ascontiguousarray(a, dtype=np.int8)
+    b = np.ascontiguousarray(b, dtype=np.int8)
+    out = np.zeros(a.shape[0], dtype=np.int8)
+    rc = lib().gqo_exp_combine(a.ctypes.data, b.ctypes.data, a.shape[0], j0, seed, step,
+                               stream_id, out.ctypes.data)
+    if rc != OK:
+        raise ValueError("gqo_exp_combine returned %d" % rc)
+    return out
+
+
+def exp_tree_allreduce(codes, seed: int, step: int, j0: int = 0) -> np.ndarray:
+    codes = np.ascontiguousarray(codes, dtype=np.int8)
+    n, w = codes.shape
+    root = np.zeros(w, dtype=np.int8)
+    rc = lib().gqo_exp_tree_allreduce(codes.ctypes.data, n, w, j0, seed, step, root.ctypes.data)
+    if rc != OK:
+        raise ValueError("gqo_exp_tree_allreduce returned %d" % rc)
+    return root
+
+
+def exp_ring_allreduce(codes, d: int, seed: int, step: int, j0: int = 0) -> np.ndarray:
+    codes = np.ascontiguousarray(codes, dtype=np.int8)
+    n, w = codes.shape
+    root = np.zeros(w, dtype=np.int8)
+    rc = lib().gqo_exp_ring_allreduce(codes.ctypes.data, n, d, w, j0, seed, step,
+                                      root.ctypes.data)
+    if rc != OK:
+        raise ValueError("gqo_exp_ring_allreduce returned %d" % rc)
+    return root

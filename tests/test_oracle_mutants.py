@@ -39,6 +39,14 @@ MUTANTS = [
      "double v = (double)load_x(x, dtype, (i * d + j) % n * d + (i * d + j) / n);"),
     ("q=2 inner sqrt dropped", "        if (q == 2)\n            inner = sqrt(inner);", ""),
     ("bf16 widened wrong", "<< 16;", "<< 8;"),
+    ("re-round probability over the wrong gap", "*T = (uint32_t)(frac << (32 - e));",
+     "*T = (uint32_t)(frac << (31 - e));"),
+    ("re-round level off by one", "    *lo = e + 1;\n", "    *lo = e;\n"),
+    ("re-round drops the sign", "    return t < 0 ? -k : k;\n}", "    return k;\n}"),
+    ("tree stream ignores the level", "return (int64_t)0x80000000LL + ((int64_t)l << 24) + m;",
+     "return (int64_t)0x80000000LL + m;"),
+    ("ring starts at worker c", "int code = codes[((c + 1) % n) * w + j];",
+     "int code = codes[(c % n) * w + j];"),
 ]
 
 
@@ -53,7 +61,8 @@ def test_pins_catch_mutant(tmp_path, name, old, new):
                     str(so), str(mutant_c), "-lm"], check=True)
     env = dict(os.environ, GQ_ORACLE_LIB=str(so))
     pins = [os.path.join(ROOT, "tests", f) for f in
-            ("test_oracle_philox.py", "test_oracle_norm.py", "test_oracle_quantize.py")]
+            ("test_oracle_philox.py", "test_oracle_norm.py", "test_oracle_quantize.py",
+             "test_oracle_exp_allreduce.py")]
     r = subprocess.run([sys.executable, "-m", "pytest", "-x", "-q", "-p", "no:cacheprovider",
                         *pins], cwd=ROOT, env=env, capture_output=True, text=True, timeout=600)
     assert r.returncode != 0, "pins did not catch mutant %r" % name
