@@ -14,6 +14,7 @@ _LIB_PATH = os.path.join(_PKG, "libgq.so")
 F32, BF16 = 0, 1
 LINEAR, EXP = 0, 1
 NORM_INF, NORM_L2 = 0, 2
+ORDER_TREE, ORDER_RING = 0, 1
 
 _lib = None
 
@@ -50,6 +51,10 @@ def lib() -> ctypes.CDLL:
         "gq_allreduce_mean_noalloc": (ci, [vp, ci, i64, i64, ci, ci, ci, ci, u64, u64, vp, vp, vp,
                                            vp]),
         "gq_philox4x32_10": (ci, [vp, vp, i64, vp]),
+        "gq_exp_tree_stream": (ctypes.c_uint32, [ci, i64]),
+        "gq_exp_ring_stream": (ctypes.c_uint32, [i64, i64]),
+        "gq_exp_combine": (ci, [vp, vp, i64, u64, u64, ctypes.c_uint32, vp, vp]),
+        "gq_exp_allreduce": (ci, [vp, ci, i64, i64, ci, vp, u64, u64, vp, vp, vp]),
         "gq_get_status": (ci, [vp, vp]),
         "gq_status_string": (ctypes.c_char_p, [ci]),
     }
@@ -212,3 +217,33 @@ def gq_philox4x32_10(ctr_key, out=None, stream=None) -> torch.Tensor:
 
 def gq_get_status(ws, stream=None) -> int:
     return lib().gq_get_status(_p(ws), _stream(stream))
+
+
+# ---- Global-E allreduce with re-rounding at every hop ------------------------------------------
+
+def gq_exp_tree_stream(level: int, m: int) -> int:
+    return int(lib().gq_exp_tree_stream(level, m))
+
+
+def gq_exp_ring_stream(h: int, c: int) -> int:
+    return int(lib().gq_exp_ring_stream(h, c))
+
+
+def gq_exp_combine(a, b, seed, step, stream_id, out=None, stream=None) -> torch.Tensor:
+    """One reduction step of the Global-E allreduce on int8 code vectors a, b."""
+    d = a.numel()
+    if out is None:
+        out = torch.empty(d, dtype=torch.int8, device=a.device)
+    _check(lib().gq_exp_combine(_p(a), _p(b), d, seed, step, stream_id, _p(out), _stream(stream)),
+           "gq_exp_combine")
+    return out
+
+
+def gq_exp_allreduce(codes, s, n, d, order, norm, seed, step, out=None, root_codes=None,
+                     stream=None) -> torch.Tensor:
+    """Tree or ring Global-E allreduce of gq_quantize's code matrix, dequantised to out."""
+    if out is None:
+        out = torch.empty(d, dtype=torch.float32, device=codes.device)
+    _check(lib().gq_exp_allreduce(_p(codes), s, n, d, order, _p(norm), seed, step, _p(out),
+                                  _p(root_codes), _stream(stream)), "gq_exp_allreduce")
+    return out

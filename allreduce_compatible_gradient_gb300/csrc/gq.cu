@@ -458,3 +458,69 @@ extern "C" gq_status gq_allreduce_mean_noalloc(const void* grads, int dtype, int
     return quant_any<true, true>(grads, dtype, a, scheme, gq_code_bits(scheme, s), codes, out_dev,
                                  cs);
 }
+
+// ---- Global-E allreduce with re-rounding at every hop --------------------------------------
+namespace {
+
+gq::ExpArgs make_exp_args(uint64_t seed, uint64_t step) {
+    gq::ExpArgs ea;
+    const uint32_t k0 = static_cast<uint32_t>(seed), k1 = static_cast<uint32_t>(seed >> 32);
+    for (int r = 0; r < 10; ++r) {  // Philox round keys: the key advanced by r Weyl steps
+        ea.rk[2 * r] = k0 + static_cast<uint32_t>(r) * 0x9E3779B9u;
+        ea.rk[2 * r + 1] = k1 + static_cast<uint32_t>(r) * 0xBB67AE85u;
+    }
+    ea.step_lo = static_cast<uint32_t>(step);
+    ea.step_hi = static_cast<uint32_t>(step >> 32);
+    return ea;
+}
+
+}  // namespace
+
+extern "C" uint32_t gq_exp_tree_stream(int level, int64_t m) {
+    return 0x80000000u + (static_cast<uint32_t>(level) << 24) + static_cast<uint32_t>(m);
+}
+
+extern "C" uint32_t gq_exp_ring_stream(int64_t h, int64_t c) {
+    return 0xC0000000u + (static_cast<uint32_t>(h) << 12) + static_cast<uint32_t>(c);
+}
+
+extern "C" gq_status gq_exp_combine(const int8_t* a, const int8_t* b, int64_t d, uint64_t seed,
+                                    uint64_t step, uint32_t stream_id, int8_t* out, void* stream) {
+    if (!a || !b || !out || !aligned16(a) || !aligned16(b) || !aligned16(out)) return GQ_ERR_INVALID;
+    if (d < 1 || d >= kMaxD) return GQ_ERR_INVALID;
+    auto k = gq::exp_combine_kernel;
+    const int64_t chunks = (d + 15) / 16;
+    k<<<grid_for(k, chunks), kThreads, 0, static_cast<cudaStream_t>(stream)>>>(
+        a, b, d, stream_id, make_exp_args(seed, step), out);
+    return launch_status();
+}
+
+extern "C" gq_status gq_exp_allreduce(const void* codes, int s, int64_t n, int64_t d, int order,
+                                      const float* norm_dev, uint64_t seed, uint64_t step,
+                                      float* out_dev, int8_t* root_codes, void* stream) {
+    if (!codes || !norm_dev || !out_dev || !aligned16(codes) || !aligned16(out_dev))
+        return GQ_ERR_INVALID;
+    if (n < 1 || n > gq::kExpMaxWorkers || d < 1 || d >= kMaxD) return GQ_ERR_INVALID;
+    if (order != GQ_ORDER_TREE && order != GQ_ORDER_RING) return GQ_ERR_INVALID;
+    gq_status st = check_scheme(GQ_EXP, s, n);
+    if (st != GQ_OK) return st;
+    const int bits = gq_code_bits(GQ_EXP, s);
+    const int64_t pitch = gq_code_pitch(d);
+    const gq::ExpArgs ea = make_exp_args(seed, step);
+    const unsigned char* c = static_cast<const unsigned char*>(codes);
+    cudaStream_t cs = static_cast<cudaStream_t>(stream);
+    const uint32_t su = static_cast<uint32_t>(s);
+#define GQ_EXP_ALLREDUCE(ORD, BITS)                                                            \
+    do {                                                                                       \
+        auto k = gq::exp_allreduce_kernel<ORD, BITS>;                                          \
+        k<<<grid_for(k, d), kThreads, 0, cs>>>(c, n, d, pitch, ea, norm_dev, su, out_dev,      \
+                                               root_codes);                                    \
+    } while (0)
+    if (order == GQ_ORDER_TREE) {
+        if (bits == 4) GQ_EXP_ALLREDUCE(0, 4); else GQ_EXP_ALLREDUCE(0, 8);
+    } else {
+        if (bits == 4) GQ_EXP_ALLREDUCE(1, 4); else GQ_EXP_ALLREDUCE(1, 8);
+    }
+#undef GQ_EXP_ALLREDUCE
+    return launch_status();
+}

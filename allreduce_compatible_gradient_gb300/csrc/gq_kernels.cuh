@@ -1044,3 +1044,202 @@ __global__ void philox_kernel(const uint32_t* __restrict__ ck, uint32_t* __restr
 }
 
 }  // namespace gq
+
+namespace gq {
+
+// ------------------------------------------------------------------------------------------
+// Global-E allreduce with re-rounding at every hop (Global-QSGD: the custom reduction of the
+// exponential-dithering allreduce; the extra variance of rounding inside the allreduce; the
+// tree allreduce preferred for its fewer reduction steps).  A partial sum stays an extended
+// Global-E code: level index k stands for 2^(k-1) units of 2^-(s-1).  One step decodes two
+// codes, adds them exactly (int64) and rounds |t| between 2^e and 2^(e+1), e = floor(log2 |t|),
+// up with probability (|t| - 2^e) / 2^e, keeping the sign.  The random word of coordinate j in
+// stream `sid` (counter word 1; worker indices are below 2^31) is built as for the quantiser:
+// high half from Philox(j/8, sid, step), low half from Philox(2^31 + j/8, sid, step).
+// ------------------------------------------------------------------------------------------
+
+__device__ __forceinline__ int64_t exp_units_dev(int c) {
+    const int k = min(c < 0 ? -c : c, 62);  // valid codes have |k| <= 62
+    const int64_t u = k ? (static_cast<int64_t>(1) << (k - 1)) : 0;
+    return c < 0 ? -u : u;
+}
+
+// Lower level index and threshold of |t| units on the extended grid (exact).
+__device__ __forceinline__ void exp_split_dev(uint64_t a, uint32_t& lo, uint32_t& T) {
+    if (a == 0) {
+        lo = 0;
+        T = 0;
+        return;
+    }
+    const int e = 63 - __clzll(static_cast<long long>(a));
+    const uint64_t frac = a - (static_cast<uint64_t>(1) << e);
+    lo = static_cast<uint32_t>(e + 1);
+    T = e <= 32 ? static_cast<uint32_t>(frac << (32 - e)) : static_cast<uint32_t>(frac >> (e - 32));
+}
+
+struct ExpArgs {
+    uint32_t rk[20];  // Philox round keys of the seed
+    uint32_t step_lo, step_hi;
+};
+
+// Re-rounded signed codes of eight sums t[c] (coordinates 8 g8 + c) in stream sid.
+__device__ __forceinline__ void exp_reround8(const int64_t (&t)[8], uint32_t g8, uint32_t sid,
+                                             const ExpArgs& ea, int32_t (&code)[8]) {
+    const uint4 ra = philox4x32_10_rk(make_uint4(g8, sid, ea.step_lo, ea.step_hi), ea.rk);
+    const uint32_t aw[4] = {ra.x, ra.y, ra.z, ra.w};
+    uint32_t lo[8], T[8];
+    bool tie = false;
+#pragma unroll
+    for (int c = 0; c < 8; ++c) {
+        exp_split_dev(static_cast<uint64_t>(t[c] < 0 ? -t[c] : t[c]), lo[c], T[c]);
+        const uint32_t h = half16(aw, c);
+        tie |= h == (T[c] >> 16);
+        code[c] = static_cast<int32_t>(lo[c] + (h < (T[c] >> 16) ? 1u : 0u));
+    }
+    if (tie) {  // the high half equals the threshold's: the low half decides (rare)
+        const uint4 rb = philox4x32_10_rk(make_uint4(g8 | 0x80000000u, sid, ea.step_lo, ea.step_hi),
+                                          ea.rk);
+        const uint32_t bw[4] = {rb.x, rb.y, rb.z, rb.w};
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+            const uint32_t r = (half16(aw, c) << 16) | half16(bw, c);
+            code[c] = static_cast<int32_t>(lo[c] + (r < T[c] ? 1u : 0u));
+        }
+    }
+#pragma unroll
+    for (int c = 0; c < 8; ++c)
+        if (t[c] < 0) code[c] = -code[c];
+}
+
+// One step on d coordinates: out = re-round(decode(a) + decode(b)).  Each thread owns 16
+// coordinates (one 16-byte load of a and of b, one 16-byte store).
+__global__ void __launch_bounds__(kThreads)
+exp_combine_kernel(const int8_t* __restrict__ a, const int8_t* __restrict__ b, int64_t d,
+                   uint32_t sid, ExpArgs ea, int8_t* __restrict__ out) {
+    const int64_t chunks = (d + 15) / 16;
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * kThreads;
+    for (int64_t q = static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x; q < chunks;
+         q += stride) {
+        const int64_t j0 = q * 16;
+        const bool full = j0 + 16 <= d;
+        int8_t av[16], bv[16];
+        if (full) {
+            *reinterpret_cast<uint4*>(av) = __ldg(reinterpret_cast<const uint4*>(a + j0));
+            *reinterpret_cast<uint4*>(bv) = __ldg(reinterpret_cast<const uint4*>(b + j0));
+        } else {
+#pragma unroll
+            for (int c = 0; c < 16; ++c) {
+                av[c] = j0 + c < d ? a[j0 + c] : 0;
+                bv[c] = j0 + c < d ? b[j0 + c] : 0;
+            }
+        }
+        int8_t ov[16];
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            int64_t t[8];
+#pragma unroll
+            for (int c = 0; c < 8; ++c) t[c] = exp_units_dev(av[8 * h + c]) + exp_units_dev(bv[8 * h + c]);
+            int32_t code[8];
+            exp_reround8(t, static_cast<uint32_t>(j0 / 8 + h), sid, ea, code);
+#pragma unroll
+            for (int c = 0; c < 8; ++c) ov[8 * h + c] = static_cast<int8_t>(code[c]);
+        }
+        if (full) {
+            *reinterpret_cast<uint4*>(out + j0) = *reinterpret_cast<const uint4*>(ov);
+        } else {
+#pragma unroll
+            for (int c = 0; c < 16; ++c)
+                if (j0 + c < d) out[j0 + c] = ov[c];
+        }
+    }
+}
+
+// Re-rounded signed code of one sum t at coordinate j in stream sid (one thread, one column).
+__device__ __forceinline__ int32_t exp_reround1(int64_t t, int64_t j, uint32_t sid,
+                                                const ExpArgs& ea) {
+    uint32_t lo, T;
+    exp_split_dev(static_cast<uint64_t>(t < 0 ? -t : t), lo, T);
+    const uint32_t g8 = static_cast<uint32_t>(j >> 3);
+    const int c = static_cast<int>(j & 7);
+    const uint4 ra = philox4x32_10_rk(make_uint4(g8, sid, ea.step_lo, ea.step_hi), ea.rk);
+    const uint32_t aw[4] = {ra.x, ra.y, ra.z, ra.w};
+    const uint32_t h = half16(aw, c);
+    uint32_t up = h < (T >> 16) ? 1u : 0u;
+    if (h == (T >> 16)) {
+        const uint4 rb = philox4x32_10_rk(make_uint4(g8 | 0x80000000u, sid, ea.step_lo, ea.step_hi),
+                                          ea.rk);
+        const uint32_t bw[4] = {rb.x, rb.y, rb.z, rb.w};
+        up = ((h << 16) | half16(bw, c)) < T ? 1u : 0u;
+    }
+    const int32_t k = static_cast<int32_t>(lo + up);
+    return t < 0 ? -k : k;
+}
+
+constexpr int kExpMaxWorkers = 64;  // rows the one-GPU allreduce simulation holds per column
+
+// Code of worker i at coordinate j from the quantiser's layout (int8, or int4 nibbles).
+template <int CODE_BITS>
+__device__ __forceinline__ int read_code(const unsigned char* __restrict__ codes, int64_t i,
+                                         int64_t j, int64_t pitch) {
+    if (CODE_BITS == 8) return static_cast<int>(reinterpret_cast<const int8_t*>(codes)[i * pitch + j]);
+    const int byte = codes[i * (pitch / 2) + (j >> 1)];
+    const int nib = (j & 1) ? (byte >> 4) : (byte & 0xF);
+    return (nib ^ 8) - 8;
+}
+
+// The whole Global-E allreduce of the code matrix, one thread per coordinate: tree (ORDER 0:
+// level l, row i a multiple of 2^l takes row i + 2^(l-1), stream 2^31 + l 2^24 + i / 2^l) or
+// ring (ORDER 1: chunk c = j / ceil(d/n) starts at worker c + 1 and visits c + 2, ..., c;
+// stream of step h: 2^31 + 2^30 + h 2^12 + c); then out = scale * (root units).
+template <int ORDER, int CODE_BITS>
+__global__ void __launch_bounds__(kThreads)
+exp_allreduce_kernel(const unsigned char* __restrict__ codes, int64_t n, int64_t d, int64_t pitch,
+                     ExpArgs ea, const float* __restrict__ norm_ptr, uint32_t s,
+                     float* __restrict__ out, int8_t* __restrict__ root_codes) {
+    __shared__ float sh_scale;
+    const float scale = block_scale<kExp>(__ldg(norm_ptr), n, s, &sh_scale);
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * kThreads;
+    const int64_t chunk = (d + n - 1) / n;
+    for (int64_t j = static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x; j < d; j += stride) {
+        int32_t root;
+        if (ORDER == 0) {
+            int64_t u[kExpMaxWorkers];
+            int32_t c0 = 0;
+            for (int64_t i = 0; i < n; ++i) {
+                const int c = read_code<CODE_BITS>(codes, i, j, pitch);
+                if (i == 0) c0 = c;
+                u[i] = exp_units_dev(c);
+            }
+            root = c0;
+            for (int l = 1; (static_cast<int64_t>(1) << (l - 1)) < n; ++l) {
+                const int64_t half = static_cast<int64_t>(1) << (l - 1);
+                for (int64_t i = 0; i + half < n; i += 2 * half) {
+                    const uint32_t sid = 0x80000000u + (static_cast<uint32_t>(l) << 24) +
+                                         static_cast<uint32_t>(i >> l);
+                    root = exp_reround1(u[i] + u[i + half], j, sid, ea);
+                    u[i] = exp_units_dev(root);
+                }
+            }
+            if (n > 1) {  // row 0 now holds one level
+                uint32_t lo, T;
+                exp_split_dev(static_cast<uint64_t>(u[0] < 0 ? -u[0] : u[0]), lo, T);
+                root = u[0] < 0 ? -static_cast<int32_t>(lo) : static_cast<int32_t>(lo);
+            }
+        } else {
+            const int64_t c = j / chunk;
+            int32_t code = read_code<CODE_BITS>(codes, (c + 1) % n, j, pitch);
+            for (int64_t h = 1; h < n; ++h) {
+                const int64_t t = exp_units_dev(code) +
+                                  exp_units_dev(read_code<CODE_BITS>(codes, (c + 1 + h) % n, j, pitch));
+                const uint32_t sid = 0xC0000000u + (static_cast<uint32_t>(h) << 12) +
+                                     static_cast<uint32_t>(c);
+                code = exp_reround1(t, j, sid, ea);
+            }
+            root = code;
+        }
+        out[j] = scale * static_cast<float>(exp_units_dev(root));
+        if (root_codes) root_codes[j] = static_cast<int8_t>(root);
+    }
+}
+
+}  // namespace gq

@@ -158,6 +158,48 @@ gq_status gq_allreduce_mean_with_norm(const void *grads, int dtype, int64_t n, i
                                       uint64_t step, float *out_dev, void *codes, void *stream);
 
 /*
+ * Global-E allreduce with re-rounding at every hop (Global-QSGD: the custom reduction the
+ * implementation paragraph uses for exponential dithering; the extra variance of "stochastic
+ * rounding during AllReduce" counted in the theta worked example; the tree allreduce of the
+ * performance model, chosen for its fewer reduction steps).  A partial sum stays an extended
+ * Global-E code: level index k stands for 2^(k-1) units of 2^-(s-1), k = 0 for 0.  One step
+ * decodes two codes, adds them exactly and rounds |t| between 2^e and 2^(e+1) (e = floor(log2
+ * |t|)), up with probability (|t| - 2^e) / 2^e, keeping the sign: unbiased.  Random word of
+ * coordinate j in stream `stream_id`: as for gq_quantize with the worker index replaced by the
+ * stream identifier (counter word 1), so every step has its own independent stream.
+ */
+#define GQ_ORDER_TREE 0
+#define GQ_ORDER_RING 1
+
+/* Stream identifier of the tree step at level `level` (1-based) that combines into node m:
+ * 2^31 + level 2^24 + m.  Of ring step h (1-based) of chunk c: 2^31 + 2^30 + h 2^12 + c. */
+uint32_t gq_exp_tree_stream(int level, int64_t m);
+uint32_t gq_exp_ring_stream(int64_t h, int64_t c);
+
+/*
+ * One reduction step on d coordinates: out[j] = re-round(decode(a[j]) + decode(b[j])).  a, b,
+ * out: int8 extended Global-E codes in device memory (16-byte aligned), |k| <= 62 on input (the
+ * result for larger codes is unspecified).  d >= 1.
+ */
+gq_status gq_exp_combine(const int8_t *a, const int8_t *b, int64_t d, uint64_t seed,
+                         uint64_t step, uint32_t stream_id, int8_t *out, void *stream);
+
+/*
+ * The whole Global-E allreduce of the n x pitch code matrix written by gq_quantize (Global-E_s,
+ * int4 or int8 by s), simulated on one GPU, then dequantised: out_j = N * R_j * 2^-(s-1) / n
+ * with R_j the reduced value in units (fp32, exact scale as gq_dequantize) from the fp32 norm at
+ * *norm_dev.  order GQ_ORDER_TREE: level l = 1, 2, ...: row i (a multiple of 2^l) takes
+ * re-round(row i + row i + 2^(l-1)) when that row exists.  GQ_ORDER_RING: the coordinates form n
+ * chunks of ceil(d/n); chunk c starts at worker c + 1 and adds workers c + 2, ..., c (mod n),
+ * re-rounding after each step (reduce-scatter; the allgather only copies).  root_codes
+ * (nullable, int8 x d) receives the reduced codes.  1 <= n <= 64; s and n as for gq_quantize
+ * (n 2^(s-1) < 2^24, so every partial sum stays below 2^24 units).
+ */
+gq_status gq_exp_allreduce(const void *codes, int s, int64_t n, int64_t d, int order,
+                           const float *norm_dev, uint64_t seed, uint64_t step, float *out_dev,
+                           int8_t *root_codes, void *stream);
+
+/*
  * gq_allreduce_mean without a workspace argument, for callers that cannot allocate device
  * memory where they need the allreduce (for example code running inside a framework's caching
  * allocator or communication hook, which may not call back into the allocator, or a process

@@ -510,7 +510,7 @@ int64_t gqo_exp_ring_stream(int64_t h, int64_t c) { return (int64_t)0xC0000000LL
 /*
  * One reduction step on w coordinates (the custom reduction of the pages' Global-E allreduce):
  * out[j] = re-round(decode(a[j]) + decode(b[j])) with the random words of stream `stream_id` at
- * coordinates j0 + j.  Codes are signed level indices (|k| <= 127).
+ * coordinates j0 + j.  Codes are signed level indices, |k| <= 62 on input.
  */
 int gqo_exp_combine(const int8_t *a, const int8_t *b, int64_t w, int64_t j0, uint64_t seed,
                     uint64_t step, int64_t stream_id, int8_t *out)
@@ -518,6 +518,9 @@ int gqo_exp_combine(const int8_t *a, const int8_t *b, int64_t w, int64_t j0, uin
     int64_t j;
     if (a == NULL || b == NULL || out == NULL || w < 0 || j0 < 0)
         return GQO_ERR_INVALID;
+    for (j = 0; j < w; ++j)  /* 2^61 units at most per operand keeps every sum in int64 */
+        if (a[j] > 62 || a[j] < -62 || b[j] > 62 || b[j] < -62)
+            return GQO_ERR_UNSUPPORTED;
     for (j = 0; j < w; ++j) {
         int64_t t = exp_units(a[j]) + exp_units(b[j]);
         int c = exp_reround(t, seed, step, stream_id, j0 + j);
