@@ -47,6 +47,8 @@ def _args():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--measure", default=None, choices=["exp-reduce"],
+                    help="extra measurement instead of the main bench line")
     return ap.parse_args()
 
 
@@ -255,8 +257,57 @@ def _config_block(cfg, ngpus):
                   % (cfg["n"] * cfg["d"] * (2 if cfg["dtype"] == "bf16" else 4) / 1e6)}
 
 
+def measure_exp_reduce(a) -> int:
+    """Cost of the Global-E custom reduction step against a native sum, on the pages' setting:
+    one GPU, a 25 MB buffer (PyTorch DDP's default bucket).  One step of each kind is timed
+    with CUDA events; the buffers (75 MB per step) stay in L2 between steps, as on the pages'
+    single-buffer micro-measurement."""
+    import torch
+
+    import allreduce_compatible_gradient_gb300 as gq
+
+    d = 25_000_000
+    g = torch.Generator(device="cuda")
+    g.manual_seed(0)
+    ca = torch.randint(-12, 13, (d,), generator=g, device="cuda", dtype=torch.int8)
+    cb = torch.randint(-12, 13, (d,), generator=g, device="cuda", dtype=torch.int8)
+    out = torch.empty(d, dtype=torch.int8, device="cuda")
+    fa = torch.randn(d // 4, generator=g, device="cuda")  # 25 MB of fp32
+    fb = torch.randn(d // 4, generator=g, device="cuda")
+    fo = torch.empty_like(fa)
+    sid = gq.gq_exp_tree_stream(1, 0)
+
+    def timeit(fn):
+        for _ in range(a.warmup):
+            fn()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(a.steps):
+            fn()
+        e1.record()
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / a.steps
+
+    t_comb = timeit(lambda: gq.gq_exp_combine(ca, cb, 1, 2, sid, out=out))
+    t_i8 = timeit(lambda: torch.add(ca, cb, out=out))
+    t_f32 = timeit(lambda: torch.add(fa, fb, out=fo))
+    line = {"measure": "exp_reduce_cost", "buffer_bytes": d, "steps": a.steps,
+            "combine_ms": round(t_comb, 5), "native_int8_sum_ms": round(t_i8, 5),
+            "native_fp32_sum_ms": round(t_f32, 5),
+            "combine_gb_per_s_of_buffer": round(d / (t_comb * 1e-3) / 1e9, 1),
+            "native_int8_gb_per_s_of_buffer": round(d / (t_i8 * 1e-3) / 1e9, 1),
+            "combine_time_over_native_int8": round(t_comb / t_i8, 3),
+            "combine_time_over_native_fp32": round(t_comb / t_f32, 3),
+            "native_sums": "torch.add on the same buffers (library kernels, reference only)"}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 def main():
     a = _args()
+    if a.measure == "exp-reduce":
+        return measure_exp_reduce(a)
     from allreduce_compatible_gradient_gb300 import workloads
 
     cfg = dict(workloads.CONFIGS[a.config], name=a.config)
