@@ -51,6 +51,11 @@ def lib() -> ctypes.CDLL:
         "gq_allreduce_mean_noalloc": (ci, [vp, ci, i64, i64, ci, ci, ci, ci, u64, u64, vp, vp, vp,
                                            vp]),
         "gq_philox4x32_10": (ci, [vp, vp, i64, vp]),
+        "gq_allreduce_mean_segments": (ci, [i64, vp, vp, ci, i64, ci, ci, ci, ci, u64, u64, vp,
+                                            vp, vp, sz, vp]),
+        "gq_norm_partial": (ci, [vp, ci, i64, i64, ci, ci, vp, vp, sz, vp]),
+        "gq_norm_finish": (ci, [vp, ci, ci, vp, vp]),
+        "gq_quantize_sum": (ci, [vp, ci, i64, i64, i64, vp, ci, ci, u64, u64, vp, vp]),
         "gq_exp_tree_stream": (ctypes.c_uint32, [ci, i64]),
         "gq_exp_ring_stream": (ctypes.c_uint32, [i64, i64]),
         "gq_exp_combine": (ci, [vp, vp, i64, u64, u64, ctypes.c_uint32, vp, vp]),
@@ -192,6 +197,73 @@ def gq_allreduce_mean_with_norm(grads, norm, scheme, s, seed, step, out=None, co
                                              _p(out), _p(codes), _stream(stream)),
            "gq_allreduce_mean_with_norm")
     return out
+
+
+def gq_allreduce_mean_segments(grads, q, p, scheme, s, seed, step, outs=None, norms=None,
+                               ws=None, stream=None):
+    """Per-segment fused pipeline: grads is a list of n x d_l CUDA tensors (same dtype and n);
+    returns the list of d_l fp32 outputs.  Segment l uses step (step << 16) | l."""
+    grads = list(grads)
+    if not grads:
+        raise ValueError("no segments")
+    dts = set()
+    n = None
+    for g in grads:
+        dt, gn, _ = _grads(g)
+        dts.add(dt)
+        if n is not None and gn != n:
+            raise ValueError("every segment needs the same number of workers")
+        n = gn
+    if len(dts) != 1:
+        raise ValueError("every segment needs the same dtype")
+    dev = grads[0].device
+    if outs is None:
+        outs = [torch.empty(g.shape[1], dtype=torch.float32, device=dev) for g in grads]
+    if len(outs) != len(grads):
+        raise ValueError("one output per segment")
+    if ws is None:
+        ws = gq_workspace(dev, stream)
+    L = len(grads)
+    gp = (ctypes.c_void_p * L)(*[g.data_ptr() for g in grads])
+    dv = (ctypes.c_int64 * L)(*[g.shape[1] for g in grads])
+    op = (ctypes.c_void_p * L)(*[o.data_ptr() for o in outs])
+    _check(lib().gq_allreduce_mean_segments(L, gp, dv, dts.pop(), n, q, p, scheme, s, seed, step,
+                                            op, _p(norms), _p(ws), ws.numel(), _stream(stream)),
+           "gq_allreduce_mean_segments")
+    return outs
+
+
+def gq_norm_partial(grads, q, p, part=None, ws=None, stream=None) -> torch.Tensor:
+    """This rank's combinable share of the global norm (fp64: a sum of squares for q = p = 2, a
+    maximum for q = p = inf)."""
+    dt, m, d = _grads(grads)
+    if part is None:
+        part = torch.empty(1, dtype=torch.float64, device=grads.device)
+    if ws is None:
+        ws = gq_workspace(grads.device, stream)
+    _check(lib().gq_norm_partial(_p(grads), dt, m, d, q, p, _p(part), _p(ws), ws.numel(),
+                                 _stream(stream)), "gq_norm_partial")
+    return part
+
+
+def gq_norm_finish(part, q, p, norm=None, stream=None) -> torch.Tensor:
+    """The fp32 norm from the ranks' combined partial."""
+    if norm is None:
+        norm = torch.empty(1, dtype=torch.float32, device=part.device)
+    _check(lib().gq_norm_finish(_p(part), q, p, _p(norm), _stream(stream)), "gq_norm_finish")
+    return norm
+
+
+def gq_quantize_sum(grads, norm, scheme, s, seed, step, worker0=0, sums=None,
+                    stream=None) -> torch.Tensor:
+    """One rank's share of a multi-GPU allreduce: integer code sums of its rows (workers
+    worker0 ..), to be summed over ranks and dequantised with the total worker count."""
+    dt, m, d = _grads(grads)
+    if sums is None:
+        sums = torch.empty(d, dtype=torch.int32, device=grads.device)
+    _check(lib().gq_quantize_sum(_p(grads), dt, m, d, worker0, _p(norm), scheme, s, seed, step,
+                                 _p(sums), _stream(stream)), "gq_quantize_sum")
+    return sums
 
 
 def gq_allreduce_mean_noalloc(grads, q, p, scheme, s, seed, step, out, norm=None, codes=None,

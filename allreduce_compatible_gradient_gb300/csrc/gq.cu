@@ -114,34 +114,34 @@ int norm_mode(int q, int p) {
 
 // ---- norm ---------------------------------------------------------------------------------
 template <typename T, int MODE>
-gq_status run_norm(const T* x, int64_t n, int64_t d, float* norm_user, unsigned char* ws,
-                   cudaStream_t st) {
+gq_status run_norm(const T* x, int64_t n, int64_t d, float* norm_user, double* part_user,
+                   unsigned char* ws, cudaStream_t st) {
     constexpr int C = gq::Elem<T>::kCols;
     const int64_t groups = (d + C - 1) / C;
     const bool vec_rows = (d % C) == 0;
     auto k = gq::norm_kernel<T, MODE>;
     const unsigned grid = grid_for(k, groups, gq::kMaxPartials);
-    k<<<grid, kThreads, 0, st>>>(x, n, d, groups, vec_rows, norm_user, ws);
+    k<<<grid, kThreads, 0, st>>>(x, n, d, groups, vec_rows, norm_user, part_user, ws);
     return launch_status();
 }
 
 template <typename T>
 gq_status dispatch_norm(const void* grads, int mode, int64_t n, int64_t d, float* norm_user,
-                        unsigned char* ws, cudaStream_t st) {
+                        double* part_user, unsigned char* ws, cudaStream_t st) {
     const T* x = static_cast<const T*>(grads);
     switch (mode) {
-        case gq::kMaxMax: return run_norm<T, gq::kMaxMax>(x, n, d, norm_user, ws, st);
-        case gq::kL2L2: return run_norm<T, gq::kL2L2>(x, n, d, norm_user, ws, st);
-        case gq::kL2Max: return run_norm<T, gq::kL2Max>(x, n, d, norm_user, ws, st);
-        default: return run_norm<T, gq::kMaxL2>(x, n, d, norm_user, ws, st);
+        case gq::kMaxMax: return run_norm<T, gq::kMaxMax>(x, n, d, norm_user, part_user, ws, st);
+        case gq::kL2L2: return run_norm<T, gq::kL2L2>(x, n, d, norm_user, part_user, ws, st);
+        case gq::kL2Max: return run_norm<T, gq::kL2Max>(x, n, d, norm_user, part_user, ws, st);
+        default: return run_norm<T, gq::kMaxL2>(x, n, d, norm_user, part_user, ws, st);
     }
 }
 
 gq_status norm_any(const void* grads, int dtype, int mode, int64_t n, int64_t d, float* norm_user,
-                   void* ws, cudaStream_t st) {
+                   void* ws, cudaStream_t st, double* part_user = nullptr) {
     unsigned char* w = static_cast<unsigned char*>(ws);
-    return dtype == GQ_F32 ? dispatch_norm<float>(grads, mode, n, d, norm_user, w, st)
-                           : dispatch_norm<uint16_t>(grads, mode, n, d, norm_user, w, st);
+    return dtype == GQ_F32 ? dispatch_norm<float>(grads, mode, n, d, norm_user, part_user, w, st)
+                           : dispatch_norm<uint16_t>(grads, mode, n, d, norm_user, part_user, w, st);
 }
 
 // ---- quantize (+ sum + dequantize) ----------------------------------------------------------
@@ -196,6 +196,8 @@ gq::QuantArgs make_args(const float* norm_ptr, int dtype, int64_t n, int64_t d, 
     a.d = d;
     a.pitch = gq_code_pitch(d);
     a.vec_rows = (d % (dtype == GQ_F32 ? 4 : 8)) == 0;
+    a.row0 = 0;
+    a.sums = nullptr;
     return a;
 }
 
@@ -208,7 +210,7 @@ int gq_abi_version(void) { return 1; }
 size_t gq_workspace_bytes(int64_t n, int64_t d) {
     (void)n;
     (void)d;
-    return static_cast<size_t>(gq::kHeaderBytes) + sizeof(uint64_t) * gq::kMaxPartials;
+    return static_cast<size_t>(gq::kWorkspaceBytes);
 }
 
 gq_status gq_workspace_init(void* ws, size_t ws_bytes, void* stream) {
@@ -523,4 +525,154 @@ extern "C" gq_status gq_exp_allreduce(const void* codes, int s, int64_t n, int64
     }
 #undef GQ_EXP_ALLREDUCE
     return launch_status();
+}
+
+// ---- one rank's share of a multi-GPU allreduce ---------------------------------------------
+extern "C" gq_status gq_norm_partial(const void* grads, int dtype, int64_t m, int64_t d, int q,
+                                     int p, double* part_dev, void* ws, size_t ws_bytes,
+                                     void* stream) {
+    gq_status st = check_grads(grads, dtype, m, d);
+    if (st != GQ_OK) return st;
+    const int mode = norm_mode(q, p);
+    if (mode < 0 || !part_dev) return GQ_ERR_INVALID;
+    if (mode != gq::kMaxMax && mode != gq::kL2L2) return GQ_ERR_UNSUPPORTED;
+    if ((st = check_ws(ws, ws_bytes, m, d)) != GQ_OK) return st;
+    return norm_any(grads, dtype, mode, m, d, nullptr, ws, static_cast<cudaStream_t>(stream),
+                    part_dev);
+}
+
+extern "C" gq_status gq_norm_finish(const double* part_dev, int q, int p, float* norm_dev,
+                                    void* stream) {
+    const int mode = norm_mode(q, p);
+    if (mode < 0 || !part_dev || !norm_dev) return GQ_ERR_INVALID;
+    if (mode != gq::kMaxMax && mode != gq::kL2L2) return GQ_ERR_UNSUPPORTED;
+    gq::norm_finish_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(
+        part_dev, mode == gq::kL2L2, norm_dev);
+    return launch_status();
+}
+
+extern "C" gq_status gq_quantize_sum(const void* grads, int dtype, int64_t m, int64_t d,
+                                     int64_t worker0, const float* norm_dev, int scheme, int s,
+                                     uint64_t seed, uint64_t step, int32_t* sum_dev,
+                                     void* stream) {
+    gq_status st = check_grads(grads, dtype, m, d);
+    if (st != GQ_OK) return st;
+    if ((st = check_scheme(scheme, s, m)) != GQ_OK) return st;
+    if (!norm_dev || !sum_dev || !aligned16(sum_dev)) return GQ_ERR_INVALID;
+    if (worker0 < 0 || worker0 + m > (int64_t(1) << 31)) return GQ_ERR_INVALID;
+    gq::QuantArgs a = make_args(norm_dev, dtype, m, d, s, seed, step);
+    a.row0 = static_cast<uint32_t>(worker0);
+    a.sums = sum_dev;
+    return quant_any<true, false>(grads, dtype, a, scheme, gq_code_bits(scheme, s), nullptr,
+                                  nullptr, static_cast<cudaStream_t>(stream));
+}
+
+// ---- segmented form: many n x d_l problems in two launches per kSegChunk segments -----------
+namespace {
+
+// Runs of blocks for a chunk of segments: each gets a share of `target` blocks in proportion to
+// its elements, at least one and at most one per 256 column groups of `cols` columns.
+void plan_runs(gq::SegLaunch& L, const int64_t* d, int64_t n, int cols, int64_t target) {
+    double total = 0.0;
+    for (int k = 0; k < L.nseg; ++k) total += static_cast<double>(d[k]);
+    int32_t b = 0;
+    for (int k = 0; k < L.nseg; ++k) {
+        const int64_t groups = (d[k] + cols - 1) / cols;
+        const int64_t most = (groups + kThreads - 1) / kThreads;
+        int64_t nb = static_cast<int64_t>(static_cast<double>(d[k]) / total * static_cast<double>(target));
+        if (nb > most) nb = most;
+        if (nb < 1) nb = 1;
+        L.seg[k].d = d[k];
+        L.seg[k].b0 = b;
+        L.seg[k].nb = static_cast<int32_t>(nb);
+        b += static_cast<int32_t>(nb);
+    }
+    (void)n;
+}
+
+int32_t total_blocks(const gq::SegLaunch& L) {
+    return L.seg[L.nseg - 1].b0 + L.seg[L.nseg - 1].nb;
+}
+
+template <typename T, int MODE>
+gq_status run_norm_segments(gq::SegLaunch& L, const int64_t* d, int64_t n, float* norms_user,
+                            unsigned char* ws, cudaStream_t st) {
+    constexpr int C = gq::Elem<T>::kCols;
+    auto k = gq::norm_segments_kernel<T, MODE>;
+    const int64_t full = static_cast<int64_t>(blocks_per_sm(k)) * sm_count();
+    int64_t target = 2 * full;
+    if (target > gq::kMaxPartials - L.nseg) target = gq::kMaxPartials - L.nseg;
+    plan_runs(L, d, n, C, target);
+    k<<<total_blocks(L), kThreads, 0, st>>>(L, n, norms_user, ws);
+    return launch_status();
+}
+
+template <typename T>
+gq_status norm_segments_any(int mode, gq::SegLaunch& L, const int64_t* d, int64_t n,
+                            float* norms_user, unsigned char* ws, cudaStream_t st) {
+    switch (mode) {
+        case gq::kMaxMax: return run_norm_segments<T, gq::kMaxMax>(L, d, n, norms_user, ws, st);
+        case gq::kL2L2: return run_norm_segments<T, gq::kL2L2>(L, d, n, norms_user, ws, st);
+        case gq::kL2Max: return run_norm_segments<T, gq::kL2Max>(L, d, n, norms_user, ws, st);
+        default: return run_norm_segments<T, gq::kMaxL2>(L, d, n, norms_user, ws, st);
+    }
+}
+
+template <typename T, int SCHEME>
+gq_status run_quant_segments(gq::SegLaunch& L, const int64_t* d, int64_t n,
+                             const gq::QuantArgs& base, unsigned char* ws, cudaStream_t st) {
+    auto k = gq::quantize_segments_kernel<T, SCHEME>;
+    constexpr int smem = gq::Staging<T>::kBytes;
+    const int64_t full = static_cast<int64_t>(blocks_per_sm(k, smem)) * sm_count();
+    plan_runs(L, d, n, gq::kQCols, full);
+    k<<<total_blocks(L), kThreads, smem, st>>>(L, base, ws);
+    return launch_status();
+}
+
+}  // namespace
+
+extern "C" gq_status gq_allreduce_mean_segments(int64_t nseg, const void* const* grads,
+                                                const int64_t* d, int dtype, int64_t n, int q,
+                                                int p, int scheme, int s, uint64_t seed,
+                                                uint64_t step, float* const* out,
+                                                float* norms_dev, void* ws, size_t ws_bytes,
+                                                void* stream) {
+    if (nseg < 1 || nseg > 65536 || !grads || !d || !out) return GQ_ERR_INVALID;
+    if (step >= (uint64_t(1) << 48)) return GQ_ERR_INVALID;
+    gq_status st;
+    for (int64_t l = 0; l < nseg; ++l) {
+        if ((st = check_grads(grads[l], dtype, n, d[l])) != GQ_OK) return st;
+        if (!out[l] || !aligned16(out[l])) return GQ_ERR_INVALID;
+    }
+    const int mode = norm_mode(q, p);
+    if (mode < 0) return GQ_ERR_INVALID;
+    if ((st = check_scheme(scheme, s, n)) != GQ_OK) return st;
+    if ((st = check_ws(ws, ws_bytes, n, 1)) != GQ_OK) return st;
+    unsigned char* w = static_cast<unsigned char*>(ws);
+    cudaStream_t cs = static_cast<cudaStream_t>(stream);
+    gq::QuantArgs base = make_args(nullptr, dtype, n, 1, s, seed, step << 16);
+    gq::SegLaunch L;  // ~8 KB of kernel parameters per launch
+    for (int64_t c0 = 0; c0 < nseg; c0 += gq::kSegChunk) {
+        const int64_t m = nseg - c0 < gq::kSegChunk ? nseg - c0 : gq::kSegChunk;
+        std::memset(&L, 0, sizeof(L));
+        L.nseg = static_cast<int32_t>(m);
+        L.seg0 = static_cast<int32_t>(c0);
+        for (int64_t k = 0; k < m; ++k) {
+            L.seg[k].x = grads[c0 + k];
+            L.seg[k].out = out[c0 + k];
+        }
+        st = dtype == GQ_F32 ? norm_segments_any<float>(mode, L, d + c0, n, norms_dev, w, cs)
+                             : norm_segments_any<uint16_t>(mode, L, d + c0, n, norms_dev, w, cs);
+        if (st != GQ_OK) return st;
+        if (dtype == GQ_F32)
+            st = scheme == GQ_LINEAR
+                     ? run_quant_segments<float, gq::kLinear>(L, d + c0, n, base, w, cs)
+                     : run_quant_segments<float, gq::kExp>(L, d + c0, n, base, w, cs);
+        else
+            st = scheme == GQ_LINEAR
+                     ? run_quant_segments<uint16_t, gq::kLinear>(L, d + c0, n, base, w, cs)
+                     : run_quant_segments<uint16_t, gq::kExp>(L, d + c0, n, base, w, cs);
+        if (st != GQ_OK) return st;
+    }
+    return GQ_OK;
 }

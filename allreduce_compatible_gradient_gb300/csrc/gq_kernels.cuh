@@ -19,6 +19,11 @@ namespace gq {
 constexpr int kThreads = 256;        // threads per block for every kernel
 constexpr int kMaxPartials = 4096;   // upper bound on norm-kernel blocks (workspace size)
 constexpr int kHeaderBytes = 256;    // workspace header, then kMaxPartials 8-byte partials
+constexpr int kSegChunk = 256;       // segments per launch of the segmented kernels
+// after the partials: kSegChunk completion tickets, then kSegChunk fp32 norms (one per segment)
+constexpr int kSegTicketsOff = kHeaderBytes + 8 * kMaxPartials;
+constexpr int kSegNormsOff = kSegTicketsOff + 4 * kSegChunk;
+constexpr int kWorkspaceBytes = kSegNormsOff + 4 * kSegChunk;
 
 // Workspace header (device memory owned by the caller).
 struct WsHeader {
@@ -309,18 +314,28 @@ __device__ __forceinline__ uint64_t block_max_bits(uint64_t v, uint64_t* sh) {
 // block writes one partial; the last block to finish (completion ticket, no waiting) combines
 // the partials in index order and writes the fp32 norm.
 // ------------------------------------------------------------------------------------------
+// Where one norm's blocks leave their partials and the result.
+struct NormSlots {
+    uint64_t* partials;     // one per block of this norm
+    unsigned int* ticket;   // completion count, zero between calls
+    unsigned int* status;   // device status word
+    float* norm;            // the fp32 norm (workspace copy)
+    float* norm_user;       // nullable: the caller's copy
+    double* part_user;      // nullable: the combinable value before the square root
+};
+
+// One norm computed by `nblk` blocks, this one being block `vb` of them.
 template <typename T, int MODE>
-__global__ void __launch_bounds__(kThreads, 4)
-norm_kernel(const T* __restrict__ x, int64_t n, int64_t d, int64_t groups, bool vec_rows,
-            float* __restrict__ norm_user, unsigned char* __restrict__ ws) {
+__device__ __forceinline__ void norm_body(const T* __restrict__ x, int64_t n, int64_t d,
+                                          int64_t groups, bool vec_rows, int64_t vb, int64_t nblk,
+                                          const NormSlots& out) {
     constexpr int C = Elem<T>::kCols;
-    WsHeader* hdr = reinterpret_cast<WsHeader*>(ws);
-    uint64_t* partials = reinterpret_cast<uint64_t*>(ws + kHeaderBytes);
+    uint64_t* partials = out.partials;
     __shared__ double sh_d[kThreads / 32];
     __shared__ uint64_t sh_u[kThreads / 32];
     __shared__ bool is_last;
 
-    const int64_t stride = static_cast<int64_t>(gridDim.x) * kThreads;
+    const int64_t stride = nblk * kThreads;
     uint32_t maxbits = 0;       // kMaxMax: max |x| bit pattern
     ScaledSumSq ssq;            // kL2L2, kMaxL2
     ssq.init();
@@ -331,8 +346,7 @@ norm_kernel(const T* __restrict__ x, int64_t n, int64_t d, int64_t groups, bool 
     // (2, inf) form, whose per-column scaled sums take C x 5 registers
     constexpr int U = (MODE == kL2Max) ? (C == 8 ? 2 : 4) : 8;
     const int64_t row_bytes = d * static_cast<int64_t>(sizeof(T));
-    for (int64_t g = static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x; g < groups;
-         g += stride) {
+    for (int64_t g = vb * kThreads + threadIdx.x; g < groups; g += stride) {
         uint32_t colmax[C];   // kMaxL2
         ScaledSumSq col[C];   // kL2Max
 #pragma unroll
@@ -415,17 +429,17 @@ norm_kernel(const T* __restrict__ x, int64_t n, int64_t d, int64_t groups, bool 
     }
 
     if (threadIdx.x == 0) {
-        partials[blockIdx.x] = part_bits;
+        partials[vb] = part_bits;
         __threadfence();
-        const unsigned int t = atomicAdd(&hdr->ticket, 1u);
-        is_last = (t == gridDim.x - 1);
+        const unsigned int t = atomicAdd(out.ticket, 1u);
+        is_last = (t == nblk - 1);
     }
     __syncthreads();
     if (!is_last) return;
     __threadfence();
 
-    // Last block: combine the gridDim.x partials in a fixed order.
-    const int nb = gridDim.x;
+    // Last block: combine the nblk partials in a fixed order.
+    const int nb = static_cast<int>(nblk);
     double result;
     if (MODE == kMaxMax || MODE == kL2Max) {
         uint64_t m = 0;
@@ -443,14 +457,36 @@ norm_kernel(const T* __restrict__ x, int64_t n, int64_t d, int64_t groups, bool 
         result = block_sum(s, sh_d);
     }
     if (threadIdx.x == 0) {
+        if (out.part_user) *out.part_user = result;  // combinable across ranks: a sum or a max
         double nrm = result;
         if (MODE != kMaxMax) nrm = sqrt(result);  // (2,2), (inf,2): sqrt of a sum; (2,inf): of a max
         const float n32 = static_cast<float>(nrm);
-        hdr->norm = n32;
-        if (norm_user) *norm_user = n32;
-        if (!(fabsf(n32) < __uint_as_float(kInfBits))) atomicCAS(&hdr->status, 0u, 4u);
-        hdr->ticket = 0;  // ready for the next call on this workspace
+        *out.norm = n32;
+        if (out.norm_user) *out.norm_user = n32;
+        if (!(fabsf(n32) < __uint_as_float(kInfBits))) atomicCAS(out.status, 0u, 4u);
+        *out.ticket = 0;  // ready for the next call on this workspace
         __threadfence();
+    }
+}
+
+template <typename T, int MODE>
+__global__ void __launch_bounds__(kThreads, 4)
+norm_kernel(const T* __restrict__ x, int64_t n, int64_t d, int64_t groups, bool vec_rows,
+            float* __restrict__ norm_user, double* __restrict__ part_user,
+            unsigned char* __restrict__ ws) {
+    WsHeader* hdr = reinterpret_cast<WsHeader*>(ws);
+    const NormSlots slots{reinterpret_cast<uint64_t*>(ws + kHeaderBytes), &hdr->ticket,
+                          &hdr->status, &hdr->norm, norm_user, part_user};
+    norm_body<T, MODE>(x, n, d, groups, vec_rows, blockIdx.x, gridDim.x, slots);
+}
+
+// The norm from the combined partials of several ranks (a sum of squares for (2,2), a maximum
+// magnitude for (inf,inf)), rounded to fp32 as norm_kernel rounds it.
+__global__ void norm_finish_kernel(const double* __restrict__ part, bool take_sqrt,
+                                   float* __restrict__ norm) {
+    if (threadIdx.x == 0 && blockIdx.x == 0) {
+        const double v = *part;
+        *norm = static_cast<float>(take_sqrt ? sqrt(v) : v);
     }
 }
 
@@ -552,6 +588,8 @@ struct QuantArgs {
     int64_t n, d;
     int64_t pitch;           // code row pitch in elements
     bool vec_rows;
+    uint32_t row0;           // worker index of local row 0 (keys the random words)
+    int32_t* sums;           // when set, the kernel writes the integer sums here instead of out
 };
 
 // Per-block fp32 dequantisation scale from the fp32 norm, computed in fp64 by one thread:
@@ -736,10 +774,11 @@ __device__ __forceinline__ void quantize_group(const T* __restrict__ x, const Qu
         for (int u = 0; u < U; ++u) {
             if (i0 + u >= a.n) break;
             const uint32_t row = static_cast<uint32_t>(i0 + u);
-            const uint4 ra = philox_row(pg, row, a.step_lo, a.rk);
+            const uint32_t worker = row + a.row0;
+            const uint4 ra = philox_row(pg, worker, a.step_lo, a.rk);
             const uint32_t aw[1][4] = {{ra.x, ra.y, ra.z, ra.w}};
             uint32_t k[1][kQCols];
-            decide_rows<SCHEME, TRUSTED, 1>(v[u], dc, a, g32, row, aw, k);
+            decide_rows<SCHEME, TRUSTED, 1>(v[u], dc, a, g32, worker, aw, k);
             int32_t code[kQCols];
             accumulate_row<SCHEME>(v[u][0], k[0], S, code);
             if (CODE_BITS) store_codes<CODE_BITS>(codes, row, g, a.pitch, code);
@@ -799,10 +838,26 @@ __device__ __forceinline__ void unstage(const uint4* piece0, const uint4* piece1
     }
 }
 
-// Output of one finished column group: dequantise the sums into out.
-__device__ __forceinline__ void store_out(float* __restrict__ out, int64_t g, int64_t d,
-                                          float scale, const float (&S)[kQCols]) {
+// Output of one finished column group: dequantise the sums into out, or, when `sums` is set,
+// write the integer sums themselves (exact: every partial sum is an integer below 2^24).
+__device__ __forceinline__ void store_out(float* __restrict__ out, int32_t* __restrict__ sums,
+                                          int64_t g, int64_t d, float scale,
+                                          const float (&S)[kQCols]) {
     const int64_t j0 = g * kQCols;
+    if (sums) {
+        if (j0 + kQCols <= d) {
+#pragma unroll
+            for (int h = 0; h < kQCols / 4; ++h)
+                reinterpret_cast<int4*>(sums + j0)[h] =
+                    make_int4(static_cast<int32_t>(S[4 * h]), static_cast<int32_t>(S[4 * h + 1]),
+                              static_cast<int32_t>(S[4 * h + 2]), static_cast<int32_t>(S[4 * h + 3]));
+        } else {
+#pragma unroll
+            for (int c = 0; c < kQCols; ++c)
+                if (j0 + c < d) sums[j0 + c] = static_cast<int32_t>(S[c]);
+        }
+        return;
+    }
     if (j0 + kQCols <= d) {
 #pragma unroll
         for (int h = 0; h < kQCols / 4; ++h)
@@ -822,11 +877,12 @@ template <typename T, int SCHEME, int CODE_BITS, bool WRITE_OUT, bool TRUSTED>
 __device__ __forceinline__ void staged_groups(const T* __restrict__ x, const QuantArgs& a,
                                               const Decide& dc, int64_t full, float scale,
                                               unsigned char* __restrict__ codes,
-                                              float* __restrict__ out, uint4* stage) {
+                                              float* __restrict__ out, uint4* stage, int64_t vb,
+                                              int64_t nblk) {
     using St = Staging<T>;
     constexpr int R = St::kRows, P = St::kPieces, NS = St::kStages;
-    const int64_t stride = static_cast<int64_t>(gridDim.x) * kThreads;
-    const int64_t it0 = static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x;
+    const int64_t stride = nblk * kThreads;
+    const int64_t it0 = vb * kThreads + threadIdx.x;
     const int64_t ngroups = it0 < full ? (full - 1 - it0) / stride + 1 : 0;
     const int64_t nb = (a.n + R - 1) / R;  // batches per group
     const int64_t total = ngroups * nb;
@@ -882,12 +938,14 @@ __device__ __forceinline__ void staged_groups(const T* __restrict__ x, const Qua
             const PhiloxGroup pg = philox_group(g32, a.step_lo, a.step_hi, a.rk);
 #pragma unroll
             for (int u = 0; u < R; ++u) {
-                const uint4 ra = philox_row(pg, static_cast<uint32_t>(r * R + u), a.step_lo, a.rk);
+                const uint4 ra = philox_row(pg, static_cast<uint32_t>(r * R + u) + a.row0,
+                                            a.step_lo, a.rk);
                 aw[u][0] = ra.x; aw[u][1] = ra.y; aw[u][2] = ra.z; aw[u][3] = ra.w;
             }
         }
         uint32_t k[R][kQCols];
-        decide_rows<SCHEME, TRUSTED, R>(v, dc, a, g32, static_cast<uint32_t>(r * R), aw, k);
+        decide_rows<SCHEME, TRUSTED, R>(v, dc, a, g32, static_cast<uint32_t>(r * R) + a.row0, aw,
+                                        k);
 #pragma unroll
         for (int u = 0; u < R; ++u) {
             const int64_t row64 = r * R + u;
@@ -899,7 +957,7 @@ __device__ __forceinline__ void staged_groups(const T* __restrict__ x, const Qua
         if (++r == nb) {
             r = 0;
             ++q;
-            if (WRITE_OUT) store_out(out, g, a.d, scale, S);
+            if (WRITE_OUT) store_out(out, a.sums, g, a.d, scale, S);
         }
     }
     cp_async_wait<0>();
@@ -911,10 +969,10 @@ __device__ __forceinline__ void staged_groups(const T* __restrict__ x, const Qua
 // pitch/8 when codes are written (padding columns get zero codes), from the last group to the
 // first: the fused path's norm pass ends on the last columns, which are still in L2.
 template <typename T, int SCHEME, int CODE_BITS, bool WRITE_OUT, bool TRUSTED>
-__global__ void __launch_bounds__(kThreads, 2)
-quantize_kernel(const T* __restrict__ x, QuantArgs a, int64_t groups,
-                unsigned char* __restrict__ codes, float* __restrict__ out) {
-    extern __shared__ uint4 stage[];
+__device__ __forceinline__ void quantize_body(const T* __restrict__ x, const QuantArgs& a,
+                                              int64_t groups, unsigned char* __restrict__ codes,
+                                              float* __restrict__ out, uint4* stage, int64_t vb,
+                                              int64_t nblk) {
     __shared__ float sh_scale;
     const float nrm = __ldg(a.norm_ptr);
     const float scale = block_scale<SCHEME>(nrm, a.n, a.s, &sh_scale);
@@ -927,12 +985,11 @@ quantize_kernel(const T* __restrict__ x, QuantArgs a, int64_t groups,
         full = (live && a.vec_rows) ? a.d / kQCols : 0;
         if (full > 0)
             staged_groups<T, SCHEME, CODE_BITS, WRITE_OUT, TRUSTED>(x, a, dc, full, scale, codes,
-                                                                    out, stage);
+                                                                    out, stage, vb, nblk);
     }
-    const int64_t stride = static_cast<int64_t>(gridDim.x) * kThreads;
+    const int64_t stride = nblk * kThreads;
     const int64_t rest = groups - full;
-    for (int64_t it = static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x; it < rest;
-         it += stride) {
+    for (int64_t it = vb * kThreads + threadIdx.x; it < rest; it += stride) {
         const int64_t g = groups - 1 - it;
         float S[kQCols];
         if (live) {
@@ -945,8 +1002,83 @@ quantize_kernel(const T* __restrict__ x, QuantArgs a, int64_t groups,
                 for (int64_t i = 0; i < a.n; ++i) store_codes<CODE_BITS>(codes, i, g, a.pitch, zero);
             }
         }
-        if (WRITE_OUT) store_out(out, g, a.d, scale, S);
+        if (WRITE_OUT) store_out(out, a.sums, g, a.d, scale, S);
     }
+}
+
+template <typename T, int SCHEME, int CODE_BITS, bool WRITE_OUT, bool TRUSTED>
+__global__ void __launch_bounds__(kThreads, 2)
+quantize_kernel(const T* __restrict__ x, QuantArgs a, int64_t groups,
+                unsigned char* __restrict__ codes, float* __restrict__ out) {
+    extern __shared__ uint4 stage[];
+    quantize_body<T, SCHEME, CODE_BITS, WRITE_OUT, TRUSTED>(x, a, groups, codes, out, stage,
+                                                            blockIdx.x, gridDim.x);
+}
+
+// ------------------------------------------------------------------------------------------
+// Segmented form: many independent problems (layers or gradient buckets), each its own n x d_l
+// matrix with its own norm, in two launches for up to kSegChunk of them.  Every segment gets a
+// run of consecutive blocks sized to its share of the elements; a block finds its segment by
+// binary search over the run starts and then runs the same body as the single-problem kernels
+// on a virtual grid of its segment's blocks.
+// ------------------------------------------------------------------------------------------
+struct SegDesc {
+    const void* x;   // the segment's n x d rows
+    float* out;      // its d outputs
+    int64_t d;
+    int32_t b0;      // first block of its run
+    int32_t nb;      // blocks in its run
+};
+struct SegLaunch {
+    SegDesc seg[kSegChunk];
+    int32_t nseg;
+    int32_t seg0;    // index of seg[0] among all segments of the call
+};
+
+__device__ __forceinline__ int find_segment(const SegLaunch& L, int32_t b) {
+    int lo = 0, hi = L.nseg - 1;  // the last segment whose run starts at or before b
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (L.seg[mid].b0 <= b) lo = mid; else hi = mid - 1;
+    }
+    return lo;
+}
+
+template <typename T, int MODE>
+__global__ void __launch_bounds__(kThreads, 4)
+norm_segments_kernel(const __grid_constant__ SegLaunch L, int64_t n,
+                     float* __restrict__ norms_user, unsigned char* __restrict__ ws) {
+    constexpr int C = Elem<T>::kCols;
+    const int k = find_segment(L, static_cast<int32_t>(blockIdx.x));
+    const SegDesc& sd = L.seg[k];
+    WsHeader* hdr = reinterpret_cast<WsHeader*>(ws);
+    uint64_t* partials = reinterpret_cast<uint64_t*>(ws + kHeaderBytes);
+    const NormSlots slots{partials + sd.b0,
+                          reinterpret_cast<unsigned int*>(ws + kSegTicketsOff) + k, &hdr->status,
+                          reinterpret_cast<float*>(ws + kSegNormsOff) + k,
+                          norms_user ? norms_user + L.seg0 + k : nullptr, nullptr};
+    norm_body<T, MODE>(static_cast<const T*>(sd.x), n, sd.d, (sd.d + C - 1) / C, sd.d % C == 0,
+                       static_cast<int64_t>(blockIdx.x) - sd.b0, sd.nb, slots);
+}
+
+// `base` holds the arguments common to every segment, with step_lo the call's step shifted left
+// by 16 bits: segment l draws its random words with step (step << 16) | l.
+template <typename T, int SCHEME>
+__global__ void __launch_bounds__(kThreads, 2)
+quantize_segments_kernel(const __grid_constant__ SegLaunch L, QuantArgs base,
+                         unsigned char* __restrict__ ws) {
+    extern __shared__ uint4 stage[];
+    const int k = find_segment(L, static_cast<int32_t>(blockIdx.x));
+    const SegDesc& sd = L.seg[k];
+    QuantArgs a = base;
+    a.norm_ptr = reinterpret_cast<const float*>(ws + kSegNormsOff) + k;
+    a.d = sd.d;
+    a.pitch = (sd.d + 31) / 32 * 32;
+    a.vec_rows = sd.d % (16 / sizeof(T)) == 0;
+    a.step_lo = base.step_lo | static_cast<uint32_t>(L.seg0 + k);
+    quantize_body<T, SCHEME, 0, true, true>(static_cast<const T*>(sd.x), a,
+                                            (sd.d + kQCols - 1) / kQCols, nullptr, sd.out, stage,
+                                            static_cast<int64_t>(blockIdx.x) - sd.b0, sd.nb);
 }
 
 // Signed contribution of a code to the integer sum: L sums the level index; E sums

@@ -40,6 +40,46 @@ def resnet50_layer_sizes() -> list:
     return sizes
 
 
+def ddp_buckets(sizes, elem_bytes: int = 4, cap_bytes: int = 25 << 20,
+                first_cap_bytes: int = 1 << 20) -> list:
+    """Gradient buckets as PyTorch DDP forms them: parameters taken in reverse registration
+    order (the order their gradients become ready), a bucket closed once it holds at least its
+    cap (1 MiB for the first, 25 MiB after); returns the buckets' sizes in elements."""
+    out, cur, cap = [], 0, first_cap_bytes
+    for sz in reversed(list(sizes)):
+        cur += sz
+        if cur * elem_bytes >= cap:
+            out.append(cur)
+            cur, cap = 0, cap_bytes
+    if cur:
+        out.append(cur)
+    return out
+
+
+def segment_tensors(n: int, sizes, dtype: str = "f32", seed: int = 0, device="cuda"):
+    """One n x d_l gradient matrix per segment, carved from a single allocation with every
+    segment starting on a 16-byte boundary; values N(0, sigma_l^2) with sigma_l log-uniform in
+    [1e-4, 1e-1] per segment (per-layer gradient scales differ by orders of magnitude)."""
+    import torch
+
+    tdt = torch.bfloat16 if dtype == "bf16" else torch.float32
+    align = 16 // (2 if dtype == "bf16" else 4)
+    offs, off = [], 0
+    for sz in sizes:
+        offs.append(off)
+        off += (n * sz + align - 1) // align * align
+    buf = torch.empty(max(off, 1), dtype=tdt, device=device)
+    g = torch.Generator(device=device)
+    g.manual_seed(seed)
+    sig = 10.0 ** np.random.default_rng(seed).uniform(-4, -1, size=len(sizes))
+    segs = []
+    for o, sz, sg in zip(offs, sizes, sig):
+        t = buf[o:o + n * sz].view(n, sz)
+        t.normal_(0.0, float(sg), generator=g)
+        segs.append(t)
+    return segs
+
+
 # Workloads: the four fixed cases and the sweep.  Philox seed 1, step 0 unless stated.
 CONFIGS = {
     "gauss_n4_d65536": dict(n=4, d=65_536, dtype="f32", dist="normal", scheme=LINEAR, s=15,

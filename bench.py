@@ -47,7 +47,7 @@ def _args():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
-    ap.add_argument("--measure", default=None, choices=["exp-reduce"],
+    ap.add_argument("--measure", default=None, choices=["exp-reduce", "segments"],
                     help="extra measurement instead of the main bench line")
     return ap.parse_args()
 
@@ -304,10 +304,79 @@ def measure_exp_reduce(a) -> int:
     return 0
 
 
+def measure_segments(a) -> int:
+    """The per-layer and per-bucket forms against the whole-vector call, on ResNet-50 with 8
+    workers (fp32, Global-L_127, max norm): the 161 parameter tensors as segments, the 5 buckets
+    PyTorch DDP forms at its 25 MiB cap, and the whole 25,557,032-vector.  Each step is timed
+    with CUDA events on the launching stream after an L2 flush; GB/s counts the fused path's
+    algorithmic bytes (x read twice, out written once)."""
+    import torch
+
+    import allreduce_compatible_gradient_gb300 as gq
+    from allreduce_compatible_gradient_gb300 import workloads
+
+    n, sc, s, q, p, seed = 8, gq.LINEAR, 127, gq.NORM_INF, gq.NORM_INF, 1
+    layers = workloads.resnet50_layer_sizes()
+    buckets = workloads.ddp_buckets(layers)
+    d = sum(layers)
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device="cuda")
+    clean = torch.ones(64 << 20, dtype=torch.float32, device="cuda")
+    ws = gq.gq_workspace()
+    stream = torch.cuda.current_stream()
+
+    def timeit(fn):
+        for k in range(a.warmup):
+            fn(k)
+        torch.cuda.synchronize()
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(a.steps)]
+        for k in range(a.steps):
+            flush.zero_()
+            clean.sum()
+            ev[k][0].record(stream)
+            fn(a.warmup + k)
+            ev[k][1].record(stream)
+        torch.cuda.synchronize()
+        return statistics.mean(e0.elapsed_time(e1) for e0, e1 in ev)
+
+    res = {}
+    for name, sizes in (("layers_161", layers), ("ddp_buckets_5", buckets), ("whole_1", [d])):
+        segs = workloads.segment_tensors(n, sizes, seed=8)
+        outs = [torch.empty(sz, dtype=torch.float32, device="cuda") for sz in sizes]
+        if len(sizes) == 1:
+            ms = timeit(lambda k: gq.gq_allreduce_mean(segs[0], q, p, sc, s, seed, k, out=outs[0],
+                                                       ws=ws, stream=stream))
+        else:
+            ms = timeit(lambda k: gq.gq_allreduce_mean_segments(segs, q, p, sc, s, seed, k,
+                                                                outs=outs, ws=ws, stream=stream))
+        res[name] = ms
+        if name == "layers_161":  # the same layers as 161 separate calls
+            def loop(k):
+                for l, (x, o) in enumerate(zip(segs, outs)):
+                    gq.gq_allreduce_mean(x, q, p, sc, s, seed, (k << 16) | l, out=o, ws=ws,
+                                         stream=stream)
+            res["layers_161_separate_calls"] = timeit(loop)
+        del segs, outs
+        torch.cuda.empty_cache()
+    if gq.gq_get_status(ws) != 0:
+        raise RuntimeError("device status not ok")
+    algo = 2 * n * d * 4 + 4 * d
+    line = {"measure": "segments", "workload": "resnet50 n=8 fp32 Global-L_127 max norm",
+            "d": d, "n": n, "steps": a.steps, "warmup": a.warmup,
+            "ddp_bucket_sizes": buckets,
+            "ms": {k: round(v, 4) for k, v in res.items()},
+            "gb_per_s": {k: round(algo / (v * 1e-3) / 1e9, 1) for k, v in res.items()},
+            "l2": "flushed between timed steps"}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 def main():
     a = _args()
     if a.measure == "exp-reduce":
         return measure_exp_reduce(a)
+    if a.measure == "segments":
+        return measure_segments(a)
     from allreduce_compatible_gradient_gb300 import workloads
 
     cfg = dict(workloads.CONFIGS[a.config], name=a.config)

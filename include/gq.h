@@ -78,8 +78,9 @@ typedef enum {
 int gq_abi_version(void);
 
 /* Bytes of workspace the norm step needs for an n x d problem (a small constant today,
- * 33,024 bytes).  The workspace holds the device status word, the block partials of the norm,
- * a completion ticket and the last norm. */
+ * 35,072 bytes).  The workspace holds the device status word, the block partials of the norm,
+ * a completion ticket and the last norm, and per-segment tickets and norms for
+ * gq_allreduce_mean_segments. */
 size_t gq_workspace_bytes(int64_t n, int64_t d);
 
 /* Zero a freshly allocated workspace (enqueued on `stream`).  Required once before its first
@@ -221,6 +222,52 @@ gq_status gq_exp_allreduce(const void *codes, int s, int64_t n, int64_t d, int o
 gq_status gq_allreduce_mean_noalloc(const void *grads, int dtype, int64_t n, int64_t d, int q,
                                     int p, int scheme, int s, uint64_t seed, uint64_t step,
                                     float *out_dev, float *norm_dev, void *codes, void *stream);
+
+/*
+ * Segmented form (per layer or per gradient bucket, as the DDP hook of Global-QSGD's
+ * implementation paragraph applies the method bucket by bucket): nseg independent problems, each
+ * its own row-major n x d[l] matrix at grads[l] (device, 16-byte aligned, dtype as gq_quantize)
+ * with its own norm ||x_l||_{q,p}, quantised, summed over the n workers and dequantised into
+ * out[l] (device, d[l] floats, 16-byte aligned).  grads, d and out are HOST arrays of nseg
+ * entries.  Segment l draws its random words with step (step << 16) | l, so it equals
+ * gq_allreduce_mean(grads[l], ..., step * 65536 + l) bit for bit; the DDP hook uses the same
+ * numbering for its buckets.  norms_dev (nullable, device) receives the nseg fp32 norms.  Two
+ * launches per 256 segments, whatever their sizes.  1 <= nseg <= 65536, step < 2^48; other
+ * errors as gq_allreduce_mean.  Codes are not written.
+ */
+gq_status gq_allreduce_mean_segments(int64_t nseg, const void *const *grads, const int64_t *d,
+                                     int dtype, int64_t n, int q, int p, int scheme, int s,
+                                     uint64_t seed, uint64_t step, float *const *out,
+                                     float *norms_dev, void *ws, size_t ws_bytes, void *stream);
+
+/*
+ * The global norm when the workers sit on different GPUs.  gq_norm_partial writes this rank's
+ * share of N = ||x||_{q,p} over its m x d rows as one fp64 value at *part_dev: the sum of squares
+ * (q = p = 2) or the largest magnitude (q = p = inf).  Combine the ranks' values with a sum or a
+ * maximum allreduce, then gq_norm_finish turns the combined value into the fp32 norm at *norm_dev
+ * (the square root of the sum, or the maximum itself, rounded to fp32).  For q = p = inf this is
+ * exactly gq_global_norm of the stacked rows; for q = p = 2 it agrees to the l2 forms' relative
+ * 1e-6.  The mixed orders need a d-vector exchange and are refused with GQ_ERR_UNSUPPORTED.  The
+ * workspace is used as by gq_global_norm.
+ */
+gq_status gq_norm_partial(const void *grads, int dtype, int64_t m, int64_t d, int q, int p,
+                          double *part_dev, void *ws, size_t ws_bytes, void *stream);
+gq_status gq_norm_finish(const double *part_dev, int q, int p, float *norm_dev, void *stream);
+
+/*
+ * One rank's share of the allreduce when the workers sit on different GPUs (the communication
+ * hook of Global-QSGD's implementation paragraph: quantise, allreduce, dequantise per gradient
+ * bucket).  Quantises the m x d rows at grads, whose workers are worker0 .. worker0 + m - 1 (the
+ * worker index keys the random words, as row i does in gq_quantize), with the fp32 global norm
+ * at *norm_dev, and writes the integer sum of their codes (Global-L: the level indices; Global-E:
+ * 2^(k-1) units of 2^-(s-1)) to int32 sum_dev[d].  Summing these over all ranks (an integer
+ * allreduce, exact) and calling gq_dequantize with n = the total number of workers gives the
+ * same result as gq_allreduce_mean on the stacked matrix with the same norm.  Errors as
+ * gq_quantize; worker0 >= 0 and worker0 + m <= 2^31.
+ */
+gq_status gq_quantize_sum(const void *grads, int dtype, int64_t m, int64_t d, int64_t worker0,
+                          const float *norm_dev, int scheme, int s, uint64_t seed, uint64_t step,
+                          int32_t *sum_dev, void *stream);
 
 /*
  * Philox4x32-10 on the device, for checking the random stream: `count` calls, input
