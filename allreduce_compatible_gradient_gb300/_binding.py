@@ -11,7 +11,7 @@ import torch
 _PKG = os.path.dirname(os.path.abspath(__file__))
 _LIB_PATH = os.path.join(_PKG, "libgq.so")
 
-F32, BF16 = 0, 1
+F32, BF16, F16 = 0, 1, 2
 LINEAR, EXP = 0, 1
 NORM_INF, NORM_L2 = 0, 2
 ORDER_TREE, ORDER_RING = 0, 1
@@ -52,7 +52,10 @@ def lib() -> ctypes.CDLL:
                                            vp]),
         "gq_philox4x32_10": (ci, [vp, vp, i64, vp]),
         "gq_allreduce_mean_segments": (ci, [i64, vp, vp, ci, i64, ci, ci, ci, ci, u64, u64, vp,
-                                            vp, vp, sz, vp]),
+                                            ci, vp, vp, sz, vp]),
+        "gq_dequantize_to": (ci, [vp, vp, ci, ci, i64, i64, vp, ci, vp]),
+        "gq_allreduce_mean_to": (ci, [vp, ci, i64, i64, ci, ci, ci, ci, u64, u64, vp, ci, vp, vp,
+                                      vp, sz, vp]),
         "gq_norm_partial": (ci, [vp, ci, i64, i64, ci, ci, vp, vp, sz, vp]),
         "gq_norm_finish": (ci, [vp, ci, ci, vp, vp]),
         "gq_quantize_sum": (ci, [vp, ci, i64, i64, i64, vp, ci, ci, u64, u64, vp, vp]),
@@ -167,25 +170,52 @@ def gq_reduce_codes(codes, scheme, s, n, d, sums=None, stream=None) -> torch.Ten
     return sums
 
 
-def gq_dequantize(sums, norm, scheme, s, n, out=None, stream=None) -> torch.Tensor:
+_OUT_TYPES = {torch.float32: F32, torch.bfloat16: BF16, torch.float16: F16}
+
+
+def _out_code(out: torch.Tensor) -> int:
+    if out.dtype not in _OUT_TYPES or not out.is_cuda or not out.is_contiguous():
+        raise TypeError("outputs must be contiguous float32, bfloat16 or float16 CUDA tensors")
+    return _OUT_TYPES[out.dtype]
+
+
+def gq_dequantize(sums, norm, scheme, s, n, out=None, stream=None,
+                  out_dtype=torch.float32) -> torch.Tensor:
+    """Dequantised mean into out (float32, bfloat16 or float16; a new tensor of out_dtype when
+    out is None)."""
     d = sums.numel()
     if out is None:
-        out = torch.empty(d, dtype=torch.float32, device=sums.device)
-    _check(lib().gq_dequantize(_p(sums), _p(norm), scheme, s, n, d, _p(out), _stream(stream)),
-           "gq_dequantize")
+        out = torch.empty(d, dtype=out_dtype, device=sums.device)
+    _check(lib().gq_dequantize_to(_p(sums), _p(norm), scheme, s, n, d, _p(out), _out_code(out),
+                                  _stream(stream)), "gq_dequantize_to")
     return out
 
 
 def gq_allreduce_mean(grads, q, p, scheme, s, seed, step, out=None, norm=None, codes=None,
-                      ws=None, stream=None) -> torch.Tensor:
+                      ws=None, stream=None, out_dtype=torch.float32) -> torch.Tensor:
+    """Fused pipeline; out is float32, bfloat16 or float16 (a new tensor of out_dtype when
+    None)."""
     dt, n, d = _grads(grads)
     if out is None:
-        out = torch.empty(d, dtype=torch.float32, device=grads.device)
+        out = torch.empty(d, dtype=out_dtype, device=grads.device)
     ws = gq_workspace(grads.device, stream) if ws is None else ws
-    _check(lib().gq_allreduce_mean(_p(grads), dt, n, d, q, p, scheme, s, seed, step, _p(out),
-                                   _p(norm), _p(codes), _p(ws), ws.numel(), _stream(stream)),
-           "gq_allreduce_mean")
+    _check(lib().gq_allreduce_mean_to(_p(grads), dt, n, d, q, p, scheme, s, seed, step, _p(out),
+                                      _out_code(out), _p(norm), _p(codes), _p(ws), ws.numel(),
+                                      _stream(stream)), "gq_allreduce_mean_to")
     return out
+
+
+def gq_dequantize_to(sums, norm, scheme, s, n, out=None, out_dtype=torch.float32,
+                     stream=None) -> torch.Tensor:
+    """gq_dequantize with an explicit output type (float32, bfloat16 or float16)."""
+    return gq_dequantize(sums, norm, scheme, s, n, out=out, stream=stream, out_dtype=out_dtype)
+
+
+def gq_allreduce_mean_to(grads, q, p, scheme, s, seed, step, out=None, out_dtype=torch.float32,
+                         norm=None, codes=None, ws=None, stream=None) -> torch.Tensor:
+    """gq_allreduce_mean with an explicit output type (float32, bfloat16 or float16)."""
+    return gq_allreduce_mean(grads, q, p, scheme, s, seed, step, out=out, norm=norm, codes=codes,
+                             ws=ws, stream=stream, out_dtype=out_dtype)
 
 
 def gq_allreduce_mean_with_norm(grads, norm, scheme, s, seed, step, out=None, codes=None,
@@ -200,9 +230,10 @@ def gq_allreduce_mean_with_norm(grads, norm, scheme, s, seed, step, out=None, co
 
 
 def gq_allreduce_mean_segments(grads, q, p, scheme, s, seed, step, outs=None, norms=None,
-                               ws=None, stream=None):
+                               ws=None, stream=None, out_dtype=torch.float32):
     """Per-segment fused pipeline: grads is a list of n x d_l CUDA tensors (same dtype and n);
-    returns the list of d_l fp32 outputs.  Segment l uses step (step << 16) | l."""
+    returns the list of d_l outputs (all of one type: float32, bfloat16 or float16).  Segment l
+    uses step (step << 16) | l."""
     grads = list(grads)
     if not grads:
         raise ValueError("no segments")
@@ -218,9 +249,12 @@ def gq_allreduce_mean_segments(grads, q, p, scheme, s, seed, step, outs=None, no
         raise ValueError("every segment needs the same dtype")
     dev = grads[0].device
     if outs is None:
-        outs = [torch.empty(g.shape[1], dtype=torch.float32, device=dev) for g in grads]
+        outs = [torch.empty(g.shape[1], dtype=out_dtype, device=dev) for g in grads]
     if len(outs) != len(grads):
         raise ValueError("one output per segment")
+    oc = {_out_code(o) for o in outs}
+    if len(oc) != 1:
+        raise ValueError("every segment output needs the same type")
     if ws is None:
         ws = gq_workspace(dev, stream)
     L = len(grads)
@@ -228,7 +262,8 @@ def gq_allreduce_mean_segments(grads, q, p, scheme, s, seed, step, outs=None, no
     dv = (ctypes.c_int64 * L)(*[g.shape[1] for g in grads])
     op = (ctypes.c_void_p * L)(*[o.data_ptr() for o in outs])
     _check(lib().gq_allreduce_mean_segments(L, gp, dv, dts.pop(), n, q, p, scheme, s, seed, step,
-                                            op, _p(norms), _p(ws), ws.numel(), _stream(stream)),
+                                            op, oc.pop(), _p(norms), _p(ws), ws.numel(),
+                                            _stream(stream)),
            "gq_allreduce_mean_segments")
     return outs
 

@@ -12,7 +12,8 @@ dequantises.  Here each rank is one worker: rank r holds x_r, the flat gradient 
      index r keying the random words;
   3. an int32 SUM allreduce of those d integers (exact in any order: |sum| < 2^24);
   4. gq_dequantize with n = world size -> the unbiased estimate of the mean gradient, written
-     back into the bucket.
+     back into the bucket in its own type (a bf16 bucket gets the fp32 value rounded to nearest
+     even).
 
 On one GPU with world size 1 this is gq_allreduce_mean of the 1 x d bucket.  The random stream
 of bucket b at iteration t uses step t * 2^16 + b (t < 2^48, b < 2^16), so every bucket and
@@ -56,7 +57,7 @@ class LibraryOps:
         return gq.gq_quantize_sum(x, norm, scheme, s, seed, step, worker0=worker0)
 
     def dequantize(self, sums, norm, scheme, s, n, out):
-        return gq.gq_dequantize(sums, norm, scheme, s, n, out=out)
+        return gq.gq_dequantize(sums, norm, scheme, s, n, out=out)  # out: fp32 or bf16 bucket
 
 
 @dataclass
@@ -128,10 +129,7 @@ def global_qsgd_hook(state: GlobalQSGDState, bucket) -> torch.futures.Future:
 
     def finish(f):
         total = f.value()[0]
-        if buf.dtype == torch.float32:
-            ops.dequantize(total, norm, state.scheme, state.s, n, buf)
-        else:
-            buf.copy_(ops.dequantize(total, norm, state.scheme, state.s, n, None))
+        ops.dequantize(total, norm, state.scheme, state.s, n, buf)  # in the bucket's own type
         return buf
 
     return fut.then(finish)

@@ -148,7 +148,7 @@ gq_status norm_any(const void* grads, int dtype, int mode, int64_t n, int64_t d,
 // TRUSTED: the norm comes from norm_kernel on the same gradients (fused path), so a finite norm
 // rules out NaN and infinite elements.
 template <typename T, int SCHEME, int BITS, bool OUT, bool TRUSTED>
-gq_status run_quant(const void* grads, const gq::QuantArgs& a, void* codes, float* out,
+gq_status run_quant(const void* grads, const gq::QuantArgs& a, void* codes, void* out,
                     cudaStream_t st) {
     const int64_t groups = BITS ? a.pitch / gq::kQCols : (a.d + gq::kQCols - 1) / gq::kQCols;
     auto k = gq::quantize_kernel<T, SCHEME, BITS, OUT, TRUSTED>;
@@ -160,7 +160,7 @@ gq_status run_quant(const void* grads, const gq::QuantArgs& a, void* codes, floa
 }
 
 template <typename T, int SCHEME, bool OUT, bool TRUSTED>
-gq_status quant_bits(const void* grads, const gq::QuantArgs& a, int bits, void* codes, float* out,
+gq_status quant_bits(const void* grads, const gq::QuantArgs& a, int bits, void* codes, void* out,
                      cudaStream_t st) {
     if (!codes) return run_quant<T, SCHEME, 0, OUT, TRUSTED>(grads, a, nullptr, out, st);
     if (bits == 4) return run_quant<T, SCHEME, 4, OUT, TRUSTED>(grads, a, codes, out, st);
@@ -169,7 +169,7 @@ gq_status quant_bits(const void* grads, const gq::QuantArgs& a, int bits, void* 
 
 template <bool OUT, bool TRUSTED>
 gq_status quant_any(const void* grads, int dtype, const gq::QuantArgs& a, int scheme, int bits,
-                    void* codes, float* out, cudaStream_t st) {
+                    void* codes, void* out, cudaStream_t st) {
     if (dtype == GQ_F32)
         return scheme == GQ_LINEAR
                    ? quant_bits<float, gq::kLinear, OUT, TRUSTED>(grads, a, bits, codes, out, st)
@@ -198,6 +198,7 @@ gq::QuantArgs make_args(const float* norm_ptr, int dtype, int64_t n, int64_t d, 
     a.vec_rows = (d % (dtype == GQ_F32 ? 4 : 8)) == 0;
     a.row0 = 0;
     a.sums = nullptr;
+    a.out_dtype = gq::kOutF32;
     return a;
 }
 
@@ -282,10 +283,11 @@ gq_status gq_reduce_codes(const void* codes, int scheme, int s, int64_t n, int64
     return launch_status();
 }
 
-gq_status gq_dequantize(const int32_t* sum_dev, const float* norm_dev, int scheme, int s,
-                        int64_t n, int64_t d, float* out_dev, void* stream) {
+gq_status gq_dequantize_to(const int32_t* sum_dev, const float* norm_dev, int scheme, int s,
+                           int64_t n, int64_t d, void* out_dev, int out_dtype, void* stream) {
     if (!sum_dev || !norm_dev || !out_dev || !aligned16(sum_dev) || !aligned16(out_dev))
         return GQ_ERR_INVALID;
+    if (out_dtype != GQ_F32 && out_dtype != GQ_BF16 && out_dtype != GQ_F16) return GQ_ERR_INVALID;
     if (n < 1 || n >= (int64_t(1) << 31) || d < 1 || d >= kMaxD) return GQ_ERR_INVALID;
     gq_status st = check_scheme(scheme, s, n);
     if (st != GQ_OK) return st;
@@ -293,31 +295,48 @@ gq_status gq_dequantize(const int32_t* sum_dev, const float* norm_dev, int schem
     const int64_t quads = (d + 3) / 4;
     if (scheme == GQ_LINEAR) {
         auto k = gq::dequantize_kernel<gq::kLinear>;
-        k<<<grid_for(k, quads), kThreads, 0, cs>>>(sum_dev, norm_dev, n, static_cast<uint32_t>(s), d, out_dev);
+        k<<<grid_for(k, quads), kThreads, 0, cs>>>(sum_dev, norm_dev, n, static_cast<uint32_t>(s), d,
+                                                   out_dev, out_dtype);
     } else {
         auto k = gq::dequantize_kernel<gq::kExp>;
-        k<<<grid_for(k, quads), kThreads, 0, cs>>>(sum_dev, norm_dev, n, static_cast<uint32_t>(s), d, out_dev);
+        k<<<grid_for(k, quads), kThreads, 0, cs>>>(sum_dev, norm_dev, n, static_cast<uint32_t>(s), d,
+                                                   out_dev, out_dtype);
     }
     return launch_status();
 }
 
-gq_status gq_allreduce_mean(const void* grads, int dtype, int64_t n, int64_t d, int q, int p,
-                            int scheme, int s, uint64_t seed, uint64_t step, float* out_dev,
-                            float* norm_dev, void* codes, void* ws, size_t ws_bytes,
-                            void* stream) {
+gq_status gq_dequantize(const int32_t* sum_dev, const float* norm_dev, int scheme, int s,
+                        int64_t n, int64_t d, float* out_dev, void* stream) {
+    return gq_dequantize_to(sum_dev, norm_dev, scheme, s, n, d, out_dev, GQ_F32, stream);
+}
+
+gq_status gq_allreduce_mean_to(const void* grads, int dtype, int64_t n, int64_t d, int q, int p,
+                               int scheme, int s, uint64_t seed, uint64_t step, void* out_dev,
+                               int out_dtype, float* norm_dev, void* codes, void* ws,
+                               size_t ws_bytes, void* stream) {
     gq_status st = check_grads(grads, dtype, n, d);
     if (st != GQ_OK) return st;
     const int mode = norm_mode(q, p);
     if (mode < 0) return GQ_ERR_INVALID;
+    if (out_dtype != GQ_F32 && out_dtype != GQ_BF16 && out_dtype != GQ_F16) return GQ_ERR_INVALID;
     if ((st = check_scheme(scheme, s, n)) != GQ_OK) return st;
     if (!out_dev || !aligned16(out_dev) || (codes && !aligned16(codes))) return GQ_ERR_INVALID;
     if ((st = check_ws(ws, ws_bytes, n, d)) != GQ_OK) return st;
     cudaStream_t cs = static_cast<cudaStream_t>(stream);
     if ((st = norm_any(grads, dtype, mode, n, d, norm_dev, ws, cs)) != GQ_OK) return st;
     const float* ws_norm = &reinterpret_cast<const gq::WsHeader*>(ws)->norm;
-    const gq::QuantArgs a = make_args(ws_norm, dtype, n, d, s, seed, step);
+    gq::QuantArgs a = make_args(ws_norm, dtype, n, d, s, seed, step);
+    a.out_dtype = out_dtype;
     return quant_any<true, true>(grads, dtype, a, scheme, gq_code_bits(scheme, s), codes, out_dev,
                                  cs);
+}
+
+gq_status gq_allreduce_mean(const void* grads, int dtype, int64_t n, int64_t d, int q, int p,
+                            int scheme, int s, uint64_t seed, uint64_t step, float* out_dev,
+                            float* norm_dev, void* codes, void* ws, size_t ws_bytes,
+                            void* stream) {
+    return gq_allreduce_mean_to(grads, dtype, n, d, q, p, scheme, s, seed, step, out_dev, GQ_F32,
+                                norm_dev, codes, ws, ws_bytes, stream);
 }
 
 gq_status gq_allreduce_mean_with_norm(const void* grads, int dtype, int64_t n, int64_t d,
@@ -634,10 +653,11 @@ gq_status run_quant_segments(gq::SegLaunch& L, const int64_t* d, int64_t n,
 extern "C" gq_status gq_allreduce_mean_segments(int64_t nseg, const void* const* grads,
                                                 const int64_t* d, int dtype, int64_t n, int q,
                                                 int p, int scheme, int s, uint64_t seed,
-                                                uint64_t step, float* const* out,
+                                                uint64_t step, void* const* out, int out_dtype,
                                                 float* norms_dev, void* ws, size_t ws_bytes,
                                                 void* stream) {
     if (nseg < 1 || nseg > 65536 || !grads || !d || !out) return GQ_ERR_INVALID;
+    if (out_dtype != GQ_F32 && out_dtype != GQ_BF16 && out_dtype != GQ_F16) return GQ_ERR_INVALID;
     if (step >= (uint64_t(1) << 48)) return GQ_ERR_INVALID;
     gq_status st;
     for (int64_t l = 0; l < nseg; ++l) {
@@ -651,6 +671,7 @@ extern "C" gq_status gq_allreduce_mean_segments(int64_t nseg, const void* const*
     unsigned char* w = static_cast<unsigned char*>(ws);
     cudaStream_t cs = static_cast<cudaStream_t>(stream);
     gq::QuantArgs base = make_args(nullptr, dtype, n, 1, s, seed, step << 16);
+    base.out_dtype = out_dtype;
     gq::SegLaunch L;  // ~8 KB of kernel parameters per launch
     for (int64_t c0 = 0; c0 < nseg; c0 += gq::kSegChunk) {
         const int64_t m = nseg - c0 < gq::kSegChunk ? nseg - c0 : gq::kSegChunk;

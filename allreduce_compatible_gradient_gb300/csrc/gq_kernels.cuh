@@ -12,11 +12,15 @@
 #pragma once
 
 #include <cstdint>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
 namespace gq {
 
 constexpr int kThreads = 256;        // threads per block for every kernel
+// output element types of the dequantised mean (the values of gq_dtype)
+constexpr int kOutF32 = 0, kOutBF16 = 1, kOutF16 = 2;
 constexpr int kMaxPartials = 4096;   // upper bound on norm-kernel blocks (workspace size)
 constexpr int kHeaderBytes = 256;    // workspace header, then kMaxPartials 8-byte partials
 constexpr int kSegChunk = 256;       // segments per launch of the segmented kernels
@@ -590,6 +594,7 @@ struct QuantArgs {
     bool vec_rows;
     uint32_t row0;           // worker index of local row 0 (keys the random words)
     int32_t* sums;           // when set, the kernel writes the integer sums here instead of out
+    int out_dtype;           // kOutF32, kOutBF16 or kOutF16
 };
 
 // Per-block fp32 dequantisation scale from the fp32 norm, computed in fp64 by one thread:
@@ -838,10 +843,30 @@ __device__ __forceinline__ void unstage(const uint4* piece0, const uint4* piece1
     }
 }
 
-// Output of one finished column group: dequantise the sums into out, or, when `sums` is set,
-// write the integer sums themselves (exact: every partial sum is an integer below 2^24).
-__device__ __forceinline__ void store_out(float* __restrict__ out, int32_t* __restrict__ sums,
-                                          int64_t g, int64_t d, float scale,
+// Round-to-nearest-even conversions of the fp32 outputs to the 16-bit output types.
+__device__ __forceinline__ uint32_t pack16(int dt, float lo, float hi) {
+    if (dt == kOutBF16) {
+        const __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+        return *reinterpret_cast<const uint32_t*>(&h);
+    }
+    const __half2 h = __floats2half2_rn(lo, hi);
+    return *reinterpret_cast<const uint32_t*>(&h);
+}
+__device__ __forceinline__ void store1(void* out, int dt, int64_t j, float v) {
+    if (dt == kOutF32) {
+        static_cast<float*>(out)[j] = v;
+    } else if (dt == kOutBF16) {
+        static_cast<__nv_bfloat16*>(out)[j] = __float2bfloat16_rn(v);
+    } else {
+        static_cast<__half*>(out)[j] = __float2half_rn(v);
+    }
+}
+
+// Output of one finished column group: dequantise the sums into out (fp32, bf16 or fp16), or,
+// when `sums` is set, write the integer sums themselves (exact: every partial sum is an integer
+// below 2^24).
+__device__ __forceinline__ void store_out(void* __restrict__ out, int32_t* __restrict__ sums,
+                                          int dt, int64_t g, int64_t d, float scale,
                                           const float (&S)[kQCols]) {
     const int64_t j0 = g * kQCols;
     if (sums) {
@@ -859,15 +884,22 @@ __device__ __forceinline__ void store_out(float* __restrict__ out, int32_t* __re
         return;
     }
     if (j0 + kQCols <= d) {
+        if (dt == kOutF32) {
+            float* o = static_cast<float*>(out);
 #pragma unroll
-        for (int h = 0; h < kQCols / 4; ++h)
-            reinterpret_cast<float4*>(out + j0)[h] =
-                make_float4(scale * S[4 * h], scale * S[4 * h + 1], scale * S[4 * h + 2],
-                            scale * S[4 * h + 3]);
+            for (int h = 0; h < kQCols / 4; ++h)
+                reinterpret_cast<float4*>(o + j0)[h] =
+                    make_float4(scale * S[4 * h], scale * S[4 * h + 1], scale * S[4 * h + 2],
+                                scale * S[4 * h + 3]);
+        } else {  // eight 16-bit values: one 16-byte store
+            *reinterpret_cast<uint4*>(static_cast<uint16_t*>(out) + j0) =
+                make_uint4(pack16(dt, scale * S[0], scale * S[1]), pack16(dt, scale * S[2], scale * S[3]),
+                           pack16(dt, scale * S[4], scale * S[5]), pack16(dt, scale * S[6], scale * S[7]));
+        }
     } else {
 #pragma unroll
         for (int c = 0; c < kQCols; ++c)
-            if (j0 + c < d) out[j0 + c] = scale * S[c];
+            if (j0 + c < d) store1(out, dt, j0 + c, scale * S[c]);
     }
 }
 
@@ -877,7 +909,7 @@ template <typename T, int SCHEME, int CODE_BITS, bool WRITE_OUT, bool TRUSTED>
 __device__ __forceinline__ void staged_groups(const T* __restrict__ x, const QuantArgs& a,
                                               const Decide& dc, int64_t full, float scale,
                                               unsigned char* __restrict__ codes,
-                                              float* __restrict__ out, uint4* stage, int64_t vb,
+                                              void* __restrict__ out, uint4* stage, int64_t vb,
                                               int64_t nblk) {
     using St = Staging<T>;
     constexpr int R = St::kRows, P = St::kPieces, NS = St::kStages;
@@ -957,7 +989,7 @@ __device__ __forceinline__ void staged_groups(const T* __restrict__ x, const Qua
         if (++r == nb) {
             r = 0;
             ++q;
-            if (WRITE_OUT) store_out(out, a.sums, g, a.d, scale, S);
+            if (WRITE_OUT) store_out(out, a.sums, a.out_dtype, g, a.d, scale, S);
         }
     }
     cp_async_wait<0>();
@@ -971,7 +1003,7 @@ __device__ __forceinline__ void staged_groups(const T* __restrict__ x, const Qua
 template <typename T, int SCHEME, int CODE_BITS, bool WRITE_OUT, bool TRUSTED>
 __device__ __forceinline__ void quantize_body(const T* __restrict__ x, const QuantArgs& a,
                                               int64_t groups, unsigned char* __restrict__ codes,
-                                              float* __restrict__ out, uint4* stage, int64_t vb,
+                                              void* __restrict__ out, uint4* stage, int64_t vb,
                                               int64_t nblk) {
     __shared__ float sh_scale;
     const float nrm = __ldg(a.norm_ptr);
@@ -1002,14 +1034,14 @@ __device__ __forceinline__ void quantize_body(const T* __restrict__ x, const Qua
                 for (int64_t i = 0; i < a.n; ++i) store_codes<CODE_BITS>(codes, i, g, a.pitch, zero);
             }
         }
-        if (WRITE_OUT) store_out(out, a.sums, g, a.d, scale, S);
+        if (WRITE_OUT) store_out(out, a.sums, a.out_dtype, g, a.d, scale, S);
     }
 }
 
 template <typename T, int SCHEME, int CODE_BITS, bool WRITE_OUT, bool TRUSTED>
 __global__ void __launch_bounds__(kThreads, 2)
 quantize_kernel(const T* __restrict__ x, QuantArgs a, int64_t groups,
-                unsigned char* __restrict__ codes, float* __restrict__ out) {
+                unsigned char* __restrict__ codes, void* __restrict__ out) {
     extern __shared__ uint4 stage[];
     quantize_body<T, SCHEME, CODE_BITS, WRITE_OUT, TRUSTED>(x, a, groups, codes, out, stage,
                                                             blockIdx.x, gridDim.x);
@@ -1024,7 +1056,7 @@ quantize_kernel(const T* __restrict__ x, QuantArgs a, int64_t groups,
 // ------------------------------------------------------------------------------------------
 struct SegDesc {
     const void* x;   // the segment's n x d rows
-    float* out;      // its d outputs
+    void* out;       // its d outputs
     int64_t d;
     int32_t b0;      // first block of its run
     int32_t nb;      // blocks in its run
@@ -1146,7 +1178,7 @@ reduce_codes_kernel(const unsigned char* __restrict__ codes, int64_t n, int64_t 
 template <int SCHEME>
 __global__ void __launch_bounds__(kThreads)
 dequantize_kernel(const int32_t* __restrict__ sums, const float* __restrict__ norm_ptr,
-                  int64_t n, uint32_t s, int64_t d, float* __restrict__ out) {
+                  int64_t n, uint32_t s, int64_t d, void* __restrict__ out, int dt) {
     __shared__ float sh_scale;
     const float scale = block_scale<SCHEME>(__ldg(norm_ptr), n, s, &sh_scale);
     const int64_t quads = (d + 3) / 4;
@@ -1156,11 +1188,15 @@ dequantize_kernel(const int32_t* __restrict__ sums, const float* __restrict__ no
         const int64_t j0 = q * 4;
         if (j0 + 4 <= d) {
             const int4 t = __ldg(reinterpret_cast<const int4*>(sums + j0));
-            reinterpret_cast<float4*>(out + j0)[0] =
-                make_float4(scale * static_cast<float>(t.x), scale * static_cast<float>(t.y),
-                            scale * static_cast<float>(t.z), scale * static_cast<float>(t.w));
+            const float v0 = scale * static_cast<float>(t.x), v1 = scale * static_cast<float>(t.y);
+            const float v2 = scale * static_cast<float>(t.z), v3 = scale * static_cast<float>(t.w);
+            if (dt == kOutF32)
+                reinterpret_cast<float4*>(out)[q] = make_float4(v0, v1, v2, v3);
+            else
+                reinterpret_cast<uint2*>(out)[q] = make_uint2(pack16(dt, v0, v1), pack16(dt, v2, v3));
         } else {
-            for (int64_t j = j0; j < d; ++j) out[j] = scale * static_cast<float>(__ldg(sums + j));
+            for (int64_t j = j0; j < d; ++j)
+                store1(out, dt, j, scale * static_cast<float>(__ldg(sums + j)));
         }
     }
 }

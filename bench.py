@@ -350,6 +350,12 @@ def measure_segments(a) -> int:
             ms = timeit(lambda k: gq.gq_allreduce_mean_segments(segs, q, p, sc, s, seed, k,
                                                                 outs=outs, ws=ws, stream=stream))
         res[name] = ms
+        if name == "whole_1":  # the same call writing a bf16 mean (half the output bytes)
+            o16 = torch.empty(d, dtype=torch.bfloat16, device="cuda")
+            res["whole_1_bf16_out"] = timeit(
+                lambda k: gq.gq_allreduce_mean(segs[0], q, p, sc, s, seed, k, out=o16, ws=ws,
+                                               stream=stream))
+            del o16
         if name == "layers_161":  # the same layers as 161 separate calls
             def loop(k):
                 for l, (x, o) in enumerate(zip(segs, outs)):

@@ -63,7 +63,9 @@ typedef enum {
     GQ_ERR_WORKSPACE = 7    /* workspace null, too small or misaligned */
 } gq_status;
 
-typedef enum { GQ_F32 = 0, GQ_BF16 = 1 } gq_dtype;
+/* Element types: gradients are GQ_F32 or GQ_BF16; the dequantised mean (the *_to entry points
+ * and the segmented form) may also be GQ_BF16 or GQ_F16. */
+typedef enum { GQ_F32 = 0, GQ_BF16 = 1, GQ_F16 = 2 } gq_dtype;
 
 typedef enum {
     GQ_LINEAR = 0, /* Global-L_s, standard dithering */
@@ -138,6 +140,15 @@ gq_status gq_dequantize(const int32_t *sum_dev, const float *norm_dev, int schem
                         int64_t n, int64_t d, float *out_dev, void *stream);
 
 /*
+ * gq_dequantize with the output type out_dtype (GQ_F32, GQ_BF16 or GQ_F16): the fp32 value above
+ * rounded to nearest even, so a 16-bit output adds at most half a unit in its last place (fp16:
+ * magnitudes past 65504 become infinite, as IEEE rounding gives).  out_dev: d elements of that
+ * type, 16-byte aligned.  Any other out_dtype: GQ_ERR_INVALID.
+ */
+gq_status gq_dequantize_to(const int32_t *sum_dev, const float *norm_dev, int scheme, int s,
+                           int64_t n, int64_t d, void *out_dev, int out_dtype, void *stream);
+
+/*
  * Steps 1-4 fused: the norm pass, then one pass that quantises, sums over the workers in
  * registers and dequantises, so codes and sums never touch memory.  Traffic: X is read twice,
  * out written once.  norm_dev (nullable) receives the fp32 norm; codes (nullable) receives the
@@ -148,6 +159,15 @@ gq_status gq_allreduce_mean(const void *grads, int dtype, int64_t n, int64_t d, 
                             int scheme, int s, uint64_t seed, uint64_t step, float *out_dev,
                             float *norm_dev, void *codes, void *ws, size_t ws_bytes,
                             void *stream);
+
+/*
+ * gq_allreduce_mean with the output type out_dtype (GQ_F32, GQ_BF16 or GQ_F16), rounded as in
+ * gq_dequantize_to; a 16-bit output halves the bytes written.
+ */
+gq_status gq_allreduce_mean_to(const void *grads, int dtype, int64_t n, int64_t d, int q, int p,
+                               int scheme, int s, uint64_t seed, uint64_t step, void *out_dev,
+                               int out_dtype, float *norm_dev, void *codes, void *ws,
+                               size_t ws_bytes, void *stream);
 
 /*
  * Steps 2-4 fused with a norm supplied in device memory (*norm_dev), e.g. one agreed on by a
@@ -228,7 +248,8 @@ gq_status gq_allreduce_mean_noalloc(const void *grads, int dtype, int64_t n, int
  * implementation paragraph applies the method bucket by bucket): nseg independent problems, each
  * its own row-major n x d[l] matrix at grads[l] (device, 16-byte aligned, dtype as gq_quantize)
  * with its own norm ||x_l||_{q,p}, quantised, summed over the n workers and dequantised into
- * out[l] (device, d[l] floats, 16-byte aligned).  grads, d and out are HOST arrays of nseg
+ * out[l] (device, d[l] elements of out_dtype as in gq_dequantize_to, 16-byte aligned).
+ * grads, d and out are HOST arrays of nseg
  * entries.  Segment l draws its random words with step (step << 16) | l, so it equals
  * gq_allreduce_mean(grads[l], ..., step * 65536 + l) bit for bit; the DDP hook uses the same
  * numbering for its buckets.  norms_dev (nullable, device) receives the nseg fp32 norms.  Two
@@ -237,8 +258,9 @@ gq_status gq_allreduce_mean_noalloc(const void *grads, int dtype, int64_t n, int
  */
 gq_status gq_allreduce_mean_segments(int64_t nseg, const void *const *grads, const int64_t *d,
                                      int dtype, int64_t n, int q, int p, int scheme, int s,
-                                     uint64_t seed, uint64_t step, float *const *out,
-                                     float *norms_dev, void *ws, size_t ws_bytes, void *stream);
+                                     uint64_t seed, uint64_t step, void *const *out,
+                                     int out_dtype, float *norms_dev, void *ws, size_t ws_bytes,
+                                     void *stream);
 
 /*
  * The global norm when the workers sit on different GPUs.  gq_norm_partial writes this rank's
