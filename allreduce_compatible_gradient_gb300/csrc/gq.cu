@@ -38,7 +38,7 @@ int sm_count() {
 // (kernel, device).  The first query for a kernel on a device also raises that kernel's
 // dynamic shared-memory limit to `smem`.
 template <typename K>
-int blocks_per_sm(K kernel, int smem = 0) {
+int blocks_per_sm(K kernel, int smem = 0, int threads = kThreads) {
     struct Entry {
         const void* fn;
         int dev;
@@ -56,7 +56,7 @@ int blocks_per_sm(K kernel, int smem = 0) {
     if (smem > 0)  // dynamic + static shared memory may pass the default 48 KB
         cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     int nb = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, kernel, kThreads, smem) != cudaSuccess ||
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, kernel, threads, smem) != cudaSuccess ||
         nb <= 0)
         nb = 1;
     if (used < 512) table[used++] = Entry{fn, dev, nb};
@@ -147,10 +147,22 @@ gq_status norm_any(const void* grads, int dtype, int mode, int64_t n, int64_t d,
 // ---- quantize (+ sum + dequantize) ----------------------------------------------------------
 // TRUSTED: the norm comes from norm_kernel on the same gradients (fused path), so a finite norm
 // rules out NaN and infinite elements.
+// Problems with at least one 3840-column chunk per SM of 16-byte aligned rows take the kernel
+// fed by bulk copies (it needs a status word for its bounded waits); the rest the direct one.
 template <typename T, int SCHEME, int BITS, bool OUT, bool TRUSTED>
 gq_status run_quant(const void* grads, const gq::QuantArgs& a, void* codes, void* out,
-                    cudaStream_t st) {
+                    cudaStream_t st, unsigned int* status = nullptr) {
     const int64_t groups = BITS ? a.pitch / gq::kQCols : (a.d + gq::kQCols - 1) / gq::kQCols;
+    const int64_t chunks = (a.d / gq::kQCols) / gq::kTmaConsumers;
+    if (status && a.vec_rows && chunks >= sm_count()) {
+        auto kt = gq::quantize_tma_kernel<T, SCHEME, BITS, OUT, TRUSTED>;
+        constexpr int tsmem = gq::TmaCfg<T>::kSmemBytes;
+        if (blocks_per_sm(kt, tsmem, gq::kTmaBlock) < 1) return GQ_ERR_CUDA;
+        const unsigned grid = static_cast<unsigned>(sm_count());
+        kt<<<grid, gq::kTmaBlock, tsmem, st>>>(static_cast<const T*>(grads), a, groups,
+                                               static_cast<unsigned char*>(codes), out, status);
+        return launch_status();
+    }
     auto k = gq::quantize_kernel<T, SCHEME, BITS, OUT, TRUSTED>;
     constexpr int smem = gq::Staging<T>::kBytes;
     const unsigned grid = grid_for(k, groups, INT32_MAX, smem);
@@ -161,22 +173,23 @@ gq_status run_quant(const void* grads, const gq::QuantArgs& a, void* codes, void
 
 template <typename T, int SCHEME, bool OUT, bool TRUSTED>
 gq_status quant_bits(const void* grads, const gq::QuantArgs& a, int bits, void* codes, void* out,
-                     cudaStream_t st) {
-    if (!codes) return run_quant<T, SCHEME, 0, OUT, TRUSTED>(grads, a, nullptr, out, st);
-    if (bits == 4) return run_quant<T, SCHEME, 4, OUT, TRUSTED>(grads, a, codes, out, st);
-    return run_quant<T, SCHEME, 8, OUT, TRUSTED>(grads, a, codes, out, st);
+                     cudaStream_t st, unsigned int* status) {
+    if (!codes) return run_quant<T, SCHEME, 0, OUT, TRUSTED>(grads, a, nullptr, out, st, status);
+    if (bits == 4) return run_quant<T, SCHEME, 4, OUT, TRUSTED>(grads, a, codes, out, st, status);
+    return run_quant<T, SCHEME, 8, OUT, TRUSTED>(grads, a, codes, out, st, status);
 }
 
+// status (nullable): the workspace status word, for the bounded waits of the bulk-copy kernel
 template <bool OUT, bool TRUSTED>
 gq_status quant_any(const void* grads, int dtype, const gq::QuantArgs& a, int scheme, int bits,
-                    void* codes, void* out, cudaStream_t st) {
+                    void* codes, void* out, cudaStream_t st, unsigned int* status = nullptr) {
     if (dtype == GQ_F32)
         return scheme == GQ_LINEAR
-                   ? quant_bits<float, gq::kLinear, OUT, TRUSTED>(grads, a, bits, codes, out, st)
-                   : quant_bits<float, gq::kExp, OUT, TRUSTED>(grads, a, bits, codes, out, st);
+                   ? quant_bits<float, gq::kLinear, OUT, TRUSTED>(grads, a, bits, codes, out, st, status)
+                   : quant_bits<float, gq::kExp, OUT, TRUSTED>(grads, a, bits, codes, out, st, status);
     return scheme == GQ_LINEAR
-               ? quant_bits<uint16_t, gq::kLinear, OUT, TRUSTED>(grads, a, bits, codes, out, st)
-               : quant_bits<uint16_t, gq::kExp, OUT, TRUSTED>(grads, a, bits, codes, out, st);
+               ? quant_bits<uint16_t, gq::kLinear, OUT, TRUSTED>(grads, a, bits, codes, out, st, status)
+               : quant_bits<uint16_t, gq::kExp, OUT, TRUSTED>(grads, a, bits, codes, out, st, status);
 }
 
 gq::QuantArgs make_args(const float* norm_ptr, int dtype, int64_t n, int64_t d, int s,
@@ -327,8 +340,9 @@ gq_status gq_allreduce_mean_to(const void* grads, int dtype, int64_t n, int64_t 
     const float* ws_norm = &reinterpret_cast<const gq::WsHeader*>(ws)->norm;
     gq::QuantArgs a = make_args(ws_norm, dtype, n, d, s, seed, step);
     a.out_dtype = out_dtype;
+    unsigned int* status = &reinterpret_cast<gq::WsHeader*>(ws)->status;
     return quant_any<true, true>(grads, dtype, a, scheme, gq_code_bits(scheme, s), codes, out_dev,
-                                 cs);
+                                 cs, status);
 }
 
 gq_status gq_allreduce_mean(const void* grads, int dtype, int64_t n, int64_t d, int q, int p,

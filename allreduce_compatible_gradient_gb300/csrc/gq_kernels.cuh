@@ -518,7 +518,8 @@ __global__ void norm_finish_kernel(const double* __restrict__ part, bool take_sq
 // Y = P_c 2^16 + (0xFFFF - H) - 2 and the true P 2^16 + rho 2^16 in [Y, Y + 5), k = Y >> 16 is
 // certain when (Y & 0xFFFF) <= 0xFFFB.  Otherwise (probability about 5/65536 per element) the
 // eight elements of the row-group take the exact path: __fdiv_rn, integer grid position, and the
-// second Philox call for the low half of r.
+// second Philox call for the low half of r.  The fast path does not clamp v to 1 for Global-L: a
+// level index above s (only when |x| exceeds the norm) sends the batch to the exact path too.
 //
 // The integer sum over the workers is accumulated in fp32: every partial sum is an integer of
 // magnitude below 2^24 (the library rejects larger n s and n 2^(s-1)), so it is exact.
@@ -642,7 +643,6 @@ struct Decide {
     float rcp;        // RN(1 / N)
     float c1;         // L: RN(s / N); E: 2^(s-1) RN(1 / N)
     bool fast;        // 2^-100 <= N <= 2^100: the fast path's products stay normal and finite
-    uint32_t clampb;  // L: bits of s + 128 (P <= s)
     uint32_t bigmin;  // E: bits of 2^-(s-1)
     uint32_t cbig;    // E: ((s - 127) << 16) + bits of 128
 };
@@ -655,12 +655,10 @@ __device__ __forceinline__ Decide make_decide(float nrm, uint32_t s) {
     dc.fast = nrm >= 0x1p-100f && nrm <= 0x1p100f;
     if (SCHEME == kLinear) {
         dc.c1 = __fdiv_rn(static_cast<float>(s), nrm);
-        dc.clampb = __float_as_uint(static_cast<float>(s) + 128.0f);
         dc.bigmin = 0u;
         dc.cbig = 0u;
     } else {
         dc.c1 = dc.rcp * exp2i(static_cast<int>(s) - 1);
-        dc.clampb = 0x3F800000u;
         dc.bigmin = (128u - s) << 23;
         dc.cbig = ((s - 127u) << 16) + 0x43000000u;
     }
@@ -668,16 +666,18 @@ __device__ __forceinline__ Decide make_decide(float nrm, uint32_t s) {
 }
 
 // Level indices k of the eight elements of R row-groups (rows row0 .. row0+R-1), given the
-// high-half Philox words aw of those rows; the rare exact path runs once for the batch if any
-// of its elements needs it.
+// high-half Philox words aw of those rows, returned as y with k = y >> 16 (the low half is
+// scratch); the rare exact path runs once for the batch if any of its elements needs it.
 template <int SCHEME, bool TRUSTED, int R>
 __device__ __forceinline__ void decide_rows(const float (&xv)[R][kQCols], const Decide& dc,
                                             const QuantArgs& a, uint32_t g32, uint32_t row0,
                                             const uint32_t (&aw)[R][4],
-                                            uint32_t (&k)[R][kQCols]) {
+                                            uint32_t (&yk)[R][kQCols]) {
     // Y = P_c 2^16 + (0xFFFF - H) - 2, with the bias of 128's bits folded in
     constexpr uint32_t kBias = 0xFFFFu - 0x43000000u - 2u;
-    uint32_t worst = dc.fast ? 0u : 0xFFFFu;  // largest (Y & 0xFFFF) of the batch
+    // per-half maxima over the batch: the low half of `worst` tracks the largest (Y & 0xFFFF),
+    // the high half the largest level index Y >> 16
+    uint32_t worst = dc.fast ? 0u : 0xFFFFu;
     bool anybig = false;
     uint32_t pbs[R][kQCols];
 #pragma unroll
@@ -687,14 +687,16 @@ __device__ __forceinline__ void decide_rows(const float (&xv)[R][kQCols], const 
             const float ax = fabsf(xv[u][c]);
             uint32_t pb;
             if (SCHEME == kLinear) {
-                pb = min(__float_as_uint(__fmaf_rn(ax, dc.c1, 128.0f)), dc.clampb);
+                // no clamp to P <= s here: a level index above s (|x| above the norm) sends
+                // the batch to the exact path through the high half of `worst`
+                pb = __float_as_uint(__fmaf_rn(ax, dc.c1, 128.0f));
             } else {
                 // below 2^-(s-1) (P < 1, the common case under l2 norms): P read as for L;
                 // at or above it the binade form is computed for the row (see below)
                 pb = __float_as_uint(__fmaf_rn(ax, dc.c1, 128.0f));
                 anybig |= pb >= 0x43010000u;  // P_c >= 1
             }
-            if (!TRUSTED && !(ax == ax)) worst = 0xFFFFu;  // NaN: decided on the exact path
+            if (!TRUSTED && !(ax == ax)) worst |= 0xFFFFu;  // NaN: decided on the exact path
             pbs[u][c] = pb;
         }
     }
@@ -713,11 +715,14 @@ __device__ __forceinline__ void decide_rows(const float (&xv)[R][kQCols], const 
 #pragma unroll
         for (int c = 0; c < kQCols; ++c) {
             const uint32_t y = pbs[u][c] - half16(aw[u], c) + kBias;
-            k[u][c] = y >> 16;
-            worst = max(worst, y & 0xFFFFu);
+            yk[u][c] = y;
+            worst = __vmaxu2(worst, y);
         }
     }
-    if (worst > 0xFFFBu) {  // exact path: the correctly rounded quotient and the full word
+    // exact path (the correctly rounded quotient and the full word): an uncertain element, or
+    // for Global-L a level index above s
+    const bool over = SCHEME == kLinear && (worst >> 16) > a.s;
+    if ((worst & 0xFFFFu) > 0xFFFBu || over) {
 #pragma unroll
         for (int u = 0; u < R; ++u) {
             const uint4 rb = philox4x32_10_rk(
@@ -730,31 +735,32 @@ __device__ __forceinline__ void decide_rows(const float (&xv)[R][kQCols], const 
                 uint32_t hi, lo;
                 grid_position<SCHEME>(vb, a.s, hi, lo);
                 const uint32_t r = (half16(aw[u], c) << 16) | half16(bw, c);
-                k[u][c] = hi + (r < lo ? 1u : 0u);
+                yk[u][c] = (hi + (r < lo ? 1u : 0u)) << 16;
             }
         }
     }
 }
 
-// Accumulate one row-group's codes into the sums (fp32, exact: integers below 2^24) and return
-// the signed codes.
+// Accumulate one row-group's codes (k = yk >> 16) into the sums (fp32, exact: integers below
+// 2^24) and return the signed codes.
 template <int SCHEME>
 __device__ __forceinline__ void accumulate_row(const float (&xv)[kQCols],
-                                               const uint32_t (&k)[kQCols], float (&S)[kQCols],
+                                               const uint32_t (&yk)[kQCols], float (&S)[kQCols],
                                                int32_t (&code)[kQCols]) {
 #pragma unroll
     for (int c = 0; c < kQCols; ++c) {
         const uint32_t xb = __float_as_uint(xv[c]);
+        const uint32_t k = yk[c] >> 16;
         // +-1 with the sign of x, and the summed value of the code as an exact fp32
         const float sgn = __uint_as_float((xb & 0x80000000u) | 0x3F800000u);
         float units;
-        if (SCHEME == kLinear)
-            units = __uint_as_float(k[c] | 0x4B000000u) - 8388608.0f;  // k < 2^23
+        if (SCHEME == kLinear)  // bits 0x4B00 : k (one byte permute) are 2^23 + k
+            units = __uint_as_float(__byte_perm(yk[c], 0x4B000000u, 0x7632u)) - 8388608.0f;
         else  // 2^(k-1), and 0 for k = 0 (0.5 + 2^23 rounds to the even 2^23)
-            units = (__uint_as_float((k[c] + 126u) << 23) + 8388608.0f) - 8388608.0f;
+            units = (__uint_as_float((k + 126u) << 23) + 8388608.0f) - 8388608.0f;
         S[c] = __fmaf_rn(sgn, units, S[c]);
         const int32_t sg = static_cast<int32_t>(xb) >> 31;
-        code[c] = (static_cast<int32_t>(k[c]) ^ sg) - sg;
+        code[c] = (static_cast<int32_t>(k) ^ sg) - sg;
     }
 }
 
@@ -1111,6 +1117,245 @@ quantize_segments_kernel(const __grid_constant__ SegLaunch L, QuantArgs base,
     quantize_body<T, SCHEME, 0, true, true>(static_cast<const T*>(sd.x), a,
                                             (sd.d + kQCols - 1) / kQCols, nullptr, sd.out, stage,
                                             static_cast<int64_t>(blockIdx.x) - sd.b0, sd.nb);
+}
+
+// ------------------------------------------------------------------------------------------
+// Quantise pass fed by the bulk-copy engine.  One block per SM: 15 consumer warps, each thread
+// owning one 8-column group of a 3840-column chunk, and a producer warp whose lane 0 keeps a
+// ring of kTmaStages shared-memory stages (kRows rows x 3840 columns each) in flight with
+// cp.async.bulk, completion counted on an mbarrier per stage.  The loads in flight no longer
+// depend on the consumers' registers.  Same arithmetic, random words and outputs as
+// quantize_kernel.  Every wait is bounded (about one second of global time): a wait that gives
+// up records GQ_ERR_TIMEOUT (5) in the status word, stops the block's work, and the producer
+// waits (bounded) for its own copies in flight before the block exits.
+// ------------------------------------------------------------------------------------------
+constexpr int kTmaWarps = 15;                       // consumer warps (16 warps in all)
+constexpr int kTmaConsumers = kTmaWarps * 32;       // 480
+constexpr int kTmaBlock = kTmaConsumers + 32;       // + the producer warp
+constexpr int kTmaCols = kTmaConsumers * kQCols;    // 3840 columns per chunk
+constexpr int kTmaStages = 6;
+constexpr uint64_t kWaitLimitNs = 1000000000ull;    // one second
+constexpr unsigned int kStatusTimeout = 5u;
+
+template <typename T>
+struct TmaCfg {
+    static constexpr int kRows = sizeof(T) == 4 ? 2 : 4;  // rows per stage: 30 KB either way
+    static constexpr int kRowBytes = kTmaCols * static_cast<int>(sizeof(T));
+    static constexpr int kStageBytes = kRows * kRowBytes;
+    static constexpr int kSmemBytes = kTmaStages * kStageBytes;  // 180 KB
+};
+
+__device__ __forceinline__ uint64_t global_ns() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+                 : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+    uint32_t done;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(done)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return done != 0;
+}
+// Wait for the completion of the phase with parity `parity`; false after kWaitLimitNs.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = global_ns();
+    for (;;) {
+#pragma unroll 1
+        for (int k = 0; k < 64; ++k)
+            if (mbar_try_wait(bar, parity)) return true;
+        if (global_ns() - t0 > kWaitLimitNs) return false;
+    }
+}
+// Bulk copy of `bytes` (a multiple of 16, both addresses 16-byte aligned) into shared memory,
+// counted on the mbarrier `bar`.
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes,
+                                          uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+        ::"r"(dst), "l"(src), "r"(bytes), "r"(bar)
+        : "memory");
+}
+
+template <typename T, int SCHEME, int CODE_BITS, bool WRITE_OUT, bool TRUSTED>
+__global__ void __launch_bounds__(kTmaBlock, 1)
+quantize_tma_kernel(const T* __restrict__ x, QuantArgs a, int64_t groups,
+                    unsigned char* __restrict__ codes, void* __restrict__ out,
+                    unsigned int* __restrict__ status) {
+    using Cfg = TmaCfg<T>;
+    constexpr int RB = Cfg::kRows;
+    constexpr int kSub = 2;  // rows decided together
+    extern __shared__ __align__(128) unsigned char tma_smem[];
+    __shared__ __align__(8) uint64_t full_bar[kTmaStages];
+    __shared__ __align__(8) uint64_t empty_bar[kTmaStages];
+    __shared__ float sh_scale;
+    __shared__ volatile int sh_abort;
+
+    const int tid = threadIdx.x;
+    const float nrm = __ldg(a.norm_ptr);
+    const float scale = block_scale<SCHEME>(nrm, a.n, a.s, &sh_scale);
+    const bool live = nrm > 0.0f && nrm < __uint_as_float(kInfBits);
+    if (tid == 0) {
+#pragma unroll
+        for (int k = 0; k < kTmaStages; ++k) {
+            mbar_init(smem_u32(&full_bar[k]), 1u);
+            mbar_init(smem_u32(&empty_bar[k]), static_cast<uint32_t>(kTmaWarps));
+        }
+        sh_abort = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    __syncthreads();
+
+    const int64_t full = live ? a.d / kQCols : 0;  // groups taken through shared memory
+    const int64_t nchunks = (full + kTmaConsumers - 1) / kTmaConsumers;
+    const int64_t nbatch = (a.n + RB - 1) / RB;
+
+    if (tid >= kTmaConsumers) {
+        // ---- producer: lane 0 of the last warp ------------------------------------------
+        if (tid == kTmaConsumers) {
+            uint32_t item = 0;
+            bool ok = true;
+            for (int64_t q = blockIdx.x; q < nchunks && ok; q += gridDim.x) {
+                const int64_t g0 = (nchunks - 1 - q) * kTmaConsumers;
+                const int64_t ng = min(static_cast<int64_t>(kTmaConsumers), full - g0);
+                const uint32_t row_bytes = static_cast<uint32_t>(ng * kQCols * sizeof(T));
+                for (int64_t b = 0; b < nbatch; ++b, ++item) {
+                    const int st = static_cast<int>(item % kTmaStages);
+                    if (item >= kTmaStages &&
+                        !mbar_wait(smem_u32(&empty_bar[st]), ((item / kTmaStages) - 1u) & 1u)) {
+                        ok = false;
+                        break;
+                    }
+                    if (sh_abort) { ok = false; break; }
+                    const int64_t r0 = b * RB;
+                    const int rows = static_cast<int>(min(static_cast<int64_t>(RB), a.n - r0));
+                    const uint32_t fb = smem_u32(&full_bar[st]);
+                    mbar_arrive_expect_tx(fb, static_cast<uint32_t>(rows) * row_bytes);
+                    const uint32_t dst = smem_u32(tma_smem + st * Cfg::kStageBytes);
+                    for (int u = 0; u < rows; ++u)
+                        bulk_load(dst + u * Cfg::kRowBytes, x + (r0 + u) * a.d + g0 * kQCols,
+                                  row_bytes, fb);
+                }
+            }
+            if (!ok) {
+                if (status) atomicCAS(status, 0u, kStatusTimeout);
+                sh_abort = 1;
+            }
+            // the block must not exit with copies in flight: wait for the last issued stages
+            const uint32_t inflight = item < kTmaStages ? item : kTmaStages;
+            for (uint32_t k = 0; k < inflight; ++k) {
+                const uint32_t it = item - 1 - k;
+                mbar_wait(smem_u32(&full_bar[it % kTmaStages]), (it / kTmaStages) & 1u);
+            }
+        }
+    } else if (nchunks > 0) {
+        // ---- consumers ------------------------------------------------------------------
+        const Decide dc = make_decide<SCHEME>(nrm, a.s);
+        const int lane = tid & 31;
+        uint32_t item = 0;
+        bool ok = true;
+        for (int64_t q = blockIdx.x; q < nchunks && ok; q += gridDim.x) {
+            const int64_t g = (nchunks - 1 - q) * kTmaConsumers + tid;
+            const bool active = g < full;
+            const uint32_t g32 = static_cast<uint32_t>(g);
+            const PhiloxGroup pg = philox_group(g32, a.step_lo, a.step_hi, a.rk);
+            float S[kQCols];
+#pragma unroll
+            for (int c = 0; c < kQCols; ++c) S[c] = 0.0f;
+            for (int64_t b = 0; b < nbatch; ++b, ++item) {
+                const int st = static_cast<int>(item % kTmaStages);
+                const bool got = mbar_wait(smem_u32(&full_bar[st]), (item / kTmaStages) & 1u);
+                if (!__all_sync(0xFFFFFFFFu, got && !sh_abort)) {  // warp-uniform decision
+                    ok = false;
+                    break;
+                }
+                const unsigned char* stage = tma_smem + st * Cfg::kStageBytes + tid * kQCols * sizeof(T);
+#pragma unroll
+                for (int u0 = 0; u0 < RB; u0 += kSub) {
+                    const int64_t r0 = b * RB + u0;
+                    float v[kSub][kQCols];
+#pragma unroll
+                    for (int u = 0; u < kSub; ++u) {
+                        const uint4* p = reinterpret_cast<const uint4*>(stage + (u0 + u) * Cfg::kRowBytes);
+                        if (active && r0 + u < a.n) {
+                            unstage<T>(p, p + 1, v[u]);
+                        } else {
+#pragma unroll
+                            for (int c = 0; c < kQCols; ++c) v[u][c] = 0.0f;
+                        }
+                    }
+                    if (u0 + kSub >= RB) {  // every row of the stage is in registers: release it
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(smem_u32(&empty_bar[st]));
+                    }
+                    if (!active) continue;
+                    uint32_t aw[kSub][4];
+#pragma unroll
+                    for (int u = 0; u < kSub; ++u) {
+                        const uint4 ra = philox_row(pg, static_cast<uint32_t>(r0 + u) + a.row0,
+                                                    a.step_lo, a.rk);
+                        aw[u][0] = ra.x; aw[u][1] = ra.y; aw[u][2] = ra.z; aw[u][3] = ra.w;
+                    }
+                    uint32_t yk[kSub][kQCols];
+                    decide_rows<SCHEME, TRUSTED, kSub>(v, dc, a, g32,
+                                                       static_cast<uint32_t>(r0) + a.row0, aw, yk);
+#pragma unroll
+                    for (int u = 0; u < kSub; ++u) {
+                        if (r0 + u >= a.n) break;
+                        int32_t code[kQCols];
+                        accumulate_row<SCHEME>(v[u], yk[u], S, code);
+                        if (CODE_BITS) store_codes<CODE_BITS>(codes, r0 + u, g, a.pitch, code);
+                    }
+                }
+            }
+            if (ok && active && WRITE_OUT) store_out(out, a.sums, a.out_dtype, g, a.d, scale, S);
+        }
+        if (!ok) {
+            if (status) atomicCAS(status, 0u, kStatusTimeout);
+            sh_abort = 1;
+        }
+    }
+    if (tid >= kTmaConsumers) return;
+
+    // ---- the groups [full, groups): ragged last group, code padding, or all of them when the
+    // norm is 0 or not finite; direct loads by the consumer threads
+    const Decide dc = make_decide<SCHEME>(nrm, a.s);
+    const int64_t rest = groups - full;
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * kTmaConsumers;
+    for (int64_t it = static_cast<int64_t>(blockIdx.x) * kTmaConsumers + tid; it < rest;
+         it += stride) {
+        const int64_t g = groups - 1 - it;
+        float S[kQCols];
+        if (live) {
+            quantize_group<T, SCHEME, CODE_BITS, TRUSTED>(x, a, dc, g, codes, S);
+        } else {
+#pragma unroll
+            for (int c = 0; c < kQCols; ++c) S[c] = 0.0f;
+            if (CODE_BITS) {
+                const int32_t zero[kQCols] = {0, 0, 0, 0, 0, 0, 0, 0};
+                for (int64_t i = 0; i < a.n; ++i) store_codes<CODE_BITS>(codes, i, g, a.pitch, zero);
+            }
+        }
+        if (WRITE_OUT) store_out(out, a.sums, a.out_dtype, g, a.d, scale, S);
+    }
 }
 
 // Signed contribution of a code to the integer sum: L sums the level index; E sums

@@ -1,0 +1,112 @@
+"""GPU parity of the fused path's bulk-copy kernel (quantize_tma_kernel).
+
+The fused call takes that kernel for 16-byte aligned rows with at least one 3840-column chunk
+per SM (d >= 583,680 on 152 SMs).  At such sizes, with ragged last groups, odd worker counts,
+one worker, both dtypes, both schemes and every code width, the fused result (out and codes)
+must equal the unfused chain (norm, quantise, sum, dequantise: the direct-load kernels, pinned
+to the oracle elsewhere) bit for bit, and sampled column windows (first, last, seeded interior)
+must match the oracle: codes bit-exact, out within 1e-6 N.  The workspace status stays 0 (no
+bounded wait gave up).
+"""
+import numpy as np
+import pytest
+
+from gpu_common import EXP, INF, LINEAR, gq_module, to_device, to_host, unpack_codes
+from allreduce_compatible_gradient_gb300 import workloads
+
+pytestmark = pytest.mark.gpu
+
+CASES = [
+    # n, d, dtype, scheme, s, with codes
+    (5, 600_004, "f32", LINEAR, 7, True),     # d % 8 = 4: the last group is half full
+    (5, 600_004, "f32", EXP, 8, False),
+    (8, 1_000_000, "f32", LINEAR, 127, True),
+    (1, 700_000, "f32", EXP, 4, True),        # one worker: a half-empty row batch
+    (7, 640_000, "f32", LINEAR, 15, False),
+    (3, 600_000, "bf16", EXP, 4, True),
+    (8, 655_360, "bf16", LINEAR, 15, False),
+    (6, 1_200_008, "bf16", EXP, 8, True),
+]
+
+
+@pytest.fixture(scope="module")
+def gq():
+    return gq_module()
+
+
+@pytest.fixture(scope="module")
+def oracle_mod():
+    from oracle import gq_oracle
+    gq_oracle.lib()
+    return gq_oracle
+
+
+def _windows(d, seed):
+    rng = np.random.default_rng(seed)
+    starts = {0, d - 1003}
+    while len(starts) < 5:
+        starts.add(int(rng.integers(0, d - 1003)) // 32 * 32)
+    return sorted((s0, min(d, s0 + 1003)) for s0 in starts)
+
+
+@pytest.mark.parametrize("n,d,dtype,scheme,s,with_codes", CASES)
+def test_bulk_copy_path(gq, oracle_mod, n, d, dtype, scheme, s, with_codes):
+    import torch
+    x = workloads.device_inputs("normal" if dtype == "f32" else "student_t3", n, d, seed=d + n,
+                                dtype=dtype)
+    seed, step = 21, 5
+    ws = gq.gq_workspace()
+    norm = torch.empty(1, dtype=torch.float32, device="cuda")
+    cb = gq.gq_code_bytes(scheme, s, n, d)
+    codes = torch.empty(cb, dtype=torch.uint8, device="cuda") if with_codes else None
+    out = gq.gq_allreduce_mean(x, INF, INF, scheme, s, seed, step, norm=norm, codes=codes, ws=ws)
+    # the unfused chain
+    n2 = gq.gq_global_norm(x, INF, INF)
+    c2 = gq.gq_quantize(x, n2, scheme, s, seed, step)
+    sums = gq.gq_reduce_codes(c2, scheme, s, n, d)
+    ref = gq.gq_dequantize(sums, n2, scheme, s, n)
+    torch.cuda.synchronize()
+    assert gq.gq_get_status(ws) == 0
+    assert torch.equal(norm, n2)
+    assert torch.equal(out, ref)
+    if with_codes:
+        assert torch.equal(codes, c2)
+
+    # sampled windows against the oracle
+    xh = to_host(x)
+    norm32 = float(norm.item())
+    assert norm32 == float(np.float32(oracle_mod.global_norm(xh, INF, INF)))
+    out_h = out.cpu().numpy().astype(np.float64)
+    bits = gq.gq_code_bits(scheme, s)
+    pitch = gq.gq_code_pitch(d)
+    codes_h = c2.cpu().numpy().reshape(n, pitch * bits // 8)
+    for j0, j1 in _windows(d, seed=d):
+        ref_codes, rc = oracle_mod.quantize(xh, norm32, scheme, s, seed, step, j0, j1)
+        assert rc == 0
+        ref_out, rc = oracle_mod.dequantize(oracle_mod.reduce_codes(ref_codes, scheme, s), norm32,
+                                            scheme, s, n)
+        assert rc == 0
+        a0 = j0 // 32 * 32
+        a1 = min(pitch, (j1 + 31) // 32 * 32)
+        win = unpack_codes(np.ascontiguousarray(codes_h[:, a0 * bits // 8:a1 * bits // 8]).ravel(),
+                           scheme, s, n, a1 - a0, check_padding=False)
+        np.testing.assert_array_equal(win[:, j0 - a0:j1 - a0], ref_codes)
+        assert np.abs(out_h[j0:j1] - ref_out).max() <= 1e-6 * norm32
+
+
+def test_bulk_copy_path_l2_norm_and_zero(gq):
+    """(2,2) norm through the bulk-copy path equals the unfused chain with the same norm; an
+    all-zero problem gives zeros and status 0."""
+    import torch
+    n, d = 4, 800_000
+    x = workloads.device_inputs("normal", n, d, seed=3)
+    ws = gq.gq_workspace()
+    norm = torch.empty(1, dtype=torch.float32, device="cuda")
+    out = gq.gq_allreduce_mean(x, 2, 2, EXP, 8, 1, 1, norm=norm, ws=ws)
+    ref = gq.gq_allreduce_mean_with_norm(x, norm, EXP, 8, 1, 1)
+    z = torch.zeros(n, d, device="cuda")
+    outz = gq.gq_allreduce_mean(z, 2, 2, LINEAR, 15, 1, 1, ws=ws)
+    torch.cuda.synchronize()
+    assert torch.equal(out, ref)
+    assert torch.count_nonzero(outz) == 0
+    assert gq.gq_get_status(ws) == 0
