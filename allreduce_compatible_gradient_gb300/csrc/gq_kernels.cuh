@@ -667,7 +667,8 @@ __device__ __forceinline__ Decide make_decide(float nrm, uint32_t s) {
 
 // Level indices k of the eight elements of R row-groups (rows row0 .. row0+R-1), given the
 // high-half Philox words aw of those rows, returned as y with k = y >> 16 (the low half is
-// scratch); the rare exact path runs once for the batch if any of its elements needs it.
+// scratch).  The rare exact path runs for a row only if one of its elements needs it, and then
+// only for those elements (one extra Philox call for the row).
 template <int SCHEME, bool TRUSTED, int R>
 __device__ __forceinline__ void decide_rows(const float (&xv)[R][kQCols], const Decide& dc,
                                             const QuantArgs& a, uint32_t g32, uint32_t row0,
@@ -675,20 +676,21 @@ __device__ __forceinline__ void decide_rows(const float (&xv)[R][kQCols], const 
                                             uint32_t (&yk)[R][kQCols]) {
     // Y = P_c 2^16 + (0xFFFF - H) - 2, with the bias of 128's bits folded in
     constexpr uint32_t kBias = 0xFFFFu - 0x43000000u - 2u;
-    // per-half maxima over the batch: the low half of `worst` tracks the largest (Y & 0xFFFF),
-    // the high half the largest level index Y >> 16
-    uint32_t worst = dc.fast ? 0u : 0xFFFFu;
+    // per-row, per-half maxima: the low half of worst[u] tracks the largest (Y & 0xFFFF) of
+    // row u, the high half its largest level index Y >> 16
+    uint32_t worst[R];
     bool anybig = false;
     uint32_t pbs[R][kQCols];
 #pragma unroll
     for (int u = 0; u < R; ++u) {
+        worst[u] = dc.fast ? 0u : 0xFFFFu;
 #pragma unroll
         for (int c = 0; c < kQCols; ++c) {
             const float ax = fabsf(xv[u][c]);
             uint32_t pb;
             if (SCHEME == kLinear) {
                 // no clamp to P <= s here: a level index above s (|x| above the norm) sends
-                // the batch to the exact path through the high half of `worst`
+                // the element to the exact path
                 pb = __float_as_uint(__fmaf_rn(ax, dc.c1, 128.0f));
             } else {
                 // below 2^-(s-1) (P < 1, the common case under l2 norms): P read as for L;
@@ -696,7 +698,7 @@ __device__ __forceinline__ void decide_rows(const float (&xv)[R][kQCols], const 
                 pb = __float_as_uint(__fmaf_rn(ax, dc.c1, 128.0f));
                 anybig |= pb >= 0x43010000u;  // P_c >= 1
             }
-            if (!TRUSTED && !(ax == ax)) worst |= 0xFFFFu;  // NaN: decided on the exact path
+            if (!TRUSTED && !(ax == ax)) worst[u] |= 0xFFFFu;  // NaN: decided on the exact path
             pbs[u][c] = pb;
         }
     }
@@ -716,20 +718,26 @@ __device__ __forceinline__ void decide_rows(const float (&xv)[R][kQCols], const 
         for (int c = 0; c < kQCols; ++c) {
             const uint32_t y = pbs[u][c] - half16(aw[u], c) + kBias;
             yk[u][c] = y;
-            worst = __vmaxu2(worst, y);
+            worst[u] = __vmaxu2(worst[u], y);
         }
     }
-    // exact path (the correctly rounded quotient and the full word): an uncertain element, or
-    // for Global-L a level index above s
-    const bool over = SCHEME == kLinear && (worst >> 16) > a.s;
-    if ((worst & 0xFFFFu) > 0xFFFBu || over) {
+    // exact path (the correctly rounded quotient and the full word) for an uncertain element,
+    // a Global-L level index above s, a NaN, or every element when the norm is out of the fast
+    // path's range
 #pragma unroll
-        for (int u = 0; u < R; ++u) {
+    for (int u = 0; u < R; ++u) {
+        const bool over = SCHEME == kLinear && (worst[u] >> 16) > a.s;
+        if ((worst[u] & 0xFFFFu) > 0xFFFBu || over) {
             const uint4 rb = philox4x32_10_rk(
                 make_uint4(g32 | 0x80000000u, row0 + u, a.step_lo, a.step_hi), a.rk);
             const uint32_t bw[4] = {rb.x, rb.y, rb.z, rb.w};
 #pragma unroll
             for (int c = 0; c < kQCols; ++c) {
+                const uint32_t y = yk[u][c];
+                const bool need = !dc.fast || (y & 0xFFFFu) > 0xFFFBu ||
+                                  (SCHEME == kLinear && (y >> 16) > a.s) ||
+                                  (!TRUSTED && !(xv[u][c] == xv[u][c]));
+                if (!need) continue;
                 uint32_t vb = __float_as_uint(__fdiv_rn(fabsf(xv[u][c]), dc.nrm));
                 vb = (vb > kInfBits) ? 0u : min(vb, 0x3F800000u);
                 uint32_t hi, lo;
