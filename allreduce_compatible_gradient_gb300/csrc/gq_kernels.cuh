@@ -642,9 +642,10 @@ struct Decide {
     float nrm;        // N
     float rcp;        // RN(1 / N)
     float c1;         // L: RN(s / N); E: 2^(s-1) RN(1 / N)
+    float c0;         // 128 + 0xFFFD 2^-16: the addend that places P in 16.16 fixed point
     bool fast;        // 2^-100 <= N <= 2^100: the fast path's products stay normal and finite
     uint32_t bigmin;  // E: bits of 2^-(s-1)
-    uint32_t cbig;    // E: ((s - 127) << 16) + bits of 128
+    uint32_t cbig;    // E: ((s - 127) << 16) + bits of c0
 };
 
 template <int SCHEME>
@@ -653,6 +654,7 @@ __device__ __forceinline__ Decide make_decide(float nrm, uint32_t s) {
     dc.nrm = nrm;
     dc.rcp = __frcp_rn(nrm);
     dc.fast = nrm >= 0x1p-100f && nrm <= 0x1p100f;
+    dc.c0 = __uint_as_float(0x4300FFFDu);
     if (SCHEME == kLinear) {
         dc.c1 = __fdiv_rn(static_cast<float>(s), nrm);
         dc.bigmin = 0u;
@@ -660,7 +662,7 @@ __device__ __forceinline__ Decide make_decide(float nrm, uint32_t s) {
     } else {
         dc.c1 = dc.rcp * exp2i(static_cast<int>(s) - 1);
         dc.bigmin = (128u - s) << 23;
-        dc.cbig = ((s - 127u) << 16) + 0x43000000u;
+        dc.cbig = ((s - 127u) << 16) + 0x4300FFFDu;
     }
     return dc;
 }
@@ -674,8 +676,11 @@ __device__ __forceinline__ void decide_rows(const float (&xv)[R][kQCols], const 
                                             const QuantArgs& a, uint32_t g32, uint32_t row0,
                                             const uint32_t (&aw)[R][4],
                                             uint32_t (&yk)[R][kQCols]) {
-    // Y = P_c 2^16 + (0xFFFF - H) - 2, with the bias of 128's bits folded in
-    constexpr uint32_t kBias = 0xFFFFu - 0x43000000u - 2u;
+    // y = bits(fp32(|x| c1) + c0) - H = 0x43000000 + P_c 2^16 + (0xFFFF - H) - 2: its low half
+    // is that of Y = P_c 2^16 + (0xFFFF - H) - 2 and its high half k + 0x4300.  (c0 is a multiple
+    // of the 2^-16 unit of [128, 256), so adding it inside the rounding moves the result by
+    // exactly 0xFFFD units; P <= s <= 127 keeps the sum below 256.)
+    constexpr uint32_t kOff = 0x4300u;
     // per-row, per-half maxima: the low half of worst[u] tracks the largest (Y & 0xFFFF) of
     // row u, the high half its largest level index Y >> 16
     uint32_t worst[R];
@@ -691,12 +696,12 @@ __device__ __forceinline__ void decide_rows(const float (&xv)[R][kQCols], const 
             if (SCHEME == kLinear) {
                 // no clamp to P <= s here: a level index above s (|x| above the norm) sends
                 // the element to the exact path
-                pb = __float_as_uint(__fmaf_rn(ax, dc.c1, 128.0f));
+                pb = __float_as_uint(__fmaf_rn(ax, dc.c1, dc.c0));
             } else {
                 // below 2^-(s-1) (P < 1, the common case under l2 norms): P read as for L;
                 // at or above it the binade form is computed for the row (see below)
-                pb = __float_as_uint(__fmaf_rn(ax, dc.c1, 128.0f));
-                anybig |= pb >= 0x43010000u;  // P_c >= 1
+                pb = __float_as_uint(__fmaf_rn(ax, dc.c1, dc.c0));
+                anybig |= pb >= 0x4301FFFDu;  // P_c >= 1
             }
             if (!TRUSTED && !(ax == ax)) worst[u] |= 0xFFFFu;  // NaN: decided on the exact path
             pbs[u][c] = pb;
@@ -716,7 +721,7 @@ __device__ __forceinline__ void decide_rows(const float (&xv)[R][kQCols], const 
     for (int u = 0; u < R; ++u) {
 #pragma unroll
         for (int c = 0; c < kQCols; ++c) {
-            const uint32_t y = pbs[u][c] - half16(aw[u], c) + kBias;
+            const uint32_t y = pbs[u][c] - half16(aw[u], c);
             yk[u][c] = y;
             worst[u] = __vmaxu2(worst[u], y);
         }
@@ -726,7 +731,7 @@ __device__ __forceinline__ void decide_rows(const float (&xv)[R][kQCols], const 
     // path's range
 #pragma unroll
     for (int u = 0; u < R; ++u) {
-        const bool over = SCHEME == kLinear && (worst[u] >> 16) > a.s;
+        const bool over = SCHEME == kLinear && (worst[u] >> 16) > a.s + kOff;
         if ((worst[u] & 0xFFFFu) > 0xFFFBu || over) {
             const uint4 rb = philox4x32_10_rk(
                 make_uint4(g32 | 0x80000000u, row0 + u, a.step_lo, a.step_hi), a.rk);
@@ -735,7 +740,7 @@ __device__ __forceinline__ void decide_rows(const float (&xv)[R][kQCols], const 
             for (int c = 0; c < kQCols; ++c) {
                 const uint32_t y = yk[u][c];
                 const bool need = !dc.fast || (y & 0xFFFFu) > 0xFFFBu ||
-                                  (SCHEME == kLinear && (y >> 16) > a.s) ||
+                                  (SCHEME == kLinear && (y >> 16) > a.s + kOff) ||
                                   (!TRUSTED && !(xv[u][c] == xv[u][c]));
                 if (!need) continue;
                 uint32_t vb = __float_as_uint(__fdiv_rn(fabsf(xv[u][c]), dc.nrm));
@@ -743,14 +748,14 @@ __device__ __forceinline__ void decide_rows(const float (&xv)[R][kQCols], const 
                 uint32_t hi, lo;
                 grid_position<SCHEME>(vb, a.s, hi, lo);
                 const uint32_t r = (half16(aw[u], c) << 16) | half16(bw, c);
-                yk[u][c] = (hi + (r < lo ? 1u : 0u)) << 16;
+                yk[u][c] = (hi + (r < lo ? 1u : 0u) + kOff) << 16;
             }
         }
     }
 }
 
-// Accumulate one row-group's codes (k = yk >> 16) into the sums (fp32, exact: integers below
-// 2^24) and return the signed codes.
+// Accumulate one row-group's codes (k = (yk >> 16) - 0x4300) into the sums (fp32, exact:
+// integers below 2^24) and return the signed codes.
 template <int SCHEME>
 __device__ __forceinline__ void accumulate_row(const float (&xv)[kQCols],
                                                const uint32_t (&yk)[kQCols], float (&S)[kQCols],
@@ -758,17 +763,19 @@ __device__ __forceinline__ void accumulate_row(const float (&xv)[kQCols],
 #pragma unroll
     for (int c = 0; c < kQCols; ++c) {
         const uint32_t xb = __float_as_uint(xv[c]);
-        const uint32_t k = yk[c] >> 16;
         // +-1 with the sign of x, and the summed value of the code as an exact fp32
         const float sgn = __uint_as_float((xb & 0x80000000u) | 0x3F800000u);
         float units;
-        if (SCHEME == kLinear)  // bits 0x4B00 : k (one byte permute) are 2^23 + k
-            units = __uint_as_float(__byte_perm(yk[c], 0x4B000000u, 0x7632u)) - 8388608.0f;
-        else  // 2^(k-1), and 0 for k = 0 (0.5 + 2^23 rounds to the even 2^23)
-            units = (__uint_as_float((k + 126u) << 23) + 8388608.0f) - 8388608.0f;
+        if (SCHEME == kLinear) {  // bits 0x4B00 : (k + 0x4300) (one byte permute): 2^23 + 0x4300 + k
+            units = __uint_as_float(__byte_perm(yk[c], 0x4B000000u, 0x7632u)) - 8405760.0f;
+        } else {  // 2^(k-1), and 0 for k = 0 (0.5 + 2^23 rounds to the even 2^23)
+            const uint32_t e = ((yk[c] >> 16) << 23) + ((126u - 0x4300u) << 23);  // (k + 126) << 23
+            units = (__uint_as_float(e) + 8388608.0f) - 8388608.0f;
+        }
         S[c] = __fmaf_rn(sgn, units, S[c]);
+        const int32_t k = static_cast<int32_t>(yk[c] >> 16) - 0x4300;
         const int32_t sg = static_cast<int32_t>(xb) >> 31;
-        code[c] = (static_cast<int32_t>(k) ^ sg) - sg;
+        code[c] = (k ^ sg) - sg;
     }
 }
 
@@ -1130,7 +1137,7 @@ quantize_segments_kernel(const __grid_constant__ SegLaunch L, QuantArgs base,
 // ------------------------------------------------------------------------------------------
 // Quantise pass fed by the bulk-copy engine.  One block per SM: 15 consumer warps, each thread
 // owning one 8-column group of a 3840-column chunk, and a producer warp whose lane 0 keeps a
-// ring of kTmaStages shared-memory stages (kRows rows x 3840 columns each) in flight with
+// ring of shared-memory stages (kRows rows x 3840 columns each) in flight with
 // cp.async.bulk, completion counted on an mbarrier per stage.  The loads in flight no longer
 // depend on the consumers' registers.  Same arithmetic, random words and outputs as
 // quantize_kernel.  Every wait is bounded (about one second of global time): a wait that gives
@@ -1141,16 +1148,16 @@ constexpr int kTmaWarps = 15;                       // consumer warps (16 warps 
 constexpr int kTmaConsumers = kTmaWarps * 32;       // 480
 constexpr int kTmaBlock = kTmaConsumers + 32;       // + the producer warp
 constexpr int kTmaCols = kTmaConsumers * kQCols;    // 3840 columns per chunk
-constexpr int kTmaStages = 6;
 constexpr uint64_t kWaitLimitNs = 1000000000ull;    // one second
 constexpr unsigned int kStatusTimeout = 5u;
 
 template <typename T>
 struct TmaCfg {
-    static constexpr int kRows = sizeof(T) == 4 ? 2 : 4;  // rows per stage: 30 KB either way
+    static constexpr int kRows = 4;                           // rows per stage
+    static constexpr int kStages = sizeof(T) == 4 ? 3 : 6;    // stages in the ring
     static constexpr int kRowBytes = kTmaCols * static_cast<int>(sizeof(T));
-    static constexpr int kStageBytes = kRows * kRowBytes;
-    static constexpr int kSmemBytes = kTmaStages * kStageBytes;  // 180 KB
+    static constexpr int kStageBytes = kRows * kRowBytes;     // 60 KB (fp32), 30 KB (bf16)
+    static constexpr int kSmemBytes = kStages * kStageBytes;  // 180 KB
 };
 
 __device__ __forceinline__ uint64_t global_ns() {
@@ -1212,8 +1219,8 @@ quantize_tma_kernel(const T* __restrict__ x, QuantArgs a, int64_t groups,
     constexpr int RB = Cfg::kRows;
     constexpr int kSub = 2;  // rows decided together
     extern __shared__ __align__(128) unsigned char tma_smem[];
-    __shared__ __align__(8) uint64_t full_bar[kTmaStages];
-    __shared__ __align__(8) uint64_t empty_bar[kTmaStages];
+    __shared__ __align__(8) uint64_t full_bar[Cfg::kStages];
+    __shared__ __align__(8) uint64_t empty_bar[Cfg::kStages];
     __shared__ float sh_scale;
     __shared__ volatile int sh_abort;
 
@@ -1223,7 +1230,7 @@ quantize_tma_kernel(const T* __restrict__ x, QuantArgs a, int64_t groups,
     const bool live = nrm > 0.0f && nrm < __uint_as_float(kInfBits);
     if (tid == 0) {
 #pragma unroll
-        for (int k = 0; k < kTmaStages; ++k) {
+        for (int k = 0; k < Cfg::kStages; ++k) {
             mbar_init(smem_u32(&full_bar[k]), 1u);
             mbar_init(smem_u32(&empty_bar[k]), static_cast<uint32_t>(kTmaWarps));
         }
@@ -1246,9 +1253,9 @@ quantize_tma_kernel(const T* __restrict__ x, QuantArgs a, int64_t groups,
                 const int64_t ng = min(static_cast<int64_t>(kTmaConsumers), full - g0);
                 const uint32_t row_bytes = static_cast<uint32_t>(ng * kQCols * sizeof(T));
                 for (int64_t b = 0; b < nbatch; ++b, ++item) {
-                    const int st = static_cast<int>(item % kTmaStages);
-                    if (item >= kTmaStages &&
-                        !mbar_wait(smem_u32(&empty_bar[st]), ((item / kTmaStages) - 1u) & 1u)) {
+                    const int st = static_cast<int>(item % Cfg::kStages);
+                    if (item >= Cfg::kStages &&
+                        !mbar_wait(smem_u32(&empty_bar[st]), ((item / Cfg::kStages) - 1u) & 1u)) {
                         ok = false;
                         break;
                     }
@@ -1268,10 +1275,10 @@ quantize_tma_kernel(const T* __restrict__ x, QuantArgs a, int64_t groups,
                 sh_abort = 1;
             }
             // the block must not exit with copies in flight: wait for the last issued stages
-            const uint32_t inflight = item < kTmaStages ? item : kTmaStages;
+            const uint32_t inflight = item < Cfg::kStages ? item : Cfg::kStages;
             for (uint32_t k = 0; k < inflight; ++k) {
                 const uint32_t it = item - 1 - k;
-                mbar_wait(smem_u32(&full_bar[it % kTmaStages]), (it / kTmaStages) & 1u);
+                mbar_wait(smem_u32(&full_bar[it % Cfg::kStages]), (it / Cfg::kStages) & 1u);
             }
         }
     } else if (nchunks > 0) {
@@ -1289,8 +1296,8 @@ quantize_tma_kernel(const T* __restrict__ x, QuantArgs a, int64_t groups,
 #pragma unroll
             for (int c = 0; c < kQCols; ++c) S[c] = 0.0f;
             for (int64_t b = 0; b < nbatch; ++b, ++item) {
-                const int st = static_cast<int>(item % kTmaStages);
-                const bool got = mbar_wait(smem_u32(&full_bar[st]), (item / kTmaStages) & 1u);
+                const int st = static_cast<int>(item % Cfg::kStages);
+                const bool got = mbar_wait(smem_u32(&full_bar[st]), (item / Cfg::kStages) & 1u);
                 if (!__all_sync(0xFFFFFFFFu, got && !sh_abort)) {  // warp-uniform decision
                     ok = false;
                     break;
