@@ -94,3 +94,65 @@ def test_missing_library_fails_loudly(tmp_path, monkeypatch):
     monkeypatch.setattr(_binding, "_lib", None)
     with pytest.raises(ImportError):
         _binding.lib()
+
+
+def test_argument_checks_of_the_bucket_and_rank_entry_points(lib):
+    """gq_allreduce_mean_segments, gq_quantize_sum, gq_norm_partial / gq_norm_finish and the
+    *_to output-type entry points refuse bad arguments before any device call."""
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("fake pointers: run only where no GPU can be reached")
+    vp, i64, u64, ci, sz = ctypes.c_void_p, ctypes.c_int64, ctypes.c_uint64, ctypes.c_int, ctypes.c_size_t
+    lib.gq_allreduce_mean_segments.argtypes = [i64, vp, vp, ci, i64, ci, ci, ci, ci, u64, u64, vp,
+                                               ci, vp, vp, sz, vp]
+    lib.gq_quantize_sum.argtypes = [vp, ci, i64, i64, i64, vp, ci, ci, u64, u64, vp, vp]
+    lib.gq_norm_partial.argtypes = [vp, ci, i64, i64, ci, ci, vp, vp, sz, vp]
+    lib.gq_norm_finish.argtypes = [vp, ci, ci, vp, vp]
+    lib.gq_dequantize_to.argtypes = [vp, vp, ci, ci, i64, i64, vp, ci, vp]
+    lib.gq_allreduce_mean_to.argtypes = [vp, ci, i64, i64, ci, ci, ci, ci, u64, u64, vp, ci, vp,
+                                         vp, vp, sz, vp]
+    fake = 1 << 20
+    ws_bytes = lib.gq_workspace_bytes(1, 1)
+    P = ctypes.c_void_p * 2
+    D = ctypes.c_int64 * 2
+    grads, outs, ds = P(fake, fake + 4096), P(fake, fake + 4096), D(100, 200)
+
+    def seg(nseg=2, g=grads, d=ds, n=4, q=0, p=0, scheme=1, s=8, step=1, o=outs, odt=0,
+            ws=fake, wsb=ws_bytes):
+        return lib.gq_allreduce_mean_segments(nseg, g, d, 0, n, q, p, scheme, s, 1, step, o, odt,
+                                              None, vp(ws) if ws else None, wsb, None)
+    assert seg(nseg=0) == 1
+    assert seg(nseg=65537) == 1
+    assert seg(step=1 << 48) == 1
+    assert seg(odt=3) == 1
+    assert seg(g=P(fake, fake + 4)) == 1                # unaligned second segment
+    assert seg(o=P(fake, fake + 8)) == 1                # unaligned second output
+    assert seg(d=D(100, 0)) == 1
+    assert seg(q=1) == 1
+    assert seg(s=25) == 2
+    assert seg(n=1 << 17) == 3                          # n 2^(s-1) >= 2^24
+    assert seg(ws=0) == 7
+    assert seg(wsb=100) == 7
+
+    def qsum(m=2, w0=0, scheme=1, s=8, out=fake):
+        return lib.gq_quantize_sum(vp(fake), 0, m, 64, w0, vp(fake), scheme, s, 1, 1,
+                                   vp(out) if out else None, None)
+    assert qsum(w0=-1) == 1
+    assert qsum(w0=(1 << 31) - 1) == 1
+    assert qsum(out=0) == 1
+    assert qsum(out=fake + 4) == 1
+    assert qsum(s=0) == 2
+    assert qsum(m=2, s=24) == 3
+
+    assert lib.gq_norm_partial(vp(fake), 0, 2, 64, 2, 0, vp(fake), vp(fake), ws_bytes, None) == 2
+    assert lib.gq_norm_partial(vp(fake), 0, 2, 64, 0, 2, vp(fake), vp(fake), ws_bytes, None) == 2
+    assert lib.gq_norm_partial(vp(fake), 0, 2, 64, 2, 2, None, vp(fake), ws_bytes, None) == 1
+    assert lib.gq_norm_partial(vp(fake), 0, 2, 64, 2, 2, vp(fake), vp(fake), 8, None) == 7
+    assert lib.gq_norm_finish(vp(fake), 2, 0, vp(fake), None) == 2
+    assert lib.gq_norm_finish(None, 2, 2, vp(fake), None) == 1
+    assert lib.gq_norm_finish(vp(fake), 3, 2, vp(fake), None) == 1
+
+    assert lib.gq_dequantize_to(vp(fake), vp(fake), 1, 8, 2, 64, vp(fake), 3, None) == 1
+    assert lib.gq_dequantize_to(vp(fake), vp(fake), 1, 8, 2, 64, vp(fake + 2), 1, None) == 1
+    assert lib.gq_allreduce_mean_to(vp(fake), 0, 2, 64, 0, 0, 1, 8, 1, 1, vp(fake), -1, None,
+                                    None, vp(fake), ws_bytes, None) == 1
