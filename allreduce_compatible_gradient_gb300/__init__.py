@@ -7,10 +7,11 @@ package is a thin ctypes binding with the same names.  PyTorch supplies device m
 streams only.  There is no CPU fallback: importing the package without a built libgq.so raises.
 """
 from ._binding import (  # noqa: F401
-    BF16, EXP, F16, F32, LINEAR, NORM_INF, NORM_L2, ORDER_RING, ORDER_TREE, GQError,
-    gq_abi_version, gq_allreduce_mean, gq_allreduce_mean_noalloc, gq_allreduce_mean_segments,
-    gq_allreduce_mean_to, gq_allreduce_mean_with_norm, gq_code_bits, gq_code_bytes, gq_code_pitch,
-    gq_dequantize, gq_dequantize_to, gq_exp_allreduce, gq_exp_combine, gq_exp_ring_stream,
-    gq_exp_tree_stream, gq_get_status, gq_global_norm, gq_norm_finish, gq_norm_partial,
-    gq_philox4x32_10, gq_quantize, gq_quantize_sum, gq_reduce_codes, gq_status_string,
-    gq_workspace, gq_workspace_bytes, lib, library_path)
+    BF16, EXP, F16, F32, LINEAR, NORM_INF, NORM_L2, ORDER_RING, ORDER_TREE, SUM_I32, SUM_I8,
+    GQError, gq_abi_version, gq_allreduce_mean, gq_allreduce_mean_noalloc,
+    gq_allreduce_mean_segments, gq_allreduce_mean_to, gq_allreduce_mean_with_norm, gq_code_bits,
+    gq_code_bytes, gq_code_pitch, gq_dequantize, gq_dequantize_sums, gq_dequantize_to,
+    gq_exp_allreduce, gq_exp_combine, gq_exp_ring_stream, gq_exp_tree_stream, gq_get_status,
+    gq_global_norm, gq_norm_finish, gq_norm_partial, gq_philox4x32_10, gq_quantize,
+    gq_quantize_sum, gq_reduce_codes, gq_status_string, gq_workspace, gq_workspace_bytes, lib,
+    library_path)

@@ -12,6 +12,7 @@ _PKG = os.path.dirname(os.path.abspath(__file__))
 _LIB_PATH = os.path.join(_PKG, "libgq.so")
 
 F32, BF16, F16 = 0, 1, 2
+SUM_I32, SUM_I8 = 0, 1
 LINEAR, EXP = 0, 1
 NORM_INF, NORM_L2 = 0, 2
 ORDER_TREE, ORDER_RING = 0, 1
@@ -58,7 +59,8 @@ def lib() -> ctypes.CDLL:
                                       vp, sz, vp]),
         "gq_norm_partial": (ci, [vp, ci, i64, i64, ci, ci, vp, vp, sz, vp]),
         "gq_norm_finish": (ci, [vp, ci, ci, vp, vp]),
-        "gq_quantize_sum": (ci, [vp, ci, i64, i64, i64, vp, ci, ci, u64, u64, vp, vp]),
+        "gq_quantize_sum": (ci, [vp, ci, i64, i64, i64, vp, ci, ci, u64, u64, vp, ci, vp, sz, vp]),
+        "gq_dequantize_sums": (ci, [vp, ci, vp, ci, ci, i64, i64, vp, ci, vp]),
         "gq_exp_tree_stream": (ctypes.c_uint32, [ci, i64]),
         "gq_exp_ring_stream": (ctypes.c_uint32, [i64, i64]),
         "gq_exp_combine": (ci, [vp, vp, i64, u64, u64, ctypes.c_uint32, vp, vp]),
@@ -289,16 +291,38 @@ def gq_norm_finish(part, q, p, norm=None, stream=None) -> torch.Tensor:
     return norm
 
 
-def gq_quantize_sum(grads, norm, scheme, s, seed, step, worker0=0, sums=None,
-                    stream=None) -> torch.Tensor:
+_SUM_TYPES = {torch.int32: SUM_I32, torch.int8: SUM_I8}
+
+
+def gq_quantize_sum(grads, norm, scheme, s, seed, step, worker0=0, sums=None, ws=None,
+                    stream=None, sum_dtype=torch.int32) -> torch.Tensor:
     """One rank's share of a multi-GPU allreduce: integer code sums of its rows (workers
-    worker0 ..), to be summed over ranks and dequantised with the total worker count."""
+    worker0 ..), int32 or int8, to be summed over ranks and dequantised with the total worker
+    count.  ws (optional workspace) lets large problems take the bulk-copy kernel."""
     dt, m, d = _grads(grads)
     if sums is None:
-        sums = torch.empty(d, dtype=torch.int32, device=grads.device)
+        sums = torch.empty(d, dtype=sum_dtype, device=grads.device)
+    if sums.dtype not in _SUM_TYPES:
+        raise TypeError("sums must be int32 or int8")
     _check(lib().gq_quantize_sum(_p(grads), dt, m, d, worker0, _p(norm), scheme, s, seed, step,
-                                 _p(sums), _stream(stream)), "gq_quantize_sum")
+                                 _p(sums), _SUM_TYPES[sums.dtype], _p(ws),
+                                 0 if ws is None else ws.numel(), _stream(stream)),
+           "gq_quantize_sum")
     return sums
+
+
+def gq_dequantize_sums(sums, norm, scheme, s, n, out=None, stream=None,
+                       out_dtype=torch.float32) -> torch.Tensor:
+    """Dequantised mean from int32 or int8 sums over n workers."""
+    if sums.dtype not in _SUM_TYPES:
+        raise TypeError("sums must be int32 or int8")
+    d = sums.numel()
+    if out is None:
+        out = torch.empty(d, dtype=out_dtype, device=sums.device)
+    _check(lib().gq_dequantize_sums(_p(sums), _SUM_TYPES[sums.dtype], _p(norm), scheme, s, n, d,
+                                    _p(out), _out_code(out), _stream(stream)),
+           "gq_dequantize_sums")
+    return out
 
 
 def gq_allreduce_mean_noalloc(grads, q, p, scheme, s, seed, step, out, norm=None, codes=None,

@@ -1,21 +1,31 @@
-"""Compile the CUDA library (csrc/gq.cu + csrc/gq_kernels.cuh) into libgq.so, in-tree.
+"""Compile the CUDA library (csrc/*.cu over csrc/gq_kernels.cuh) into libgq.so, in-tree.
 
-One translation unit, one -gencode (sm_103a), static CUDA runtime: the library depends on
-nothing but the driver at load time.  -fmad=false keeps every fp32 operation a separately
-rounded IEEE operation (the rounding decisions must be bit-identical to their definition).
+Five translation units (the C ABI and the other kernels in gq.cu; the quantise launchers, one per
+gradient type and scheme) compiled in parallel with one -gencode (sm_103a), then linked with the
+static CUDA runtime: the library depends on nothing but the driver at load time.  -fmad=false
+keeps every fp32 operation a separately rounded IEEE operation (the rounding decisions must be
+bit-identical to their definition).
 """
 from __future__ import annotations
 
+import glob
 import os
 import shutil
 import subprocess
 
 PKG = os.path.dirname(os.path.abspath(__file__))
 ROOT = os.path.dirname(PKG)
-SOURCES = [os.path.join(PKG, "csrc", "gq.cu"), os.path.join(PKG, "csrc", "gq_kernels.cuh"),
-           os.path.join(ROOT, "include", "gq.h")]
+CSRC = os.path.join(PKG, "csrc")
+UNITS = ["gq.cu", "gq_quant_f32_l.cu", "gq_quant_f32_e.cu", "gq_quant_bf16_l.cu",
+         "gq_quant_bf16_e.cu"]
+OBJ_DIR = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libgq.so")
 ARCH = "-gencode=arch=compute_103a,code=sm_103a"
+
+
+def sources() -> list:
+    return sorted(glob.glob(os.path.join(CSRC, "*.cu")) + glob.glob(os.path.join(CSRC, "*.cuh"))
+                  + [os.path.join(ROOT, "include", "gq.h")])
 
 
 def nvcc() -> str:
@@ -25,24 +35,37 @@ def nvcc() -> str:
     return cand
 
 
-def command(out: str, extra=()) -> list:
+def compile_command(unit: str, obj: str, extra=()) -> list:
     return [nvcc(), ARCH, "-O3", "-lineinfo", "-fmad=false", "-std=c++17", "-Xcompiler", "-fPIC",
-            "-shared", "-I" + os.path.join(ROOT, "include"), *extra, "-o", out,
-            os.path.join(PKG, "csrc", "gq.cu")]
+            "-I" + os.path.join(ROOT, "include"), *extra, "-c", "-o", obj,
+            os.path.join(CSRC, unit)]
+
+
+def link_command(objs: list, out: str) -> list:
+    return [nvcc(), ARCH, "-shared", "-o", out, *objs]
 
 
 def is_stale() -> bool:
     if not os.path.exists(LIB):
         return True
     t = os.path.getmtime(LIB)
-    return any(os.path.getmtime(s) > t for s in SOURCES)
+    return any(os.path.getmtime(s) > t for s in sources())
 
 
 def build_library(force: bool = False, verbose: bool = False) -> str:
     """Build libgq.so if missing or older than its sources; return its path."""
     if force or is_stale():
-        tmp = LIB + ".tmp.%d" % os.getpid()
+        os.makedirs(OBJ_DIR, exist_ok=True)
         extra = ("-Xptxas", "-v") if verbose else ()
-        subprocess.run(command(tmp, extra), check=True)
+        tag = ".%d" % os.getpid()
+        objs = [os.path.join(OBJ_DIR, u[:-3] + tag + ".o") for u in UNITS]
+        procs = [subprocess.Popen(compile_command(u, o, extra)) for u, o in zip(UNITS, objs)]
+        codes = [p.wait() for p in procs]
+        if any(codes):
+            raise subprocess.CalledProcessError(next(c for c in codes if c), "nvcc")
+        tmp = LIB + ".tmp" + tag
+        subprocess.run(link_command(objs, tmp), check=True)
         os.replace(tmp, LIB)
+        for o in objs:
+            os.remove(o)
     return LIB

@@ -10,10 +10,13 @@ dequantises.  Here each rank is one worker: rank r holds x_r, the flat gradient 
   2. gq_quantize_sum: the rank's stochastically rounded level codes, already in summable integer
      form (Global-L_s: the level index; Global-E_s: 2^(k-1) units of 2^-(s-1)), with worker
      index r keying the random words;
-  3. an int32 SUM allreduce of those d integers (exact in any order: |sum| < 2^24);
-  4. gq_dequantize with n = world size -> the unbiased estimate of the mean gradient, written
-     back into the bucket in its own type (a bf16 bucket gets the fp32 value rounded to nearest
-     even).
+  3. a SUM allreduce of those d integers, exact in any order: int8 on the wire when the total
+     over all workers fits (n s <= 127 for Global-L, n 2^(s-1) <= 127 for Global-E; the pages
+     sum 8-bit codes natively, which is exact only in that range), a quarter of an fp32
+     allreduce's bytes; int32 otherwise;
+  4. gq_dequantize_sums with n = world size -> the unbiased estimate of the mean gradient,
+     written back into the bucket in its own type (a bf16 bucket gets the fp32 value rounded to
+     nearest even).
 
 On one GPU with world size 1 this is gq_allreduce_mean of the 1 x d bucket.  The random stream
 of bucket b at iteration t uses step t * 2^16 + b (t < 2^48, b < 2^16), so every bucket and
@@ -53,11 +56,12 @@ class LibraryOps:
     def norm_finish(self, part, q, p):
         return gq.gq_norm_finish(part, q, p)
 
-    def quantize_sum(self, x, norm, scheme, s, seed, step, worker0):
-        return gq.gq_quantize_sum(x, norm, scheme, s, seed, step, worker0=worker0)
+    def quantize_sum(self, x, norm, scheme, s, seed, step, worker0, sum_dtype):
+        return gq.gq_quantize_sum(x, norm, scheme, s, seed, step, worker0=worker0,
+                                  ws=self._workspace(x.device), sum_dtype=sum_dtype)
 
     def dequantize(self, sums, norm, scheme, s, n, out):
-        return gq.gq_dequantize(sums, norm, scheme, s, n, out=out)  # out: fp32 or bf16 bucket
+        return gq.gq_dequantize_sums(sums, norm, scheme, s, n, out=out)  # out: the bucket
 
 
 @dataclass
@@ -74,6 +78,7 @@ class GlobalQSGDState:
     ops: object = None
     step: int = 0
     buckets_seen: int = field(default=0, init=False)
+    wire_dtype: object = field(default=None, init=False)  # int8 or int32, set from the world size
 
     def __post_init__(self):
         if (self.q, self.p) not in ((gq.NORM_INF, gq.NORM_INF), (gq.NORM_L2, gq.NORM_L2)):
@@ -88,6 +93,8 @@ class GlobalQSGDState:
         if n * per_worker >= 1 << 24:
             raise ValueError("world size %d x %d units per worker reaches 2^24: the integer sums "
                              "would not convert exactly" % (n, per_worker))
+        # the narrowest integer type that holds the sum over all workers exactly
+        self.wire_dtype = torch.int8 if n * per_worker <= 127 else torch.int32
         if self.ops is None:
             self.ops = LibraryOps()
 
@@ -120,7 +127,8 @@ def global_qsgd_hook(state: GlobalQSGDState, bucket) -> torch.futures.Future:
     norm = ops.norm_finish(part, state.q, state.p)
 
     step = state.bucket_step(bucket.index())
-    sums = ops.quantize_sum(x, norm, state.scheme, state.s, state.seed, step, state.rank)
+    sums = ops.quantize_sum(x, norm, state.scheme, state.s, state.seed, step, state.rank,
+                            state.wire_dtype)
     state.buckets_seen += 1
     if bucket.is_last():
         state.step += 1

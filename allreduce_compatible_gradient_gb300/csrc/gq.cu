@@ -1,9 +1,11 @@
-// gq.cu -- C ABI (include/gq.h) over the sm_103a kernels in gq_kernels.cuh.
+// gq.cu -- C ABI (include/gq.h) over the sm_103a kernels in gq_kernels.cuh (the quantise
+// launchers are in gq_quant_<type>_<scheme>.cu).
 //
 // Host side only: argument checks (returned synchronously, before anything is enqueued),
 // launch geometry (grid = resident blocks per SM x SM count, capped by the work), and kernel
 // dispatch on (dtype, scheme, code width, norm order).  No memory is allocated here.
 #include "gq.h"
+#include "gq_host.cuh"
 #include "gq_kernels.cuh"
 
 #include <cuda_runtime.h>
@@ -12,78 +14,21 @@
 #include <cstring>
 #include <mutex>
 
+using namespace gqh;
+
 namespace {
-
-using gq::kThreads;
-
-constexpr int64_t kMaxD = int64_t(1) << 34;  // Philox counter word 0 holds j / 8 in 31 bits
-constexpr int kMaxDevices = 64;
-
-bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
-
-int sm_count() {
-    static int cache[kMaxDevices] = {0};
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 152;
-    if (cache[dev] == 0) {
-        int v = 0;
-        if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || v <= 0)
-            v = 152;
-        cache[dev] = v;
-    }
-    return cache[dev];
-}
-
-// Resident blocks per SM for a kernel with `smem` bytes of dynamic shared memory, cached per
-// (kernel, device).  The first query for a kernel on a device also raises that kernel's
-// dynamic shared-memory limit to `smem`.
-template <typename K>
-int blocks_per_sm(K kernel, int smem = 0, int threads = kThreads) {
-    struct Entry {
-        const void* fn;
-        int dev;
-        int nb;
-    };
-    static Entry table[512];
-    static int used = 0;
-    static std::mutex mu;
-    const void* fn = reinterpret_cast<const void*>(kernel);
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) dev = 0;
-    std::lock_guard<std::mutex> lock(mu);
-    for (int e = 0; e < used; ++e)
-        if (table[e].fn == fn && table[e].dev == dev) return table[e].nb;
-    if (smem > 0)  // dynamic + static shared memory may pass the default 48 KB
-        cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    int nb = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, kernel, threads, smem) != cudaSuccess ||
-        nb <= 0)
-        nb = 1;
-    if (used < 512) table[used++] = Entry{fn, dev, nb};
-    return nb;
-}
-
-// Grid for a grid-stride kernel over `work` thread-items: one full wave of resident blocks
-// (a multiple of the SM count), fewer when the work is smaller.
-template <typename K>
-unsigned grid_for(K kernel, int64_t work, int64_t cap = INT32_MAX, int smem = 0) {
-    const int64_t full = static_cast<int64_t>(blocks_per_sm(kernel, smem)) * sm_count();
-    int64_t need = (work + kThreads - 1) / kThreads;
-    int64_t g = need < full ? need : full;
-    if (g > cap) g = cap;
-    if (g < 1) g = 1;
-    return static_cast<unsigned>(g);
-}
-
-gq_status launch_status() {
-    return cudaGetLastError() == cudaSuccess ? GQ_OK : GQ_ERR_CUDA;
-}
 
 gq_status check_grads(const void* grads, int dtype, int64_t n, int64_t d) {
     if (!grads || !aligned16(grads)) return GQ_ERR_INVALID;
     if (dtype != GQ_F32 && dtype != GQ_BF16) return GQ_ERR_INVALID;
     if (n < 1 || n >= (int64_t(1) << 31) || d < 1 || d >= kMaxD) return GQ_ERR_INVALID;
     return GQ_OK;
+}
+
+// The sum of n workers' codes fits int8: n s <= 127 (L) or n 2^(s-1) <= 127 (E).
+bool fits_i8(int scheme, int s, int64_t n) {
+    const int64_t unit = scheme == GQ_LINEAR ? s : (int64_t(1) << (s - 1));
+    return n * unit <= 127;
 }
 
 gq_status check_scheme(int scheme, int s, int64_t n) {
@@ -144,52 +89,17 @@ gq_status norm_any(const void* grads, int dtype, int mode, int64_t n, int64_t d,
                            : dispatch_norm<uint16_t>(grads, mode, n, d, norm_user, part_user, w, st);
 }
 
-// ---- quantize (+ sum + dequantize) ----------------------------------------------------------
-// TRUSTED: the norm comes from norm_kernel on the same gradients (fused path), so a finite norm
-// rules out NaN and infinite elements.
-// Problems with at least one 3840-column chunk per SM of 16-byte aligned rows take the kernel
-// fed by bulk copies (it needs a status word for its bounded waits); the rest the direct one.
-template <typename T, int SCHEME, int BITS, bool OUT, bool TRUSTED>
-gq_status run_quant(const void* grads, const gq::QuantArgs& a, void* codes, void* out,
-                    cudaStream_t st, unsigned int* status = nullptr) {
-    const int64_t groups = BITS ? a.pitch / gq::kQCols : (a.d + gq::kQCols - 1) / gq::kQCols;
-    const int64_t chunks = (a.d / gq::kQCols) / gq::kTmaConsumers;
-    if (status && a.vec_rows && chunks >= sm_count()) {
-        auto kt = gq::quantize_tma_kernel<T, SCHEME, BITS, OUT, TRUSTED>;
-        constexpr int tsmem = gq::TmaCfg<T>::kSmemBytes;
-        if (blocks_per_sm(kt, tsmem, gq::kTmaBlock) < 1) return GQ_ERR_CUDA;
-        const unsigned grid = static_cast<unsigned>(sm_count());
-        kt<<<grid, gq::kTmaBlock, tsmem, st>>>(static_cast<const T*>(grads), a, groups,
-                                               static_cast<unsigned char*>(codes), out, status);
-        return launch_status();
-    }
-    auto k = gq::quantize_kernel<T, SCHEME, BITS, OUT, TRUSTED>;
-    constexpr int smem = gq::Staging<T>::kBytes;
-    const unsigned grid = grid_for(k, groups, INT32_MAX, smem);
-    k<<<grid, kThreads, smem, st>>>(static_cast<const T*>(grads), a, groups,
-                                    static_cast<unsigned char*>(codes), out);
-    return launch_status();
-}
-
-template <typename T, int SCHEME, bool OUT, bool TRUSTED>
-gq_status quant_bits(const void* grads, const gq::QuantArgs& a, int bits, void* codes, void* out,
-                     cudaStream_t st, unsigned int* status) {
-    if (!codes) return run_quant<T, SCHEME, 0, OUT, TRUSTED>(grads, a, nullptr, out, st, status);
-    if (bits == 4) return run_quant<T, SCHEME, 4, OUT, TRUSTED>(grads, a, codes, out, st, status);
-    return run_quant<T, SCHEME, 8, OUT, TRUSTED>(grads, a, codes, out, st, status);
-}
-
+// ---- quantize (+ sum + dequantize): one launcher per (gradient type, scheme) --------------
 // status (nullable): the workspace status word, for the bounded waits of the bulk-copy kernel
 template <bool OUT, bool TRUSTED>
 gq_status quant_any(const void* grads, int dtype, const gq::QuantArgs& a, int scheme, int bits,
                     void* codes, void* out, cudaStream_t st, unsigned int* status = nullptr) {
     if (dtype == GQ_F32)
         return scheme == GQ_LINEAR
-                   ? quant_bits<float, gq::kLinear, OUT, TRUSTED>(grads, a, bits, codes, out, st, status)
-                   : quant_bits<float, gq::kExp, OUT, TRUSTED>(grads, a, bits, codes, out, st, status);
-    return scheme == GQ_LINEAR
-               ? quant_bits<uint16_t, gq::kLinear, OUT, TRUSTED>(grads, a, bits, codes, out, st, status)
-               : quant_bits<uint16_t, gq::kExp, OUT, TRUSTED>(grads, a, bits, codes, out, st, status);
+                   ? quant_f32_l(grads, a, bits, OUT, TRUSTED, codes, out, st, status)
+                   : quant_f32_e(grads, a, bits, OUT, TRUSTED, codes, out, st, status);
+    return scheme == GQ_LINEAR ? quant_bf16_l(grads, a, bits, OUT, TRUSTED, codes, out, st, status)
+                               : quant_bf16_e(grads, a, bits, OUT, TRUSTED, codes, out, st, status);
 }
 
 gq::QuantArgs make_args(const float* norm_ptr, int dtype, int64_t n, int64_t d, int s,
@@ -211,6 +121,7 @@ gq::QuantArgs make_args(const float* norm_ptr, int dtype, int64_t n, int64_t d, 
     a.vec_rows = (d % (dtype == GQ_F32 ? 4 : 8)) == 0;
     a.row0 = 0;
     a.sums = nullptr;
+    a.sums_i8 = 0;
     a.out_dtype = gq::kOutF32;
     return a;
 }
@@ -296,26 +207,35 @@ gq_status gq_reduce_codes(const void* codes, int scheme, int s, int64_t n, int64
     return launch_status();
 }
 
-gq_status gq_dequantize_to(const int32_t* sum_dev, const float* norm_dev, int scheme, int s,
-                           int64_t n, int64_t d, void* out_dev, int out_dtype, void* stream) {
+gq_status gq_dequantize_sums(const void* sum_dev, int sum_type, const float* norm_dev, int scheme,
+                             int s, int64_t n, int64_t d, void* out_dev, int out_dtype,
+                             void* stream) {
     if (!sum_dev || !norm_dev || !out_dev || !aligned16(sum_dev) || !aligned16(out_dev))
         return GQ_ERR_INVALID;
     if (out_dtype != GQ_F32 && out_dtype != GQ_BF16 && out_dtype != GQ_F16) return GQ_ERR_INVALID;
+    if (sum_type != GQ_SUM_I32 && sum_type != GQ_SUM_I8) return GQ_ERR_INVALID;
     if (n < 1 || n >= (int64_t(1) << 31) || d < 1 || d >= kMaxD) return GQ_ERR_INVALID;
     gq_status st = check_scheme(scheme, s, n);
     if (st != GQ_OK) return st;
+    if (sum_type == GQ_SUM_I8 && !fits_i8(scheme, s, n)) return GQ_ERR_OVERFLOW;
     cudaStream_t cs = static_cast<cudaStream_t>(stream);
     const int64_t quads = (d + 3) / 4;
+    const uint32_t su = static_cast<uint32_t>(s);
+    const bool i8 = sum_type == GQ_SUM_I8;
     if (scheme == GQ_LINEAR) {
-        auto k = gq::dequantize_kernel<gq::kLinear>;
-        k<<<grid_for(k, quads), kThreads, 0, cs>>>(sum_dev, norm_dev, n, static_cast<uint32_t>(s), d,
-                                                   out_dev, out_dtype);
+        auto k = i8 ? gq::dequantize_kernel<gq::kLinear, true> : gq::dequantize_kernel<gq::kLinear, false>;
+        k<<<grid_for(k, quads), kThreads, 0, cs>>>(sum_dev, norm_dev, n, su, d, out_dev, out_dtype);
     } else {
-        auto k = gq::dequantize_kernel<gq::kExp>;
-        k<<<grid_for(k, quads), kThreads, 0, cs>>>(sum_dev, norm_dev, n, static_cast<uint32_t>(s), d,
-                                                   out_dev, out_dtype);
+        auto k = i8 ? gq::dequantize_kernel<gq::kExp, true> : gq::dequantize_kernel<gq::kExp, false>;
+        k<<<grid_for(k, quads), kThreads, 0, cs>>>(sum_dev, norm_dev, n, su, d, out_dev, out_dtype);
     }
     return launch_status();
+}
+
+gq_status gq_dequantize_to(const int32_t* sum_dev, const float* norm_dev, int scheme, int s,
+                           int64_t n, int64_t d, void* out_dev, int out_dtype, void* stream) {
+    return gq_dequantize_sums(sum_dev, GQ_SUM_I32, norm_dev, scheme, s, n, d, out_dev, out_dtype,
+                              stream);
 }
 
 gq_status gq_dequantize(const int32_t* sum_dev, const float* norm_dev, int scheme, int s,
@@ -586,46 +506,27 @@ extern "C" gq_status gq_norm_finish(const double* part_dev, int q, int p, float*
 
 extern "C" gq_status gq_quantize_sum(const void* grads, int dtype, int64_t m, int64_t d,
                                      int64_t worker0, const float* norm_dev, int scheme, int s,
-                                     uint64_t seed, uint64_t step, int32_t* sum_dev,
-                                     void* stream) {
+                                     uint64_t seed, uint64_t step, void* sum_dev, int sum_type,
+                                     void* ws, size_t ws_bytes, void* stream) {
     gq_status st = check_grads(grads, dtype, m, d);
     if (st != GQ_OK) return st;
     if ((st = check_scheme(scheme, s, m)) != GQ_OK) return st;
     if (!norm_dev || !sum_dev || !aligned16(sum_dev)) return GQ_ERR_INVALID;
+    if (sum_type != GQ_SUM_I32 && sum_type != GQ_SUM_I8) return GQ_ERR_INVALID;
     if (worker0 < 0 || worker0 + m > (int64_t(1) << 31)) return GQ_ERR_INVALID;
+    if (sum_type == GQ_SUM_I8 && !fits_i8(scheme, s, m)) return GQ_ERR_OVERFLOW;
+    if (ws && (st = check_ws(ws, ws_bytes, m, d)) != GQ_OK) return st;
     gq::QuantArgs a = make_args(norm_dev, dtype, m, d, s, seed, step);
     a.row0 = static_cast<uint32_t>(worker0);
     a.sums = sum_dev;
+    a.sums_i8 = sum_type == GQ_SUM_I8;
+    unsigned int* status = ws ? &reinterpret_cast<gq::WsHeader*>(ws)->status : nullptr;
     return quant_any<true, false>(grads, dtype, a, scheme, gq_code_bits(scheme, s), nullptr,
-                                  nullptr, static_cast<cudaStream_t>(stream));
+                                  nullptr, static_cast<cudaStream_t>(stream), status);
 }
 
 // ---- segmented form: many n x d_l problems in two launches per kSegChunk segments -----------
 namespace {
-
-// Runs of blocks for a chunk of segments: each gets a share of `target` blocks in proportion to
-// its elements, at least one and at most one per 256 column groups of `cols` columns.
-void plan_runs(gq::SegLaunch& L, const int64_t* d, int64_t n, int cols, int64_t target) {
-    double total = 0.0;
-    for (int k = 0; k < L.nseg; ++k) total += static_cast<double>(d[k]);
-    int32_t b = 0;
-    for (int k = 0; k < L.nseg; ++k) {
-        const int64_t groups = (d[k] + cols - 1) / cols;
-        const int64_t most = (groups + kThreads - 1) / kThreads;
-        int64_t nb = static_cast<int64_t>(static_cast<double>(d[k]) / total * static_cast<double>(target));
-        if (nb > most) nb = most;
-        if (nb < 1) nb = 1;
-        L.seg[k].d = d[k];
-        L.seg[k].b0 = b;
-        L.seg[k].nb = static_cast<int32_t>(nb);
-        b += static_cast<int32_t>(nb);
-    }
-    (void)n;
-}
-
-int32_t total_blocks(const gq::SegLaunch& L) {
-    return L.seg[L.nseg - 1].b0 + L.seg[L.nseg - 1].nb;
-}
 
 template <typename T, int MODE>
 gq_status run_norm_segments(gq::SegLaunch& L, const int64_t* d, int64_t n, float* norms_user,
@@ -649,17 +550,6 @@ gq_status norm_segments_any(int mode, gq::SegLaunch& L, const int64_t* d, int64_
         case gq::kL2Max: return run_norm_segments<T, gq::kL2Max>(L, d, n, norms_user, ws, st);
         default: return run_norm_segments<T, gq::kMaxL2>(L, d, n, norms_user, ws, st);
     }
-}
-
-template <typename T, int SCHEME>
-gq_status run_quant_segments(gq::SegLaunch& L, const int64_t* d, int64_t n,
-                             const gq::QuantArgs& base, unsigned char* ws, cudaStream_t st) {
-    auto k = gq::quantize_segments_kernel<T, SCHEME>;
-    constexpr int smem = gq::Staging<T>::kBytes;
-    const int64_t full = static_cast<int64_t>(blocks_per_sm(k, smem)) * sm_count();
-    plan_runs(L, d, n, gq::kQCols, full);
-    k<<<total_blocks(L), kThreads, smem, st>>>(L, base, ws);
-    return launch_status();
 }
 
 }  // namespace
@@ -700,13 +590,11 @@ extern "C" gq_status gq_allreduce_mean_segments(int64_t nseg, const void* const*
                              : norm_segments_any<uint16_t>(mode, L, d + c0, n, norms_dev, w, cs);
         if (st != GQ_OK) return st;
         if (dtype == GQ_F32)
-            st = scheme == GQ_LINEAR
-                     ? run_quant_segments<float, gq::kLinear>(L, d + c0, n, base, w, cs)
-                     : run_quant_segments<float, gq::kExp>(L, d + c0, n, base, w, cs);
+            st = scheme == GQ_LINEAR ? quant_segments_f32_l(L, d + c0, n, base, w, cs)
+                                     : quant_segments_f32_e(L, d + c0, n, base, w, cs);
         else
-            st = scheme == GQ_LINEAR
-                     ? run_quant_segments<uint16_t, gq::kLinear>(L, d + c0, n, base, w, cs)
-                     : run_quant_segments<uint16_t, gq::kExp>(L, d + c0, n, base, w, cs);
+            st = scheme == GQ_LINEAR ? quant_segments_bf16_l(L, d + c0, n, base, w, cs)
+                                     : quant_segments_bf16_e(L, d + c0, n, base, w, cs);
         if (st != GQ_OK) return st;
     }
     return GQ_OK;

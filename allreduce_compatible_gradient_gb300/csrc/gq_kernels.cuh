@@ -486,7 +486,7 @@ norm_kernel(const T* __restrict__ x, int64_t n, int64_t d, int64_t groups, bool 
 
 // The norm from the combined partials of several ranks (a sum of squares for (2,2), a maximum
 // magnitude for (inf,inf)), rounded to fp32 as norm_kernel rounds it.
-__global__ void norm_finish_kernel(const double* __restrict__ part, bool take_sqrt,
+static __global__ void norm_finish_kernel(const double* __restrict__ part, bool take_sqrt,
                                    float* __restrict__ norm) {
     if (threadIdx.x == 0 && blockIdx.x == 0) {
         const double v = *part;
@@ -594,7 +594,8 @@ struct QuantArgs {
     int64_t pitch;           // code row pitch in elements
     bool vec_rows;
     uint32_t row0;           // worker index of local row 0 (keys the random words)
-    int32_t* sums;           // when set, the kernel writes the integer sums here instead of out
+    void* sums;              // when set, the kernel writes the integer sums here instead of out
+    int sums_i8;             // 1: the sums as int8 (they fit: |sum| <= 127), 0: as int32
     int out_dtype;           // kOutF32, kOutBF16 or kOutF16
 };
 
@@ -884,23 +885,40 @@ __device__ __forceinline__ void store1(void* out, int dt, int64_t j, float v) {
 }
 
 // Output of one finished column group: dequantise the sums into out (fp32, bf16 or fp16), or,
-// when `sums` is set, write the integer sums themselves (exact: every partial sum is an integer
-// below 2^24).
-__device__ __forceinline__ void store_out(void* __restrict__ out, int32_t* __restrict__ sums,
-                                          int dt, int64_t g, int64_t d, float scale,
+// when `sums` is set, write the integer sums themselves as int32 or int8 (exact: every partial
+// sum is an integer below 2^24, and below 128 in magnitude when int8 is asked for).
+__device__ __forceinline__ void store_out(void* __restrict__ out, void* __restrict__ sums,
+                                          int sums_i8, int dt, int64_t g, int64_t d, float scale,
                                           const float (&S)[kQCols]) {
     const int64_t j0 = g * kQCols;
     if (sums) {
+        if (sums_i8) {
+            int8_t* q = static_cast<int8_t*>(sums);
+            if (j0 + kQCols <= d) {
+                uint32_t w[2] = {0u, 0u};
+#pragma unroll
+                for (int c = 0; c < kQCols; ++c)
+                    w[c >> 2] |= (static_cast<uint32_t>(static_cast<int32_t>(S[c])) & 0xFFu)
+                                 << (8 * (c & 3));
+                *reinterpret_cast<uint2*>(q + j0) = make_uint2(w[0], w[1]);
+            } else {
+#pragma unroll
+                for (int c = 0; c < kQCols; ++c)
+                    if (j0 + c < d) q[j0 + c] = static_cast<int8_t>(static_cast<int32_t>(S[c]));
+            }
+            return;
+        }
+        int32_t* q = static_cast<int32_t*>(sums);
         if (j0 + kQCols <= d) {
 #pragma unroll
             for (int h = 0; h < kQCols / 4; ++h)
-                reinterpret_cast<int4*>(sums + j0)[h] =
+                reinterpret_cast<int4*>(q + j0)[h] =
                     make_int4(static_cast<int32_t>(S[4 * h]), static_cast<int32_t>(S[4 * h + 1]),
                               static_cast<int32_t>(S[4 * h + 2]), static_cast<int32_t>(S[4 * h + 3]));
         } else {
 #pragma unroll
             for (int c = 0; c < kQCols; ++c)
-                if (j0 + c < d) sums[j0 + c] = static_cast<int32_t>(S[c]);
+                if (j0 + c < d) q[j0 + c] = static_cast<int32_t>(S[c]);
         }
         return;
     }
@@ -1010,7 +1028,7 @@ __device__ __forceinline__ void staged_groups(const T* __restrict__ x, const Qua
         if (++r == nb) {
             r = 0;
             ++q;
-            if (WRITE_OUT) store_out(out, a.sums, a.out_dtype, g, a.d, scale, S);
+            if (WRITE_OUT) store_out(out, a.sums, a.sums_i8, a.out_dtype, g, a.d, scale, S);
         }
     }
     cp_async_wait<0>();
@@ -1055,7 +1073,7 @@ __device__ __forceinline__ void quantize_body(const T* __restrict__ x, const Qua
                 for (int64_t i = 0; i < a.n; ++i) store_codes<CODE_BITS>(codes, i, g, a.pitch, zero);
             }
         }
-        if (WRITE_OUT) store_out(out, a.sums, a.out_dtype, g, a.d, scale, S);
+        if (WRITE_OUT) store_out(out, a.sums, a.sums_i8, a.out_dtype, g, a.d, scale, S);
     }
 }
 
@@ -1210,14 +1228,15 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_
         : "memory");
 }
 
-template <typename T, int SCHEME, int CODE_BITS, bool WRITE_OUT, bool TRUSTED>
+// SUB: rows decided together (2; 1 for a single worker, whose stages hold one row).
+template <typename T, int SCHEME, int CODE_BITS, bool WRITE_OUT, bool TRUSTED, int SUB>
 __global__ void __launch_bounds__(kTmaBlock, 1)
 quantize_tma_kernel(const T* __restrict__ x, QuantArgs a, int64_t groups,
                     unsigned char* __restrict__ codes, void* __restrict__ out,
                     unsigned int* __restrict__ status) {
     using Cfg = TmaCfg<T>;
     constexpr int RB = Cfg::kRows;
-    constexpr int kSub = 2;  // rows decided together
+    constexpr int kSub = SUB;
     extern __shared__ __align__(128) unsigned char tma_smem[];
     __shared__ __align__(8) uint64_t full_bar[Cfg::kStages];
     __shared__ __align__(8) uint64_t empty_bar[Cfg::kStages];
@@ -1321,7 +1340,7 @@ quantize_tma_kernel(const T* __restrict__ x, QuantArgs a, int64_t groups,
                         __syncwarp();
                         if (lane == 0) mbar_arrive(smem_u32(&empty_bar[st]));
                     }
-                    if (!active) continue;
+                    if (!active || r0 >= a.n) continue;  // past the last worker: nothing to do
                     uint32_t aw[kSub][4];
 #pragma unroll
                     for (int u = 0; u < kSub; ++u) {
@@ -1341,7 +1360,7 @@ quantize_tma_kernel(const T* __restrict__ x, QuantArgs a, int64_t groups,
                     }
                 }
             }
-            if (ok && active && WRITE_OUT) store_out(out, a.sums, a.out_dtype, g, a.d, scale, S);
+            if (ok && active && WRITE_OUT) store_out(out, a.sums, a.sums_i8, a.out_dtype, g, a.d, scale, S);
         }
         if (!ok) {
             if (status) atomicCAS(status, 0u, kStatusTimeout);
@@ -1369,7 +1388,7 @@ quantize_tma_kernel(const T* __restrict__ x, QuantArgs a, int64_t groups,
                 for (int64_t i = 0; i < a.n; ++i) store_codes<CODE_BITS>(codes, i, g, a.pitch, zero);
             }
         }
-        if (WRITE_OUT) store_out(out, a.sums, a.out_dtype, g, a.d, scale, S);
+        if (WRITE_OUT) store_out(out, a.sums, a.sums_i8, a.out_dtype, g, a.d, scale, S);
     }
 }
 
@@ -1434,20 +1453,29 @@ reduce_codes_kernel(const unsigned char* __restrict__ codes, int64_t n, int64_t 
     }
 }
 
-// Step 4 unfused: out_j = scale * S_j.
-template <int SCHEME>
+// Step 4 unfused: out_j = scale * S_j, the sums S int32 or (SUM_I8) int8.
+template <int SCHEME, bool SUM_I8>
 __global__ void __launch_bounds__(kThreads)
-dequantize_kernel(const int32_t* __restrict__ sums, const float* __restrict__ norm_ptr,
+dequantize_kernel(const void* __restrict__ sums_v, const float* __restrict__ norm_ptr,
                   int64_t n, uint32_t s, int64_t d, void* __restrict__ out, int dt) {
     __shared__ float sh_scale;
     const float scale = block_scale<SCHEME>(__ldg(norm_ptr), n, s, &sh_scale);
     const int64_t quads = (d + 3) / 4;
     const int64_t stride = static_cast<int64_t>(gridDim.x) * kThreads;
+    const int32_t* sums = static_cast<const int32_t*>(sums_v);
+    const int8_t* sums8 = static_cast<const int8_t*>(sums_v);
     for (int64_t q = static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x; q < quads;
          q += stride) {
         const int64_t j0 = q * 4;
         if (j0 + 4 <= d) {
-            const int4 t = __ldg(reinterpret_cast<const int4*>(sums + j0));
+            int4 t;
+            if (SUM_I8) {
+                const uint32_t w = __ldg(reinterpret_cast<const unsigned int*>(sums8 + j0));
+                t = make_int4(static_cast<int8_t>(w), static_cast<int8_t>(w >> 8),
+                              static_cast<int8_t>(w >> 16), static_cast<int8_t>(w >> 24));
+            } else {
+                t = __ldg(reinterpret_cast<const int4*>(sums + j0));
+            }
             const float v0 = scale * static_cast<float>(t.x), v1 = scale * static_cast<float>(t.y);
             const float v2 = scale * static_cast<float>(t.z), v3 = scale * static_cast<float>(t.w);
             if (dt == kOutF32)
@@ -1456,13 +1484,14 @@ dequantize_kernel(const int32_t* __restrict__ sums, const float* __restrict__ no
                 reinterpret_cast<uint2*>(out)[q] = make_uint2(pack16(dt, v0, v1), pack16(dt, v2, v3));
         } else {
             for (int64_t j = j0; j < d; ++j)
-                store1(out, dt, j, scale * static_cast<float>(__ldg(sums + j)));
+                store1(out, dt, j, scale * static_cast<float>(SUM_I8 ? static_cast<int32_t>(sums8[j])
+                                                                      : __ldg(sums + j)));
         }
     }
 }
 
 // Philox check kernel: one call per thread.
-__global__ void philox_kernel(const uint32_t* __restrict__ ck, uint32_t* __restrict__ out,
+static __global__ void philox_kernel(const uint32_t* __restrict__ ck, uint32_t* __restrict__ out,
                               int64_t count) {
     const int64_t t = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
     if (t >= count) return;
@@ -1541,7 +1570,7 @@ __device__ __forceinline__ void exp_reround8(const int64_t (&t)[8], uint32_t g8,
 
 // One step on d coordinates: out = re-round(decode(a) + decode(b)).  Each thread owns 16
 // coordinates (one 16-byte load of a and of b, one 16-byte store).
-__global__ void __launch_bounds__(kThreads)
+static __global__ void __launch_bounds__(kThreads)
 exp_combine_kernel(const int8_t* __restrict__ a, const int8_t* __restrict__ b, int64_t d,
                    uint32_t sid, ExpArgs ea, int8_t* __restrict__ out) {
     const int64_t chunks = (d + 15) / 16;

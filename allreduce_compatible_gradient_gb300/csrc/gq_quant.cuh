@@ -1,0 +1,80 @@
+// gq_quant.cuh -- quantise launch templates, instantiated once per (gradient type, scheme) by
+// gq_quant_<type>_<scheme>.cu.
+#pragma once
+#include "gq_host.cuh"
+
+namespace gqh {
+
+// ---- quantize (+ sum + dequantize) ----------------------------------------------------------
+// TRUSTED: the norm comes from norm_kernel on the same gradients (fused path), so a finite norm
+// rules out NaN and infinite elements.
+// Problems with at least one 3840-column chunk per SM of 16-byte aligned rows take the kernel
+// fed by bulk copies (it needs a status word for its bounded waits); the rest the direct one.
+template <typename T, int SCHEME, int BITS, bool OUT, bool TRUSTED>
+gq_status run_quant(const void* grads, const gq::QuantArgs& a, void* codes, void* out,
+                    cudaStream_t st, unsigned int* status = nullptr) {
+    const int64_t groups = BITS ? a.pitch / gq::kQCols : (a.d + gq::kQCols - 1) / gq::kQCols;
+    const int64_t chunks = (a.d / gq::kQCols) / gq::kTmaConsumers;
+    if (status && a.vec_rows && chunks >= sm_count()) {
+        auto kt = gq::quantize_tma_kernel<T, SCHEME, BITS, OUT, TRUSTED, 2>;
+        if constexpr (BITS == 0 && OUT && !TRUSTED) {  // one rank's sums: often a single worker
+            if (a.n == 1) kt = gq::quantize_tma_kernel<T, SCHEME, BITS, OUT, TRUSTED, 1>;
+        }
+        constexpr int tsmem = gq::TmaCfg<T>::kSmemBytes;
+        if (blocks_per_sm(kt, tsmem, gq::kTmaBlock) < 1) return GQ_ERR_CUDA;
+        const unsigned grid = static_cast<unsigned>(sm_count());
+        kt<<<grid, gq::kTmaBlock, tsmem, st>>>(static_cast<const T*>(grads), a, groups,
+                                               static_cast<unsigned char*>(codes), out, status);
+        return launch_status();
+    }
+    auto k = gq::quantize_kernel<T, SCHEME, BITS, OUT, TRUSTED>;
+    constexpr int smem = gq::Staging<T>::kBytes;
+    const unsigned grid = grid_for(k, groups, INT32_MAX, smem);
+    k<<<grid, kThreads, smem, st>>>(static_cast<const T*>(grads), a, groups,
+                                    static_cast<unsigned char*>(codes), out);
+    return launch_status();
+}
+
+template <typename T, int SCHEME, bool OUT, bool TRUSTED>
+gq_status quant_bits(const void* grads, const gq::QuantArgs& a, int bits, void* codes, void* out,
+                     cudaStream_t st, unsigned int* status) {
+    if (!codes) return run_quant<T, SCHEME, 0, OUT, TRUSTED>(grads, a, nullptr, out, st, status);
+    if (bits == 4) return run_quant<T, SCHEME, 4, OUT, TRUSTED>(grads, a, codes, out, st, status);
+    return run_quant<T, SCHEME, 8, OUT, TRUSTED>(grads, a, codes, out, st, status);
+}
+
+
+template <typename T, int SCHEME>
+gq_status run_quant_segments(gq::SegLaunch& L, const int64_t* d, int64_t n,
+                             const gq::QuantArgs& base, unsigned char* ws, cudaStream_t st) {
+    auto k = gq::quantize_segments_kernel<T, SCHEME>;
+    constexpr int smem = gq::Staging<T>::kBytes;
+    const int64_t full = static_cast<int64_t>(blocks_per_sm(k, smem)) * sm_count();
+    plan_runs(L, d, n, gq::kQCols, full);
+    k<<<total_blocks(L), kThreads, smem, st>>>(L, base, ws);
+    return launch_status();
+}
+
+
+template <typename T, int SCHEME>
+gq_status quant_entry(const void* grads, const gq::QuantArgs& a, int bits, bool out, bool trusted,
+                      void* codes, void* outp, cudaStream_t st, unsigned int* status) {
+    if (!out) return quant_bits<T, SCHEME, false, false>(grads, a, bits, codes, outp, st, status);
+    if (trusted) return quant_bits<T, SCHEME, true, true>(grads, a, bits, codes, outp, st, status);
+    return quant_bits<T, SCHEME, true, false>(grads, a, bits, codes, outp, st, status);
+}
+
+}  // namespace gqh
+
+// The two launchers of one (gradient type, scheme) pair.
+#define GQH_DEFINE_QUANT(NAME, T, SCHEME)                                                         \
+    gq_status gqh::quant_##NAME(const void* grads, const gq::QuantArgs& a, int bits, bool out,     \
+                                bool trusted, void* codes, void* outp, cudaStream_t st,            \
+                                unsigned int* status) {                                            \
+        return quant_entry<T, SCHEME>(grads, a, bits, out, trusted, codes, outp, st, status);      \
+    }                                                                                              \
+    gq_status gqh::quant_segments_##NAME(gq::SegLaunch& L, const int64_t* d, int64_t n,           \
+                                         const gq::QuantArgs& base, unsigned char* ws,             \
+                                         cudaStream_t st) {                                        \
+        return run_quant_segments<T, SCHEME>(L, d, n, base, ws, st);                               \
+    }

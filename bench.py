@@ -64,10 +64,11 @@ def _peaks():
 
 def _kernel_source_hash() -> str:
     h = hashlib.sha256()
-    for rel in ("allreduce_compatible_gradient_gb300/csrc/gq.cu",
-                "allreduce_compatible_gradient_gb300/csrc/gq_kernels.cuh"):
-        with open(os.path.join(ROOT, rel), "rb") as f:
-            h.update(f.read())
+    csrc = os.path.join(ROOT, "allreduce_compatible_gradient_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        if name.endswith((".cu", ".cuh")):
+            with open(os.path.join(csrc, name), "rb") as f:
+                h.update(f.read())
     return h.hexdigest()[:16]
 
 

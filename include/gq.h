@@ -67,6 +67,12 @@ typedef enum {
  * and the segmented form) may also be GQ_BF16 or GQ_F16. */
 typedef enum { GQ_F32 = 0, GQ_BF16 = 1, GQ_F16 = 2 } gq_dtype;
 
+/* Integer type of the code sums that ranks exchange (gq_quantize_sum, gq_dequantize_sums):
+ * int32 always holds them; int8 holds them when the total number of workers n satisfies
+ * n s <= 127 (Global-L) or n 2^(s-1) <= 127 (Global-E), and then the allreduce moves one byte
+ * per coordinate, a quarter of an fp32 gradient's. */
+typedef enum { GQ_SUM_I32 = 0, GQ_SUM_I8 = 1 } gq_sum_type;
+
 typedef enum {
     GQ_LINEAR = 0, /* Global-L_s, standard dithering */
     GQ_EXP = 1     /* Global-E_s, exponential dithering */
@@ -147,6 +153,14 @@ gq_status gq_dequantize(const int32_t *sum_dev, const float *norm_dev, int schem
  */
 gq_status gq_dequantize_to(const int32_t *sum_dev, const float *norm_dev, int scheme, int s,
                            int64_t n, int64_t d, void *out_dev, int out_dtype, void *stream);
+
+/*
+ * gq_dequantize_to with the sums given as sum_type (GQ_SUM_I32 or GQ_SUM_I8, d elements, 16-byte
+ * aligned).  GQ_SUM_I8 needs n s <= 127 (L) or n 2^(s-1) <= 127 (E), else GQ_ERR_OVERFLOW.
+ */
+gq_status gq_dequantize_sums(const void *sum_dev, int sum_type, const float *norm_dev, int scheme,
+                             int s, int64_t n, int64_t d, void *out_dev, int out_dtype,
+                             void *stream);
 
 /*
  * Steps 1-4 fused: the norm pass, then one pass that quantises, sums over the workers in
@@ -282,14 +296,18 @@ gq_status gq_norm_finish(const double *part_dev, int q, int p, float *norm_dev, 
  * bucket).  Quantises the m x d rows at grads, whose workers are worker0 .. worker0 + m - 1 (the
  * worker index keys the random words, as row i does in gq_quantize), with the fp32 global norm
  * at *norm_dev, and writes the integer sum of their codes (Global-L: the level indices; Global-E:
- * 2^(k-1) units of 2^-(s-1)) to int32 sum_dev[d].  Summing these over all ranks (an integer
- * allreduce, exact) and calling gq_dequantize with n = the total number of workers gives the
- * same result as gq_allreduce_mean on the stacked matrix with the same norm.  Errors as
- * gq_quantize; worker0 >= 0 and worker0 + m <= 2^31.
+ * 2^(k-1) units of 2^-(s-1)) to sum_dev[d] as sum_type (int32, or int8 when m s <= 127 for L,
+ * m 2^(s-1) <= 127 for E, else GQ_ERR_OVERFLOW; the caller keeps the total over ranks in range
+ * too).  Summing these over all ranks (an integer allreduce, exact) and calling
+ * gq_dequantize_sums with n = the total number of workers gives the same result as
+ * gq_allreduce_mean on the stacked matrix with the same norm.  ws (nullable; as for
+ * gq_global_norm) lets a large problem take the bulk-copy kernel, whose bounded waits report
+ * GQ_ERR_TIMEOUT in its status word.  Errors as gq_quantize; worker0 >= 0 and
+ * worker0 + m <= 2^31.
  */
 gq_status gq_quantize_sum(const void *grads, int dtype, int64_t m, int64_t d, int64_t worker0,
                           const float *norm_dev, int scheme, int s, uint64_t seed, uint64_t step,
-                          int32_t *sum_dev, void *stream);
+                          void *sum_dev, int sum_type, void *ws, size_t ws_bytes, void *stream);
 
 /*
  * Philox4x32-10 on the device, for checking the random stream: `count` calls, input

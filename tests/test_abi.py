@@ -105,7 +105,9 @@ def test_argument_checks_of_the_bucket_and_rank_entry_points(lib):
     vp, i64, u64, ci, sz = ctypes.c_void_p, ctypes.c_int64, ctypes.c_uint64, ctypes.c_int, ctypes.c_size_t
     lib.gq_allreduce_mean_segments.argtypes = [i64, vp, vp, ci, i64, ci, ci, ci, ci, u64, u64, vp,
                                                ci, vp, vp, sz, vp]
-    lib.gq_quantize_sum.argtypes = [vp, ci, i64, i64, i64, vp, ci, ci, u64, u64, vp, vp]
+    lib.gq_quantize_sum.argtypes = [vp, ci, i64, i64, i64, vp, ci, ci, u64, u64, vp, ci, vp, sz,
+                                    vp]
+    lib.gq_dequantize_sums.argtypes = [vp, ci, vp, ci, ci, i64, i64, vp, ci, vp]
     lib.gq_norm_partial.argtypes = [vp, ci, i64, i64, ci, ci, vp, vp, sz, vp]
     lib.gq_norm_finish.argtypes = [vp, ci, ci, vp, vp]
     lib.gq_dequantize_to.argtypes = [vp, vp, ci, ci, i64, i64, vp, ci, vp]
@@ -134,15 +136,21 @@ def test_argument_checks_of_the_bucket_and_rank_entry_points(lib):
     assert seg(ws=0) == 7
     assert seg(wsb=100) == 7
 
-    def qsum(m=2, w0=0, scheme=1, s=8, out=fake):
+    def qsum(m=2, w0=0, scheme=1, s=8, out=fake, st=0, ws=None, wsb=0):
         return lib.gq_quantize_sum(vp(fake), 0, m, 64, w0, vp(fake), scheme, s, 1, 1,
-                                   vp(out) if out else None, None)
+                                   vp(out) if out else None, st, vp(ws) if ws else None, wsb, None)
     assert qsum(w0=-1) == 1
     assert qsum(w0=(1 << 31) - 1) == 1
     assert qsum(out=0) == 1
     assert qsum(out=fake + 4) == 1
+    assert qsum(st=2) == 1
     assert qsum(s=0) == 2
     assert qsum(m=2, s=24) == 3
+    assert qsum(m=2, s=8, st=1) == 3        # int8 sums: 2 workers x 2^7 units exceed 127
+    assert qsum(m=8, scheme=0, s=16, st=1) == 3
+    assert qsum(ws=fake, wsb=8) == 7
+    assert lib.gq_dequantize_sums(vp(fake), 1, vp(fake), 0, 15, 9, 64, vp(fake), 0, None) == 3
+    assert lib.gq_dequantize_sums(vp(fake), 2, vp(fake), 0, 15, 2, 64, vp(fake), 0, None) == 1
 
     assert lib.gq_norm_partial(vp(fake), 0, 2, 64, 2, 0, vp(fake), vp(fake), ws_bytes, None) == 2
     assert lib.gq_norm_partial(vp(fake), 0, 2, 64, 0, 2, vp(fake), vp(fake), ws_bytes, None) == 2

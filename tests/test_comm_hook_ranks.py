@@ -35,6 +35,7 @@ class OracleOps:
     def __init__(self, oracle):
         self.o = oracle
         self.norms = []
+        self.wire = []
 
     @staticmethod
     def _host(x):
@@ -55,7 +56,7 @@ class OracleOps:
         self.norms.append(float(n32))
         return torch.tensor([n32], dtype=torch.float32)
 
-    def quantize_sum(self, x, norm, scheme, s, seed, step, worker0):
+    def quantize_sum(self, x, norm, scheme, s, seed, step, worker0, sum_dtype):
         import torch
         xh = self._host(x)
         # the oracle numbers workers by row: put this rank's row at index worker0
@@ -64,7 +65,10 @@ class OracleOps:
         codes, rc = self.o.quantize(stacked, float(norm.item()), scheme, s, seed, step)
         assert rc == 0
         sums = self.o.reduce_codes(codes[worker0:worker0 + 1], scheme, s)
-        return torch.from_numpy(sums.astype(np.int32))
+        self.wire.append(sum_dtype)
+        np_type = np.int8 if sum_dtype == torch.int8 else np.int32
+        assert np.abs(sums).max(initial=0) <= np.iinfo(np_type).max
+        return torch.from_numpy(sums.astype(np_type))
 
     def dequantize(self, sums, norm, scheme, s, n, out):
         import torch
@@ -126,7 +130,7 @@ def _rank_main(rank, port, cfg, q):
         for _ in range(ITERS):
             x = torch.randn(16, 64, generator=gen).to(dtype)
             ddp(x).float().square().mean().backward()
-        q.put((rank, "ok", records))
+        q.put((rank, "ok", (records, sorted({str(w) for w in ops.wire}))))
     except Exception as e:  # noqa: BLE001 - the failure path is what the test looks at
         q.put((rank, "failed", str(e)[:300]))
     finally:
@@ -169,7 +173,11 @@ def test_hook_matches_the_oracle(oracle, cfg):
     for r in range(WORLD):
         assert res[r][0] == "ok", res[r][1]
     # completions may be recorded in a different order on each rank: match them by step
-    recs = [sorted(res[r][1], key=lambda rec: rec[0]) for r in range(WORLD)]
+    recs = [sorted(res[r][1][0], key=lambda rec: rec[0]) for r in range(WORLD)]
+    # the wire type: int8 when the sum over the workers fits, else int32
+    units = cfg["s"] if cfg["scheme"] == 0 else 1 << (cfg["s"] - 1)
+    want_wire = "torch.int8" if WORLD * units <= 127 else "torch.int32"
+    assert res[0][1][1] == [want_wire] and res[1][1][1] == [want_wire]
     assert len(recs[0]) == len(recs[1]) and len(recs[0]) >= 2 * ITERS  # several buckets per pass
     steps = [rec[0] for rec in recs[0]]
     assert len(set(steps)) == len(steps)  # every (iteration, bucket) draws its own stream

@@ -1,8 +1,9 @@
 """GPU parity of the multi-rank pieces and of the DDP communication hook.
 
-  * gq_quantize_sum: each rank's integer code sums, with its worker offset, equal the oracle's
-    sums over the same rows (bit-exact); summed over the ranks and dequantised they give
-    gq_allreduce_mean_with_norm of the stacked matrix bit for bit;
+  * gq_quantize_sum: each rank's integer code sums (int32, or int8 when the total fits), with its
+    worker offset, equal the oracle's sums over the same rows (bit-exact); summed over the ranks
+    and dequantised (gq_dequantize_sums) they give gq_allreduce_mean_with_norm of the stacked
+    matrix bit for bit, also at sizes that take the bulk-copy kernel;
   * gq_norm_partial + gq_norm_finish over row blocks combine to the global norm (exactly for the
     max norm, relative 1e-6 for the l2 norm);
   * the hook under DistributedDataParallel (NCCL, world size 1, one GPU): every bucket's result
@@ -15,7 +16,7 @@ import socket
 import numpy as np
 import pytest
 
-from gpu_common import EXP, INF, LINEAR, gq_module, to_device
+from gpu_common import EXP, INF, LINEAR, gq_module, to_device, to_host
 from allreduce_compatible_gradient_gb300 import workloads
 
 pytestmark = pytest.mark.gpu
@@ -41,11 +42,19 @@ def _inputs(n, d, dtype, seed):
 SPLITS = [(5, 1000, [2, 3]), (8, 4099, [1, 3, 4]), (3, 65536 + 24, [3]), (6, 2053, [1] * 6)]
 
 
+def _units(scheme, s):
+    return s if scheme == LINEAR else 1 << (s - 1)
+
+
+@pytest.mark.parametrize("wire", ["i32", "i8"])
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
 @pytest.mark.parametrize("n,d,parts", SPLITS)
 @pytest.mark.parametrize("scheme,s", [(LINEAR, 7), (LINEAR, 127), (EXP, 4), (EXP, 8)])
-def test_quantize_sum_over_ranks(gq, oracle_mod, dtype, n, d, parts, scheme, s):
+def test_quantize_sum_over_ranks(gq, oracle_mod, wire, dtype, n, d, parts, scheme, s):
     import torch
+    if wire == "i8" and n * _units(scheme, s) > 127:
+        pytest.skip("the sum over the workers does not fit int8")
+    sum_dtype = torch.int8 if wire == "i8" else torch.int32
     x = _inputs(n, d, dtype, seed=7 * n + d)
     norm32 = np.float32(oracle_mod.global_norm(x, INF, INF))
     norm = torch.tensor([float(norm32)], device="cuda")
@@ -57,15 +66,55 @@ def test_quantize_sum_over_ranks(gq, oracle_mod, dtype, n, d, parts, scheme, s):
     r0 = 0
     for m in parts:
         # each rank holds its rows in its own allocation (a row slice of an odd d is unaligned)
-        got = gq.gq_quantize_sum(xd[r0:r0 + m].clone(), norm, scheme, s, seed, step, worker0=r0)
+        got = gq.gq_quantize_sum(xd[r0:r0 + m].clone(), norm, scheme, s, seed, step, worker0=r0,
+                                 sum_dtype=sum_dtype)
+        assert got.dtype == sum_dtype
         want = oracle_mod.reduce_codes(codes[r0:r0 + m], scheme, s)
         np.testing.assert_array_equal(got.cpu().numpy().astype(np.int64), want)
-        total += got
+        total += got.to(torch.int32)
         r0 += m
-    out = gq.gq_dequantize(total, norm, scheme, s, n)
+    out = gq.gq_dequantize_sums(total.to(sum_dtype), norm, scheme, s, n)
     ref = gq.gq_allreduce_mean_with_norm(xd, norm, scheme, s, seed, step)
     torch.cuda.synchronize()
     assert torch.equal(out, ref)
+
+
+@pytest.mark.parametrize("dtype,d", [("f32", 700_004), ("bf16", 800_000)])
+@pytest.mark.parametrize("scheme,s,wire", [(LINEAR, 15, "i8"), (EXP, 8, "i32"), (EXP, 4, "i8")])
+def test_quantize_sum_bulk_copy_path(gq, oracle_mod, dtype, d, scheme, s, wire):
+    """Ranks of 1, 2 and 1 workers at a size that takes the bulk-copy kernel (a single-worker
+    rank uses its one-row form): sums against the oracle on windows, and the dequantised total
+    equal to the single-GPU call."""
+    import torch
+    n, parts = 4, [1, 2, 1]
+    sum_dtype = torch.int8 if wire == "i8" else torch.int32
+    x = workloads.device_inputs("normal" if dtype == "f32" else "student_t3", n, d, seed=d,
+                                dtype=dtype)
+    norm = gq.gq_global_norm(x, INF, INF)
+    ws = gq.gq_workspace()
+    seed, step = 3, 4
+    total = torch.zeros(d, dtype=torch.int32, device="cuda")
+    sums = []
+    r0 = 0
+    for m in parts:
+        got = gq.gq_quantize_sum(x[r0:r0 + m].clone(), norm, scheme, s, seed, step, worker0=r0,
+                                 sum_dtype=sum_dtype, ws=ws)
+        sums.append((r0, m, got))
+        total += got.to(torch.int32)
+        r0 += m
+    out = gq.gq_dequantize_sums(total.to(sum_dtype), norm, scheme, s, n)
+    ref = gq.gq_allreduce_mean_with_norm(x, norm, scheme, s, seed, step)
+    torch.cuda.synchronize()
+    assert gq.gq_get_status(ws) == 0
+    assert torch.equal(out, ref)
+    xh = to_host(x)
+    norm32 = float(norm.item())
+    for j0, j1 in [(0, 1000), (d // 2, d // 2 + 1000), (d - 1000, d)]:
+        codes, rc = oracle_mod.quantize(xh, norm32, scheme, s, seed, step, j0, j1)
+        assert rc == 0
+        for r0, m, got in sums:
+            want = oracle_mod.reduce_codes(codes[r0:r0 + m], scheme, s)
+            np.testing.assert_array_equal(got[j0:j1].cpu().numpy().astype(np.int64), want)
 
 
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
