@@ -1521,6 +1521,13 @@ __device__ __forceinline__ int64_t exp_units_dev(int c) {
     return c < 0 ? -u : u;
 }
 
+// The same for |c| <= 30: sign 2^(|c|-1) in 32 bits.
+__device__ __forceinline__ int32_t exp_units32(int c) {
+    const uint32_t k = static_cast<uint32_t>(c < 0 ? -c : c);
+    const int32_t u = static_cast<int32_t>((1u << k) >> 1);  // 0 for k = 0
+    return c < 0 ? -u : u;
+}
+
 // Lower level index and threshold of |t| units on the extended grid (exact).
 __device__ __forceinline__ void exp_split_dev(uint64_t a, uint32_t& lo, uint32_t& T) {
     if (a == 0) {
@@ -1539,8 +1546,17 @@ struct ExpArgs {
     uint32_t step_lo, step_hi;
 };
 
-// Re-rounded signed codes of eight sums t[c] (coordinates 8 g8 + c) in stream sid.
-__device__ __forceinline__ void exp_reround8(const int64_t (&t)[8], uint32_t g8, uint32_t sid,
+// The same split for a 32-bit magnitude (|t| < 2^31).
+__device__ __forceinline__ void exp_split32(uint32_t a, uint32_t& lo, uint32_t& T) {
+    const int e = 31 - __clz(static_cast<int>(a));  // -1 for a = 0
+    lo = static_cast<uint32_t>(e + 1);
+    T = e > 0 ? (a - (1u << e)) << (32 - e) : 0u;   // 2^32 (a - 2^e) / 2^e, exact; 0 for a <= 1
+}
+
+// Re-rounded signed codes of eight sums t[c] (coordinates 8 g8 + c) in stream sid.  TI: int64_t
+// for any extended codes, int32_t when every |t| < 2^31 (codes with |k| <= 30).
+template <typename TI>
+__device__ __forceinline__ void exp_reround8(const TI (&t)[8], uint32_t g8, uint32_t sid,
                                              const ExpArgs& ea, int32_t (&code)[8]) {
     const uint4 ra = philox4x32_10_rk(make_uint4(g8, sid, ea.step_lo, ea.step_hi), ea.rk);
     const uint32_t aw[4] = {ra.x, ra.y, ra.z, ra.w};
@@ -1548,7 +1564,10 @@ __device__ __forceinline__ void exp_reround8(const int64_t (&t)[8], uint32_t g8,
     bool tie = false;
 #pragma unroll
     for (int c = 0; c < 8; ++c) {
-        exp_split_dev(static_cast<uint64_t>(t[c] < 0 ? -t[c] : t[c]), lo[c], T[c]);
+        if (sizeof(TI) == 8)
+            exp_split_dev(static_cast<uint64_t>(t[c] < 0 ? -t[c] : t[c]), lo[c], T[c]);
+        else
+            exp_split32(static_cast<uint32_t>(t[c] < 0 ? -t[c] : t[c]), lo[c], T[c]);
         const uint32_t h = half16(aw, c);
         tie |= h == (T[c] >> 16);
         code[c] = static_cast<int32_t>(lo[c] + (h < (T[c] >> 16) ? 1u : 0u));
@@ -1570,7 +1589,7 @@ __device__ __forceinline__ void exp_reround8(const int64_t (&t)[8], uint32_t g8,
 
 // One step on d coordinates: out = re-round(decode(a) + decode(b)).  Each thread owns 16
 // coordinates (one 16-byte load of a and of b, one 16-byte store).
-static __global__ void __launch_bounds__(kThreads)
+static __global__ void __launch_bounds__(kThreads, 3)
 exp_combine_kernel(const int8_t* __restrict__ a, const int8_t* __restrict__ b, int64_t d,
                    uint32_t sid, ExpArgs ea, int8_t* __restrict__ out) {
     const int64_t chunks = (d + 15) / 16;
@@ -1590,14 +1609,29 @@ exp_combine_kernel(const int8_t* __restrict__ a, const int8_t* __restrict__ b, i
                 bv[c] = j0 + c < d ? b[j0 + c] : 0;
             }
         }
+        // codes up to |k| = 30 (every code a quantiser writes, s <= 24) sum in 32 bits
+        uint32_t wide = 0;  // largest c + 30 as unsigned: above 60 iff some |c| > 30
+#pragma unroll
+        for (int c = 0; c < 16; ++c)
+            wide = max(wide, max(static_cast<uint32_t>(av[c] + 30), static_cast<uint32_t>(bv[c] + 30)));
+        const bool big = wide > 60u;
         int8_t ov[16];
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
-            int64_t t[8];
-#pragma unroll
-            for (int c = 0; c < 8; ++c) t[c] = exp_units_dev(av[8 * h + c]) + exp_units_dev(bv[8 * h + c]);
             int32_t code[8];
-            exp_reround8(t, static_cast<uint32_t>(j0 / 8 + h), sid, ea, code);
+            if (!big) {
+                int32_t t[8];
+#pragma unroll
+                for (int c = 0; c < 8; ++c)
+                    t[c] = exp_units32(av[8 * h + c]) + exp_units32(bv[8 * h + c]);
+                exp_reround8(t, static_cast<uint32_t>(j0 / 8 + h), sid, ea, code);
+            } else {
+                int64_t t[8];
+#pragma unroll
+                for (int c = 0; c < 8; ++c)
+                    t[c] = exp_units_dev(av[8 * h + c]) + exp_units_dev(bv[8 * h + c]);
+                exp_reround8(t, static_cast<uint32_t>(j0 / 8 + h), sid, ea, code);
+            }
 #pragma unroll
             for (int c = 0; c < 8; ++c) ov[8 * h + c] = static_cast<int8_t>(code[c]);
         }
