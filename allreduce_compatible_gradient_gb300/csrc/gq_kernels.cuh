@@ -755,28 +755,60 @@ __device__ __forceinline__ void decide_rows(const float (&xv)[R][kQCols], const 
     }
 }
 
+// Packed fp32 pairs for the paired arithmetic of sm_100-class GPUs (add.f32x2, fma.f32x2: two
+// IEEE operations, round to nearest even, in one instruction).
+__device__ __forceinline__ unsigned long long pk2(float a, float b) {
+    unsigned long long r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
+    return r;
+}
+__device__ __forceinline__ void up2(unsigned long long r, float& a, float& b) {
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(r));
+}
+__device__ __forceinline__ unsigned long long add2(unsigned long long a, unsigned long long b) {
+    unsigned long long d;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+__device__ __forceinline__ unsigned long long fma2(unsigned long long a, unsigned long long b,
+                                                   unsigned long long c) {
+    unsigned long long d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
+}
 // Accumulate one row-group's codes (k = (yk >> 16) - 0x4300) into the sums (fp32, exact:
-// integers below 2^24) and return the signed codes.
+// integers below 2^24) and return the signed codes.  The level value is read off bit patterns:
+// L: bits 0x4B00 : (k + 0x4300) (one byte permute) are 2^23 + 0x4300 + k; E: the float with
+// exponent field k + 126 is 2^(k-1), and (v + 2^23) - 2^23 turns k = 0 (0.5) into 0 (the tie
+// rounds to the even 2^23).  The subtraction and the signed accumulation run on column pairs.
 template <int SCHEME>
 __device__ __forceinline__ void accumulate_row(const float (&xv)[kQCols],
                                                const uint32_t (&yk)[kQCols], float (&S)[kQCols],
                                                int32_t (&code)[kQCols]) {
 #pragma unroll
-    for (int c = 0; c < kQCols; ++c) {
-        const uint32_t xb = __float_as_uint(xv[c]);
-        // +-1 with the sign of x, and the summed value of the code as an exact fp32
-        const float sgn = __uint_as_float((xb & 0x80000000u) | 0x3F800000u);
-        float units;
-        if (SCHEME == kLinear) {  // bits 0x4B00 : (k + 0x4300) (one byte permute): 2^23 + 0x4300 + k
-            units = __uint_as_float(__byte_perm(yk[c], 0x4B000000u, 0x7632u)) - 8405760.0f;
-        } else {  // 2^(k-1), and 0 for k = 0 (0.5 + 2^23 rounds to the even 2^23)
-            const uint32_t e = ((yk[c] >> 16) << 23) + ((126u - 0x4300u) << 23);  // (k + 126) << 23
-            units = (__uint_as_float(e) + 8388608.0f) - 8388608.0f;
+    for (int c = 0; c < kQCols; c += 2) {
+        float sg[2], raw[2];
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const uint32_t xb = __float_as_uint(xv[c + h]);
+            sg[h] = __uint_as_float((xb & 0x80000000u) | 0x3F800000u);
+            if (SCHEME == kLinear)
+                raw[h] = __uint_as_float(__byte_perm(yk[c + h], 0x4B000000u, 0x7632u));
+            else
+                raw[h] = __uint_as_float(((yk[c + h] >> 16) << 23) + ((126u - 0x4300u) << 23));
+            const int32_t k = static_cast<int32_t>(yk[c + h] >> 16) - 0x4300;
+            const int32_t sgi = static_cast<int32_t>(xb) >> 31;
+            code[c + h] = (k ^ sgi) - sgi;
         }
-        S[c] = __fmaf_rn(sgn, units, S[c]);
-        const int32_t k = static_cast<int32_t>(yk[c] >> 16) - 0x4300;
-        const int32_t sg = static_cast<int32_t>(xb) >> 31;
-        code[c] = (k ^ sg) - sg;
+        unsigned long long units;
+        if (SCHEME == kLinear) {
+            units = add2(pk2(raw[0], raw[1]), pk2(-8405760.0f, -8405760.0f));
+        } else {
+            units = add2(add2(pk2(raw[0], raw[1]), pk2(8388608.0f, 8388608.0f)),
+                         pk2(-8388608.0f, -8388608.0f));
+        }
+        const unsigned long long s2 = fma2(pk2(sg[0], sg[1]), units, pk2(S[c], S[c + 1]));
+        up2(s2, S[c], S[c + 1]);
     }
 }
 
