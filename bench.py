@@ -47,7 +47,9 @@ def _args():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
-    ap.add_argument("--measure", default=None, choices=["exp-reduce", "segments"],
+    ap.add_argument("--sweep-max-gb", type=float, default=120.0,
+                    help="--measure sweep: skip points whose n*d*4 bytes exceed this")
+    ap.add_argument("--measure", default=None, choices=["exp-reduce", "segments", "sweep"],
                     help="extra measurement instead of the main bench line")
     return ap.parse_args()
 
@@ -378,12 +380,75 @@ def measure_segments(a) -> int:
     return 0
 
 
+def measure_sweep(a) -> int:
+    """The fused call over the sweep grid: n in {2..64} x d in {2^20..2^28}, fp32 N(0,1),
+    Global-L_7 and Global-E_4, q = p = 2 (points above --sweep-max-gb skipped).  Each step is
+    timed with CUDA events after an L2 flush; GB/s counts n*d*4 bytes of gradient."""
+    import torch
+
+    import allreduce_compatible_gradient_gb300 as gq
+    from allreduce_compatible_gradient_gb300 import workloads
+
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device="cuda")
+    clean = torch.ones(64 << 20, dtype=torch.float32, device="cuda")
+    ws = gq.gq_workspace()
+    stream = torch.cuda.current_stream()
+    points = []
+    peak, peak_kind = _peaks()
+    for n in workloads.SWEEP_N:
+        for d in workloads.SWEEP_D:
+            if n * d * 4 > a.sweep_max_gb * 1e9:
+                points.append({"n": n, "d": d, "skipped": "n*d*4 above --sweep-max-gb"})
+                continue
+            try:
+                x = workloads.device_inputs("normal", n, d, seed=0)
+                out = torch.empty(d, dtype=torch.float32, device="cuda")
+            except torch.OutOfMemoryError:
+                points.append({"n": n, "d": d, "skipped": "device memory"})
+                torch.cuda.empty_cache()
+                continue
+            for scheme, s in workloads.SWEEP_SCHEMES:
+                def step(k):
+                    gq.gq_allreduce_mean(x, gq.NORM_L2, gq.NORM_L2, scheme, s, 1, k, out=out,
+                                         ws=ws, stream=stream)
+                for k in range(a.warmup):
+                    step(k)
+                torch.cuda.synchronize()
+                ts = []
+                for k in range(a.steps):
+                    flush.zero_()
+                    clean.sum()
+                    e0 = torch.cuda.Event(enable_timing=True)
+                    e1 = torch.cuda.Event(enable_timing=True)
+                    e0.record(stream)
+                    step(a.warmup + k)
+                    e1.record(stream)
+                    torch.cuda.synchronize()
+                    ts.append(e0.elapsed_time(e1))
+                ms = statistics.median(ts)
+                algo = 2 * n * d * 4 + 4 * d
+                points.append({"n": n, "d": d, "scheme": "LE"[scheme] + str(s),
+                               "ms": round(ms, 4),
+                               "gb_per_s": round(n * d * 4 / (ms * 1e-3) / 1e9, 1),
+                               "frac_of_measured_peak": round(algo / (ms * 1e-3) / 1e9 / peak, 4)})
+            del x, out
+            torch.cuda.empty_cache()
+    if gq.gq_get_status(ws) != 0:
+        raise RuntimeError("device status not ok")
+    print(json.dumps({"measure": "sweep", "peak_gbs": peak, "peak_kind": peak_kind,
+                      "steps": a.steps, "warmup": a.warmup, "l2": "flushed between timed steps",
+                      "points": points}), flush=True)
+    return 0
+
+
 def main():
     a = _args()
     if a.measure == "exp-reduce":
         return measure_exp_reduce(a)
     if a.measure == "segments":
         return measure_segments(a)
+    if a.measure == "sweep":
+        return measure_sweep(a)
     from allreduce_compatible_gradient_gb300 import workloads
 
     cfg = dict(workloads.CONFIGS[a.config], name=a.config)

@@ -21,6 +21,8 @@
  *   gqo_global_norm        pinned: closed forms, numpy.linalg.norm per axis, exact fsum
  *   gqo_level_split        pinned: exact expectation E[Q]=x, closed-form variance, fixed levels
  *   gqo_quantize           pinned: level split + Philox word, Monte-Carlo unbiasedness
+ *   gqo_quantize_cols      the same arithmetic on a column window given alone: pinned equal to
+ *                          gqo_quantize on the window of the whole matrix
  *   gqo_reduce_codes       pinned: hand-decoded codes, exact level values
  *   gqo_dequantize         pinned: hand examples, Monte-Carlo mean
  *
@@ -288,20 +290,22 @@ int gqo_level_split(float absx, float norm, int scheme, int s, int32_t *lo, uint
 }
 
 /*
- * Quantise the coordinate window [j0, j1) of all n workers to signed integer codes.
+ * Quantise coordinates j0 .. j0 + w - 1 of all n workers to signed integer codes, reading
+ * x_ij at element i * ld + (j - j0) of xw (the window's columns, row stride ld).
  * Code c_ij = sign(x_ij) * k_ij where k_ij = lo + (r_ij < T_ij) is the level index chosen by
- * the stochastic rounding and r_ij = gqo_philox_word(seed, step, i, j).  The stored code is
- * the signed level index (Global-QSGD, theta example: one bit of sign and the remaining bits for
- * the level).  codes is n x (j1 - j0), worker-major, one int8 per element.
+ * the stochastic rounding and r_ij = gqo_philox_word(seed, step, i, j): the random word is keyed
+ * by the coordinate's index j in the whole vector.  The stored code is the signed level index
+ * (Global-QSGD, theta example: one bit of sign and the remaining bits for the level).  codes is
+ * n x w, worker-major, one int8 per element.
  *
  * norm is the fp32 global norm.  norm == 0 (all-zero input) gives all-zero codes and GQO_OK; a
  * non-finite norm gives all-zero codes and GQO_ERR_NONFINITE.
  */
-int gqo_quantize(const void *x, int dtype, int64_t n, int64_t d, int64_t j0, int64_t j1,
-                 float norm, int scheme, int s, uint64_t seed, uint64_t step, int8_t *codes)
+int gqo_quantize_cols(const void *xw, int dtype, int64_t n, int64_t ld, int64_t j0, int64_t w,
+                      float norm, int scheme, int s, uint64_t seed, uint64_t step, int8_t *codes)
 {
-    int64_t i, j, w = j1 - j0;
-    if (x == NULL || codes == NULL || n < 1 || d < 1 || j0 < 0 || j1 > d || j0 > j1)
+    int64_t i, j;
+    if (xw == NULL || codes == NULL || n < 1 || w < 0 || ld < w || j0 < 0)
         return GQO_ERR_INVALID;
     if (dtype != GQO_F32 && dtype != GQO_BF16)
         return GQO_ERR_INVALID;
@@ -318,20 +322,34 @@ int gqo_quantize(const void *x, int dtype, int64_t n, int64_t d, int64_t j0, int
         return GQO_OK;
     }
     for (i = 0; i < n; ++i) {
-        for (j = j0; j < j1; ++j) {
-            float xv = load_x(x, dtype, i * d + j);
+        for (j = 0; j < w; ++j) {
+            float xv = load_x(xw, dtype, i * ld + j);
             int32_t lo;
             uint32_t T, r;
             int32_t k;
             int rc = gqo_level_split(xv, norm, scheme, s, &lo, &T);
             if (rc != GQO_OK)
                 return rc;
-            r = gqo_philox_word(seed, step, i, j);
+            r = gqo_philox_word(seed, step, i, j0 + j);
             k = lo + (r < T ? 1 : 0);
-            codes[i * w + (j - j0)] = (int8_t)(xv < 0.0f ? -k : k);
+            codes[i * w + j] = (int8_t)(xv < 0.0f ? -k : k);
         }
     }
     return GQO_OK;
+}
+
+/*
+ * Quantise the coordinate window [j0, j1) of the n x d matrix x (row-major): gqo_quantize_cols
+ * on its columns j0 .. j1 - 1.
+ */
+int gqo_quantize(const void *x, int dtype, int64_t n, int64_t d, int64_t j0, int64_t j1,
+                 float norm, int scheme, int s, uint64_t seed, uint64_t step, int8_t *codes)
+{
+    size_t esize = dtype == GQO_BF16 ? 2 : 4;
+    if (x == NULL || codes == NULL || n < 1 || d < 1 || j0 < 0 || j1 > d || j0 > j1)
+        return GQO_ERR_INVALID;
+    return gqo_quantize_cols((const unsigned char *)x + (size_t)j0 * esize, dtype, n, d, j0,
+                             j1 - j0, norm, scheme, s, seed, step, codes);
 }
 
 /*

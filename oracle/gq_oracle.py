@@ -65,6 +65,9 @@ def lib() -> ctypes.CDLL:
         L.gqo_quantize.argtypes = [vp, ctypes.c_int, i64, i64, i64, i64, ctypes.c_float,
                                    ctypes.c_int, ctypes.c_int, u64, u64, vp]
         L.gqo_quantize.restype = ctypes.c_int
+        L.gqo_quantize_cols.argtypes = [vp, ctypes.c_int, i64, i64, i64, i64, ctypes.c_float,
+                                        ctypes.c_int, ctypes.c_int, u64, u64, vp]
+        L.gqo_quantize_cols.restype = ctypes.c_int
         L.gqo_reduce_codes.argtypes = [vp, ctypes.c_int, ctypes.c_int, i64, i64, vp]
         L.gqo_reduce_codes.restype = ctypes.c_int
         L.gqo_dequantize.argtypes = [vp, ctypes.c_float, ctypes.c_int, ctypes.c_int, i64, i64, vp]
@@ -143,6 +146,17 @@ def quantize(x: np.ndarray, norm32: float, scheme: int, s: int, seed: int, step:
     codes = np.zeros((n, j1 - j0), dtype=np.int8)
     rc = lib().gqo_quantize(ptr, code, n, d, j0, j1, float(norm32), scheme, s, seed, step,
                             codes.ctypes.data)
+    return codes, rc
+
+
+def quantize_cols(xw: np.ndarray, j0: int, norm32: float, scheme: int, s: int, seed: int,
+                  step: int):
+    """Codes of the columns j0 .. j0 + w - 1 of a larger matrix, given only those columns (an
+    n x w array): the random words are keyed by the columns' global indices."""
+    ptr, code, n, w = _grads(xw)
+    codes = np.zeros((n, w), dtype=np.int8)
+    rc = lib().gqo_quantize_cols(ptr, code, n, w, j0, w, float(norm32), scheme, s, seed, step,
+                                 codes.ctypes.data)
     return codes, rc
 
 

@@ -384,3 +384,25 @@ def test_nan_element_under_supplied_norm(oracle):
     codes, rc = oracle.quantize(x, np.float32(2.0), LINEAR, 5, 1, 1)
     assert rc == 0
     assert codes[0, 0] == 0 and codes[0, 2] == 5 and codes[0, 3] == -5
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("scheme,s", [(0, 7), (0, 127), (1, 4), (1, 24)])
+def test_column_window_given_alone(oracle, dtype, scheme, s):
+    """quantize_cols on a window's columns alone equals quantize on that window of the whole
+    matrix: the random words stay keyed by the global column index."""
+    from allreduce_compatible_gradient_gb300 import workloads
+    n, d = 5, 4099
+    x = workloads.host_inputs("normal", n, d, seed=17, dtype=dtype)
+    norm32 = float(np.float32(oracle.global_norm(x, 2, 2)))
+    for j0, j1 in [(0, 8), (3, 1003), (1001, 4099), (4096, 4099)]:
+        want, rc = oracle.quantize(x, norm32, scheme, s, 9, 2, j0, j1)
+        assert rc == 0
+        got, rc = oracle.quantize_cols(np.ascontiguousarray(x[:, j0:j1]), j0, norm32, scheme, s,
+                                       9, 2)
+        assert rc == 0
+        np.testing.assert_array_equal(got, want)
+    # keyed by the global index: the same columns under another offset decide differently
+    other, _ = oracle.quantize_cols(np.ascontiguousarray(x[:, 1001:4099]), 0, norm32, scheme, s,
+                                    9, 2)
+    assert not np.array_equal(other, oracle.quantize(x, norm32, scheme, s, 9, 2, 1001, 4099)[0])
