@@ -58,15 +58,30 @@ int norm_mode(int q, int p) {
 }
 
 // ---- norm ---------------------------------------------------------------------------------
+// Blocks of the norm step for an n x d problem (the flat kernel for the (inf,inf) and (2,2)
+// forms, whose threads take eight 16-byte vectors per iteration; the per-column kernel else).
+template <typename T, int MODE>
+unsigned norm_grid(int64_t n, int64_t d) {
+    constexpr int C = gq::Elem<T>::kCols;
+    if constexpr (MODE == gq::kMaxMax || MODE == gq::kL2L2)
+        return grid_for(gq::norm_flat_kernel<T, MODE>, (n * d / C + 7) / 8, gq::kMaxPartials);
+    else
+        return grid_for(gq::norm_kernel<T, MODE>, (d + C - 1) / C, gq::kMaxPartials);
+}
+
 template <typename T, int MODE>
 gq_status run_norm(const T* x, int64_t n, int64_t d, float* norm_user, double* part_user,
                    unsigned char* ws, cudaStream_t st) {
     constexpr int C = gq::Elem<T>::kCols;
-    const int64_t groups = (d + C - 1) / C;
-    const bool vec_rows = (d % C) == 0;
-    auto k = gq::norm_kernel<T, MODE>;
-    const unsigned grid = grid_for(k, groups, gq::kMaxPartials);
-    k<<<grid, kThreads, 0, st>>>(x, n, d, groups, vec_rows, norm_user, part_user, ws);
+    const unsigned grid = norm_grid<T, MODE>(n, d);
+    if constexpr (MODE == gq::kMaxMax || MODE == gq::kL2L2) {
+        gq::norm_flat_kernel<T, MODE><<<grid, kThreads, 0, st>>>(x, n * d, norm_user, part_user, ws);
+    } else {
+        const int64_t groups = (d + C - 1) / C;
+        const bool vec_rows = (d % C) == 0;
+        gq::norm_kernel<T, MODE><<<grid, kThreads, 0, st>>>(x, n, d, groups, vec_rows, norm_user,
+                                                            part_user, ws);
+    }
     return launch_status();
 }
 
@@ -364,26 +379,20 @@ gq_status noalloc_scratch(unsigned char** out) {
 }
 
 // Blocks the norm step launches for this problem (the same rule as gq_global_norm).
-template <typename T, int MODE>
-int64_t norm_blocks(int64_t d) {
-    constexpr int C = gq::Elem<T>::kCols;
-    return grid_for(gq::norm_kernel<T, MODE>, (d + C - 1) / C, gq::kMaxPartials);
-}
-
-int64_t norm_blocks_any(int dtype, int mode, int64_t d) {
+int64_t norm_blocks_any(int dtype, int mode, int64_t n, int64_t d) {
     if (dtype == GQ_F32) {
         switch (mode) {
-            case gq::kMaxMax: return norm_blocks<float, gq::kMaxMax>(d);
-            case gq::kL2L2: return norm_blocks<float, gq::kL2L2>(d);
-            case gq::kL2Max: return norm_blocks<float, gq::kL2Max>(d);
-            default: return norm_blocks<float, gq::kMaxL2>(d);
+            case gq::kMaxMax: return norm_grid<float, gq::kMaxMax>(n, d);
+            case gq::kL2L2: return norm_grid<float, gq::kL2L2>(n, d);
+            case gq::kL2Max: return norm_grid<float, gq::kL2Max>(n, d);
+            default: return norm_grid<float, gq::kMaxL2>(n, d);
         }
     }
     switch (mode) {
-        case gq::kMaxMax: return norm_blocks<uint16_t, gq::kMaxMax>(d);
-        case gq::kL2L2: return norm_blocks<uint16_t, gq::kL2L2>(d);
-        case gq::kL2Max: return norm_blocks<uint16_t, gq::kL2Max>(d);
-        default: return norm_blocks<uint16_t, gq::kMaxL2>(d);
+        case gq::kMaxMax: return norm_grid<uint16_t, gq::kMaxMax>(n, d);
+        case gq::kL2L2: return norm_grid<uint16_t, gq::kL2L2>(n, d);
+        case gq::kL2Max: return norm_grid<uint16_t, gq::kL2Max>(n, d);
+        default: return norm_grid<uint16_t, gq::kMaxL2>(n, d);
     }
 }
 
@@ -400,7 +409,7 @@ extern "C" gq_status gq_allreduce_mean_noalloc(const void* grads, int dtype, int
     if ((st = check_scheme(scheme, s, n)) != GQ_OK) return st;
     if (!out_dev || !aligned16(out_dev) || (codes && !aligned16(codes))) return GQ_ERR_INVALID;
     // the fixed scratch holds kNoAllocPartials block partials: refuse a launch that needs more
-    if (norm_blocks_any(dtype, mode, d) > kNoAllocPartials) return GQ_ERR_WORKSPACE;
+    if (norm_blocks_any(dtype, mode, n, d) > kNoAllocPartials) return GQ_ERR_WORKSPACE;
     unsigned char* ws = nullptr;
     if ((st = noalloc_scratch(&ws)) != GQ_OK) return st;
     cudaStream_t cs = static_cast<cudaStream_t>(stream);

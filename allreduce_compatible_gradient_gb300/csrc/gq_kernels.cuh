@@ -328,17 +328,79 @@ struct NormSlots {
     double* part_user;      // nullable: the combinable value before the square root
 };
 
+// The block's partial (a max or a sum, as a non-negative fp64 stored by its bits), then, in the
+// last of the nblk blocks of this norm to finish (completion ticket, no waiting), the fixed-order
+// combine of the partials and the fp32 norm.
+template <int MODE>
+__device__ __forceinline__ void norm_finalize(uint32_t maxbits, const ScaledSumSq& ssq,
+                                              int64_t best_key, uint32_t bad_col, int64_t vb,
+                                              int64_t nblk, const NormSlots& out) {
+    uint64_t* partials = out.partials;
+    __shared__ double sh_d[kThreads / 32];
+    __shared__ uint64_t sh_u[kThreads / 32];
+    __shared__ bool is_last;
+
+    uint64_t part_bits;
+    if (MODE == kMaxMax) {
+        const double m = static_cast<double>(__uint_as_float(maxbits));
+        part_bits = block_max_bits(static_cast<uint64_t>(__double_as_longlong(m)), sh_u);
+    } else if (MODE == kL2Max) {
+        double m = best_key == INT64_MIN ? 0.0 : key_value(best_key);
+        if (bad_col) m = static_cast<double>(__uint_as_float(bad_col));
+        part_bits = block_max_bits(static_cast<uint64_t>(__double_as_longlong(m)), sh_u);
+    } else {
+        const double s = block_sum(ssq.value(), sh_d);
+        part_bits = static_cast<uint64_t>(__double_as_longlong(s));
+    }
+
+    if (threadIdx.x == 0) {
+        partials[vb] = part_bits;
+        __threadfence();
+        const unsigned int t = atomicAdd(out.ticket, 1u);
+        is_last = (t == nblk - 1);
+    }
+    __syncthreads();
+    if (!is_last) return;
+    __threadfence();
+
+    // Last block: combine the nblk partials in a fixed order.
+    const int nb = static_cast<int>(nblk);
+    double result;
+    if (MODE == kMaxMax || MODE == kL2Max) {
+        uint64_t m = 0;
+        for (int b = threadIdx.x; b < nb; b += kThreads) {
+            const uint64_t v = __ldcg(reinterpret_cast<const unsigned long long*>(partials + b));
+            m = v > m ? v : m;
+        }
+        m = block_max_bits(m, sh_u);
+        result = __longlong_as_double(static_cast<long long>(m));
+    } else {
+        double s = 0.0;
+        for (int b = threadIdx.x; b < nb; b += kThreads)
+            s += __longlong_as_double(
+                static_cast<long long>(__ldcg(reinterpret_cast<const unsigned long long*>(partials + b))));
+        result = block_sum(s, sh_d);
+    }
+    if (threadIdx.x == 0) {
+        if (out.part_user) *out.part_user = result;  // combinable across ranks: a sum or a max
+        double nrm = result;
+        if (MODE != kMaxMax) nrm = sqrt(result);  // (2,2), (inf,2): sqrt of a sum; (2,inf): of a max
+        const float n32 = static_cast<float>(nrm);
+        *out.norm = n32;
+        if (out.norm_user) *out.norm_user = n32;
+        if (!(fabsf(n32) < __uint_as_float(kInfBits))) atomicCAS(out.status, 0u, 4u);
+        *out.ticket = 0;  // ready for the next call on this workspace
+        __threadfence();
+    }
+}
+
+
 // One norm computed by `nblk` blocks, this one being block `vb` of them.
 template <typename T, int MODE>
 __device__ __forceinline__ void norm_body(const T* __restrict__ x, int64_t n, int64_t d,
                                           int64_t groups, bool vec_rows, int64_t vb, int64_t nblk,
                                           const NormSlots& out) {
     constexpr int C = Elem<T>::kCols;
-    uint64_t* partials = out.partials;
-    __shared__ double sh_d[kThreads / 32];
-    __shared__ uint64_t sh_u[kThreads / 32];
-    __shared__ bool is_last;
-
     const int64_t stride = nblk * kThreads;
     uint32_t maxbits = 0;       // kMaxMax: max |x| bit pattern
     ScaledSumSq ssq;            // kL2L2, kMaxL2
@@ -418,59 +480,7 @@ __device__ __forceinline__ void norm_body(const T* __restrict__ x, int64_t n, in
         }
     }
 
-    // Block partial: a non-negative fp64 value, stored by its bits.
-    uint64_t part_bits;
-    if (MODE == kMaxMax) {
-        const double m = static_cast<double>(__uint_as_float(maxbits));
-        part_bits = block_max_bits(static_cast<uint64_t>(__double_as_longlong(m)), sh_u);
-    } else if (MODE == kL2Max) {
-        double m = best_key == INT64_MIN ? 0.0 : key_value(best_key);
-        if (bad_col) m = static_cast<double>(__uint_as_float(bad_col));
-        part_bits = block_max_bits(static_cast<uint64_t>(__double_as_longlong(m)), sh_u);
-    } else {
-        const double s = block_sum(ssq.value(), sh_d);
-        part_bits = static_cast<uint64_t>(__double_as_longlong(s));
-    }
-
-    if (threadIdx.x == 0) {
-        partials[vb] = part_bits;
-        __threadfence();
-        const unsigned int t = atomicAdd(out.ticket, 1u);
-        is_last = (t == nblk - 1);
-    }
-    __syncthreads();
-    if (!is_last) return;
-    __threadfence();
-
-    // Last block: combine the nblk partials in a fixed order.
-    const int nb = static_cast<int>(nblk);
-    double result;
-    if (MODE == kMaxMax || MODE == kL2Max) {
-        uint64_t m = 0;
-        for (int b = threadIdx.x; b < nb; b += kThreads) {
-            const uint64_t v = __ldcg(reinterpret_cast<const unsigned long long*>(partials + b));
-            m = v > m ? v : m;
-        }
-        m = block_max_bits(m, sh_u);
-        result = __longlong_as_double(static_cast<long long>(m));
-    } else {
-        double s = 0.0;
-        for (int b = threadIdx.x; b < nb; b += kThreads)
-            s += __longlong_as_double(
-                static_cast<long long>(__ldcg(reinterpret_cast<const unsigned long long*>(partials + b))));
-        result = block_sum(s, sh_d);
-    }
-    if (threadIdx.x == 0) {
-        if (out.part_user) *out.part_user = result;  // combinable across ranks: a sum or a max
-        double nrm = result;
-        if (MODE != kMaxMax) nrm = sqrt(result);  // (2,2), (inf,2): sqrt of a sum; (2,inf): of a max
-        const float n32 = static_cast<float>(nrm);
-        *out.norm = n32;
-        if (out.norm_user) *out.norm_user = n32;
-        if (!(fabsf(n32) < __uint_as_float(kInfBits))) atomicCAS(out.status, 0u, 4u);
-        *out.ticket = 0;  // ready for the next call on this workspace
-        __threadfence();
-    }
+    norm_finalize<MODE>(maxbits, ssq, best_key, bad_col, vb, nblk, out);
 }
 
 template <typename T, int MODE>
@@ -482,6 +492,61 @@ norm_kernel(const T* __restrict__ x, int64_t n, int64_t d, int64_t groups, bool 
     const NormSlots slots{reinterpret_cast<uint64_t*>(ws + kHeaderBytes), &hdr->ticket,
                           &hdr->status, &hdr->norm, norm_user, part_user};
     norm_body<T, MODE>(x, n, d, groups, vec_rows, blockIdx.x, gridDim.x, slots);
+}
+
+// The (inf, inf) and (2, 2) norms do not depend on which coordinate an element belongs to: they
+// are the max |x| and the sum of squares over all n d elements, read here as one flat array
+// (eight 16-byte loads in flight per thread whatever n is).
+template <typename T, int MODE>
+__global__ void __launch_bounds__(kThreads, 4)
+norm_flat_kernel(const T* __restrict__ x, int64_t total, float* __restrict__ norm_user,
+                 double* __restrict__ part_user, unsigned char* __restrict__ ws) {
+    static_assert(MODE == kMaxMax || MODE == kL2L2, "flat norms: (inf, inf) and (2, 2)");
+    constexpr int C = Elem<T>::kCols;
+    constexpr int U = 8;
+    WsHeader* hdr = reinterpret_cast<WsHeader*>(ws);
+    const NormSlots slots{reinterpret_cast<uint64_t*>(ws + kHeaderBytes), &hdr->ticket,
+                          &hdr->status, &hdr->norm, norm_user, part_user};
+    const uint4* xv = reinterpret_cast<const uint4*>(x);
+    const int64_t nvec = total / C;
+    uint32_t maxbits = 0;
+    ScaledSumSq ssq;
+    ssq.init();
+    const int64_t step = static_cast<int64_t>(gridDim.x) * kThreads * U;
+    for (int64_t v0 = static_cast<int64_t>(blockIdx.x) * kThreads * U + threadIdx.x; v0 < nvec;
+         v0 += step) {
+        uint4 raw[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int64_t v = v0 + static_cast<int64_t>(u) * kThreads;
+            raw[u] = v < nvec ? __ldg(xv + v) : make_uint4(0u, 0u, 0u, 0u);  // zeros add nothing
+        }
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            float vals[C];
+            widen16<T>(raw[u], vals);
+            if (MODE == kMaxMax) {
+#pragma unroll
+                for (int c = 0; c < C; ++c) {
+                    const uint32_t b = __float_as_uint(vals[c]) & 0x7FFFFFFFu;
+                    maxbits = b > maxbits ? b : maxbits;
+                }
+            } else {
+                ssq.add<C>(vals);
+            }
+        }
+    }
+    const int64_t tail = total - nvec * C;  // fewer than C elements past the last 16 bytes
+    if (blockIdx.x == 0 && threadIdx.x < tail) {
+        const float v[1] = {Elem<T>::load_one(x + nvec * C + threadIdx.x)};
+        if (MODE == kMaxMax) {
+            const uint32_t b = __float_as_uint(v[0]) & 0x7FFFFFFFu;
+            maxbits = b > maxbits ? b : maxbits;
+        } else {
+            ssq.add<1>(v);
+        }
+    }
+    norm_finalize<MODE>(maxbits, ssq, INT64_MIN, 0u, blockIdx.x, gridDim.x, slots);
 }
 
 // The norm from the combined partials of several ranks (a sum of squares for (2,2), a maximum
