@@ -66,6 +66,7 @@ def lib() -> ctypes.CDLL:
         "gq_exp_combine": (ci, [vp, vp, i64, u64, u64, ctypes.c_uint32, vp, vp]),
         "gq_exp_allreduce": (ci, [vp, ci, i64, i64, ci, vp, u64, u64, vp, vp, vp]),
         "gq_get_status": (ci, [vp, vp]),
+        "gq_selftest_wait_timeout": (ci, [vp, sz, u64, vp, vp]),
         "gq_status_string": (ctypes.c_char_p, [ci]),
     }
     for name, (res, args) in sig.items():
@@ -344,6 +345,17 @@ def gq_philox4x32_10(ctr_key, out=None, stream=None) -> torch.Tensor:
     _check(lib().gq_philox4x32_10(_p(ctr_key), _p(out), count, _stream(stream)),
            "gq_philox4x32_10")
     return out
+
+
+def gq_selftest_wait_timeout(limit_ns: int, ws=None, stream=None):
+    """Run the bounded-wait self-test: a wait that nothing completes gives up after limit_ns.
+    Returns (status read from the workspace, nanoseconds waited)."""
+    ws = gq_workspace(None, stream) if ws is None else ws
+    elapsed = torch.zeros(1, dtype=torch.int64, device=ws.device)
+    _check(lib().gq_selftest_wait_timeout(_p(ws), ws.numel(), limit_ns, _p(elapsed),
+                                          _stream(stream)), "gq_selftest_wait_timeout")
+    status = gq_get_status(ws, stream)
+    return status, int(elapsed.item())
 
 
 def gq_get_status(ws, stream=None) -> int:

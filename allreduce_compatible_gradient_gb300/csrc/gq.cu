@@ -608,3 +608,15 @@ extern "C" gq_status gq_allreduce_mean_segments(int64_t nseg, const void* const*
     }
     return GQ_OK;
 }
+
+// ---- self-test of the bounded waits ---------------------------------------------------------
+extern "C" gq_status gq_selftest_wait_timeout(void* ws, size_t ws_bytes, uint64_t limit_ns,
+                                              unsigned long long* elapsed_dev, void* stream) {
+    gq_status st = check_ws(ws, ws_bytes, 1, 1);
+    if (st != GQ_OK) return st;
+    if (!elapsed_dev || limit_ns < 1000 || limit_ns > 4000000000ull) return GQ_ERR_INVALID;
+    unsigned int* status = &static_cast<gq::WsHeader*>(ws)->status;
+    gq::wait_timeout_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(status, limit_ns,
+                                                                              elapsed_dev);
+    return launch_status();
+}

@@ -1304,16 +1304,32 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
         : "memory");
     return done != 0;
 }
-// Wait for the completion of the phase with parity `parity`; false after kWaitLimitNs.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
+// Wait for the completion of the phase with parity `parity`; false after limit_ns.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity,
+                                          uint64_t limit_ns = kWaitLimitNs) {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = global_ns();
     for (;;) {
 #pragma unroll 1
         for (int k = 0; k < 64; ++k)
             if (mbar_try_wait(bar, parity)) return true;
-        if (global_ns() - t0 > kWaitLimitNs) return false;
+        if (global_ns() - t0 > limit_ns) return false;
     }
+}
+
+// Self-test of the bounded wait: one thread waits on an mbarrier that nothing arrives on, gives
+// up after limit_ns and records GQ_ERR_TIMEOUT in the status word, as the quantise kernels do;
+// *elapsed_ns receives the time it waited.
+static __global__ void wait_timeout_kernel(unsigned int* __restrict__ status, uint64_t limit_ns,
+                                           unsigned long long* __restrict__ elapsed_ns) {
+    __shared__ __align__(8) uint64_t bar;
+    if (threadIdx.x != 0) return;
+    mbar_init(smem_u32(&bar), 1u);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    const uint64_t t0 = global_ns();
+    const bool done = mbar_wait(smem_u32(&bar), 0u, limit_ns);
+    *elapsed_ns = global_ns() - t0;
+    if (!done) atomicCAS(status, 0u, kStatusTimeout);
 }
 // Bulk copy of `bytes` (a multiple of 16, both addresses 16-byte aligned) into shared memory,
 // counted on the mbarrier `bar`.

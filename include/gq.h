@@ -58,7 +58,7 @@ typedef enum {
     GQ_ERR_OVERFLOW = 3,    /* n * s >= 2^24 (L) or n * 2^(s-1) >= 2^24 (E): the code sum
                                would not convert to fp32 exactly */
     GQ_ERR_NONFINITE = 4,   /* device: the norm is NaN or infinite */
-    GQ_ERR_TIMEOUT = 5,     /* device: a bounded wait gave up (no kernel waits today) */
+    GQ_ERR_TIMEOUT = 5,     /* device: a bounded wait of a bulk-copy kernel gave up (~1 s) */
     GQ_ERR_CUDA = 6,        /* a CUDA runtime call or kernel launch failed */
     GQ_ERR_WORKSPACE = 7    /* workspace null, too small or misaligned */
 } gq_status;
@@ -322,6 +322,16 @@ gq_status gq_get_status(void *ws, void *stream);
 
 /* Static string naming a status value. */
 const char *gq_status_string(int status);
+
+/*
+ * Self-test of the bounded waits of the bulk-copy kernels: one GPU thread waits on an mbarrier
+ * that nothing completes, gives up after limit_ns nanoseconds (1,000 .. 4e9) of global time and
+ * records GQ_ERR_TIMEOUT in the workspace status word (read it with gq_get_status), exactly as a
+ * quantise kernel whose copies never arrive would.  *elapsed_dev (device, 8 bytes) receives the
+ * time waited.  The kernel then returns normally: the context stays usable.
+ */
+gq_status gq_selftest_wait_timeout(void *ws, size_t ws_bytes, uint64_t limit_ns,
+                                   unsigned long long *elapsed_dev, void *stream);
 
 #ifdef __cplusplus
 }
