@@ -538,26 +538,31 @@ extern "C" gq_status gq_quantize_sum(const void* grads, int dtype, int64_t m, in
 namespace {
 
 template <typename T, int MODE>
-gq_status run_norm_segments(gq::SegLaunch& L, const int64_t* d, int64_t n, float* norms_user,
-                            unsigned char* ws, cudaStream_t st) {
+gq_status run_norm_segments(gq::SegLaunch& L, const int64_t* d, int64_t n, int scheme, int s,
+                            float* norms_user, unsigned char* ws, cudaStream_t st) {
     constexpr int C = gq::Elem<T>::kCols;
     auto k = gq::norm_segments_kernel<T, MODE>;
     const int64_t full = static_cast<int64_t>(blocks_per_sm(k)) * sm_count();
     int64_t target = 2 * full;
     if (target > gq::kMaxPartials - L.nseg) target = gq::kMaxPartials - L.nseg;
     plan_runs(L, d, n, C, target);
-    k<<<total_blocks(L), kThreads, 0, st>>>(L, n, norms_user, ws);
+    k<<<total_blocks(L), kThreads, 0, st>>>(L, n, scheme, static_cast<uint32_t>(s), norms_user,
+                                            ws);
     return launch_status();
 }
 
 template <typename T>
-gq_status norm_segments_any(int mode, gq::SegLaunch& L, const int64_t* d, int64_t n,
-                            float* norms_user, unsigned char* ws, cudaStream_t st) {
+gq_status norm_segments_any(int mode, gq::SegLaunch& L, const int64_t* d, int64_t n, int scheme,
+                            int s, float* norms_user, unsigned char* ws, cudaStream_t st) {
     switch (mode) {
-        case gq::kMaxMax: return run_norm_segments<T, gq::kMaxMax>(L, d, n, norms_user, ws, st);
-        case gq::kL2L2: return run_norm_segments<T, gq::kL2L2>(L, d, n, norms_user, ws, st);
-        case gq::kL2Max: return run_norm_segments<T, gq::kL2Max>(L, d, n, norms_user, ws, st);
-        default: return run_norm_segments<T, gq::kMaxL2>(L, d, n, norms_user, ws, st);
+        case gq::kMaxMax:
+            return run_norm_segments<T, gq::kMaxMax>(L, d, n, scheme, s, norms_user, ws, st);
+        case gq::kL2L2:
+            return run_norm_segments<T, gq::kL2L2>(L, d, n, scheme, s, norms_user, ws, st);
+        case gq::kL2Max:
+            return run_norm_segments<T, gq::kL2Max>(L, d, n, scheme, s, norms_user, ws, st);
+        default:
+            return run_norm_segments<T, gq::kMaxL2>(L, d, n, scheme, s, norms_user, ws, st);
     }
 }
 
@@ -595,8 +600,9 @@ extern "C" gq_status gq_allreduce_mean_segments(int64_t nseg, const void* const*
             L.seg[k].x = grads[c0 + k];
             L.seg[k].out = out[c0 + k];
         }
-        st = dtype == GQ_F32 ? norm_segments_any<float>(mode, L, d + c0, n, norms_dev, w, cs)
-                             : norm_segments_any<uint16_t>(mode, L, d + c0, n, norms_dev, w, cs);
+        st = dtype == GQ_F32
+                 ? norm_segments_any<float>(mode, L, d + c0, n, scheme, s, norms_dev, w, cs)
+                 : norm_segments_any<uint16_t>(mode, L, d + c0, n, scheme, s, norms_dev, w, cs);
         if (st != GQ_OK) return st;
         if (dtype == GQ_F32)
             st = scheme == GQ_LINEAR ? quant_segments_f32_l(L, d + c0, n, base, w, cs)

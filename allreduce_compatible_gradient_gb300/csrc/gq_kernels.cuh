@@ -24,10 +24,12 @@ constexpr int kOutF32 = 0, kOutBF16 = 1, kOutF16 = 2;
 constexpr int kMaxPartials = 4096;   // upper bound on norm-kernel blocks (workspace size)
 constexpr int kHeaderBytes = 256;    // workspace header, then kMaxPartials 8-byte partials
 constexpr int kSegChunk = 256;       // segments per launch of the segmented kernels
-// after the partials: kSegChunk completion tickets, then kSegChunk fp32 norms (one per segment)
+// after the partials: kSegChunk completion tickets, kSegChunk fp32 norms and kSegChunk fp32
+// dequantisation scales (one each per segment of a segmented launch)
 constexpr int kSegTicketsOff = kHeaderBytes + 8 * kMaxPartials;
 constexpr int kSegNormsOff = kSegTicketsOff + 4 * kSegChunk;
-constexpr int kWorkspaceBytes = kSegNormsOff + 4 * kSegChunk;
+constexpr int kSegScalesOff = kSegNormsOff + 4 * kSegChunk;  // fp32 dequantisation scales
+constexpr int kWorkspaceBytes = kSegScalesOff + 4 * kSegChunk;
 
 // Workspace header (device memory owned by the caller).
 struct WsHeader {
@@ -40,6 +42,16 @@ static_assert(sizeof(WsHeader) == kHeaderBytes, "workspace header is 256 bytes")
 
 enum NormMode { kMaxMax = 0, kL2L2 = 1, kL2Max = 2, kMaxL2 = 3 };  // (q, p) pairs
 enum Scheme { kLinear = 0, kExp = 1 };
+
+// The fp32 dequantisation scale from the fp32 norm, computed in fp64: N / (n s) for Global-L_s,
+// N 2^-(s-1) / n for Global-E_s; 0 when the norm is 0 or not finite.
+__device__ __forceinline__ float dequant_scale(int scheme, float nrm, int64_t n, uint32_t s) {
+    if (!(nrm > 0.0f && nrm < __uint_as_float(0x7F800000u))) return 0.0f;
+    const double num = static_cast<double>(nrm);
+    return scheme == kLinear
+               ? static_cast<float>(num / (static_cast<double>(n) * static_cast<double>(s)))
+               : static_cast<float>(ldexp(num, -static_cast<int>(s - 1)) / static_cast<double>(n));
+}
 
 // ------------------------------------------------------------------------------------------
 // Philox4x32-10 (Salmon, Moraes, Dror, Shaw, SC'11): ten rounds of the Philox-4x32 bijection.
@@ -326,6 +338,10 @@ struct NormSlots {
     float* norm;            // the fp32 norm (workspace copy)
     float* norm_user;       // nullable: the caller's copy
     double* part_user;      // nullable: the combinable value before the square root
+    float* scale = nullptr; // nullable: the dequantisation scale of (scheme, s, n) below
+    int scheme = 0;
+    uint32_t s = 1;
+    int64_t n = 1;
 };
 
 // The block's partial (a max or a sum, as a non-negative fp64 stored by its bits), then, in the
@@ -388,6 +404,7 @@ __device__ __forceinline__ void norm_finalize(uint32_t maxbits, const ScaledSumS
         const float n32 = static_cast<float>(nrm);
         *out.norm = n32;
         if (out.norm_user) *out.norm_user = n32;
+        if (out.scale) *out.scale = dequant_scale(out.scheme, n32, out.n, out.s);
         if (!(fabsf(n32) < __uint_as_float(kInfBits))) atomicCAS(out.status, 0u, 4u);
         *out.ticket = 0;  // ready for the next call on this workspace
         __threadfence();
@@ -668,16 +685,7 @@ struct QuantArgs {
 // N / (n s) for Global-L_s, N 2^-(s-1) / n for Global-E_s.  0 when the norm is 0 or non-finite.
 template <int SCHEME>
 __device__ __forceinline__ float block_scale(float nrm, int64_t n, uint32_t s, float* sh) {
-    if (threadIdx.x == 0) {
-        float sc = 0.0f;
-        if (nrm > 0.0f && nrm < __uint_as_float(kInfBits)) {
-            const double num = static_cast<double>(nrm);
-            sc = (SCHEME == kLinear)
-                     ? static_cast<float>(num / (static_cast<double>(n) * static_cast<double>(s)))
-                     : static_cast<float>(ldexp(num, -static_cast<int>(s - 1)) / static_cast<double>(n));
-        }
-        *sh = sc;
-    }
+    if (threadIdx.x == 0) *sh = dequant_scale(SCHEME, nrm, n, s);
     __syncthreads();
     return *sh;
 }
@@ -1214,17 +1222,21 @@ __device__ __forceinline__ int find_segment(const SegLaunch& L, int32_t b) {
 
 template <typename T, int MODE>
 __global__ void __launch_bounds__(kThreads, 4)
-norm_segments_kernel(const __grid_constant__ SegLaunch L, int64_t n,
+norm_segments_kernel(const __grid_constant__ SegLaunch L, int64_t n, int scheme, uint32_t s,
                      float* __restrict__ norms_user, unsigned char* __restrict__ ws) {
     constexpr int C = Elem<T>::kCols;
     const int k = find_segment(L, static_cast<int32_t>(blockIdx.x));
     const SegDesc& sd = L.seg[k];
     WsHeader* hdr = reinterpret_cast<WsHeader*>(ws);
     uint64_t* partials = reinterpret_cast<uint64_t*>(ws + kHeaderBytes);
-    const NormSlots slots{partials + sd.b0,
-                          reinterpret_cast<unsigned int*>(ws + kSegTicketsOff) + k, &hdr->status,
-                          reinterpret_cast<float*>(ws + kSegNormsOff) + k,
-                          norms_user ? norms_user + L.seg0 + k : nullptr, nullptr};
+    NormSlots slots{partials + sd.b0,
+                    reinterpret_cast<unsigned int*>(ws + kSegTicketsOff) + k, &hdr->status,
+                    reinterpret_cast<float*>(ws + kSegNormsOff) + k,
+                    norms_user ? norms_user + L.seg0 + k : nullptr, nullptr};
+    slots.scale = reinterpret_cast<float*>(ws + kSegScalesOff) + k;
+    slots.scheme = scheme;
+    slots.s = s;
+    slots.n = n;
     norm_body<T, MODE>(static_cast<const T*>(sd.x), n, sd.d, (sd.d + C - 1) / C, sd.d % C == 0,
                        static_cast<int64_t>(blockIdx.x) - sd.b0, sd.nb, slots);
 }
@@ -1342,6 +1354,121 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_
 }
 
 // SUB: rows decided together (2; 1 for a single worker, whose stages hold one row).
+// One stage of RB rows (rows b*RB ..) of one chunk, for consumer thread tid (group g of its
+// problem): rows into registers SUB at a time, the stage released once its last rows are read,
+// then random words, decisions and sums.  a: the problem's arguments (d, n, step, row0, s, rk).
+template <typename T, int SCHEME, int CODE_BITS, bool TRUSTED, int SUB>
+__device__ __forceinline__ void tma_consume_stage(const unsigned char* stage, int lane, bool active,
+                                                  int64_t b, int64_t g, const PhiloxGroup& pg,
+                                                  const QuantArgs& a, const Decide& dc,
+                                                  uint32_t empty_bar, float (&S)[kQCols],
+                                                  unsigned char* __restrict__ codes) {
+    using Cfg = TmaCfg<T>;
+    constexpr int RB = Cfg::kRows;
+    const uint32_t g32 = static_cast<uint32_t>(g);
+#pragma unroll
+    for (int u0 = 0; u0 < RB; u0 += SUB) {
+        const int64_t r0 = b * RB + u0;
+        float v[SUB][kQCols];
+#pragma unroll
+        for (int u = 0; u < SUB; ++u) {
+            const uint4* p = reinterpret_cast<const uint4*>(stage + (u0 + u) * Cfg::kRowBytes);
+            if (active && r0 + u < a.n) {
+                unstage<T>(p, p + 1, v[u]);
+            } else {
+#pragma unroll
+                for (int c = 0; c < kQCols; ++c) v[u][c] = 0.0f;
+            }
+        }
+        if (u0 + SUB >= RB) {  // every row of the stage is in registers: release it
+            __syncwarp();
+            if (lane == 0) mbar_arrive(empty_bar);
+        }
+        if (!active || r0 >= a.n) continue;  // past the last worker: nothing to do
+        uint32_t aw[SUB][4];
+#pragma unroll
+        for (int u = 0; u < SUB; ++u) {
+            const uint4 ra = philox_row(pg, static_cast<uint32_t>(r0 + u) + a.row0, a.step_lo,
+                                        a.rk);
+            aw[u][0] = ra.x; aw[u][1] = ra.y; aw[u][2] = ra.z; aw[u][3] = ra.w;
+        }
+        uint32_t yk[SUB][kQCols];
+        decide_rows<SCHEME, TRUSTED, SUB>(v, dc, a, g32, static_cast<uint32_t>(r0) + a.row0, aw,
+                                          yk);
+#pragma unroll
+        for (int u = 0; u < SUB; ++u) {
+            if (r0 + u >= a.n) break;
+            int32_t code[kQCols];
+            accumulate_row<SCHEME>(v[u], yk[u], S, code);
+            if (CODE_BITS) store_codes<CODE_BITS>(codes, r0 + u, g, a.pitch, code);
+        }
+    }
+}
+
+// Barriers of the ring: full[k] completes when stage k's copies land (the producer's arrival
+// plus the bytes), empty[k] when every consumer warp has read it.
+template <int STAGES>
+__device__ __forceinline__ void tma_init_barriers(uint64_t (&full_bar)[STAGES],
+                                                  uint64_t (&empty_bar)[STAGES],
+                                                  volatile int* abort_flag) {
+    if (threadIdx.x == 0) {
+#pragma unroll
+        for (int k = 0; k < STAGES; ++k) {
+            mbar_init(smem_u32(&full_bar[k]), 1u);
+            mbar_init(smem_u32(&empty_bar[k]), static_cast<uint32_t>(kTmaWarps));
+        }
+        *abort_flag = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    __syncthreads();
+}
+
+// Producer, item `item` of the block: wait (bounded) until its stage is free, then copy `rows`
+// rows of row_bytes starting at src (row stride ld elements) into it.  False if the wait gave up
+// or the consumers stopped.
+template <typename T, int STAGES>
+__device__ __forceinline__ bool tma_issue(uint32_t item, const T* src, int64_t ld, int rows,
+                                          uint32_t row_bytes, unsigned char* smem,
+                                          uint64_t (&full_bar)[STAGES],
+                                          uint64_t (&empty_bar)[STAGES],
+                                          volatile int* abort_flag) {
+    using Cfg = TmaCfg<T>;
+    const int st = static_cast<int>(item % STAGES);
+    if (item >= STAGES && !mbar_wait(smem_u32(&empty_bar[st]), ((item / STAGES) - 1u) & 1u))
+        return false;
+    if (*abort_flag) return false;
+    const uint32_t fb = smem_u32(&full_bar[st]);
+    mbar_arrive_expect_tx(fb, static_cast<uint32_t>(rows) * row_bytes);
+    const uint32_t dst = smem_u32(smem + st * Cfg::kStageBytes);
+    for (int u = 0; u < rows; ++u) bulk_load(dst + u * Cfg::kRowBytes, src + u * ld, row_bytes, fb);
+    return true;
+}
+
+// Producer epilogue: on failure record the timeout and stop the consumers; then wait (bounded)
+// for the last issued stages, so that the block never exits with copies in flight.
+template <int STAGES>
+__device__ __forceinline__ void tma_drain(bool ok, uint32_t item, uint64_t (&full_bar)[STAGES],
+                                          volatile int* abort_flag,
+                                          unsigned int* __restrict__ status) {
+    if (!ok) {
+        if (status) atomicCAS(status, 0u, kStatusTimeout);
+        *abort_flag = 1;
+    }
+    const uint32_t inflight = item < STAGES ? item : STAGES;
+    for (uint32_t k = 0; k < inflight; ++k) {
+        const uint32_t it = item - 1 - k;
+        mbar_wait(smem_u32(&full_bar[it % STAGES]), (it / STAGES) & 1u);
+    }
+}
+
+// Consumer wait for item `item`: bounded, and decided uniformly by the warp.
+template <int STAGES>
+__device__ __forceinline__ bool tma_wait_full(uint32_t item, uint64_t (&full_bar)[STAGES],
+                                              volatile int* abort_flag) {
+    const bool got = mbar_wait(smem_u32(&full_bar[item % STAGES]), (item / STAGES) & 1u);
+    return __all_sync(0xFFFFFFFFu, got && !*abort_flag);
+}
+
 template <typename T, int SCHEME, int CODE_BITS, bool WRITE_OUT, bool TRUSTED, int SUB>
 __global__ void __launch_bounds__(kTmaBlock, 1)
 quantize_tma_kernel(const T* __restrict__ x, QuantArgs a, int64_t groups,
@@ -1349,10 +1476,10 @@ quantize_tma_kernel(const T* __restrict__ x, QuantArgs a, int64_t groups,
                     unsigned int* __restrict__ status) {
     using Cfg = TmaCfg<T>;
     constexpr int RB = Cfg::kRows;
-    constexpr int kSub = SUB;
+    constexpr int NS = Cfg::kStages;
     extern __shared__ __align__(128) unsigned char tma_smem[];
-    __shared__ __align__(8) uint64_t full_bar[Cfg::kStages];
-    __shared__ __align__(8) uint64_t empty_bar[Cfg::kStages];
+    __shared__ __align__(8) uint64_t full_bar[NS];
+    __shared__ __align__(8) uint64_t empty_bar[NS];
     __shared__ float sh_scale;
     __shared__ volatile int sh_abort;
 
@@ -1360,61 +1487,31 @@ quantize_tma_kernel(const T* __restrict__ x, QuantArgs a, int64_t groups,
     const float nrm = __ldg(a.norm_ptr);
     const float scale = block_scale<SCHEME>(nrm, a.n, a.s, &sh_scale);
     const bool live = nrm > 0.0f && nrm < __uint_as_float(kInfBits);
-    if (tid == 0) {
-#pragma unroll
-        for (int k = 0; k < Cfg::kStages; ++k) {
-            mbar_init(smem_u32(&full_bar[k]), 1u);
-            mbar_init(smem_u32(&empty_bar[k]), static_cast<uint32_t>(kTmaWarps));
-        }
-        sh_abort = 0;
-        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-    }
-    __syncthreads();
+    tma_init_barriers<NS>(full_bar, empty_bar, &sh_abort);
 
     const int64_t full = live ? a.d / kQCols : 0;  // groups taken through shared memory
     const int64_t nchunks = (full + kTmaConsumers - 1) / kTmaConsumers;
     const int64_t nbatch = (a.n + RB - 1) / RB;
 
     if (tid >= kTmaConsumers) {
-        // ---- producer: lane 0 of the last warp ------------------------------------------
-        if (tid == kTmaConsumers) {
+        if (tid == kTmaConsumers) {  // producer: lane 0 of the last warp
             uint32_t item = 0;
             bool ok = true;
             for (int64_t q = blockIdx.x; q < nchunks && ok; q += gridDim.x) {
                 const int64_t g0 = (nchunks - 1 - q) * kTmaConsumers;
                 const int64_t ng = min(static_cast<int64_t>(kTmaConsumers), full - g0);
                 const uint32_t row_bytes = static_cast<uint32_t>(ng * kQCols * sizeof(T));
-                for (int64_t b = 0; b < nbatch; ++b, ++item) {
-                    const int st = static_cast<int>(item % Cfg::kStages);
-                    if (item >= Cfg::kStages &&
-                        !mbar_wait(smem_u32(&empty_bar[st]), ((item / Cfg::kStages) - 1u) & 1u)) {
-                        ok = false;
-                        break;
-                    }
-                    if (sh_abort) { ok = false; break; }
-                    const int64_t r0 = b * RB;
-                    const int rows = static_cast<int>(min(static_cast<int64_t>(RB), a.n - r0));
-                    const uint32_t fb = smem_u32(&full_bar[st]);
-                    mbar_arrive_expect_tx(fb, static_cast<uint32_t>(rows) * row_bytes);
-                    const uint32_t dst = smem_u32(tma_smem + st * Cfg::kStageBytes);
-                    for (int u = 0; u < rows; ++u)
-                        bulk_load(dst + u * Cfg::kRowBytes, x + (r0 + u) * a.d + g0 * kQCols,
-                                  row_bytes, fb);
+                for (int64_t b = 0; b < nbatch; ++b) {
+                    const int rows = static_cast<int>(min(static_cast<int64_t>(RB), a.n - b * RB));
+                    ok = tma_issue<T, NS>(item, x + b * RB * a.d + g0 * kQCols, a.d, rows,
+                                          row_bytes, tma_smem, full_bar, empty_bar, &sh_abort);
+                    if (!ok) break;
+                    ++item;  // counts the stages actually issued
                 }
             }
-            if (!ok) {
-                if (status) atomicCAS(status, 0u, kStatusTimeout);
-                sh_abort = 1;
-            }
-            // the block must not exit with copies in flight: wait for the last issued stages
-            const uint32_t inflight = item < Cfg::kStages ? item : Cfg::kStages;
-            for (uint32_t k = 0; k < inflight; ++k) {
-                const uint32_t it = item - 1 - k;
-                mbar_wait(smem_u32(&full_bar[it % Cfg::kStages]), (it / Cfg::kStages) & 1u);
-            }
+            tma_drain<NS>(ok, item, full_bar, &sh_abort, status);
         }
-    } else if (nchunks > 0) {
-        // ---- consumers ------------------------------------------------------------------
+    } else if (nchunks > 0) {  // consumers
         const Decide dc = make_decide<SCHEME>(nrm, a.s);
         const int lane = tid & 31;
         uint32_t item = 0;
@@ -1422,58 +1519,23 @@ quantize_tma_kernel(const T* __restrict__ x, QuantArgs a, int64_t groups,
         for (int64_t q = blockIdx.x; q < nchunks && ok; q += gridDim.x) {
             const int64_t g = (nchunks - 1 - q) * kTmaConsumers + tid;
             const bool active = g < full;
-            const uint32_t g32 = static_cast<uint32_t>(g);
-            const PhiloxGroup pg = philox_group(g32, a.step_lo, a.step_hi, a.rk);
+            const PhiloxGroup pg = philox_group(static_cast<uint32_t>(g), a.step_lo, a.step_hi, a.rk);
             float S[kQCols];
 #pragma unroll
             for (int c = 0; c < kQCols; ++c) S[c] = 0.0f;
             for (int64_t b = 0; b < nbatch; ++b, ++item) {
-                const int st = static_cast<int>(item % Cfg::kStages);
-                const bool got = mbar_wait(smem_u32(&full_bar[st]), (item / Cfg::kStages) & 1u);
-                if (!__all_sync(0xFFFFFFFFu, got && !sh_abort)) {  // warp-uniform decision
+                if (!tma_wait_full<NS>(item, full_bar, &sh_abort)) {
                     ok = false;
                     break;
                 }
-                const unsigned char* stage = tma_smem + st * Cfg::kStageBytes + tid * kQCols * sizeof(T);
-#pragma unroll
-                for (int u0 = 0; u0 < RB; u0 += kSub) {
-                    const int64_t r0 = b * RB + u0;
-                    float v[kSub][kQCols];
-#pragma unroll
-                    for (int u = 0; u < kSub; ++u) {
-                        const uint4* p = reinterpret_cast<const uint4*>(stage + (u0 + u) * Cfg::kRowBytes);
-                        if (active && r0 + u < a.n) {
-                            unstage<T>(p, p + 1, v[u]);
-                        } else {
-#pragma unroll
-                            for (int c = 0; c < kQCols; ++c) v[u][c] = 0.0f;
-                        }
-                    }
-                    if (u0 + kSub >= RB) {  // every row of the stage is in registers: release it
-                        __syncwarp();
-                        if (lane == 0) mbar_arrive(smem_u32(&empty_bar[st]));
-                    }
-                    if (!active || r0 >= a.n) continue;  // past the last worker: nothing to do
-                    uint32_t aw[kSub][4];
-#pragma unroll
-                    for (int u = 0; u < kSub; ++u) {
-                        const uint4 ra = philox_row(pg, static_cast<uint32_t>(r0 + u) + a.row0,
-                                                    a.step_lo, a.rk);
-                        aw[u][0] = ra.x; aw[u][1] = ra.y; aw[u][2] = ra.z; aw[u][3] = ra.w;
-                    }
-                    uint32_t yk[kSub][kQCols];
-                    decide_rows<SCHEME, TRUSTED, kSub>(v, dc, a, g32,
-                                                       static_cast<uint32_t>(r0) + a.row0, aw, yk);
-#pragma unroll
-                    for (int u = 0; u < kSub; ++u) {
-                        if (r0 + u >= a.n) break;
-                        int32_t code[kQCols];
-                        accumulate_row<SCHEME>(v[u], yk[u], S, code);
-                        if (CODE_BITS) store_codes<CODE_BITS>(codes, r0 + u, g, a.pitch, code);
-                    }
-                }
+                const unsigned char* stage =
+                    tma_smem + (item % NS) * Cfg::kStageBytes + tid * kQCols * sizeof(T);
+                tma_consume_stage<T, SCHEME, CODE_BITS, TRUSTED, SUB>(
+                    stage, lane, active, b, g, pg, a, dc, smem_u32(&empty_bar[item % NS]), S,
+                    codes);
             }
-            if (ok && active && WRITE_OUT) store_out(out, a.sums, a.sums_i8, a.out_dtype, g, a.d, scale, S);
+            if (ok && active && WRITE_OUT)
+                store_out(out, a.sums, a.sums_i8, a.out_dtype, g, a.d, scale, S);
         }
         if (!ok) {
             if (status) atomicCAS(status, 0u, kStatusTimeout);
@@ -1502,6 +1564,116 @@ quantize_tma_kernel(const T* __restrict__ x, QuantArgs a, int64_t groups,
             }
         }
         if (WRITE_OUT) store_out(out, a.sums, a.sums_i8, a.out_dtype, g, a.d, scale, S);
+    }
+}
+
+// The segmented form of the bulk-copy pass: the chunks of all segments of a launch (segment k
+// owns chunks L.seg[k].b0 .. b0 + nb - 1 of 3840 columns; nb = 0 for a segment whose rows are
+// not 16-byte aligned) run through one ring, last chunk first; each chunk takes its segment's
+// norm and scale (written by norm_segments_kernel) and its random stream (step << 16) | l.  The
+// groups outside the chunks (a ragged last group, or every group of an unaligned segment) are
+// done afterwards with direct loads.  No codes; trusted norms.
+template <typename T, int SCHEME>
+__global__ void __launch_bounds__(kTmaBlock, 1)
+quantize_seg_tma_kernel(const __grid_constant__ SegLaunch L, QuantArgs base, int32_t nchunks,
+                        unsigned char* __restrict__ ws) {
+    using Cfg = TmaCfg<T>;
+    constexpr int RB = Cfg::kRows;
+    constexpr int NS = Cfg::kStages;
+    extern __shared__ __align__(128) unsigned char tma_smem[];
+    __shared__ __align__(8) uint64_t full_bar[NS];
+    __shared__ __align__(8) uint64_t empty_bar[NS];
+    __shared__ volatile int sh_abort;
+
+    const int tid = threadIdx.x;
+    unsigned int* status = &reinterpret_cast<WsHeader*>(ws)->status;
+    const float* norms = reinterpret_cast<const float*>(ws + kSegNormsOff);
+    const float* scales = reinterpret_cast<const float*>(ws + kSegScalesOff);
+    tma_init_barriers<NS>(full_bar, empty_bar, &sh_abort);
+    const int64_t nbatch = (base.n + RB - 1) / RB;
+
+    if (tid >= kTmaConsumers) {
+        if (tid == kTmaConsumers) {  // producer: lane 0 of the last warp
+            uint32_t item = 0;
+            bool ok = true;
+            for (int32_t q = blockIdx.x; q < nchunks && ok; q += gridDim.x) {
+                const int32_t cg = nchunks - 1 - q;
+                const SegDesc& sd = L.seg[find_segment(L, cg)];
+                const int64_t g0 = static_cast<int64_t>(cg - sd.b0) * kTmaConsumers;
+                const int64_t ng = min(static_cast<int64_t>(kTmaConsumers), sd.d / kQCols - g0);
+                const uint32_t row_bytes = static_cast<uint32_t>(ng * kQCols * sizeof(T));
+                const T* x = static_cast<const T*>(sd.x);
+                for (int64_t b = 0; b < nbatch; ++b) {
+                    const int rows = static_cast<int>(min(static_cast<int64_t>(RB), base.n - b * RB));
+                    ok = tma_issue<T, NS>(item, x + b * RB * sd.d + g0 * kQCols, sd.d, rows,
+                                          row_bytes, tma_smem, full_bar, empty_bar, &sh_abort);
+                    if (!ok) break;
+                    ++item;
+                }
+            }
+            tma_drain<NS>(ok, item, full_bar, &sh_abort, status);
+        }
+        return;
+    }
+
+    // consumers
+    const int lane = tid & 31;
+    uint32_t item = 0;
+    bool ok = true;
+    for (int32_t q = blockIdx.x; q < nchunks && ok; q += gridDim.x) {
+        const int32_t cg = nchunks - 1 - q;
+        const int k = find_segment(L, cg);
+        const SegDesc& sd = L.seg[k];
+        QuantArgs a = base;
+        a.d = sd.d;
+        a.step_lo = base.step_lo | static_cast<uint32_t>(L.seg0 + k);
+        const float nrm = norms[k];
+        const Decide dc = make_decide<SCHEME>(nrm, a.s);
+        const int64_t g = static_cast<int64_t>(cg - sd.b0) * kTmaConsumers + tid;
+        const bool active = g < sd.d / kQCols;
+        const PhiloxGroup pg = philox_group(static_cast<uint32_t>(g), a.step_lo, a.step_hi, a.rk);
+        float S[kQCols];
+#pragma unroll
+        for (int c = 0; c < kQCols; ++c) S[c] = 0.0f;
+        for (int64_t b = 0; b < nbatch; ++b, ++item) {
+            if (!tma_wait_full<NS>(item, full_bar, &sh_abort)) {
+                ok = false;
+                break;
+            }
+            const unsigned char* stage =
+                tma_smem + (item % NS) * Cfg::kStageBytes + tid * kQCols * sizeof(T);
+            tma_consume_stage<T, SCHEME, 0, true, 2>(stage, lane, active, b, g, pg, a, dc,
+                                                     smem_u32(&empty_bar[item % NS]), S, nullptr);
+        }
+        if (ok && active) store_out(sd.out, nullptr, 0, base.out_dtype, g, sd.d, scales[k], S);
+    }
+    if (!ok) {
+        atomicCAS(status, 0u, kStatusTimeout);
+        sh_abort = 1;
+        return;
+    }
+
+    // groups outside the chunks, direct loads
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * kTmaConsumers;
+    for (int k = 0; k < L.nseg; ++k) {
+        const SegDesc& sd = L.seg[k];
+        const int64_t groups = (sd.d + kQCols - 1) / kQCols;
+        const int64_t full = sd.nb > 0 ? sd.d / kQCols : 0;
+        if (full == groups) continue;
+        QuantArgs a = base;
+        a.d = sd.d;
+        a.pitch = (sd.d + 31) / 32 * 32;
+        a.vec_rows = sd.nb > 0;
+        a.step_lo = base.step_lo | static_cast<uint32_t>(L.seg0 + k);
+        a.norm_ptr = norms + k;
+        const Decide dc = make_decide<SCHEME>(norms[k], a.s);
+        for (int64_t it = static_cast<int64_t>(blockIdx.x) * kTmaConsumers + tid;
+             it < groups - full; it += stride) {
+            const int64_t g = groups - 1 - it;
+            float S[kQCols];
+            quantize_group<T, SCHEME, 0, true>(static_cast<const T*>(sd.x), a, dc, g, nullptr, S);
+            store_out(sd.out, nullptr, 0, base.out_dtype, g, sd.d, scales[k], S);
+        }
     }
 }
 

@@ -47,6 +47,25 @@ gq_status quant_bits(const void* grads, const gq::QuantArgs& a, int bits, void* 
 template <typename T, int SCHEME>
 gq_status run_quant_segments(gq::SegLaunch& L, const int64_t* d, int64_t n,
                              const gq::QuantArgs& base, unsigned char* ws, cudaStream_t st) {
+    // Chunks of 3840 columns for every segment whose rows are 16-byte aligned; with at least one
+    // chunk per SM they all go through the bulk-copy ring (runs b0 / nb now count chunks).
+    constexpr int vec = 16 / static_cast<int>(sizeof(T));
+    int32_t chunks = 0;
+    for (int k = 0; k < L.nseg; ++k) {
+        const int64_t full = d[k] % vec == 0 ? d[k] / gq::kQCols : 0;
+        const int64_t nc = (full + gq::kTmaConsumers - 1) / gq::kTmaConsumers;
+        L.seg[k].d = d[k];
+        L.seg[k].b0 = chunks;
+        L.seg[k].nb = static_cast<int32_t>(nc);
+        chunks += static_cast<int32_t>(nc);
+    }
+    if (chunks >= sm_count()) {
+        auto kt = gq::quantize_seg_tma_kernel<T, SCHEME>;
+        constexpr int tsmem = gq::TmaCfg<T>::kSmemBytes;
+        if (blocks_per_sm(kt, tsmem, gq::kTmaBlock) < 1) return GQ_ERR_CUDA;
+        kt<<<static_cast<unsigned>(sm_count()), gq::kTmaBlock, tsmem, st>>>(L, base, chunks, ws);
+        return launch_status();
+    }
     auto k = gq::quantize_segments_kernel<T, SCHEME>;
     constexpr int smem = gq::Staging<T>::kBytes;
     const int64_t full = static_cast<int64_t>(blocks_per_sm(k, smem)) * sm_count();

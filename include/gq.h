@@ -86,9 +86,9 @@ typedef enum {
 int gq_abi_version(void);
 
 /* Bytes of workspace the norm step needs for an n x d problem (a small constant today,
- * 35,072 bytes).  The workspace holds the device status word, the block partials of the norm,
- * a completion ticket and the last norm, and per-segment tickets and norms for
- * gq_allreduce_mean_segments. */
+ * 36,096 bytes).  The workspace holds the device status word, the block partials of the norm,
+ * a completion ticket and the last norm, and per-segment tickets, norms and dequantisation
+ * scales for gq_allreduce_mean_segments. */
 size_t gq_workspace_bytes(int64_t n, int64_t d);
 
 /* Zero a freshly allocated workspace (enqueued on `stream`).  Required once before its first

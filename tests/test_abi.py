@@ -47,7 +47,7 @@ def test_binding_covers_every_entry_point():
 def test_host_only_functions():
     import allreduce_compatible_gradient_gb300 as gq
     assert gq.gq_abi_version() == 1
-    assert gq.gq_workspace_bytes(8, 10**9) == 256 + 8 * 4096 + 2 * 4 * 256
+    assert gq.gq_workspace_bytes(8, 10**9) == 256 + 8 * 4096 + 3 * 4 * 256
     assert [gq.gq_code_bits(0, s) for s in (0, 1, 7, 8, 127, 128)] == [0, 4, 4, 8, 8, 0]
     assert [gq.gq_code_bits(1, s) for s in (0, 1, 7, 8, 24, 25)] == [0, 4, 4, 8, 8, 0]
     assert gq.gq_code_bits(2, 5) == 0

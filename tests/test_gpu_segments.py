@@ -138,3 +138,26 @@ def test_resnet50_layers_full_size(gq, oracle_mod):
         win = (max(0, d - 4099), d) if d > 8192 else None
         _check_segment(oracle_mod, xh, float(nh[l]), INF, INF, LINEAR, 127, seed,
                        (step << 16) | l, outs[l].cpu().numpy(), j=win)
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("scheme,s", [(LINEAR, 127), (EXP, 8)])
+def test_segments_bulk_copy_path(gq, dtype, scheme, s):
+    """Enough 3840-column chunks for the segmented bulk-copy kernel, with a ragged last group,
+    an unaligned segment (its groups all by direct loads), tiny segments and 5 workers: every
+    segment equals its own gq_allreduce_mean call bit for bit (max norm)."""
+    import torch
+    sizes = [700_004, 300_001, 1_000_000, 8, 3, 65_544] if dtype == "f32" else \
+        [700_008, 300_004, 1_000_000, 8, 3, 65_544]
+    n, seed, step = 5, 3, 11
+    segs = workloads.segment_tensors(n, sizes, dtype=dtype, seed=12)
+    ws = gq.gq_workspace()
+    norms = torch.empty(len(segs), dtype=torch.float32, device="cuda")
+    outs = gq.gq_allreduce_mean_segments(segs, INF, INF, scheme, s, seed, step, norms=norms, ws=ws)
+    torch.cuda.synchronize()
+    assert gq.gq_get_status(ws) == 0
+    for l, (x, out) in enumerate(zip(segs, outs)):
+        ref = gq.gq_allreduce_mean(x, INF, INF, scheme, s, seed, step * 65536 + l, ws=ws)
+        torch.cuda.synchronize()
+        assert torch.equal(out, ref), l
+        assert norms[l].item() == float(gq.gq_global_norm(x, INF, INF).item())
