@@ -63,10 +63,12 @@ def lib() -> ctypes.CDLL:
         "gq_dequantize_sums": (ci, [vp, ci, vp, ci, ci, i64, i64, vp, ci, vp]),
         "gq_exp_tree_stream": (ctypes.c_uint32, [ci, i64]),
         "gq_exp_ring_stream": (ctypes.c_uint32, [i64, i64]),
-        "gq_exp_combine": (ci, [vp, vp, i64, u64, u64, ctypes.c_uint32, vp, vp]),
+        "gq_exp_combine": (ci, [vp, vp, i64, i64, u64, u64, ctypes.c_uint32, vp, vp]),
         "gq_exp_allreduce": (ci, [vp, ci, i64, i64, ci, vp, u64, u64, vp, vp, vp]),
         "gq_get_status": (ci, [vp, vp]),
         "gq_selftest_wait_timeout": (ci, [vp, sz, u64, vp, vp]),
+        "gq_quantize_codes": (ci, [vp, ci, i64, i64, i64, vp, ci, ci, u64, u64, vp, ci, vp, sz, vp]),
+        "gq_exp_dequantize": (ci, [vp, i64, vp, ci, i64, vp, ci, vp]),
         "gq_status_string": (ctypes.c_char_p, [ci]),
     }
     for name, (res, args) in sig.items():
@@ -347,6 +349,30 @@ def gq_philox4x32_10(ctr_key, out=None, stream=None) -> torch.Tensor:
     return out
 
 
+def gq_quantize_codes(grads, norm, scheme, s, seed, step, worker0=0, code_bits=8, codes=None,
+                      ws=None, stream=None) -> torch.Tensor:
+    """One rank's codes (m x pitch, int8 or int4-packed) with its worker offset."""
+    dt, m, d = _grads(grads)
+    if codes is None:
+        codes = torch.empty(m * gq_code_pitch(d) * code_bits // 8, dtype=torch.uint8,
+                            device=grads.device)
+    _check(lib().gq_quantize_codes(_p(grads), dt, m, d, worker0, _p(norm), scheme, s, seed, step,
+                                   _p(codes), code_bits, _p(ws), 0 if ws is None else ws.numel(),
+                                   _stream(stream)), "gq_quantize_codes")
+    return codes
+
+
+def gq_exp_dequantize(codes, norm, s, n, d=None, out=None, stream=None,
+                      out_dtype=torch.float32) -> torch.Tensor:
+    """Mean from extended Global-E codes (int8) reduced over n workers."""
+    d = codes.numel() if d is None else d
+    if out is None:
+        out = torch.empty(d, dtype=out_dtype, device=codes.device)
+    _check(lib().gq_exp_dequantize(_p(codes), d, _p(norm), s, n, _p(out), _out_code(out),
+                                   _stream(stream)), "gq_exp_dequantize")
+    return out
+
+
 def gq_selftest_wait_timeout(limit_ns: int, ws=None, stream=None):
     """Run the bounded-wait self-test: a wait that nothing completes gives up after limit_ns.
     Returns (status read from the workspace, nanoseconds waited)."""
@@ -372,13 +398,14 @@ def gq_exp_ring_stream(h: int, c: int) -> int:
     return int(lib().gq_exp_ring_stream(h, c))
 
 
-def gq_exp_combine(a, b, seed, step, stream_id, out=None, stream=None) -> torch.Tensor:
-    """One reduction step of the Global-E allreduce on int8 code vectors a, b."""
+def gq_exp_combine(a, b, seed, step, stream_id, out=None, stream=None, j0=0) -> torch.Tensor:
+    """One reduction step of the Global-E allreduce on int8 code vectors a, b whose element j is
+    coordinate j0 + j of the whole vector (j0 a multiple of 8)."""
     d = a.numel()
     if out is None:
         out = torch.empty(d, dtype=torch.int8, device=a.device)
-    _check(lib().gq_exp_combine(_p(a), _p(b), d, seed, step, stream_id, _p(out), _stream(stream)),
-           "gq_exp_combine")
+    _check(lib().gq_exp_combine(_p(a), _p(b), d, j0, seed, step, stream_id, _p(out),
+                                _stream(stream)), "gq_exp_combine")
     return out
 
 

@@ -59,13 +59,16 @@ def build_library(force: bool = False, verbose: bool = False) -> str:
         extra = ("-Xptxas", "-v") if verbose else ()
         tag = ".%d" % os.getpid()
         objs = [os.path.join(OBJ_DIR, u[:-3] + tag + ".o") for u in UNITS]
-        procs = [subprocess.Popen(compile_command(u, o, extra)) for u, o in zip(UNITS, objs)]
-        codes = [p.wait() for p in procs]
-        if any(codes):
-            raise subprocess.CalledProcessError(next(c for c in codes if c), "nvcc")
         tmp = LIB + ".tmp" + tag
-        subprocess.run(link_command(objs, tmp), check=True)
-        os.replace(tmp, LIB)
-        for o in objs:
-            os.remove(o)
+        try:
+            procs = [subprocess.Popen(compile_command(u, o, extra)) for u, o in zip(UNITS, objs)]
+            codes = [p.wait() for p in procs]
+            if any(codes):
+                raise subprocess.CalledProcessError(next(c for c in codes if c), "nvcc")
+            subprocess.run(link_command(objs, tmp), check=True)
+            os.replace(tmp, LIB)
+        finally:
+            for f in objs + [tmp]:
+                if os.path.exists(f):
+                    os.remove(f)
     return LIB

@@ -448,14 +448,15 @@ extern "C" uint32_t gq_exp_ring_stream(int64_t h, int64_t c) {
     return 0xC0000000u + (static_cast<uint32_t>(h) << 12) + static_cast<uint32_t>(c);
 }
 
-extern "C" gq_status gq_exp_combine(const int8_t* a, const int8_t* b, int64_t d, uint64_t seed,
-                                    uint64_t step, uint32_t stream_id, int8_t* out, void* stream) {
+extern "C" gq_status gq_exp_combine(const int8_t* a, const int8_t* b, int64_t d, int64_t j0,
+                                    uint64_t seed, uint64_t step, uint32_t stream_id, int8_t* out,
+                                    void* stream) {
     if (!a || !b || !out || !aligned16(a) || !aligned16(b) || !aligned16(out)) return GQ_ERR_INVALID;
-    if (d < 1 || d >= kMaxD) return GQ_ERR_INVALID;
+    if (d < 1 || j0 < 0 || j0 % 8 != 0 || j0 + d >= kMaxD) return GQ_ERR_INVALID;
     auto k = gq::exp_combine_kernel;
     const int64_t chunks = (d + 15) / 16;
     k<<<grid_for(k, chunks), kThreads, 0, static_cast<cudaStream_t>(stream)>>>(
-        a, b, d, stream_id, make_exp_args(seed, step), out);
+        a, b, d, j0, stream_id, make_exp_args(seed, step), out);
     return launch_status();
 }
 
@@ -486,6 +487,20 @@ extern "C" gq_status gq_exp_allreduce(const void* codes, int s, int64_t n, int64
         if (bits == 4) GQ_EXP_ALLREDUCE(1, 4); else GQ_EXP_ALLREDUCE(1, 8);
     }
 #undef GQ_EXP_ALLREDUCE
+    return launch_status();
+}
+
+extern "C" gq_status gq_exp_dequantize(const int8_t* codes, int64_t d, const float* norm_dev,
+                                       int s, int64_t n, void* out_dev, int out_dtype,
+                                       void* stream) {
+    if (!codes || !norm_dev || !out_dev || !aligned16(codes) || !aligned16(out_dev))
+        return GQ_ERR_INVALID;
+    if (out_dtype != GQ_F32 && out_dtype != GQ_BF16 && out_dtype != GQ_F16) return GQ_ERR_INVALID;
+    if (d < 1 || d >= kMaxD || n < 1 || n >= (int64_t(1) << 31)) return GQ_ERR_INVALID;
+    if (s < 1 || s > 24) return GQ_ERR_UNSUPPORTED;
+    auto k = gq::exp_dequantize_kernel;
+    k<<<grid_for(k, (d + 15) / 16), kThreads, 0, static_cast<cudaStream_t>(stream)>>>(
+        codes, d, norm_dev, static_cast<uint32_t>(s), n, out_dev, out_dtype);
     return launch_status();
 }
 
@@ -625,4 +640,22 @@ extern "C" gq_status gq_selftest_wait_timeout(void* ws, size_t ws_bytes, uint64_
     gq::wait_timeout_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(status, limit_ns,
                                                                               elapsed_dev);
     return launch_status();
+}
+
+extern "C" gq_status gq_quantize_codes(const void* grads, int dtype, int64_t m, int64_t d,
+                                       int64_t worker0, const float* norm_dev, int scheme, int s,
+                                       uint64_t seed, uint64_t step, void* codes, int code_bits,
+                                       void* ws, size_t ws_bytes, void* stream) {
+    gq_status st = check_grads(grads, dtype, m, d);
+    if (st != GQ_OK) return st;
+    if ((st = check_scheme(scheme, s, m)) != GQ_OK) return st;
+    if (!norm_dev || !codes || !aligned16(codes)) return GQ_ERR_INVALID;
+    if (code_bits != 8 && !(code_bits == 4 && s <= 7)) return GQ_ERR_INVALID;
+    if (worker0 < 0 || worker0 + m > (int64_t(1) << 31)) return GQ_ERR_INVALID;
+    if (ws && (st = check_ws(ws, ws_bytes, m, d)) != GQ_OK) return st;
+    gq::QuantArgs a = make_args(norm_dev, dtype, m, d, s, seed, step);
+    a.row0 = static_cast<uint32_t>(worker0);
+    unsigned int* status = ws ? &reinterpret_cast<gq::WsHeader*>(ws)->status : nullptr;
+    return quant_any<false, false>(grads, dtype, a, scheme, code_bits, codes, nullptr,
+                                   static_cast<cudaStream_t>(stream), status);
 }

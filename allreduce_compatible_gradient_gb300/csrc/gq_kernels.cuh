@@ -1872,11 +1872,12 @@ __device__ __forceinline__ void exp_reround8(const TI (&t)[8], uint32_t g8, uint
         if (t[c] < 0) code[c] = -code[c];
 }
 
-// One step on d coordinates: out = re-round(decode(a) + decode(b)).  Each thread owns 16
-// coordinates (one 16-byte load of a and of b, one 16-byte store).
+// One step on d coordinates: out = re-round(decode(a) + decode(b)); coordinate j of the buffers
+// is coordinate jbase + j of the whole vector (jbase a multiple of 8), which keys its random
+// word.  Each thread owns 16 coordinates (one 16-byte load of a and of b, one 16-byte store).
 static __global__ void __launch_bounds__(kThreads, 3)
 exp_combine_kernel(const int8_t* __restrict__ a, const int8_t* __restrict__ b, int64_t d,
-                   uint32_t sid, ExpArgs ea, int8_t* __restrict__ out) {
+                   int64_t jbase, uint32_t sid, ExpArgs ea, int8_t* __restrict__ out) {
     const int64_t chunks = (d + 15) / 16;
     const int64_t stride = static_cast<int64_t>(gridDim.x) * kThreads;
     for (int64_t q = static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x; q < chunks;
@@ -1909,13 +1910,13 @@ exp_combine_kernel(const int8_t* __restrict__ a, const int8_t* __restrict__ b, i
 #pragma unroll
                 for (int c = 0; c < 8; ++c)
                     t[c] = exp_units32(av[8 * h + c]) + exp_units32(bv[8 * h + c]);
-                exp_reround8(t, static_cast<uint32_t>(j0 / 8 + h), sid, ea, code);
+                exp_reround8(t, static_cast<uint32_t>((jbase + j0) / 8 + h), sid, ea, code);
             } else {
                 int64_t t[8];
 #pragma unroll
                 for (int c = 0; c < 8; ++c)
                     t[c] = exp_units_dev(av[8 * h + c]) + exp_units_dev(bv[8 * h + c]);
-                exp_reround8(t, static_cast<uint32_t>(j0 / 8 + h), sid, ea, code);
+                exp_reround8(t, static_cast<uint32_t>((jbase + j0) / 8 + h), sid, ea, code);
             }
 #pragma unroll
             for (int c = 0; c < 8; ++c) ov[8 * h + c] = static_cast<int8_t>(code[c]);
@@ -1951,6 +1952,44 @@ __device__ __forceinline__ int32_t exp_reround1(int64_t t, int64_t j, uint32_t s
     return t < 0 ? -k : k;
 }
 
+// Dequantise extended Global-E codes (the root of a re-rounding allreduce over n workers):
+// out_j = scale * sign 2^(|k|-1) with scale = fp32(N 2^-(s-1) / n), 0 for k = 0.  Each thread
+// owns 16 coordinates.
+static __global__ void __launch_bounds__(kThreads)
+exp_dequantize_kernel(const int8_t* __restrict__ codes, int64_t d,
+                      const float* __restrict__ norm_ptr, uint32_t s, int64_t n,
+                      void* __restrict__ out, int dt) {
+    __shared__ float sh_scale;
+    const float scale = block_scale<kExp>(__ldg(norm_ptr), n, s, &sh_scale);
+    const int64_t chunks = (d + 15) / 16;
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * kThreads;
+    for (int64_t q = static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x; q < chunks;
+         q += stride) {
+        const int64_t j0 = q * 16;
+        if (j0 + 16 <= d) {
+            const uint4 w = __ldg(reinterpret_cast<const uint4*>(codes + j0));
+            const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+            for (int h = 0; h < 4; ++h) {
+                float v[4];
+#pragma unroll
+                for (int c = 0; c < 4; ++c)
+                    v[c] = scale * static_cast<float>(
+                                       exp_units_dev(static_cast<int8_t>(ws[h] >> (8 * c))));
+                if (dt == kOutF32)
+                    reinterpret_cast<float4*>(static_cast<float*>(out) + j0)[h] =
+                        make_float4(v[0], v[1], v[2], v[3]);
+                else
+                    reinterpret_cast<uint2*>(static_cast<uint16_t*>(out) + j0)[h] =
+                        make_uint2(pack16(dt, v[0], v[1]), pack16(dt, v[2], v[3]));
+            }
+        } else {
+            for (int64_t j = j0; j < d; ++j)
+                store1(out, dt, j, scale * static_cast<float>(exp_units_dev(codes[j])));
+        }
+    }
+}
+
 constexpr int kExpMaxWorkers = 64;  // rows the one-GPU allreduce simulation holds per column
 
 // Code of worker i at coordinate j from the quantiser's layout (int8, or int4 nibbles).
@@ -1965,7 +2004,8 @@ __device__ __forceinline__ int read_code(const unsigned char* __restrict__ codes
 
 // The whole Global-E allreduce of the code matrix, one thread per coordinate: tree (ORDER 0:
 // level l, row i a multiple of 2^l takes row i + 2^(l-1), stream 2^31 + l 2^24 + i / 2^l) or
-// ring (ORDER 1: chunk c = j / ceil(d/n) starts at worker c + 1 and visits c + 2, ..., c;
+// ring (ORDER 1: chunk c = j / chunk, chunk = ceil(d/n) rounded up to a multiple of 16, starts
+// at worker c + 1 and visits c + 2, ..., c;
 // stream of step h: 2^31 + 2^30 + h 2^12 + c); then out = scale * (root units).
 template <int ORDER, int CODE_BITS>
 __global__ void __launch_bounds__(kThreads)
@@ -1975,7 +2015,7 @@ exp_allreduce_kernel(const unsigned char* __restrict__ codes, int64_t n, int64_t
     __shared__ float sh_scale;
     const float scale = block_scale<kExp>(__ldg(norm_ptr), n, s, &sh_scale);
     const int64_t stride = static_cast<int64_t>(gridDim.x) * kThreads;
-    const int64_t chunk = (d + n - 1) / n;
+    const int64_t chunk = ((d + n - 1) / n + 15) / 16 * 16;
     for (int64_t j = static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x; j < d; j += stride) {
         int32_t root;
         if (ORDER == 0) {

@@ -214,9 +214,11 @@ uint32_t gq_exp_ring_stream(int64_t h, int64_t c);
 /*
  * One reduction step on d coordinates: out[j] = re-round(decode(a[j]) + decode(b[j])).  a, b,
  * out: int8 extended Global-E codes in device memory (16-byte aligned), |k| <= 62 on input (the
- * result for larger codes is unspecified).  d >= 1.
+ * result for larger codes is unspecified).  Element j is coordinate j0 + j of the whole vector
+ * (its random word is that coordinate's); j0 >= 0 is a multiple of 8 (a ring chunk's start).
+ * d >= 1.
  */
-gq_status gq_exp_combine(const int8_t *a, const int8_t *b, int64_t d, uint64_t seed,
+gq_status gq_exp_combine(const int8_t *a, const int8_t *b, int64_t d, int64_t j0, uint64_t seed,
                          uint64_t step, uint32_t stream_id, int8_t *out, void *stream);
 
 /*
@@ -322,6 +324,26 @@ gq_status gq_get_status(void *ws, void *stream);
 
 /* Static string naming a status value. */
 const char *gq_status_string(int status);
+
+/*
+ * One rank's codes for a multi-GPU allreduce that moves codes rather than sums (the Global-E
+ * re-rounding allreduce of Global-QSGD's performance-model paragraph): the m x d rows at grads,
+ * whose workers are worker0 .. worker0 + m - 1, quantised as gq_quantize would quantise those
+ * rows of the stacked matrix, written as m x gq_code_pitch(d) codes of code_bits (8, or 4 when
+ * s <= 7; int8 whatever s is, for gq_exp_combine).  ws (nullable) as for gq_quantize_sum.
+ */
+gq_status gq_quantize_codes(const void *grads, int dtype, int64_t m, int64_t d, int64_t worker0,
+                            const float *norm_dev, int scheme, int s, uint64_t seed,
+                            uint64_t step, void *codes, int code_bits, void *ws, size_t ws_bytes,
+                            void *stream);
+
+/*
+ * Dequantise d extended Global-E codes (int8, |k| <= 62, 16-byte aligned; the result of a
+ * re-rounding allreduce over n workers) into out (d elements of out_dtype):
+ * out_j = fp32(N 2^-(s-1) / n) * sign 2^(|k|-1), 0 for k = 0, N the fp32 norm at *norm_dev.
+ */
+gq_status gq_exp_dequantize(const int8_t *codes, int64_t d, const float *norm_dev, int s,
+                            int64_t n, void *out_dev, int out_dtype, void *stream);
 
 /*
  * Self-test of the bounded waits of the bulk-copy kernels: one GPU thread waits on an mbarrier

@@ -598,7 +598,9 @@ int gqo_exp_tree_allreduce(const int8_t *codes, int64_t n, int64_t w, int64_t j0
 
 /*
  * Ring allreduce of n code rows over d coordinates (the window [j0, j0 + w)): the coordinates
- * are split into n chunks of ceil(d / n); chunk c is accumulated starting from worker c + 1 and
+ * are split into n chunks of ceil(d / n) rounded up to a multiple of 16 (so that every chunk
+ * starts on a group of 8 coordinates that share one Philox call; the last chunks may be short
+ * or empty); chunk c is accumulated starting from worker c + 1 and
  * visits workers c + 2, ..., c (indices mod n), re-rounding after every step h = 1..n-1 (the
  * reduce-scatter; the allgather only copies).  root receives the reduced codes.
  */
@@ -608,7 +610,7 @@ int gqo_exp_ring_allreduce(const int8_t *codes, int64_t n, int64_t d, int64_t w,
     int64_t j, h, chunk;
     if (codes == NULL || root == NULL || n < 1 || n > 4096 || w < 0 || j0 < 0 || j0 + w > d)
         return GQO_ERR_INVALID;
-    chunk = (d + n - 1) / n;
+    chunk = ((d + n - 1) / n + 15) / 16 * 16;
     for (j = 0; j < w; ++j) {
         int64_t c = (j0 + j) / chunk;
         int code = codes[((c + 1) % n) * w + j];

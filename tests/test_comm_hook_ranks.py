@@ -70,6 +70,34 @@ class OracleOps:
         assert np.abs(sums).max(initial=0) <= np.iinfo(np_type).max
         return torch.from_numpy(sums.astype(np_type))
 
+    # the re-rounding allreduce of Global-E
+    def quantize_codes(self, x, norm, scheme, s, seed, step, worker0):
+        import torch
+        xh = self._host(x)
+        stacked = np.zeros((worker0 + 1, xh.shape[1]), dtype=xh.dtype)
+        stacked[worker0] = xh[0]
+        codes, rc = self.o.quantize(stacked, float(norm.item()), scheme, s, seed, step)
+        assert rc == 0
+        return torch.from_numpy(codes[worker0].copy())
+
+    def exp_combine(self, a, b, seed, step, stream_id, j0):
+        import torch
+        return torch.from_numpy(self.o.exp_combine(a.numpy(), b.numpy(), seed, step, stream_id,
+                                                   j0=j0))
+
+    def exp_dequantize(self, codes, norm, s, n, out):
+        got, rc = self.o.dequantize(self.o.exp_units(codes.numpy()), float(norm.item()), 1, s, n)
+        assert rc == 0
+        import torch
+        out.view(-1).copy_(torch.from_numpy(got.astype(np.float32)))
+        return out
+
+    def exp_tree_stream(self, level, m):
+        return self.o.exp_tree_stream(level, m)
+
+    def exp_ring_stream(self, h, c):
+        return self.o.exp_ring_stream(h, c)
+
     def dequantize(self, sums, norm, scheme, s, n, out):
         import torch
         got, rc = self.o.dequantize(sums.numpy().astype(np.int64), float(norm.item()), scheme, s, n)
@@ -92,7 +120,7 @@ def _model(dtype):
     return m.to(dtype)
 
 
-def _rank_main(rank, port, cfg, q):
+def _rank_main(rank, port, cfg, q, world):
     sys.path.insert(0, ROOT)
     import torch
     import torch.distributed as dist
@@ -100,7 +128,7 @@ def _rank_main(rank, port, cfg, q):
     from allreduce_compatible_gradient_gb300 import comm_hook
 
     os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
-    dist.init_process_group("gloo", rank=rank, world_size=WORLD,
+    dist.init_process_group("gloo", rank=rank, world_size=world,
                             timeout=datetime.timedelta(seconds=8))
     try:
         dtype = torch.bfloat16 if cfg["dtype"] == "bf16" else torch.float32
@@ -108,7 +136,7 @@ def _rank_main(rank, port, cfg, q):
         ops = OracleOps(gq_oracle)
         state = comm_hook.GlobalQSGDState(scheme=cfg["scheme"], s=cfg["s"], q=cfg["q"],
                                           p=cfg["q"], seed=cfg["seed"], step=cfg["step0"],
-                                          ops=ops)
+                                          reduce=cfg.get("reduce", "sum"), ops=ops)
         records = []
 
         def recording_hook(st, bucket):
@@ -140,16 +168,16 @@ def _rank_main(rank, port, cfg, q):
             pass
 
 
-def _run(cfg):
+def _run(cfg, world=WORLD):
     import multiprocessing as mp
     ctx = mp.get_context("spawn")
     q = ctx.Queue()
     port = _free_port()
-    procs = [ctx.Process(target=_rank_main, args=(r, port, cfg, q)) for r in range(WORLD)]
+    procs = [ctx.Process(target=_rank_main, args=(r, port, cfg, q, world)) for r in range(world)]
     for p in procs:
         p.start()
     res = {}
-    for _ in range(WORLD):
+    for _ in range(world):
         rank, status, payload = q.get(timeout=180)
         res[rank] = (status, payload)
     for p in procs:
@@ -229,3 +257,31 @@ def test_state_rejects_bad_configurations():
             st.bucket_step(1 << 16)
     finally:
         dist.destroy_process_group()
+
+
+@pytest.mark.parametrize("world", [3, 4])
+@pytest.mark.parametrize("reduce", ["tree", "ring"])
+def test_hook_reround_allreduce_matches_the_oracle(oracle, reduce, world):
+    """reduce="tree" / "ring": int8 codes over point-to-point sends, re-rounded at every hop;
+    every bucket on every rank equals the oracle's tree / ring allreduce of the stacked codes,
+    dequantised with n = world size."""
+    cfg = dict(dtype="f32", scheme=1, s=8, q=0, seed=21, step0=2, reduce=reduce)
+    res = _run(cfg, world)
+    for r in range(world):
+        assert res[r][0] == "ok", res[r][1]
+    recs = [sorted(res[r][1][0], key=lambda rec: rec[0]) for r in range(world)]
+    assert all(len(rc) == len(recs[0]) for rc in recs) and len(recs[0]) >= 2 * ITERS
+    for k in range(len(recs[0])):
+        step, norm_used = recs[0][k][0], recs[0][k][3]
+        stacked = np.ascontiguousarray(np.stack([recs[r][k][1] for r in range(world)]))
+        assert norm_used == float(np.float32(oracle.global_norm(stacked, 0, 0)))
+        codes, rc = oracle.quantize(stacked, norm_used, 1, 8, 21, step)
+        assert rc == 0
+        d = stacked.shape[1]
+        root = (oracle.exp_tree_allreduce(codes, 21, step) if reduce == "tree"
+                else oracle.exp_ring_allreduce(codes, d, 21, step))
+        want, rc = oracle.dequantize(oracle.exp_units(root), norm_used, 1, 8, world)
+        assert rc == 0
+        for r in range(world):
+            assert recs[r][k][0] == step
+            np.testing.assert_array_equal(recs[r][k][2], want.astype(np.float32))

@@ -66,8 +66,8 @@ def _rank_main(rank, port, mode, fail_rank, q):
             dist.broadcast(root, src=0)  # the allgather half only copies
             result = root.numpy()
         else:  # ring reduce-scatter, then allgather
-            chunk = -(-D // N)
-            bounds = [(c * chunk, min(D, (c + 1) * chunk)) for c in range(N)]
+            chunk = -(-(-(-D // N)) // 16) * 16  # ceil(D / N) rounded up to a multiple of 16
+            bounds = [(min(D, c * chunk), min(D, (c + 1) * chunk)) for c in range(N)]
             acc = {}
             c0 = (rank - 1) % N  # this rank starts chunk c0 (worker c0 + 1)
             acc[c0] = mine[bounds[c0][0]:bounds[c0][1]].copy()

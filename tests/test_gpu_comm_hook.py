@@ -177,9 +177,12 @@ def nccl_group(gq):
     dist.destroy_process_group()
 
 
-@pytest.mark.parametrize("dtype,scheme,s,q", [("f32", EXP, 8, INF), ("f32", LINEAR, 15, 2),
-                                              ("bf16", EXP, 4, INF)])
-def test_ddp_hook_world_one(gq, oracle_mod, nccl_group, dtype, scheme, s, q):
+@pytest.mark.parametrize("dtype,scheme,s,q,reduce", [("f32", EXP, 8, INF, "sum"),
+                                                     ("f32", LINEAR, 15, 2, "sum"),
+                                                     ("bf16", EXP, 4, INF, "sum"),
+                                                     ("f32", EXP, 8, INF, "tree"),
+                                                     ("bf16", EXP, 6, 2, "ring")])
+def test_ddp_hook_world_one(gq, oracle_mod, nccl_group, dtype, scheme, s, q, reduce):
     import torch
     from allreduce_compatible_gradient_gb300 import comm_hook
 
@@ -201,7 +204,8 @@ def test_ddp_hook_world_one(gq, oracle_mod, nccl_group, dtype, scheme, s, q):
                                 torch.nn.Linear(256, 10)).to(device="cuda", dtype=tdt)
     ddp = torch.nn.parallel.DistributedDataParallel(model, device_ids=[0], bucket_cap_mb=0.25)
     ops = RecordingOps()
-    state = comm_hook.GlobalQSGDState(scheme=scheme, s=s, q=q, p=q, seed=5, ops=ops)
+    state = comm_hook.GlobalQSGDState(scheme=scheme, s=s, q=q, p=q, seed=5, ops=ops,
+                                      reduce=reduce)
     records = []
 
     def recording_hook(st, bucket):

@@ -74,3 +74,69 @@ def test_allreduce_argument_checks(gq):
     with pytest.raises(gq.GQError) as e:
         gq.gq_exp_allreduce(codes, 25, 4, 32, 0, norm, 1, 1)   # s beyond Global-E's range
     assert e.value.status == 2
+
+
+@pytest.mark.parametrize("j0", [0, 16, 4096, 812_512])
+def test_combine_with_column_base(gq, oracle_mod, j0):
+    """gq_exp_combine on a window whose first element is coordinate j0 of the whole vector (a ring
+    chunk): the random words are those of the global coordinates."""
+    import torch
+    rng = np.random.default_rng(j0 + 1)
+    d = 1000 + j0 % 37
+    a = rng.integers(-12, 13, d).astype(np.int8)
+    b = rng.integers(-12, 13, d).astype(np.int8)
+    sid = gq.gq_exp_ring_stream(3, 2)
+    got = gq.gq_exp_combine(torch.from_numpy(a).cuda(), torch.from_numpy(b).cuda(), 5, 6, sid,
+                            j0=j0).cpu().numpy()
+    np.testing.assert_array_equal(got, oracle_mod.exp_combine(a, b, 5, 6, sid, j0=j0))
+
+
+def test_combine_rejects_unaligned_base(gq):
+    import torch
+    a = torch.zeros(64, dtype=torch.int8, device="cuda")
+    with pytest.raises(gq.GQError):
+        gq.gq_exp_combine(a, a, 1, 1, 0, j0=4)
+
+
+@pytest.mark.parametrize("s", [4, 8])
+@pytest.mark.parametrize("out16", [False, True])
+def test_exp_dequantize_matches_oracle(gq, oracle_mod, s, out16):
+    import torch
+    rng = np.random.default_rng(s)
+    d, n = 4099, 5
+    codes = rng.integers(-20, 21, d).astype(np.int8)  # extended codes, as a reduction leaves them
+    norm = torch.tensor([3.25], device="cuda")
+    odt = torch.bfloat16 if out16 else torch.float32
+    got = gq.gq_exp_dequantize(torch.from_numpy(codes).cuda(), norm, s, n, out_dtype=odt)
+    want, rc = oracle_mod.dequantize(oracle_mod.exp_units(codes), 3.25, 1, s, n)
+    assert rc == 0
+    g = got.float().cpu().numpy().astype(np.float64)
+    # out = fp32(scale) * 2^m exactly: relative error of the rounded scale only (plus bf16)
+    tol = np.abs(want) * (2.0 ** -23 + (2.0 ** -8 if out16 else 0.0))
+    assert np.all(np.abs(g - want) <= tol)
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("s,bits", [(4, 4), (4, 8), (8, 8)])
+def test_quantize_codes_with_worker_offset(gq, oracle_mod, dtype, s, bits):
+    """One rank's codes (rows worker0 ..) as int8 or int4, equal to the oracle's rows of the
+    stacked matrix."""
+    import torch
+    from allreduce_compatible_gradient_gb300 import workloads
+    from gpu_common import unpack_codes
+    n, d = 5, 1003
+    x = workloads.host_inputs("normal", n, d, seed=4, dtype=dtype)
+    norm32 = float(np.float32(oracle_mod.global_norm(x, 0, 0)))
+    want, rc = oracle_mod.quantize(x, norm32, 1, s, 9, 3)
+    assert rc == 0
+    xd = __import__("gpu_common").to_device(x)
+    norm = torch.tensor([norm32], device="cuda")
+    for r0, m in [(0, 2), (2, 3)]:
+        got = gq.gq_quantize_codes(xd[r0:r0 + m].clone(), norm, gq.EXP, s, 9, 3, worker0=r0,
+                                   code_bits=bits).cpu().numpy()
+        if bits == 8:
+            pitch = gq.gq_code_pitch(d)
+            rows = got.view(np.int8).reshape(m, pitch)[:, :d]
+        else:
+            rows = unpack_codes(got, gq.EXP, s, m, d)
+        np.testing.assert_array_equal(rows, want[r0:r0 + m])

@@ -106,7 +106,7 @@ def test_ring_matches_definition(oracle, n):
     d = 29
     rows = rng.integers(-8, 9, (n, d)).astype(np.int8)
     got = oracle.exp_ring_allreduce(rows, d, 99, 5)
-    chunk = -(-d // n)
+    chunk = -(-(-(-d // n)) // 16) * 16  # ceil(d / n) rounded up to a multiple of 16
     for j in range(d):
         c = j // chunk
         code = np.array([rows[(c + 1) % n, j]], dtype=np.int8)

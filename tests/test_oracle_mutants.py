@@ -29,8 +29,10 @@ MUTANTS = [
     ("E level off by one", "*lo = s + e; /* 2^e = 2^-(s - lo) */", "*lo = s + e + 1;"),
     ("E first interval scale", "f = (double)v / smallest;", "f = (double)v / (2.0 * smallest);"),
     ("L fraction dropped", "f = t - m; /* exact */", "f = 0.0;"),
-    ("sign dropped", "codes[i * w + (j - j0)] = (int8_t)(xv < 0.0f ? -k : k);",
-     "codes[i * w + (j - j0)] = (int8_t)k;"),
+    ("sign dropped", "codes[i * w + j] = (int8_t)(xv < 0.0f ? -k : k);",
+     "codes[i * w + j] = (int8_t)k;"),
+    ("window keyed by its local column", "r = gqo_philox_word(seed, step, i, j0 + j);",
+     "r = gqo_philox_word(seed, step, i, j);"),
     ("E decode 2^k", "int64_t units = (int64_t)1 << (k - 1);", "int64_t units = (int64_t)1 << k;"),
     ("mean not divided by n", "out[j] = ldexp(num, -(s - 1)) / (double)n;",
      "out[j] = ldexp(num, -(s - 1));"),
