@@ -198,42 +198,58 @@ def _barrier(world):
         dist.barrier()
 
 
-def cpu_baseline(cfg: dict, seconds: float, host_x=None) -> dict:
-    """Time the CPU oracle (as it stands, single-threaded) on a column window of the workload."""
-    import numpy as np
-
+def _oracle_window(cfg: dict, seconds: float):
+    """A column window of the workload sized to about `seconds` of single-threaded oracle work,
+    generated on the host once: (window width, host inputs)."""
     from allreduce_compatible_gradient_gb300 import workloads
     from oracle import gq_oracle
 
-    n, d = cfg["n"], cfg["d"]
-    elt = 2 if cfg["dtype"] == "bf16" else 4
+    d = cfg["d"]
     w = min(d, 1 << 14)
-    x = workloads.host_inputs(cfg["dist"], n, w, seed=cfg["input_seed"], dtype=cfg["dtype"])
+    x = workloads.host_inputs(cfg["dist"], cfg["n"], w, seed=cfg["input_seed"], dtype=cfg["dtype"])
     t0 = time.perf_counter()
     gq_oracle.allreduce_mean(x, cfg["q"], cfg["p"], cfg["scheme"], cfg["s"], cfg["seed"],
                              cfg["step"])
     dt = time.perf_counter() - t0
-    # grow the window to fill about `seconds` of CPU work
     w = int(min(d, max(w, w * seconds / max(dt, 1e-6))))
     w = max(32, w // 32 * 32) if w < d else d
-    x = workloads.host_inputs(cfg["dist"], n, w, seed=cfg["input_seed"], dtype=cfg["dtype"])
+    x = workloads.host_inputs(cfg["dist"], cfg["n"], w, seed=cfg["input_seed"], dtype=cfg["dtype"])
+    return w, x
+
+
+def _time_oracle(cfg: dict, w: int, x) -> dict:
+    from oracle import gq_oracle
+
+    elt = 2 if cfg["dtype"] == "bf16" else 4
     t0 = time.perf_counter()
     gq_oracle.allreduce_mean(x, cfg["q"], cfg["p"], cfg["scheme"], cfg["s"], cfg["seed"],
                              cfg["step"])
     dt = time.perf_counter() - t0
-    return {"value": round(n * w * elt / dt / 1e9, 6), "unit": UNIT, "cores": 1, "kind": "oracle",
+    return {"value": round(cfg["n"] * w * elt / dt / 1e9, 6), "unit": UNIT, "cores": 1,
+            "kind": "oracle",
             "sample": "%d x %d columns of %s (same distribution; whole pipeline: norm of the "
-                      "window, quantise, sum, dequantise), %.1f s" % (n, w, cfg["name"], dt),
+                      "window, quantise, sum, dequantise), %.1f s" % (cfg["n"], w, cfg["name"], dt),
             "seconds": round(dt, 3), "window_columns": w}
 
 
+def cpu_baseline(cfg: dict, seconds: float, host_x=None) -> dict:
+    """Time the CPU oracle (as it stands, single-threaded) on a column window of the workload."""
+    w, x = _oracle_window(cfg, seconds)
+    return _time_oracle(cfg, w, x)
+
+
 def run_reference(a, cfg):
+    """The oracle as the reference arm: rank 0 only; each step times the oracle on one column
+    window of the workload (generated once), sized so that the whole run stays near two
+    minutes of CPU work."""
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
         return 0
+    per_step = max(0.2, min(a.cpu_seconds, 120.0 / (a.steps + a.warmup)))
+    w, x = _oracle_window(cfg, per_step)
     steps = []
     for i in range(a.warmup + a.steps):
-        r = cpu_baseline(cfg, seconds=max(1.0, min(a.cpu_seconds, 120.0 / (a.steps + a.warmup))))
+        r = _time_oracle(cfg, w, x)
         if i >= a.warmup:
             steps.append(r)
     val = statistics.median(r["value"] for r in steps)
