@@ -88,3 +88,35 @@ def test_full_size(gq, name):
         tail = unpack_codes(np.ascontiguousarray(codes_h[:, (pitch - 32) * bits // 8:]).ravel(),
                             sc, s, n, 32, check_padding=False)
         assert not tail[:, d - (pitch - 32):].any()
+
+
+@pytest.mark.parametrize("dtype,scheme,s", [("f32", 0, 127), ("bf16", 1, 8)])
+def test_columns_past_2_31(gq, dtype, scheme, s):
+    """One worker with d = 2^31 + 2^20 + 5 columns (8.6 GB fp32): column indices and Philox
+    counters past 2^31 (word 0 = j / 8 past 2^28), a ragged tail, the bulk-copy kernel's largest
+    chunk numbers.  The max norm against a library reduction, sampled windows (first, around
+    2^31, last) against the oracle."""
+    import torch
+    from oracle import gq_oracle as oracle
+    # a ragged last group (d % 8 != 0) on 16-byte aligned rows: 2^31 + 2^20 + 4 (fp32); bf16
+    # rows take the direct-load path here (d % 8 != 0)
+    d = 2**31 + 2**20 + 4
+    x = workloads.device_inputs("normal", 1, d, seed=31, dtype=dtype)
+    ws = gq.gq_workspace()
+    norm = torch.empty(1, dtype=torch.float32, device="cuda")
+    out = gq.gq_allreduce_mean(x, 0, 0, scheme, s, 7, 3, norm=norm, ws=ws)
+    torch.cuda.synchronize()
+    assert gq.gq_get_status(ws) == 0
+    norm32 = float(norm.item())
+    assert norm32 == float(x.abs().max().float().item())
+    for j0 in (0, 2**31 - 512, 2**31 + 2**20 - 1000, d - 1003):
+        j1 = min(d, j0 + 1003)
+        xw = to_host(x[:, j0:j1].contiguous())
+        codes, rc = oracle.quantize_cols(xw, j0, norm32, scheme, s, 7, 3)
+        assert rc == 0
+        want, rc = oracle.dequantize(oracle.reduce_codes(codes, scheme, s), norm32, scheme, s, 1)
+        assert rc == 0
+        got = out[j0:j1].cpu().numpy().astype(np.float64)
+        assert np.abs(got - want).max() <= 1e-6 * norm32, j0
+    del x, out
+    torch.cuda.empty_cache()
