@@ -429,6 +429,79 @@ __device__ __forceinline__ void norm_body(const T* __restrict__ x, int64_t n, in
     // (2, inf) form, whose per-column scaled sums take C x 5 registers
     constexpr int U = (MODE == kL2Max) ? (C == 8 ? 2 : 4) : 8;
     const int64_t row_bytes = d * static_cast<int64_t>(sizeof(T));
+    if constexpr (MODE == kL2Max) {
+        // Plain fp32 column sums of squares (exact squares by FMA into NA interleaved
+        // accumulators: relative error below (n/NA + 1) u <= 17 u, so below 1e-6 on the norm)
+        // when n <= 16 NA; a column whose sum is not a normal number of at least 2^-100 (a NaN,
+        // an overflow, or tiny values whose squares lose bits) is summed again with the scaled
+        // form below.
+        constexpr int NA = C == 8 ? 2 : 4;
+        constexpr int UF = 8;  // rows in flight
+        if (n <= 16 * NA) {
+            for (int64_t g = vb * kThreads + threadIdx.x; g < groups; g += stride) {
+                float acc[NA][C];
+#pragma unroll
+                for (int a = 0; a < NA; ++a)
+#pragma unroll
+                    for (int c = 0; c < C; ++c) acc[a][c] = 0.0f;
+                const bool vec = vec_rows && (g + 1) * C <= d;
+                for (int64_t i0 = 0; i0 < n; i0 += UF) {
+                    uint4 raw[UF];
+                    if (vec) {
+#pragma unroll
+                        for (int u = 0; u < UF; ++u)
+                            raw[u] = (i0 + u < n) ? load_raw16(x, i0 + u, g, row_bytes)
+                                                  : make_uint4(0u, 0u, 0u, 0u);
+                    }
+#pragma unroll
+                    for (int u = 0; u < UF; ++u) {
+                        float v[C];
+                        if (vec) {
+                            widen16<T>(raw[u], v);
+                        } else if (i0 + u < n) {
+                            load_group<T>(x, i0 + u, g, d, false, v);
+                        } else {
+#pragma unroll
+                            for (int c = 0; c < C; ++c) v[c] = 0.0f;
+                        }
+#pragma unroll
+                        for (int c = 0; c < C; ++c)
+                            acc[u % NA][c] = __fmaf_rn(v[c], v[c], acc[u % NA][c]);
+                    }
+                }
+#pragma unroll
+                for (int c = 0; c < C; ++c) {
+                    float sum = acc[0][c];
+#pragma unroll
+                    for (int a = 1; a < NA; ++a) sum = sum + acc[a][c];
+                    if (sum >= 0x1p-100f && sum < __uint_as_float(kInfBits)) {
+                        const int64_t key = scaled_key(sum, 0);
+                        best_key = key > best_key ? key : best_key;
+                        continue;
+                    }
+                    if (sum == 0.0f) continue;  // an all-zero column adds nothing
+                    // rare: the scaled form for this column
+                    ScaledSumSq cs;
+                    cs.init();
+                    for (int64_t i = 0; i < n; ++i) {
+                        const int64_t j = g * C + c;
+                        const float one[1] = {j < d ? Elem<T>::load_one(x + i * d + j) : 0.0f};
+                        cs.add<1>(one);
+                    }
+                    const float ssum = cs.sum();
+                    if (!(ssum < __uint_as_float(kInfBits))) {  // NaN or Inf column
+                        const uint32_t b = __float_as_uint(ssum) & 0x7FFFFFFFu;
+                        bad_col = b > bad_col ? b : bad_col;
+                    } else if (ssum > 0.0f) {
+                        const int64_t key = scaled_key(ssum, cs.e);
+                        best_key = key > best_key ? key : best_key;
+                    }
+                }
+            }
+            norm_finalize<MODE>(maxbits, ssq, best_key, bad_col, vb, nblk, out);
+            return;
+        }
+    }
     for (int64_t g = vb * kThreads + threadIdx.x; g < groups; g += stride) {
         uint32_t colmax[C];   // kMaxL2
         ScaledSumSq col[C];   // kL2Max
@@ -500,8 +573,10 @@ __device__ __forceinline__ void norm_body(const T* __restrict__ x, int64_t n, in
     norm_finalize<MODE>(maxbits, ssq, best_key, bad_col, vb, nblk, out);
 }
 
+// The mixed forms keep per-column state (more registers): two blocks per SM for (2, inf), three
+// for (inf, 2), else four.
 template <typename T, int MODE>
-__global__ void __launch_bounds__(kThreads, 4)
+__global__ void __launch_bounds__(kThreads, MODE == kL2Max ? 2 : (MODE == kMaxL2 ? 3 : 4))
 norm_kernel(const T* __restrict__ x, int64_t n, int64_t d, int64_t groups, bool vec_rows,
             float* __restrict__ norm_user, double* __restrict__ part_user,
             unsigned char* __restrict__ ws) {
@@ -1221,7 +1296,7 @@ __device__ __forceinline__ int find_segment(const SegLaunch& L, int32_t b) {
 }
 
 template <typename T, int MODE>
-__global__ void __launch_bounds__(kThreads, 4)
+__global__ void __launch_bounds__(kThreads, MODE == kL2Max ? 2 : (MODE == kMaxL2 ? 3 : 4))
 norm_segments_kernel(const __grid_constant__ SegLaunch L, int64_t n, int scheme, uint32_t s,
                      float* __restrict__ norms_user, unsigned char* __restrict__ ws) {
     constexpr int C = Elem<T>::kCols;
