@@ -49,6 +49,9 @@ def _args():
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--sweep-max-gb", type=float, default=120.0,
                     help="--measure sweep: skip points whose n*d*4 bytes exceed this")
+    ap.add_argument("--columns", type=int, default=None,
+                    help="run the workload with d columns instead of its own (a smaller case of the "
+                         "same kernels, e.g. for an ncu capture); named '<workload>_d<columns>'")
     ap.add_argument("--measure", default=None, choices=["exp-reduce", "segments", "sweep"],
                     help="extra measurement instead of the main bench line")
     return ap.parse_args()
@@ -468,6 +471,10 @@ def main():
     from allreduce_compatible_gradient_gb300 import workloads
 
     cfg = dict(workloads.CONFIGS[a.config], name=a.config)
+    if a.columns is not None:
+        if a.columns < 1:
+            raise SystemExit("--columns must be positive")
+        cfg["d"], cfg["name"] = a.columns, "%s_d%d" % (a.config, a.columns)
     if a.impl == "reference":
         return run_reference(a, cfg)
 
