@@ -1279,11 +1279,13 @@ struct SegDesc {
     int64_t d;
     int32_t b0;      // first block of its run
     int32_t nb;      // blocks in its run
+    int64_t t0;      // bulk-copy pass: index of its first direct-load group among the launch's
 };
 struct SegLaunch {
     SegDesc seg[kSegChunk];
     int32_t nseg;
     int32_t seg0;    // index of seg[0] among all segments of the call
+    int64_t ntail;   // bulk-copy pass: groups outside the chunks, all segments
 };
 
 __device__ __forceinline__ int find_segment(const SegLaunch& L, int32_t b) {
@@ -1291,6 +1293,17 @@ __device__ __forceinline__ int find_segment(const SegLaunch& L, int32_t b) {
     while (lo < hi) {
         const int mid = (lo + hi + 1) >> 1;
         if (L.seg[mid].b0 <= b) lo = mid; else hi = mid - 1;
+    }
+    return lo;
+}
+
+// The segment of direct-load group `t` (numbered across the launch): the last whose first such
+// group is at or before t.
+__device__ __forceinline__ int find_tail_segment(const SegLaunch& L, int64_t t) {
+    int lo = 0, hi = L.nseg - 1;
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (L.seg[mid].t0 <= t) lo = mid; else hi = mid - 1;
     }
     return lo;
 }
@@ -1671,9 +1684,12 @@ quantize_seg_tma_kernel(const __grid_constant__ SegLaunch L, QuantArgs base, int
         if (tid == kTmaConsumers) {  // producer: lane 0 of the last warp
             uint32_t item = 0;
             bool ok = true;
+            int k = -1;
             for (int32_t q = blockIdx.x; q < nchunks && ok; q += gridDim.x) {
                 const int32_t cg = nchunks - 1 - q;
-                const SegDesc& sd = L.seg[find_segment(L, cg)];
+                // chunks come in decreasing order: search only when cg leaves segment k
+                if (k < 0 || cg < L.seg[k].b0) k = find_segment(L, cg);
+                const SegDesc& sd = L.seg[k];
                 const int64_t g0 = static_cast<int64_t>(cg - sd.b0) * kTmaConsumers;
                 const int64_t ng = min(static_cast<int64_t>(kTmaConsumers), sd.d / kQCols - g0);
                 const uint32_t row_bytes = static_cast<uint32_t>(ng * kQCols * sizeof(T));
@@ -1691,19 +1707,25 @@ quantize_seg_tma_kernel(const __grid_constant__ SegLaunch L, QuantArgs base, int
         return;
     }
 
-    // consumers
+    // consumers; the segment of the current chunk, its arguments and decision constants are
+    // kept while consecutive chunks stay in it
     const int lane = tid & 31;
     uint32_t item = 0;
     bool ok = true;
+    int k = -1;
+    QuantArgs a = base;
+    Decide dc;
+    float scale = 0.0f;
     for (int32_t q = blockIdx.x; q < nchunks && ok; q += gridDim.x) {
         const int32_t cg = nchunks - 1 - q;
-        const int k = find_segment(L, cg);
+        if (k < 0 || cg < L.seg[k].b0) {
+            k = find_segment(L, cg);
+            a.d = L.seg[k].d;
+            a.step_lo = base.step_lo | static_cast<uint32_t>(L.seg0 + k);
+            dc = make_decide<SCHEME>(norms[k], a.s);
+            scale = scales[k];
+        }
         const SegDesc& sd = L.seg[k];
-        QuantArgs a = base;
-        a.d = sd.d;
-        a.step_lo = base.step_lo | static_cast<uint32_t>(L.seg0 + k);
-        const float nrm = norms[k];
-        const Decide dc = make_decide<SCHEME>(nrm, a.s);
         const int64_t g = static_cast<int64_t>(cg - sd.b0) * kTmaConsumers + tid;
         const bool active = g < sd.d / kQCols;
         const PhiloxGroup pg = philox_group(static_cast<uint32_t>(g), a.step_lo, a.step_hi, a.rk);
@@ -1720,7 +1742,7 @@ quantize_seg_tma_kernel(const __grid_constant__ SegLaunch L, QuantArgs base, int
             tma_consume_stage<T, SCHEME, 0, true, 2>(stage, lane, active, b, g, pg, a, dc,
                                                      smem_u32(&empty_bar[item % NS]), S, nullptr);
         }
-        if (ok && active) store_out(sd.out, nullptr, 0, base.out_dtype, g, sd.d, scales[k], S);
+        if (ok && active) store_out(sd.out, nullptr, 0, base.out_dtype, g, sd.d, scale, S);
     }
     if (!ok) {
         atomicCAS(status, 0u, kStatusTimeout);
@@ -1728,27 +1750,28 @@ quantize_seg_tma_kernel(const __grid_constant__ SegLaunch L, QuantArgs base, int
         return;
     }
 
-    // groups outside the chunks, direct loads
+    // groups outside the chunks, numbered across the launch (segment k owns t0 .. t0 + its
+    // count - 1, last group first), direct loads
     const int64_t stride = static_cast<int64_t>(gridDim.x) * kTmaConsumers;
-    for (int k = 0; k < L.nseg; ++k) {
-        const SegDesc& sd = L.seg[k];
-        const int64_t groups = (sd.d + kQCols - 1) / kQCols;
-        const int64_t full = sd.nb > 0 ? sd.d / kQCols : 0;
-        if (full == groups) continue;
-        QuantArgs a = base;
-        a.d = sd.d;
-        a.pitch = (sd.d + 31) / 32 * 32;
-        a.vec_rows = sd.nb > 0;
-        a.step_lo = base.step_lo | static_cast<uint32_t>(L.seg0 + k);
-        a.norm_ptr = norms + k;
-        const Decide dc = make_decide<SCHEME>(norms[k], a.s);
-        for (int64_t it = static_cast<int64_t>(blockIdx.x) * kTmaConsumers + tid;
-             it < groups - full; it += stride) {
-            const int64_t g = groups - 1 - it;
-            float S[kQCols];
-            quantize_group<T, SCHEME, 0, true>(static_cast<const T*>(sd.x), a, dc, g, nullptr, S);
-            store_out(sd.out, nullptr, 0, base.out_dtype, g, sd.d, scales[k], S);
+    k = -1;
+    for (int64_t it = static_cast<int64_t>(blockIdx.x) * kTmaConsumers + tid; it < L.ntail;
+         it += stride) {
+        const int kt = find_tail_segment(L, it);
+        const SegDesc& sd = L.seg[kt];
+        if (kt != k) {
+            k = kt;
+            a.d = sd.d;
+            a.pitch = (sd.d + 31) / 32 * 32;
+            a.vec_rows = sd.nb > 0;
+            a.step_lo = base.step_lo | static_cast<uint32_t>(L.seg0 + k);
+            a.norm_ptr = norms + k;
+            dc = make_decide<SCHEME>(norms[k], a.s);
+            scale = scales[k];
         }
+        const int64_t g = (sd.d + kQCols - 1) / kQCols - 1 - (it - sd.t0);
+        float S[kQCols];
+        quantize_group<T, SCHEME, 0, true>(static_cast<const T*>(sd.x), a, dc, g, nullptr, S);
+        store_out(sd.out, nullptr, 0, base.out_dtype, g, sd.d, scale, S);
     }
 }
 

@@ -49,16 +49,22 @@ gq_status run_quant_segments(gq::SegLaunch& L, const int64_t* d, int64_t n,
                              const gq::QuantArgs& base, unsigned char* ws, cudaStream_t st) {
     // Chunks of 3840 columns for every segment whose rows are 16-byte aligned; with at least one
     // chunk per SM they all go through the bulk-copy ring (runs b0 / nb now count chunks).
+    // The groups outside the chunks (a ragged last group, or all groups of a segment without
+    // chunks) are numbered across the launch: segment k's start at t0.
     constexpr int vec = 16 / static_cast<int>(sizeof(T));
     int32_t chunks = 0;
+    int64_t tails = 0;
     for (int k = 0; k < L.nseg; ++k) {
         const int64_t full = d[k] % vec == 0 ? d[k] / gq::kQCols : 0;
         const int64_t nc = (full + gq::kTmaConsumers - 1) / gq::kTmaConsumers;
         L.seg[k].d = d[k];
         L.seg[k].b0 = chunks;
         L.seg[k].nb = static_cast<int32_t>(nc);
+        L.seg[k].t0 = tails;
         chunks += static_cast<int32_t>(nc);
+        tails += (d[k] + gq::kQCols - 1) / gq::kQCols - (nc > 0 ? full : 0);
     }
+    L.ntail = tails;
     if (chunks >= sm_count()) {
         auto kt = gq::quantize_seg_tma_kernel<T, SCHEME>;
         constexpr int tsmem = gq::TmaCfg<T>::kSmemBytes;
