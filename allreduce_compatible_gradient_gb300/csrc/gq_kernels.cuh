@@ -924,11 +924,19 @@ __device__ __forceinline__ unsigned long long fma2(unsigned long long a, unsigne
     asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
     return d;
 }
+// Paired add rounded toward zero (add.rz.f32x2).
+__device__ __forceinline__ unsigned long long add2rz(unsigned long long a, unsigned long long b) {
+    unsigned long long d;
+    asm("add.rz.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
 // Accumulate one row-group's codes (k = (yk >> 16) - 0x4300) into the sums (fp32, exact:
 // integers below 2^24) and return the signed codes.  The level value is read off bit patterns:
-// L: bits 0x4B00 : (k + 0x4300) (one byte permute) are 2^23 + 0x4300 + k; E: the float with
-// exponent field k + 126 is 2^(k-1), and (v + 2^23) - 2^23 turns k = 0 (0.5) into 0 (the tie
-// rounds to the even 2^23).  The subtraction and the signed accumulation run on column pairs.
+// L: yk read as a float is 128 + k + f, f = (low half) 2^-16 < 1 (at most 0xFFFB on the fast
+// path, 0 from the exact one), so adding 2^23 - 128 with rounding toward zero gives exactly
+// 2^23 + k (floating-point adds, off the integer pipe); E: the float with exponent field k + 126
+// is 2^(k-1), and (v + 2^23) - 2^23 turns k = 0 (0.5) into 0 (the tie rounds to the even 2^23).
+// The subtractions and the signed accumulation run on column pairs.
 template <int SCHEME>
 __device__ __forceinline__ void accumulate_row(const float (&xv)[kQCols],
                                                const uint32_t (&yk)[kQCols], float (&S)[kQCols],
@@ -941,7 +949,7 @@ __device__ __forceinline__ void accumulate_row(const float (&xv)[kQCols],
             const uint32_t xb = __float_as_uint(xv[c + h]);
             sg[h] = __uint_as_float((xb & 0x80000000u) | 0x3F800000u);
             if (SCHEME == kLinear)
-                raw[h] = __uint_as_float(__byte_perm(yk[c + h], 0x4B000000u, 0x7632u));
+                raw[h] = __uint_as_float(yk[c + h]);  // 128 + k + (low half) 2^-16
             else
                 raw[h] = __uint_as_float(((yk[c + h] >> 16) << 23) + ((126u - 0x4300u) << 23));
             const int32_t k = static_cast<int32_t>(yk[c + h] >> 16) - 0x4300;
@@ -950,7 +958,9 @@ __device__ __forceinline__ void accumulate_row(const float (&xv)[kQCols],
         }
         unsigned long long units;
         if (SCHEME == kLinear) {
-            units = add2(pk2(raw[0], raw[1]), pk2(-8405760.0f, -8405760.0f));
+            // 128 + k + f (0 <= f < 1) plus 2^23 - 128, rounded toward zero, is 2^23 + k
+            units = add2(add2rz(pk2(raw[0], raw[1]), pk2(8388480.0f, 8388480.0f)),
+                         pk2(-8388608.0f, -8388608.0f));
         } else {
             units = add2(add2(pk2(raw[0], raw[1]), pk2(8388608.0f, 8388608.0f)),
                          pk2(-8388608.0f, -8388608.0f));
