@@ -41,6 +41,7 @@ def lib() -> ctypes.CDLL:
         "gq_workspace_init": (ci, [vp, sz, vp]),
         "gq_code_bits": (ci, [ci, ci]),
         "gq_code_pitch": (i64, [i64]),
+        "gq_fused_launches": (ci, [ci, i64, i64, ci]),
         "gq_code_bytes": (sz, [ci, ci, i64, i64]),
         "gq_global_norm": (ci, [vp, ci, i64, i64, ci, ci, vp, vp, sz, vp]),
         "gq_quantize": (ci, [vp, ci, i64, i64, vp, ci, ci, u64, u64, vp, vp]),
@@ -133,6 +134,13 @@ def gq_code_bits(scheme: int, s: int) -> int:
 
 def gq_code_pitch(d: int) -> int:
     return lib().gq_code_pitch(d)
+
+
+def gq_fused_launches(dtype, n: int, d: int, with_codes: bool = False) -> int:
+    """1 if gq_allreduce_mean runs as one launch for this problem, 2 if as two, 0 if invalid;
+    dtype: torch.float32 / torch.bfloat16 or F32 / BF16."""
+    code = {torch.float32: F32, torch.bfloat16: BF16}.get(dtype, dtype)
+    return lib().gq_fused_launches(int(code), n, d, 1 if with_codes else 0)
 
 
 def gq_code_bytes(scheme: int, s: int, n: int, d: int) -> int:

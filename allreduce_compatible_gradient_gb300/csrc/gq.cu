@@ -153,6 +153,19 @@ size_t gq_workspace_bytes(int64_t n, int64_t d) {
     return static_cast<size_t>(gq::kWorkspaceBytes);
 }
 
+int gq_fused_launches(int dtype, int64_t n, int64_t d, int with_codes) {
+    if ((dtype != GQ_F32 && dtype != GQ_BF16) || n < 1 || n >= (int64_t(1) << 31) || d < 1 ||
+        d >= kMaxD)
+        return 0;
+    const int elt = dtype == GQ_F32 ? 4 : 2;
+    int64_t gpb = 0;
+    unsigned nblk = 0;
+    size_t smem = 0;
+    if (!with_codes && d % (16 / elt) == 0 && resident_plan(n, d, elt, &gpb, &nblk, &smem))
+        return 1;
+    return 2;
+}
+
 gq_status gq_workspace_init(void* ws, size_t ws_bytes, void* stream) {
     if (!ws || !aligned16(ws) || ws_bytes < gq_workspace_bytes(1, 1))
         return GQ_ERR_WORKSPACE;
@@ -271,10 +284,23 @@ gq_status gq_allreduce_mean_to(const void* grads, int dtype, int64_t n, int64_t 
     if (!out_dev || !aligned16(out_dev) || (codes && !aligned16(codes))) return GQ_ERR_INVALID;
     if ((st = check_ws(ws, ws_bytes, n, d)) != GQ_OK) return st;
     cudaStream_t cs = static_cast<cudaStream_t>(stream);
-    if ((st = norm_any(grads, dtype, mode, n, d, norm_dev, ws, cs)) != GQ_OK) return st;
     const float* ws_norm = &reinterpret_cast<const gq::WsHeader*>(ws)->norm;
     gq::QuantArgs a = make_args(ws_norm, dtype, n, d, s, seed, step);
     a.out_dtype = out_dtype;
+    if (!codes) {  // small problems: one launch, the matrix read once
+        unsigned char* w = static_cast<unsigned char*>(ws);
+        bool taken = false;
+        if (dtype == GQ_F32)
+            st = scheme == GQ_LINEAR
+                     ? resident_f32_l(grads, a, mode, out_dev, norm_dev, w, cs, &taken)
+                     : resident_f32_e(grads, a, mode, out_dev, norm_dev, w, cs, &taken);
+        else
+            st = scheme == GQ_LINEAR
+                     ? resident_bf16_l(grads, a, mode, out_dev, norm_dev, w, cs, &taken)
+                     : resident_bf16_e(grads, a, mode, out_dev, norm_dev, w, cs, &taken);
+        if (taken) return st;
+    }
+    if ((st = norm_any(grads, dtype, mode, n, d, norm_dev, ws, cs)) != GQ_OK) return st;
     unsigned int* status = &reinterpret_cast<gq::WsHeader*>(ws)->status;
     return quant_any<true, true>(grads, dtype, a, scheme, gq_code_bits(scheme, s), codes, out_dev,
                                  cs, status);
@@ -323,6 +349,12 @@ gq_status gq_get_status(void* ws, void* stream) {
     if (v != 0) {
         const unsigned int zero = 0;
         if (cudaMemcpy(&hdr->status, &zero, sizeof zero, cudaMemcpyHostToDevice) != cudaSuccess)
+            return GQ_ERR_CUDA;
+        // a wait that gave up may have left a completion ticket or the grid barrier's arrival
+        // count short of a full set: start both again from zero
+        if (v == GQ_ERR_TIMEOUT &&
+            (cudaMemcpy(&hdr->ticket, &zero, sizeof zero, cudaMemcpyHostToDevice) != cudaSuccess ||
+             cudaMemcpy(&hdr->bar_count, &zero, sizeof zero, cudaMemcpyHostToDevice) != cudaSuccess))
             return GQ_ERR_CUDA;
     }
     return static_cast<gq_status>(v);

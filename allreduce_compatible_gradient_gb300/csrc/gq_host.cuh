@@ -105,6 +105,20 @@ inline int32_t total_blocks(const gq::SegLaunch& L) {
 }
 
 
+// The single-launch form of the fused call: blocks of gpb column groups, at most one per SM,
+// each holding its n x (8 gpb) slice in shared memory; false when a slice would not fit.
+inline bool resident_plan(int64_t n, int64_t d, int elt, int64_t* gpb, unsigned* nblk,
+                          size_t* smem) {
+    const int64_t groups = (d + gq::kQCols - 1) / gq::kQCols;
+    const int64_t nsm = sm_count();
+    const int64_t g = (groups + nsm - 1) / nsm;
+    if (n > gq::kResTileBytes / (g * gq::kQCols * elt)) return false;
+    *gpb = g;
+    *nblk = static_cast<unsigned>((groups + g - 1) / g);
+    *smem = static_cast<size_t>(n * g * gq::kQCols * elt);
+    return true;
+}
+
 // Quantise launchers, one translation unit per (gradient type, scheme).  out: dequantise into
 // outp (else only codes); trusted: the norm was computed from these gradients; status
 // (nullable): the workspace status word, which lets large aligned problems take the bulk-copy
@@ -114,7 +128,9 @@ inline int32_t total_blocks(const gq::SegLaunch& L) {
                            bool trusted, void* codes, void* outp, cudaStream_t st,                 \
                            unsigned int* status);                                                  \
     gq_status quant_segments_##NAME(gq::SegLaunch& L, const int64_t* d, int64_t n,                \
-                                    const gq::QuantArgs& base, unsigned char* ws, cudaStream_t st);
+                                    const gq::QuantArgs& base, unsigned char* ws, cudaStream_t st); \
+    gq_status resident_##NAME(const void* grads, const gq::QuantArgs& a, int mode, void* out,       \
+                              float* norm_user, unsigned char* ws, cudaStream_t st, bool* taken);
 GQH_QUANT_LAUNCHERS(f32_l)
 GQH_QUANT_LAUNCHERS(f32_e)
 GQH_QUANT_LAUNCHERS(bf16_l)

@@ -36,7 +36,9 @@ struct WsHeader {
     unsigned int status;  // sticky device-detected status (0 = ok)
     unsigned int ticket;  // blocks of the running norm kernel that have finished; 0 between calls
     float norm;           // fp32 norm written by the last norm kernel
-    unsigned int pad[61];
+    unsigned int bar_count;  // grid barrier of the single-launch kernel: blocks arrived (0 between)
+    unsigned int bar_gen;    // and its generation (advances by one per barrier)
+    unsigned int pad[59];
 };
 static_assert(sizeof(WsHeader) == kHeaderBytes, "workspace header is 256 bytes");
 
@@ -294,6 +296,8 @@ __device__ __forceinline__ double key_value(int64_t key) {
 // ------------------------------------------------------------------------------------------
 // Block reductions (fixed order: deterministic for a given grid and block size).
 // ------------------------------------------------------------------------------------------
+// NT: threads of the block; sh holds NT / 32 values.
+template <int NT = kThreads>
 __device__ __forceinline__ double block_sum(double v, double* sh) {
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) v += __shfl_down_sync(0xFFFFFFFFu, v, o);
@@ -302,12 +306,13 @@ __device__ __forceinline__ double block_sum(double v, double* sh) {
     __syncthreads();
     double r = 0.0;
     if (threadIdx.x == 0)
-        for (int w = 0; w < kThreads / 32; ++w) r += sh[w];
+        for (int w = 0; w < NT / 32; ++w) r += sh[w];
     __syncthreads();
     return r;  // valid in thread 0
 }
 // Max over non-negative fp64 values by their bit patterns: NaN (sign clear) orders above +Inf,
 // so a NaN anywhere wins.
+template <int NT = kThreads>
 __device__ __forceinline__ uint64_t block_max_bits(uint64_t v, uint64_t* sh) {
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
@@ -319,7 +324,7 @@ __device__ __forceinline__ uint64_t block_max_bits(uint64_t v, uint64_t* sh) {
     __syncthreads();
     uint64_t r = 0;
     if (threadIdx.x == 0)
-        for (int w = 0; w < kThreads / 32; ++w) r = sh[w] > r ? sh[w] : r;
+        for (int w = 0; w < NT / 32; ++w) r = sh[w] > r ? sh[w] : r;
     __syncthreads();
     return r;
 }
@@ -344,9 +349,54 @@ struct NormSlots {
     int64_t n = 1;
 };
 
-// The block's partial (a max or a sum, as a non-negative fp64 stored by its bits), then, in the
-// last of the nblk blocks of this norm to finish (completion ticket, no waiting), the fixed-order
-// combine of the partials and the fp32 norm.
+// The block's partial of a norm: a max or a sum, as a non-negative fp64 stored by its bits
+// (valid in thread 0).  NT: threads of the block.
+template <int MODE, int NT = kThreads>
+__device__ __forceinline__ uint64_t block_partial(uint32_t maxbits, const ScaledSumSq& ssq,
+                                                  int64_t best_key, uint32_t bad_col,
+                                                  double* sh_d, uint64_t* sh_u) {
+    if (MODE == kMaxMax) {
+        const double m = static_cast<double>(__uint_as_float(maxbits));
+        return block_max_bits<NT>(static_cast<uint64_t>(__double_as_longlong(m)), sh_u);
+    } else if (MODE == kL2Max) {
+        double m = best_key == INT64_MIN ? 0.0 : key_value(best_key);
+        if (bad_col) m = static_cast<double>(__uint_as_float(bad_col));
+        return block_max_bits<NT>(static_cast<uint64_t>(__double_as_longlong(m)), sh_u);
+    } else {
+        return static_cast<uint64_t>(__double_as_longlong(block_sum<NT>(ssq.value(), sh_d)));
+    }
+}
+
+// The fixed-order combine of nb block partials (valid in thread 0): their max or their sum.
+template <int MODE, int NT = kThreads>
+__device__ __forceinline__ double combine_partials(const uint64_t* partials, int nb, double* sh_d,
+                                                   uint64_t* sh_u) {
+    if (MODE == kMaxMax || MODE == kL2Max) {
+        uint64_t m = 0;
+        for (int b = threadIdx.x; b < nb; b += NT) {
+            const uint64_t v = __ldcg(reinterpret_cast<const unsigned long long*>(partials + b));
+            m = v > m ? v : m;
+        }
+        m = block_max_bits<NT>(m, sh_u);
+        return __longlong_as_double(static_cast<long long>(m));
+    } else {
+        double s = 0.0;
+        for (int b = threadIdx.x; b < nb; b += NT)
+            s += __longlong_as_double(static_cast<long long>(
+                __ldcg(reinterpret_cast<const unsigned long long*>(partials + b))));
+        return block_sum<NT>(s, sh_d);
+    }
+}
+
+// The fp32 norm from the combined value: the max itself for (inf,inf), else the square root of
+// a sum ((2,2), (inf,2)) or of a max of column sums ((2,inf)).
+template <int MODE>
+__device__ __forceinline__ float norm_from_combined(double v) {
+    return static_cast<float>(MODE == kMaxMax ? v : sqrt(v));
+}
+
+// The block's partial, then, in the last of the nblk blocks of this norm to finish (completion
+// ticket, no waiting), the fixed-order combine of the partials and the fp32 norm.
 template <int MODE>
 __device__ __forceinline__ void norm_finalize(uint32_t maxbits, const ScaledSumSq& ssq,
                                               int64_t best_key, uint32_t bad_col, int64_t vb,
@@ -356,19 +406,7 @@ __device__ __forceinline__ void norm_finalize(uint32_t maxbits, const ScaledSumS
     __shared__ uint64_t sh_u[kThreads / 32];
     __shared__ bool is_last;
 
-    uint64_t part_bits;
-    if (MODE == kMaxMax) {
-        const double m = static_cast<double>(__uint_as_float(maxbits));
-        part_bits = block_max_bits(static_cast<uint64_t>(__double_as_longlong(m)), sh_u);
-    } else if (MODE == kL2Max) {
-        double m = best_key == INT64_MIN ? 0.0 : key_value(best_key);
-        if (bad_col) m = static_cast<double>(__uint_as_float(bad_col));
-        part_bits = block_max_bits(static_cast<uint64_t>(__double_as_longlong(m)), sh_u);
-    } else {
-        const double s = block_sum(ssq.value(), sh_d);
-        part_bits = static_cast<uint64_t>(__double_as_longlong(s));
-    }
-
+    const uint64_t part_bits = block_partial<MODE>(maxbits, ssq, best_key, bad_col, sh_d, sh_u);
     if (threadIdx.x == 0) {
         partials[vb] = part_bits;
         __threadfence();
@@ -380,28 +418,10 @@ __device__ __forceinline__ void norm_finalize(uint32_t maxbits, const ScaledSumS
     __threadfence();
 
     // Last block: combine the nblk partials in a fixed order.
-    const int nb = static_cast<int>(nblk);
-    double result;
-    if (MODE == kMaxMax || MODE == kL2Max) {
-        uint64_t m = 0;
-        for (int b = threadIdx.x; b < nb; b += kThreads) {
-            const uint64_t v = __ldcg(reinterpret_cast<const unsigned long long*>(partials + b));
-            m = v > m ? v : m;
-        }
-        m = block_max_bits(m, sh_u);
-        result = __longlong_as_double(static_cast<long long>(m));
-    } else {
-        double s = 0.0;
-        for (int b = threadIdx.x; b < nb; b += kThreads)
-            s += __longlong_as_double(
-                static_cast<long long>(__ldcg(reinterpret_cast<const unsigned long long*>(partials + b))));
-        result = block_sum(s, sh_d);
-    }
+    const double result = combine_partials<MODE>(partials, static_cast<int>(nblk), sh_d, sh_u);
     if (threadIdx.x == 0) {
         if (out.part_user) *out.part_user = result;  // combinable across ranks: a sum or a max
-        double nrm = result;
-        if (MODE != kMaxMax) nrm = sqrt(result);  // (2,2), (inf,2): sqrt of a sum; (2,inf): of a max
-        const float n32 = static_cast<float>(nrm);
+        const float n32 = norm_from_combined<MODE>(result);
         *out.norm = n32;
         if (out.norm_user) *out.norm_user = n32;
         if (out.scale) *out.scale = dequant_scale(out.scheme, n32, out.n, out.s);
@@ -1782,6 +1802,300 @@ quantize_seg_tma_kernel(const __grid_constant__ SegLaunch L, QuantArgs base, int
         float S[kQCols];
         quantize_group<T, SCHEME, 0, true>(static_cast<const T*>(sd.x), a, dc, g, nullptr, S);
         store_out(sd.out, nullptr, 0, base.out_dtype, g, sd.d, scale, S);
+    }
+}
+
+// ------------------------------------------------------------------------------------------
+// Single-launch form for problems whose n x d matrix fits in the grid's shared memory.  Each
+// block copies its slice of columns (all n rows, 16-byte aligned rows) into shared memory with
+// bulk copies, takes its partial of the norm from there, meets the other blocks at a grid
+// barrier (cooperative launch: every block resident; the wait is bounded), combines the partials
+// into the same norm in every block, and then quantises, sums over the workers and dequantises
+// from shared memory: the matrix crosses DRAM once, in one launch.  Random words, decisions and
+// outputs are those of the two-pass kernels; the (2,2) and (inf,2) norms are sums whose rounding
+// depends on how the blocks split them (the others are maxima and equal the two-pass norm).
+// ------------------------------------------------------------------------------------------
+constexpr int kResThreads = 512;
+constexpr int kResTileBytes = 200 * 1024;  // at most this much of a block's slice
+
+__device__ __forceinline__ unsigned int ld_acquire_u32(const unsigned int* p) {
+    unsigned int v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+// Barrier of the nblk blocks of a cooperative launch on two workspace words: the last block to
+// arrive resets the count and advances the generation the others wait on.  A block that waits
+// longer than kWaitLimitNs records GQ_ERR_TIMEOUT and gets false (the same in all its threads).
+__device__ __forceinline__ bool grid_barrier(unsigned int* count, unsigned int* gen,
+                                             unsigned int nblk, unsigned int* status,
+                                             volatile int* sh_flag) {
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        const unsigned int g = ld_acquire_u32(gen);  // read before arriving
+        __threadfence();                              // this block's writes before its arrival
+        bool ok = true;
+        if (atomicAdd(count, 1u) == nblk - 1) {
+            atomicExch(count, 0u);
+            __threadfence();
+            atomicAdd(gen, 1u);
+        } else {
+            const uint64_t t0 = global_ns();
+            while (ld_acquire_u32(gen) == g) {
+                if (global_ns() - t0 > kWaitLimitNs) {
+                    ok = false;
+                    break;
+                }
+                __nanosleep(64);
+            }
+            if (!ok) atomicCAS(status, 0u, kStatusTimeout);
+        }
+        __threadfence();
+        *sh_flag = ok ? 1 : 0;
+    }
+    __syncthreads();
+    return *sh_flag != 0;
+}
+
+// One element of a shared-memory tile, widened to fp32.
+__device__ __forceinline__ float smem_one(const float* p) { return *p; }
+__device__ __forceinline__ float smem_one(const uint16_t* p) {
+    return __uint_as_float(static_cast<uint32_t>(*p) << 16);
+}
+
+// Block b owns column groups [b gpb, (b + 1) gpb) of kQCols columns, all n rows, as an n x
+// (gpb kQCols) tile in dynamic shared memory.
+template <typename T, int SCHEME, int MODE>
+__global__ void __launch_bounds__(kResThreads, 1)
+resident_kernel(const T* __restrict__ x, QuantArgs a, int64_t gpb, void* __restrict__ out,
+                float* __restrict__ norm_user, unsigned char* __restrict__ ws) {
+    extern __shared__ __align__(128) unsigned char res_smem[];
+    __shared__ __align__(8) uint64_t bar;
+    __shared__ double sh_d[kResThreads / 32];
+    __shared__ uint64_t sh_u[kResThreads / 32];
+    __shared__ float sh_norm;
+    __shared__ volatile int sh_flag;
+    WsHeader* hdr = reinterpret_cast<WsHeader*>(ws);
+    uint64_t* partials = reinterpret_cast<uint64_t*>(ws + kHeaderBytes);
+    const int tid = threadIdx.x;
+    const int64_t n = a.n, d = a.d;
+    const int64_t groups = (d + kQCols - 1) / kQCols;
+    const int64_t g0 = static_cast<int64_t>(blockIdx.x) * gpb;
+    const int64_t ng = max(min(groups - g0, gpb), static_cast<int64_t>(0));
+    const int64_t c0 = g0 * kQCols;
+    const int64_t cols = ng > 0 ? min(d - c0, gpb * kQCols) : 0;  // columns present
+    const int64_t pitch = gpb * kQCols;                              // tile row, elements
+    const T* tile = reinterpret_cast<const T*>(res_smem);
+
+    // 1. the slice into shared memory: one bulk copy per row, counted on one mbarrier
+    if (tid == 0) {
+        mbar_init(smem_u32(&bar), 1u);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    __syncthreads();
+    bool ok = true;
+    if (ng > 0) {
+        const uint32_t row_bytes = static_cast<uint32_t>(cols * static_cast<int64_t>(sizeof(T)));
+        if (tid < 32) {
+            if (tid == 0)
+                mbar_arrive_expect_tx(smem_u32(&bar), static_cast<uint32_t>(n) * row_bytes);
+            __syncwarp();
+            for (int64_t i = tid; i < n; i += 32)
+                bulk_load(smem_u32(tile + i * pitch), x + i * d + c0, row_bytes, smem_u32(&bar));
+        }
+        ok = mbar_wait(smem_u32(&bar), 0u, kWaitLimitNs);
+    }
+    ok = __syncthreads_and(ok) != 0;
+    if (!ok) {
+        if (tid == 0) {
+            atomicCAS(&hdr->status, 0u, kStatusTimeout);
+            mbar_wait(smem_u32(&bar), 0u, kWaitLimitNs);  // let the copies in flight land
+        }
+    } else if (ng * kQCols > cols) {
+        // the ragged last group: zero the columns past d (they add nothing to the norm)
+        T* t = reinterpret_cast<T*>(res_smem);
+        for (int64_t e = tid; e < n * (ng * kQCols - cols); e += kResThreads) {
+            const int64_t i = e / (ng * kQCols - cols), c = cols + e % (ng * kQCols - cols);
+            t[i * pitch + c] = T(0);
+        }
+    }
+    __syncthreads();
+
+    // 2. this block's partial of the norm
+    uint32_t maxbits = 0;
+    ScaledSumSq ssq;
+    ssq.init();
+    int64_t best_key = INT64_MIN;
+    uint32_t bad_col = 0;
+    if (ok) {
+        for (int64_t gl = tid; gl < ng; gl += kResThreads) {
+            const T* col0 = tile + gl * kQCols;
+            if (MODE == kMaxMax || MODE == kL2L2 || MODE == kMaxL2) {
+                uint32_t colmax[kQCols];
+#pragma unroll
+                for (int c = 0; c < kQCols; ++c) colmax[c] = 0u;
+                for (int64_t i = 0; i < n; ++i) {
+                    float v[kQCols];
+                    const uint4* p = reinterpret_cast<const uint4*>(col0 + i * pitch);
+                    unstage<T>(p, p + 1, v);
+                    if (MODE == kL2L2) {
+                        ssq.add<kQCols>(v);
+                    } else {
+#pragma unroll
+                        for (int c = 0; c < kQCols; ++c) {
+                            const uint32_t b = __float_as_uint(v[c]) & 0x7FFFFFFFu;
+                            colmax[c] = b > colmax[c] ? b : colmax[c];
+                        }
+                    }
+                }
+                if (MODE == kMaxMax) {
+#pragma unroll
+                    for (int c = 0; c < kQCols; ++c) maxbits = colmax[c] > maxbits ? colmax[c] : maxbits;
+                } else if (MODE == kMaxL2) {
+                    float m[kQCols];
+#pragma unroll
+                    for (int c = 0; c < kQCols; ++c) m[c] = __uint_as_float(colmax[c]);
+                    ssq.add<kQCols>(m);
+                }
+            } else {
+                // (2, inf): column sums of squares with the arithmetic of norm_kernel (plain FMA
+                // into NA interleaved accumulators, row i into accumulator i mod NA, when
+                // n <= 16 NA; a scaled sum for the rest and for columns outside the normal range)
+                constexpr int NA = Elem<T>::kCols == 8 ? 2 : 4;
+                if (n <= 16 * NA) {
+                    float acc[NA][kQCols];
+#pragma unroll
+                    for (int q = 0; q < NA; ++q)
+#pragma unroll
+                        for (int c = 0; c < kQCols; ++c) acc[q][c] = 0.0f;
+                    for (int64_t i0 = 0; i0 < n; i0 += NA) {
+#pragma unroll
+                        for (int q = 0; q < NA; ++q) {
+                            if (i0 + q >= n) break;
+                            float v[kQCols];
+                            const uint4* p = reinterpret_cast<const uint4*>(col0 + (i0 + q) * pitch);
+                            unstage<T>(p, p + 1, v);
+#pragma unroll
+                            for (int c = 0; c < kQCols; ++c) acc[q][c] = __fmaf_rn(v[c], v[c], acc[q][c]);
+                        }
+                    }
+#pragma unroll
+                    for (int c = 0; c < kQCols; ++c) {
+                        float sum = acc[0][c];
+#pragma unroll
+                        for (int q = 1; q < NA; ++q) sum = sum + acc[q][c];
+                        if (sum >= 0x1p-100f && sum < __uint_as_float(kInfBits)) {
+                            const int64_t key = scaled_key(sum, 0);
+                            best_key = key > best_key ? key : best_key;
+                            continue;
+                        }
+                        if (sum == 0.0f) continue;
+                        ScaledSumSq cs;
+                        cs.init();
+                        for (int64_t i = 0; i < n; ++i) {
+                            const float one[1] = {smem_one(col0 + i * pitch + c)};
+                            cs.add<1>(one);
+                        }
+                        const float ssum = cs.sum();
+                        if (!(ssum < __uint_as_float(kInfBits))) {
+                            const uint32_t b = __float_as_uint(ssum) & 0x7FFFFFFFu;
+                            bad_col = b > bad_col ? b : bad_col;
+                        } else if (ssum > 0.0f) {
+                            const int64_t key = scaled_key(ssum, cs.e);
+                            best_key = key > best_key ? key : best_key;
+                        }
+                    }
+                } else {
+                    ScaledSumSq col[kQCols];
+#pragma unroll
+                    for (int c = 0; c < kQCols; ++c) col[c].init();
+                    for (int64_t i = 0; i < n; ++i) {
+                        float v[kQCols];
+                        const uint4* p = reinterpret_cast<const uint4*>(col0 + i * pitch);
+                        unstage<T>(p, p + 1, v);
+#pragma unroll
+                        for (int c = 0; c < kQCols; ++c) {
+                            const float one[1] = {v[c]};
+                            col[c].add<1>(one);
+                        }
+                    }
+#pragma unroll
+                    for (int c = 0; c < kQCols; ++c) {
+                        const float sum = col[c].sum();
+                        if (!(sum < __uint_as_float(kInfBits))) {
+                            const uint32_t b = __float_as_uint(sum) & 0x7FFFFFFFu;
+                            bad_col = b > bad_col ? b : bad_col;
+                        } else if (sum > 0.0f) {
+                            const int64_t key = scaled_key(sum, col[c].e);
+                            best_key = key > best_key ? key : best_key;
+                        }
+                    }
+                }
+            }
+        }
+    }
+
+    // 3. the partials of all blocks, the same norm in every block
+    const uint64_t part =
+        block_partial<MODE, kResThreads>(maxbits, ssq, best_key, bad_col, sh_d, sh_u);
+    if (tid == 0) partials[blockIdx.x] = part;
+    if (!grid_barrier(&hdr->bar_count, &hdr->bar_gen, gridDim.x, &hdr->status, &sh_flag)) return;
+    const double comb =
+        combine_partials<MODE, kResThreads>(partials, static_cast<int>(gridDim.x), sh_d, sh_u);
+    if (tid == 0) {
+        const float n32 = norm_from_combined<MODE>(comb);
+        sh_norm = n32;
+        if (blockIdx.x == 0) {
+            hdr->norm = n32;
+            if (norm_user) *norm_user = n32;
+            if (!(fabsf(n32) < __uint_as_float(kInfBits))) atomicCAS(&hdr->status, 0u, 4u);
+        }
+    }
+    __syncthreads();
+    if (!ok) return;
+    const float nrm = sh_norm;
+    const bool live = nrm > 0.0f && nrm < __uint_as_float(kInfBits);
+    const float scale = dequant_scale(SCHEME, nrm, n, a.s);
+    const Decide dc = make_decide<SCHEME>(nrm, a.s);
+
+    // 4. quantise, sum over the workers and dequantise, two rows per decision
+    for (int64_t gl = tid; gl < ng; gl += kResThreads) {
+        const int64_t g = g0 + gl;
+        float S[kQCols];
+#pragma unroll
+        for (int c = 0; c < kQCols; ++c) S[c] = 0.0f;
+        if (live) {
+            const uint32_t g32 = static_cast<uint32_t>(g);
+            const PhiloxGroup pg = philox_group(g32, a.step_lo, a.step_hi, a.rk);
+            const T* col0 = tile + gl * kQCols;
+            for (int64_t r0 = 0; r0 < n; r0 += 2) {
+                float v[2][kQCols];
+                uint32_t aw[2][4];
+#pragma unroll
+                for (int u = 0; u < 2; ++u) {
+                    if (r0 + u < n) {
+                        const uint4* p = reinterpret_cast<const uint4*>(col0 + (r0 + u) * pitch);
+                        unstage<T>(p, p + 1, v[u]);
+                    } else {
+#pragma unroll
+                        for (int c = 0; c < kQCols; ++c) v[u][c] = 0.0f;
+                    }
+                    const uint4 ra = philox_row(pg, static_cast<uint32_t>(r0 + u) + a.row0,
+                                                a.step_lo, a.rk);
+                    aw[u][0] = ra.x; aw[u][1] = ra.y; aw[u][2] = ra.z; aw[u][3] = ra.w;
+                }
+                uint32_t yk[2][kQCols];
+                decide_rows<SCHEME, true, 2>(v, dc, a, g32, static_cast<uint32_t>(r0) + a.row0,
+                                             aw, yk);
+#pragma unroll
+                for (int u = 0; u < 2; ++u) {
+                    if (r0 + u >= n) break;
+                    int32_t code[kQCols];
+                    accumulate_row<SCHEME>(v[u], yk[u], S, code);
+                }
+            }
+        }
+        store_out(out, nullptr, 0, a.out_dtype, g, d, scale, S);
     }
 }
 

@@ -81,6 +81,62 @@ gq_status run_quant_segments(gq::SegLaunch& L, const int64_t* d, int64_t n,
 }
 
 
+// ---- single launch for problems that fit in shared memory ------------------------------------
+template <typename T, int SCHEME, int MODE>
+gq_status launch_resident(const T* x, const gq::QuantArgs& a, int64_t gpb, unsigned nblk,
+                          size_t smem, void* out, float* norm_user, unsigned char* ws,
+                          cudaStream_t st) {
+    auto k = gq::resident_kernel<T, SCHEME, MODE>;
+    if (blocks_per_sm(k, gq::kResTileBytes, gq::kResThreads) < 1) return GQ_ERR_CUDA;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(nblk);
+    cfg.blockDim = dim3(gq::kResThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeCooperative;  // all blocks resident: they wait on each other
+    attr[0].val.cooperative = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, k, x, a, gpb, out, norm_user, ws) == cudaSuccess ? GQ_OK
+                                                                                     : GQ_ERR_CUDA;
+}
+
+// The fused call in one launch when the problem fits (aligned rows, no codes requested):
+// *taken tells whether it ran.  A cooperative launch the device refuses (too many blocks for
+// what is free of it) is not taken, and the two-pass form runs instead.
+template <typename T, int SCHEME>
+gq_status run_resident(const void* grads, const gq::QuantArgs& a, int mode, void* out,
+                       float* norm_user, unsigned char* ws, cudaStream_t st, bool* taken) {
+    int64_t gpb = 0;
+    unsigned nblk = 0;
+    size_t smem = 0;
+    *taken = false;
+    if (!a.vec_rows || !resident_plan(a.n, a.d, static_cast<int>(sizeof(T)), &gpb, &nblk, &smem))
+        return GQ_OK;
+    const T* x = static_cast<const T*>(grads);
+    gq_status st_launch;
+    switch (mode) {
+        case gq::kMaxMax:
+            st_launch = launch_resident<T, SCHEME, gq::kMaxMax>(x, a, gpb, nblk, smem, out, norm_user, ws, st);
+            break;
+        case gq::kL2L2:
+            st_launch = launch_resident<T, SCHEME, gq::kL2L2>(x, a, gpb, nblk, smem, out, norm_user, ws, st);
+            break;
+        case gq::kL2Max:
+            st_launch = launch_resident<T, SCHEME, gq::kL2Max>(x, a, gpb, nblk, smem, out, norm_user, ws, st);
+            break;
+        default:
+            st_launch = launch_resident<T, SCHEME, gq::kMaxL2>(x, a, gpb, nblk, smem, out, norm_user, ws, st);
+    }
+    if (st_launch != GQ_OK) {
+        cudaGetLastError();  // a refused launch leaves no lasting error
+        return GQ_OK;
+    }
+    *taken = true;
+    return GQ_OK;
+}
+
 template <typename T, int SCHEME>
 gq_status quant_entry(const void* grads, const gq::QuantArgs& a, int bits, bool out, bool trusted,
                       void* codes, void* outp, cudaStream_t st, unsigned int* status) {
@@ -102,4 +158,9 @@ gq_status quant_entry(const void* grads, const gq::QuantArgs& a, int bits, bool 
                                          const gq::QuantArgs& base, unsigned char* ws,             \
                                          cudaStream_t st) {                                        \
         return run_quant_segments<T, SCHEME>(L, d, n, base, ws, st);                               \
+    }                                                                                              \
+    gq_status gqh::resident_##NAME(const void* grads, const gq::QuantArgs& a, int mode, void* out, \
+                                   float* norm_user, unsigned char* ws, cudaStream_t st,           \
+                                   bool* taken) {                                                  \
+        return run_resident<T, SCHEME>(grads, a, mode, out, norm_user, ws, st, taken);             \
     }

@@ -88,8 +88,9 @@ int gq_abi_version(void);
 
 /* Bytes of workspace the norm step needs for an n x d problem (a small constant today,
  * 36,096 bytes).  The workspace holds the device status word, the block partials of the norm,
- * a completion ticket and the last norm, and per-segment tickets, norms and dequantisation
- * scales for gq_allreduce_mean_segments. */
+ * a completion ticket and the last norm, the grid-barrier words of the single-launch form of
+ * gq_allreduce_mean, and per-segment tickets, norms and dequantisation scales for
+ * gq_allreduce_mean_segments. */
 size_t gq_workspace_bytes(int64_t n, int64_t d);
 
 /* Zero a freshly allocated workspace (enqueued on `stream`).  Required once before its first
@@ -98,6 +99,11 @@ gq_status gq_workspace_init(void *ws, size_t ws_bytes, void *stream);
 
 /* 4 or 8: bits per stored code for this scheme and s; 0 if s is unsupported. */
 int gq_code_bits(int scheme, int s);
+
+/* Kernel launches of one gq_allreduce_mean call on the current device for an n x d matrix of
+ * dtype, with (with_codes != 0) or without a code output: 1 for the single-launch form, 2 for
+ * the norm pass + quantise pass; 0 for invalid sizes.  (16-byte aligned grads assumed.) */
+int gq_fused_launches(int dtype, int64_t n, int64_t d, int with_codes);
 
 /* Row pitch of the code matrix in elements: round_up(d, 32); 0 if d < 1. */
 int64_t gq_code_pitch(int64_t d);
@@ -169,6 +175,18 @@ gq_status gq_dequantize_sums(const void *sum_dev, int sum_type, const float *nor
  * out written once.  norm_dev (nullable) receives the fp32 norm; codes (nullable) receives the
  * code matrix as gq_quantize would write it.  Bit-identical to gq_global_norm + gq_quantize +
  * gq_reduce_codes + gq_dequantize on the same stream.
+ *
+ * Small problems take one launch instead (gq_fused_launches says which): when codes is NULL,
+ * the rows are 16-byte aligned (d a multiple of 4 for fp32, 8 for bf16) and the matrix fits in
+ * the GPU's shared memory (n * 8 * ceil(ceil(d / 8) / SMs) * element bytes <= 204,800: about
+ * 30 MB on 152 SMs), each SM holds its slice of columns on chip, the blocks meet at a grid
+ * barrier (cooperative launch; the wait is bounded and reports GQ_ERR_TIMEOUT) to combine the
+ * norm, and X is read once.  Decisions, random words and outputs are the same; for the
+ * (inf, inf) and (2, inf) norms (maxima) the norm is bit-identical too, while the (2, 2) and
+ * (inf, 2) norms are sums that the single launch splits differently, so their last bits may
+ * differ from gq_global_norm's (both within its error bound): the outputs are then exactly
+ * those of gq_allreduce_mean_with_norm given the norm written to norm_dev.  Calls that share a
+ * workspace must not overlap on the GPU (they share its completion ticket and barrier words).
  */
 gq_status gq_allreduce_mean(const void *grads, int dtype, int64_t n, int64_t d, int q, int p,
                             int scheme, int s, uint64_t seed, uint64_t step, float *out_dev,

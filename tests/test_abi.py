@@ -60,6 +60,22 @@ def test_host_only_functions():
     assert gq.gq_status_string(99) == "unknown status"
 
 
+def test_fused_launch_count_query():
+    """One launch for small aligned problems without a code output, two otherwise (far from the
+    size boundary, which depends on the SM count); 0 for invalid arguments."""
+    import allreduce_compatible_gradient_gb300 as gq
+    assert gq.gq_fused_launches(gq.F32, 4, 65_536) == 1
+    assert gq.gq_fused_launches(gq.BF16, 8, 1 << 20) == 1
+    assert gq.gq_fused_launches(gq.F32, 4, 65_536, with_codes=True) == 2
+    assert gq.gq_fused_launches(gq.F32, 4, 65_538) == 2   # rows not 16-byte aligned
+    assert gq.gq_fused_launches(gq.BF16, 4, 65_540) == 2  # (8 bf16 per 16 bytes)
+    assert gq.gq_fused_launches(gq.F32, 8, 25_557_032) == 2
+    assert gq.gq_fused_launches(gq.F32, 1 << 20, 8) == 2
+    assert gq.gq_fused_launches(gq.F16, 4, 64) == 0      # not a gradient type
+    assert gq.gq_fused_launches(gq.F32, 0, 64) == 0
+    assert gq.gq_fused_launches(gq.F32, 4, 0) == 0
+
+
 def test_argument_checks_return_before_any_device_call(lib):
     import torch
     if torch.cuda.is_available():
