@@ -351,10 +351,10 @@ gq_status gq_get_status(void* ws, void* stream) {
         if (cudaMemcpy(&hdr->status, &zero, sizeof zero, cudaMemcpyHostToDevice) != cudaSuccess)
             return GQ_ERR_CUDA;
         // a wait that gave up may have left a completion ticket or the grid barrier's arrival
-        // count short of a full set: start both again from zero
+        // counts short of a full set: start them again from zero
         if (v == GQ_ERR_TIMEOUT &&
             (cudaMemcpy(&hdr->ticket, &zero, sizeof zero, cudaMemcpyHostToDevice) != cudaSuccess ||
-             cudaMemcpy(&hdr->bar_count, &zero, sizeof zero, cudaMemcpyHostToDevice) != cudaSuccess))
+             cudaMemcpy(&hdr->bar, &zero, sizeof zero, cudaMemcpyHostToDevice) != cudaSuccess))
             return GQ_ERR_CUDA;
     }
     return static_cast<gq_status>(v);

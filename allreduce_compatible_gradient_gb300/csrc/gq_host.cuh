@@ -112,6 +112,7 @@ inline bool resident_plan(int64_t n, int64_t d, int elt, int64_t* gpb, unsigned*
     const int64_t groups = (d + gq::kQCols - 1) / gq::kQCols;
     const int64_t nsm = sm_count();
     const int64_t g = (groups + nsm - 1) / nsm;
+    if (nsm > 255) return false;  // the grid barrier counts arrivals in 8 bits
     if (n > gq::kResTileBytes / (g * gq::kQCols * elt)) return false;
     *gpb = g;
     *nblk = static_cast<unsigned>((groups + g - 1) / g);

@@ -36,9 +36,8 @@ struct WsHeader {
     unsigned int status;  // sticky device-detected status (0 = ok)
     unsigned int ticket;  // blocks of the running norm kernel that have finished; 0 between calls
     float norm;           // fp32 norm written by the last norm kernel
-    unsigned int bar_count;  // grid barrier of the single-launch kernel: blocks arrived (0 between)
-    unsigned int bar_gen;    // and its generation (advances by one per barrier)
-    unsigned int pad[59];
+    unsigned int bar;     // grid barrier of the single-launch kernel: generation << 8 | arrivals
+    unsigned int pad[60];
 };
 static_assert(sizeof(WsHeader) == kHeaderBytes, "workspace header is 256 bytes");
 
@@ -274,9 +273,10 @@ struct ScaledSumSq {
         kahan_add(sq[0]);
     }
     __device__ __forceinline__ float sum() const { return acc - comp; }
-    // The sum as fp64, scale removed.
+    // The sum as fp64, scale removed: times 2^(2E), |2E| <= 300, an exact power of two in fp64.
     __device__ __forceinline__ double value() const {
-        return ldexp(static_cast<double>(acc) - static_cast<double>(comp), 2 * e);
+        const double p2 = __longlong_as_double(static_cast<long long>(2 * e + 1023) << 52);
+        return (static_cast<double>(acc) - static_cast<double>(comp)) * p2;
     }
 };
 
@@ -1824,37 +1824,74 @@ __device__ __forceinline__ unsigned int ld_acquire_u32(const unsigned int* p) {
     return v;
 }
 
-// Barrier of the nblk blocks of a cooperative launch on two workspace words: the last block to
-// arrive resets the count and advances the generation the others wait on.  A block that waits
-// longer than kWaitLimitNs records GQ_ERR_TIMEOUT and gets false (the same in all its threads).
-__device__ __forceinline__ bool grid_barrier(unsigned int* count, unsigned int* gen,
-                                             unsigned int nblk, unsigned int* status,
+__device__ __forceinline__ unsigned int atom_add_acq_rel(unsigned int* p, unsigned int v) {
+    unsigned int old;
+    asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v)
+                 : "memory");
+    return old;
+}
+__device__ __forceinline__ void red_add_release(unsigned int* p, unsigned int v) {
+    asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+// Barrier of the nblk (< 256) blocks of a cooperative launch on one workspace word holding
+// generation << 8 | arrivals.  Thread 0 of each block arrives with an acquire-release add
+// (releasing the block's writes made by thread 0); the last arrival adds 256 - nblk, which
+// clears the arrivals and advances the generation in one release, and the others wait, with
+// acquire loads, for the generation to move.  Only writes of thread 0 before the barrier are
+// published to the other blocks.  A block that waits longer than kWaitLimitNs records
+// GQ_ERR_TIMEOUT and gets false (the same in all its threads).
+__device__ __forceinline__ bool grid_barrier(WsHeader* hdr, unsigned int nblk,
                                              volatile int* sh_flag) {
     __syncthreads();
     if (threadIdx.x == 0) {
-        const unsigned int g = ld_acquire_u32(gen);  // read before arriving
-        __threadfence();                              // this block's writes before its arrival
+        const unsigned int old = atom_add_acq_rel(&hdr->bar, 1u);
         bool ok = true;
-        if (atomicAdd(count, 1u) == nblk - 1) {
-            atomicExch(count, 0u);
-            __threadfence();
-            atomicAdd(gen, 1u);
+        if ((old & 0xFFu) == nblk - 1u) {
+            red_add_release(&hdr->bar, 256u - nblk);
         } else {
+            const unsigned int gen = old >> 8;
             const uint64_t t0 = global_ns();
-            while (ld_acquire_u32(gen) == g) {
+            while ((ld_acquire_u32(&hdr->bar) >> 8) == gen) {
                 if (global_ns() - t0 > kWaitLimitNs) {
                     ok = false;
                     break;
                 }
-                __nanosleep(64);
+                __nanosleep(20);
             }
-            if (!ok) atomicCAS(status, 0u, kStatusTimeout);
+            if (!ok) atomicCAS(&hdr->status, 0u, kStatusTimeout);
         }
-        __threadfence();
         *sh_flag = ok ? 1 : 0;
     }
     __syncthreads();
     return *sh_flag != 0;
+}
+
+// The fixed-order combine of nb block partials by one warp (valid in lane 0): their max or sum.
+template <int MODE>
+__device__ __forceinline__ double warp_combine(const uint64_t* partials, int nb) {
+    const int lane = threadIdx.x & 31;
+    if (MODE == kMaxMax || MODE == kL2Max) {
+        uint64_t m = 0;
+        for (int b = lane; b < nb; b += 32) {
+            const uint64_t v = __ldcg(reinterpret_cast<const unsigned long long*>(partials + b));
+            m = v > m ? v : m;
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            const uint64_t t = __shfl_down_sync(0xFFFFFFFFu, m, o);
+            m = t > m ? t : m;
+        }
+        return __longlong_as_double(static_cast<long long>(m));
+    } else {
+        double v = 0.0;
+        for (int b = lane; b < nb; b += 32)
+            v += __longlong_as_double(static_cast<long long>(
+                __ldcg(reinterpret_cast<const unsigned long long*>(partials + b))));
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) v += __shfl_down_sync(0xFFFFFFFFu, v, o);
+        return v;
+    }
 }
 
 // One element of a shared-memory tile, widened to fp32.
@@ -1873,8 +1910,10 @@ resident_kernel(const T* __restrict__ x, QuantArgs a, int64_t gpb, void* __restr
     __shared__ __align__(8) uint64_t bar;
     __shared__ double sh_d[kResThreads / 32];
     __shared__ uint64_t sh_u[kResThreads / 32];
-    __shared__ float sh_norm;
+    __shared__ float sh_norm, sh_scale;
+    __shared__ Decide sh_dc;
     __shared__ volatile int sh_flag;
+    __shared__ float sh_S[kResThreads / 2][kQCols];  // split row pairs' sums (ng <= 256)
     WsHeader* hdr = reinterpret_cast<WsHeader*>(ws);
     uint64_t* partials = reinterpret_cast<uint64_t*>(ws + kHeaderBytes);
     const int tid = threadIdx.x;
@@ -1887,7 +1926,8 @@ resident_kernel(const T* __restrict__ x, QuantArgs a, int64_t gpb, void* __restr
     const int64_t pitch = gpb * kQCols;                              // tile row, elements
     const T* tile = reinterpret_cast<const T*>(res_smem);
 
-    // 1. the slice into shared memory: one bulk copy per row, counted on one mbarrier
+    // 1. the slice into shared memory: bulk copies of up to 8 KB of a row, issued by the lanes
+    // of the first warp and counted on one mbarrier
     if (tid == 0) {
         mbar_init(smem_u32(&bar), 1u);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -1895,13 +1935,21 @@ resident_kernel(const T* __restrict__ x, QuantArgs a, int64_t gpb, void* __restr
     __syncthreads();
     bool ok = true;
     if (ng > 0) {
+        constexpr uint32_t kPiece = 8192;
         const uint32_t row_bytes = static_cast<uint32_t>(cols * static_cast<int64_t>(sizeof(T)));
+        const uint32_t pieces = (row_bytes + kPiece - 1) / kPiece;  // per row
         if (tid < 32) {
             if (tid == 0)
                 mbar_arrive_expect_tx(smem_u32(&bar), static_cast<uint32_t>(n) * row_bytes);
             __syncwarp();
-            for (int64_t i = tid; i < n; i += 32)
-                bulk_load(smem_u32(tile + i * pitch), x + i * d + c0, row_bytes, smem_u32(&bar));
+            for (uint32_t q = tid; q < static_cast<uint32_t>(n) * pieces; q += 32) {
+                const uint32_t i = q / pieces, k = q - i * pieces;
+                const uint32_t off = k * kPiece;  // bytes into the row, a multiple of 16
+                const uint32_t len = min(kPiece, row_bytes - off);
+                bulk_load(smem_u32(reinterpret_cast<const unsigned char*>(tile + i * pitch) + off),
+                          reinterpret_cast<const unsigned char*>(x + i * d + c0) + off, len,
+                          smem_u32(&bar));
+            }
         }
         ok = mbar_wait(smem_u32(&bar), 0u, kWaitLimitNs);
     }
@@ -1927,10 +1975,30 @@ resident_kernel(const T* __restrict__ x, QuantArgs a, int64_t gpb, void* __restr
     ssq.init();
     int64_t best_key = INT64_MIN;
     uint32_t bad_col = 0;
-    if (ok) {
+    if (ok && (MODE == kMaxMax || MODE == kL2L2)) {
+        // these two do not depend on the column: the tile's n x (8 ng) elements, 16 bytes per
+        // thread step, all threads busy however few the column groups
+        constexpr int V = 16 / static_cast<int>(sizeof(T));
+        const uint32_t vrow = static_cast<uint32_t>(ng * kQCols / V);
+        const uint32_t nv = static_cast<uint32_t>(n) * vrow;  // <= 200 KB / 16
+        for (uint32_t e = tid; e < nv; e += kResThreads) {
+            const uint32_t i = e / vrow, vc = e - i * vrow;
+            float v[Elem<T>::kCols];
+            widen16<T>(*reinterpret_cast<const uint4*>(tile + i * pitch + vc * V), v);
+            if (MODE == kMaxMax) {
+#pragma unroll
+                for (int c = 0; c < Elem<T>::kCols; ++c) {
+                    const uint32_t b = __float_as_uint(v[c]) & 0x7FFFFFFFu;
+                    maxbits = b > maxbits ? b : maxbits;
+                }
+            } else {
+                ssq.add<Elem<T>::kCols>(v);
+            }
+        }
+    } else if (ok) {
         for (int64_t gl = tid; gl < ng; gl += kResThreads) {
             const T* col0 = tile + gl * kQCols;
-            if (MODE == kMaxMax || MODE == kL2L2 || MODE == kMaxL2) {
+            if (MODE == kMaxL2) {
                 uint32_t colmax[kQCols];
 #pragma unroll
                 for (int c = 0; c < kQCols; ++c) colmax[c] = 0u;
@@ -1938,25 +2006,16 @@ resident_kernel(const T* __restrict__ x, QuantArgs a, int64_t gpb, void* __restr
                     float v[kQCols];
                     const uint4* p = reinterpret_cast<const uint4*>(col0 + i * pitch);
                     unstage<T>(p, p + 1, v);
-                    if (MODE == kL2L2) {
-                        ssq.add<kQCols>(v);
-                    } else {
 #pragma unroll
-                        for (int c = 0; c < kQCols; ++c) {
-                            const uint32_t b = __float_as_uint(v[c]) & 0x7FFFFFFFu;
-                            colmax[c] = b > colmax[c] ? b : colmax[c];
-                        }
+                    for (int c = 0; c < kQCols; ++c) {
+                        const uint32_t b = __float_as_uint(v[c]) & 0x7FFFFFFFu;
+                        colmax[c] = b > colmax[c] ? b : colmax[c];
                     }
                 }
-                if (MODE == kMaxMax) {
+                float m[kQCols];
 #pragma unroll
-                    for (int c = 0; c < kQCols; ++c) maxbits = colmax[c] > maxbits ? colmax[c] : maxbits;
-                } else if (MODE == kMaxL2) {
-                    float m[kQCols];
-#pragma unroll
-                    for (int c = 0; c < kQCols; ++c) m[c] = __uint_as_float(colmax[c]);
-                    ssq.add<kQCols>(m);
-                }
+                for (int c = 0; c < kQCols; ++c) m[c] = __uint_as_float(colmax[c]);
+                ssq.add<kQCols>(m);
             } else {
                 // (2, inf): column sums of squares with the arithmetic of norm_kernel (plain FMA
                 // into NA interleaved accumulators, row i into accumulator i mod NA, when
@@ -2039,12 +2098,14 @@ resident_kernel(const T* __restrict__ x, QuantArgs a, int64_t gpb, void* __restr
     const uint64_t part =
         block_partial<MODE, kResThreads>(maxbits, ssq, best_key, bad_col, sh_d, sh_u);
     if (tid == 0) partials[blockIdx.x] = part;
-    if (!grid_barrier(&hdr->bar_count, &hdr->bar_gen, gridDim.x, &hdr->status, &sh_flag)) return;
-    const double comb =
-        combine_partials<MODE, kResThreads>(partials, static_cast<int>(gridDim.x), sh_d, sh_u);
-    if (tid == 0) {
+    if (!grid_barrier(hdr, gridDim.x, &sh_flag)) return;
+    double comb = 0.0;
+    if (tid < 32) comb = warp_combine<MODE>(partials, static_cast<int>(gridDim.x));
+    if (tid == 0) {  // the norm, the scale and the decision constants once per block
         const float n32 = norm_from_combined<MODE>(comb);
         sh_norm = n32;
+        sh_scale = dequant_scale(SCHEME, n32, n, a.s);
+        sh_dc = make_decide<SCHEME>(n32, a.s);
         if (blockIdx.x == 0) {
             hdr->norm = n32;
             if (norm_user) *norm_user = n32;
@@ -2055,11 +2116,23 @@ resident_kernel(const T* __restrict__ x, QuantArgs a, int64_t gpb, void* __restr
     if (!ok) return;
     const float nrm = sh_norm;
     const bool live = nrm > 0.0f && nrm < __uint_as_float(kInfBits);
-    const float scale = dequant_scale(SCHEME, nrm, n, a.s);
-    const Decide dc = make_decide<SCHEME>(nrm, a.s);
+    const float scale = sh_scale;
+    const Decide dc = sh_dc;
 
-    // 4. quantise, sum over the workers and dequantise, two rows per decision
-    for (int64_t gl = tid; gl < ng; gl += kResThreads) {
+    // 4. quantise, sum over the workers and dequantise, two rows per decision.  With fewer
+    // column groups than half the threads, each group's row pairs are split P ways and the
+    // partial sums (exact integers in fp32, so the order of the additions does not matter)
+    // meet in shared memory.
+    const int64_t npairs = (n + 1) / 2;
+    int64_t P = 1;
+    if (ng <= kResThreads / 2) P = min(npairs, static_cast<int64_t>(kResThreads) / ng);
+    if (P > 1) {
+        for (int64_t e = tid; e < ng * kQCols; e += kResThreads) sh_S[e / kQCols][e % kQCols] = 0.0f;
+        __syncthreads();
+    }
+    for (int64_t u = tid; u < ng * P; u += kResThreads) {
+        const uint32_t u32 = static_cast<uint32_t>(u), ng32 = static_cast<uint32_t>(ng);
+        const int64_t part = u32 / ng32, gl = u32 - static_cast<uint32_t>(part) * ng32;
         const int64_t g = g0 + gl;
         float S[kQCols];
 #pragma unroll
@@ -2068,7 +2141,7 @@ resident_kernel(const T* __restrict__ x, QuantArgs a, int64_t gpb, void* __restr
             const uint32_t g32 = static_cast<uint32_t>(g);
             const PhiloxGroup pg = philox_group(g32, a.step_lo, a.step_hi, a.rk);
             const T* col0 = tile + gl * kQCols;
-            for (int64_t r0 = 0; r0 < n; r0 += 2) {
+            for (int64_t r0 = 2 * part; r0 < n; r0 += 2 * P) {
                 float v[2][kQCols];
                 uint32_t aw[2][4];
 #pragma unroll
@@ -2095,7 +2168,21 @@ resident_kernel(const T* __restrict__ x, QuantArgs a, int64_t gpb, void* __restr
                 }
             }
         }
-        store_out(out, nullptr, 0, a.out_dtype, g, d, scale, S);
+        if (P == 1) {
+            store_out(out, nullptr, 0, a.out_dtype, g, d, scale, S);
+        } else {
+#pragma unroll
+            for (int c = 0; c < kQCols; ++c) atomicAdd(&sh_S[gl][c], S[c]);
+        }
+    }
+    if (P > 1) {
+        __syncthreads();
+        for (int64_t gl = tid; gl < ng; gl += kResThreads) {
+            float S[kQCols];
+#pragma unroll
+            for (int c = 0; c < kQCols; ++c) S[c] = sh_S[gl][c];
+            store_out(out, nullptr, 0, a.out_dtype, g0 + gl, d, scale, S);
+        }
     }
 }
 
