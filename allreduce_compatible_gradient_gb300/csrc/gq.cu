@@ -59,12 +59,14 @@ int norm_mode(int q, int p) {
 
 // ---- norm ---------------------------------------------------------------------------------
 // Blocks of the norm step for an n x d problem (the flat kernel for the (inf,inf) and (2,2)
-// forms, whose threads take eight 16-byte vectors per iteration; the per-column kernel else).
+// forms, whose threads take sixteen or eight 16-byte vectors per iteration; the per-column
+// kernel else).
 template <typename T, int MODE>
 unsigned norm_grid(int64_t n, int64_t d) {
     constexpr int C = gq::Elem<T>::kCols;
+    constexpr int U = MODE == gq::kMaxMax ? 16 : 8;
     if constexpr (MODE == gq::kMaxMax || MODE == gq::kL2L2)
-        return grid_for(gq::norm_flat_kernel<T, MODE>, (n * d / C + 7) / 8, gq::kMaxPartials);
+        return grid_for(gq::norm_flat_kernel<T, MODE>, (n * d / C + U - 1) / U, gq::kMaxPartials);
     else
         return grid_for(gq::norm_kernel<T, MODE>, (d + C - 1) / C, gq::kMaxPartials);
 }

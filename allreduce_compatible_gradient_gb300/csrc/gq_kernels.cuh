@@ -608,14 +608,14 @@ norm_kernel(const T* __restrict__ x, int64_t n, int64_t d, int64_t groups, bool 
 
 // The (inf, inf) and (2, 2) norms do not depend on which coordinate an element belongs to: they
 // are the max |x| and the sum of squares over all n d elements, read here as one flat array
-// (eight 16-byte loads in flight per thread whatever n is).
+// (sixteen 16-byte loads in flight per thread for (inf, inf), eight for (2, 2), whatever n is).
 template <typename T, int MODE>
 __global__ void __launch_bounds__(kThreads, 4)
 norm_flat_kernel(const T* __restrict__ x, int64_t total, float* __restrict__ norm_user,
                  double* __restrict__ part_user, unsigned char* __restrict__ ws) {
     static_assert(MODE == kMaxMax || MODE == kL2L2, "flat norms: (inf, inf) and (2, 2)");
     constexpr int C = Elem<T>::kCols;
-    constexpr int U = 8;
+    constexpr int U = MODE == kMaxMax ? 16 : 8;  // 16-byte loads in flight per thread
     WsHeader* hdr = reinterpret_cast<WsHeader*>(ws);
     const NormSlots slots{reinterpret_cast<uint64_t*>(ws + kHeaderBytes), &hdr->ticket,
                           &hdr->status, &hdr->norm, norm_user, part_user};
@@ -897,7 +897,11 @@ __device__ __forceinline__ void decide_rows(const float (&xv)[R][kQCols], const 
     }
     // exact path (the correctly rounded quotient and the full word) for an uncertain element,
     // a Global-L level index above s, a NaN, or every element when the norm is out of the fast
-    // path's range
+    // path's range; one test for all R rows first (almost always none needs it)
+    uint32_t wall = worst[0];
+#pragma unroll
+    for (int u = 1; u < R; ++u) wall = __vmaxu2(wall, worst[u]);
+    if ((wall & 0xFFFFu) <= 0xFFFBu && !(SCHEME == kLinear && (wall >> 16) > a.s + kOff)) return;
 #pragma unroll
     for (int u = 0; u < R; ++u) {
         const bool over = SCHEME == kLinear && (worst[u] >> 16) > a.s + kOff;
