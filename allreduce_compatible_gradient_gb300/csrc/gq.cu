@@ -140,6 +140,7 @@ gq::QuantArgs make_args(const float* norm_ptr, int dtype, int64_t n, int64_t d, 
     a.sums = nullptr;
     a.sums_i8 = 0;
     a.out_dtype = gq::kOutF32;
+    a.smallk = 0;
     return a;
 }
 
@@ -289,6 +290,7 @@ gq_status gq_allreduce_mean_to(const void* grads, int dtype, int64_t n, int64_t 
     const float* ws_norm = &reinterpret_cast<const gq::WsHeader*>(ws)->norm;
     gq::QuantArgs a = make_args(ws_norm, dtype, n, d, s, seed, step);
     a.out_dtype = out_dtype;
+    a.smallk = mode == gq::kL2L2;  // under the (2,2) norm Global-E levels above 1 are rare
     if (!codes) {  // small problems: one launch, the matrix read once
         unsigned char* w = static_cast<unsigned char*>(ws);
         bool taken = false;

@@ -774,6 +774,7 @@ struct QuantArgs {
     void* sums;              // when set, the kernel writes the integer sums here instead of out
     int sums_i8;             // 1: the sums as int8 (they fit: |sum| <= 127), 0: as int32
     int out_dtype;           // kOutF32, kOutBF16 or kOutF16
+    int smallk;              // host hint: Global-E levels above 1 are rare (the (2,2) norm)
 };
 
 // Per-block fp32 dequantisation scale from the fp32 norm, computed in fp64 by one thread:
@@ -841,7 +842,7 @@ __device__ __forceinline__ Decide make_decide(float nrm, uint32_t s) {
 // scratch).  The rare exact path runs for a row only if one of its elements needs it, and then
 // only for those elements (one extra Philox call for the row).
 template <int SCHEME, bool TRUSTED, int R>
-__device__ __forceinline__ void decide_rows(const float (&xv)[R][kQCols], const Decide& dc,
+__device__ __forceinline__ uint32_t decide_rows(const float (&xv)[R][kQCols], const Decide& dc,
                                             const QuantArgs& a, uint32_t g32, uint32_t row0,
                                             const uint32_t (&aw)[R][4],
                                             uint32_t (&yk)[R][kQCols]) {
@@ -898,10 +899,16 @@ __device__ __forceinline__ void decide_rows(const float (&xv)[R][kQCols], const 
     // exact path (the correctly rounded quotient and the full word) for an uncertain element,
     // a Global-L level index above s, a NaN, or every element when the norm is out of the fast
     // path's range; one test for all R rows first (almost always none needs it)
+    uint32_t big = 0;  // returned: Global-E rows that may hold a level index of 2 or more
+    if (SCHEME == kExp) {
+#pragma unroll
+        for (int u = 0; u < R; ++u) big |= (worst[u] >= ((kOff + 2u) << 16) ? 1u : 0u) << u;
+    }
     uint32_t wall = worst[0];
 #pragma unroll
     for (int u = 1; u < R; ++u) wall = __vmaxu2(wall, worst[u]);
-    if ((wall & 0xFFFFu) <= 0xFFFBu && !(SCHEME == kLinear && (wall >> 16) > a.s + kOff)) return;
+    if ((wall & 0xFFFFu) <= 0xFFFBu && !(SCHEME == kLinear && (wall >> 16) > a.s + kOff))
+        return big;
 #pragma unroll
     for (int u = 0; u < R; ++u) {
         const bool over = SCHEME == kLinear && (worst[u] >> 16) > a.s + kOff;
@@ -921,10 +928,13 @@ __device__ __forceinline__ void decide_rows(const float (&xv)[R][kQCols], const 
                 uint32_t hi, lo;
                 grid_position<SCHEME>(vb, a.s, hi, lo);
                 const uint32_t r = (half16(aw[u], c) << 16) | half16(bw, c);
-                yk[u][c] = (hi + (r < lo ? 1u : 0u) + kOff) << 16;
+                const uint32_t k = hi + (r < lo ? 1u : 0u);
+                yk[u][c] = (k + kOff) << 16;
+                if (k >= 2u) big |= 1u << u;
             }
         }
     }
+    return big;
 }
 
 // Packed fp32 pairs for the paired arithmetic of sm_100-class GPUs (add.f32x2, fma.f32x2: two
@@ -1479,7 +1489,7 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_
 // One stage of RB rows (rows b*RB ..) of one chunk, for consumer thread tid (group g of its
 // problem): rows into registers SUB at a time, the stage released once its last rows are read,
 // then random words, decisions and sums.  a: the problem's arguments (d, n, step, row0, s, rk).
-template <typename T, int SCHEME, int CODE_BITS, bool TRUSTED, int SUB>
+template <typename T, int SCHEME, int CODE_BITS, bool TRUSTED, int SUB, bool SMALLK = false>
 __device__ __forceinline__ void tma_consume_stage(const unsigned char* stage, int lane, bool active,
                                                   int64_t b, int64_t g, const PhiloxGroup& pg,
                                                   const QuantArgs& a, const Decide& dc,
@@ -1515,13 +1525,20 @@ __device__ __forceinline__ void tma_consume_stage(const unsigned char* stage, in
             aw[u][0] = ra.x; aw[u][1] = ra.y; aw[u][2] = ra.z; aw[u][3] = ra.w;
         }
         uint32_t yk[SUB][kQCols];
-        decide_rows<SCHEME, TRUSTED, SUB>(v, dc, a, g32, static_cast<uint32_t>(r0) + a.row0, aw,
-                                          yk);
+        const uint32_t big = decide_rows<SCHEME, TRUSTED, SUB>(
+            v, dc, a, g32, static_cast<uint32_t>(r0) + a.row0, aw, yk);
+        // SMALLK (Global-E under the (2,2) norm, where levels above 1 are rare): when no row of
+        // the warp holds one, the level value 2^(k-1) [k >= 1] is k itself and the rows take the
+        // Global-L accumulation (decided per warp, so the warp does not diverge)
+        const bool small = SMALLK && SCHEME == kExp && !__any_sync(__activemask(), big != 0u);
 #pragma unroll
         for (int u = 0; u < SUB; ++u) {
             if (r0 + u >= a.n) break;
             int32_t code[kQCols];
-            accumulate_row<SCHEME>(v[u], yk[u], S, code);
+            if (small)
+                accumulate_row<kLinear>(v[u], yk[u], S, code);
+            else
+                accumulate_row<SCHEME>(v[u], yk[u], S, code);
             if (CODE_BITS) store_codes<CODE_BITS>(codes, r0 + u, g, a.pitch, code);
         }
     }
@@ -1591,7 +1608,8 @@ __device__ __forceinline__ bool tma_wait_full(uint32_t item, uint64_t (&full_bar
     return __all_sync(0xFFFFFFFFu, got && !*abort_flag);
 }
 
-template <typename T, int SCHEME, int CODE_BITS, bool WRITE_OUT, bool TRUSTED, int SUB>
+template <typename T, int SCHEME, int CODE_BITS, bool WRITE_OUT, bool TRUSTED, int SUB,
+          bool SMALLK = false>
 __global__ void __launch_bounds__(kTmaBlock, 1)
 quantize_tma_kernel(const T* __restrict__ x, QuantArgs a, int64_t groups,
                     unsigned char* __restrict__ codes, void* __restrict__ out,
@@ -1652,7 +1670,7 @@ quantize_tma_kernel(const T* __restrict__ x, QuantArgs a, int64_t groups,
                 }
                 const unsigned char* stage =
                     tma_smem + (item % NS) * Cfg::kStageBytes + tid * kQCols * sizeof(T);
-                tma_consume_stage<T, SCHEME, CODE_BITS, TRUSTED, SUB>(
+                tma_consume_stage<T, SCHEME, CODE_BITS, TRUSTED, SUB, SMALLK>(
                     stage, lane, active, b, g, pg, a, dc, smem_u32(&empty_bar[item % NS]), S,
                     codes);
             }

@@ -20,6 +20,9 @@ gq_status run_quant(const void* grads, const gq::QuantArgs& a, void* codes, void
         if constexpr (BITS == 0 && OUT && !TRUSTED) {  // one rank's sums: often a single worker
             if (a.n == 1) kt = gq::quantize_tma_kernel<T, SCHEME, BITS, OUT, TRUSTED, 1>;
         }
+        if constexpr (SCHEME == gq::kExp && BITS == 0 && OUT && TRUSTED) {
+            if (a.smallk) kt = gq::quantize_tma_kernel<T, SCHEME, BITS, OUT, TRUSTED, 2, true>;
+        }
         constexpr int tsmem = gq::TmaCfg<T>::kSmemBytes;
         if (blocks_per_sm(kt, tsmem, gq::kTmaBlock) < 1) return GQ_ERR_CUDA;
         const unsigned grid = static_cast<unsigned>(sm_count());
