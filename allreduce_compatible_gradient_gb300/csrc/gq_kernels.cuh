@@ -2,10 +2,12 @@
 //
 // Method: "Global-QSGD: Practical Floatless Quantization for Distributed Learning with
 // Theoretical Guarantees" (arXiv 2305.18627), cited as "Global-QSGD".  All kernels are
-// HBM-bandwidth kernels (nothing here is a dense contraction): each thread owns one 16-byte
-// column group (4 fp32 or 8 bf16 coordinates) and walks the n worker rows of that group, so a
-// warp reads 512 contiguous bytes of one row per load.  Grids are grid-stride loops sized to
-// the resident capacity of the GPU (a multiple of its SM count).
+// HBM-bandwidth kernels (nothing here is a dense contraction): each thread owns a column group
+// (8 coordinates in the quantise kernels) and walks the n worker rows of that group, so a warp
+// reads contiguous bytes of one row per load; the (inf, inf) and (2, 2) norms read the matrix
+// flat.  Grids are grid-stride loops sized to the resident capacity of the GPU (a multiple of
+// its SM count); the bulk-copy quantise kernels and the single-launch form run one block per
+// SM.  Every wait on another thread's progress (mbarrier, grid barrier) is bounded in time.
 //
 // Built with -fmad=false: every fp32 operation is a separately rounded IEEE operation, and the
 // normalisation is the correctly rounded quotient (__fdiv_rn).

@@ -21,6 +21,7 @@ from __future__ import annotations
 import argparse
 import hashlib
 import json
+import re
 import os
 import statistics
 import subprocess
@@ -68,12 +69,18 @@ def _peaks():
 
 
 def _kernel_source_hash() -> str:
+    """Hash of the CUDA sources with comments and blank lines removed (a comment edit does not
+    make the committed ncu traffic figures stale; a code edit does)."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "allreduce_compatible_gradient_gb300", "csrc")
     for name in sorted(os.listdir(csrc)):
         if name.endswith((".cu", ".cuh")):
-            with open(os.path.join(csrc, name), "rb") as f:
-                h.update(f.read())
+            with open(os.path.join(csrc, name)) as f:
+                text = re.sub(r"/\*.*?\*/", "", f.read(), flags=re.S)
+            for line in text.splitlines():
+                code = line.split("//", 1)[0].rstrip()
+                if code:
+                    h.update(code.encode() + b"\n")
     return h.hexdigest()[:16]
 
 
