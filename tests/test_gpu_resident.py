@@ -13,7 +13,8 @@ the norm at a grid barrier and quantise from shared memory.  Checked here:
     than the (2, inf) fast column sums take, the largest slice that fits; both dtypes, both
     schemes, all four norms, 16-bit outputs;
   * zero and non-finite inputs, and many calls in a row on one workspace (the barrier words
-    return to their rest state), with the status word read after each.
+    return to their rest state), with the status word read after each;
+  * two problems on two streams at once, each with its own workspace.
 """
 import numpy as np
 import pytest
@@ -189,3 +190,31 @@ def test_many_calls_one_workspace(gq):
             first[key] = out
     torch.cuda.synchronize()
     assert gq.gq_get_status(ws) == 0
+
+
+def test_two_streams_two_workspaces(gq):
+    """Single launches of two problems on two streams at once (each with its own workspace)
+    give the results of the same calls made one after the other; neither wait runs out."""
+    import torch
+    xa = workloads.device_inputs("normal", 4, 65_536, seed=11)
+    xb = workloads.device_inputs("normal", 8, 300_000, seed=12)
+    assert gq.gq_fused_launches(xa.dtype, 4, 65_536) == 1
+    assert gq.gq_fused_launches(xb.dtype, 8, 300_000) == 1
+    wa, wb = gq.gq_workspace(), gq.gq_workspace()
+    ref_a = gq.gq_allreduce_mean(xa, 2, 2, LINEAR, 15, 1, 3, ws=wa)
+    ref_b = gq.gq_allreduce_mean(xb, INF, INF, EXP, 8, 2, 4, ws=wb)
+    torch.cuda.synchronize()
+    sa, sb = torch.cuda.Stream(), torch.cuda.Stream()
+    sa.wait_stream(torch.cuda.current_stream())
+    sb.wait_stream(torch.cuda.current_stream())
+    outs_a, outs_b = [], []
+    for _ in range(20):
+        with torch.cuda.stream(sa):
+            outs_a.append(gq.gq_allreduce_mean(xa, 2, 2, LINEAR, 15, 1, 3, ws=wa, stream=sa))
+        with torch.cuda.stream(sb):
+            outs_b.append(gq.gq_allreduce_mean(xb, INF, INF, EXP, 8, 2, 4, ws=wb, stream=sb))
+    torch.cuda.synchronize()
+    assert gq.gq_get_status(wa) == 0 and gq.gq_get_status(wb) == 0
+    for oa, ob in zip(outs_a, outs_b):
+        assert torch.equal(oa, ref_a)
+        assert torch.equal(ob, ref_b)
