@@ -1,5 +1,6 @@
 """Host logic of bench.py without a GPU: the replica aggregation across ranks (world size 2 over
-gloo, on the CPU) and the reference arm's rank and JSON-line behaviour."""
+gloo, on the CPU), the reference arm's rank and JSON-line behaviour, the --columns option, and
+the kernel source hash that keys the committed ncu traffic figures."""
 import json
 import os
 import socket
@@ -70,3 +71,29 @@ def test_reference_arm_rank0_prints_one_line_others_exit_quietly():
     assert rec["value"] > 0 and rec["e2e"]["value"] == rec["value"]
     assert rec["e2e"]["h2d_bytes_per_step"] == 0 and rec["cpu_baseline"]["kind"] == "oracle"
     assert rec["config"]["workload"] == "gauss_n4_d65536"
+
+
+def test_columns_option_names_a_smaller_case():
+    env = dict(os.environ, RANK="0", WORLD_SIZE="1", LOCAL_RANK="0")
+    r = subprocess.run([sys.executable, "bench.py", "--impl", "reference", "--config",
+                        "bert_large_n16_sparse", "--columns", "4096", "--steps", "1", "--warmup",
+                        "1", "--cpu-seconds", "0.2"], cwd=ROOT, env=env, capture_output=True,
+                       text=True, timeout=600)
+    assert r.returncode == 0, r.stderr[-2000:]
+    rec = json.loads([ln for ln in r.stdout.splitlines() if ln.strip()][-1])
+    assert rec["config"]["workload"] == "bert_large_n16_sparse_d4096"
+    assert rec["config"]["d"] == 4096 and rec["config"]["n"] == 16
+
+
+def test_kernel_source_hash_ignores_comments(tmp_path, monkeypatch):
+    sys.path.insert(0, ROOT)
+    import bench
+    csrc = tmp_path / "allreduce_compatible_gradient_gb300" / "csrc"
+    csrc.mkdir(parents=True)
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    (csrc / "k.cuh").write_text("// a comment\nint f() { return 1; }  // trailing\n/* block\n */\n")
+    h0 = bench._kernel_source_hash()
+    (csrc / "k.cuh").write_text("// another comment\n\nint f() { return 1; }\n")
+    assert bench._kernel_source_hash() == h0
+    (csrc / "k.cuh").write_text("int f() { return 2; }\n")
+    assert bench._kernel_source_hash() != h0
