@@ -47,6 +47,11 @@ MUTANTS = [
     ("re-round drops the sign", "    return t < 0 ? -k : k;\n}", "    return k;\n}"),
     ("tree stream ignores the level", "return (int64_t)0x80000000LL + ((int64_t)l << 24) + m;",
      "return (int64_t)0x80000000LL + m;"),
+    ("p=2 outer sum of norms, not squares", "outer += inner * inner;", "outer += inner;"),
+    ("q=inf signed maximum", "else if (fabs(v) > inner)\n                inner = fabs(v);",
+     "else if (v > inner)\n                inner = v;"),
+    ("NaN not propagated", "if (has_nan)\n        return NAN;", "if (0)\n        return NAN;"),
+    ("final square root dropped", "return p == 2 ? sqrt(outer) : outer;", "return outer;"),
     ("ring starts at worker c", "int code = codes[((c + 1) % n) * w + j];",
      "int code = codes[(c % n) * w + j];"),
 ]
