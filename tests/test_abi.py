@@ -76,6 +76,25 @@ def test_fused_launch_count_query():
     assert gq.gq_fused_launches(gq.F32, 4, 0) == 0
 
 
+def test_fused_launch_rule_matches_its_documentation():
+    """The size rule gq.h states for the single launch, n * 8 * ceil(ceil(d / 8) / SMs) * bytes
+    <= 204,800 with 16-byte aligned rows and no code output, over a grid of shapes (152 SMs: the
+    count the library assumes where no GPU answers)."""
+    import torch
+    import allreduce_compatible_gradient_gb300 as gq
+    if torch.cuda.is_available():
+        pytest.skip("the SM count of a present GPU decides; checked on the GPU by the resident tests")
+    for dtype, elt in ((gq.F32, 4), (gq.BF16, 2)):
+        for n in (1, 2, 3, 8, 16, 64, 257):
+            for d in (1, 4, 8, 12, 1000, 65_536, 65_540, 972_800, 972_808, 5_187_456, 7_782_400,
+                      7_782_408, 40_000_000):
+                groups = -(-d // 8)
+                gpb = -(-groups // 152)
+                want = 1 if (d % (16 // elt) == 0 and n * 8 * gpb * elt <= 204_800) else 2
+                assert gq.gq_fused_launches(dtype, n, d) == want, (dtype, n, d)
+                assert gq.gq_fused_launches(dtype, n, d, with_codes=True) == 2
+
+
 def test_argument_checks_return_before_any_device_call(lib):
     import torch
     if torch.cuda.is_available():
