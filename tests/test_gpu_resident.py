@@ -105,7 +105,8 @@ def _check(gq, oracle_mod, x, q, p, scheme, s, seed=3, step=5, windows=None):
         assert np.abs(out_h[j0:j1] - want_out).max() <= 1e-6 * n32
 
 
-SMALL = [(1, 8), (3, 16), (4, 65_536), (5, 1000), (7, 4100), (2, 8196), (16, 3000), (65, 512)]
+SMALL = [(1, 8), (3, 16), (4, 65_536), (5, 1000), (7, 4100), (2, 8196), (16, 3000), (65, 512),
+         (300, 1024)]
 
 
 @pytest.mark.parametrize("n,d", SMALL)
