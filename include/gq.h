@@ -34,9 +34,9 @@
  *     is asynchronous on that stream; argument errors are returned synchronously before anything
  *     is enqueued.  Calls on different streams may run concurrently if they use different
  *     workspaces.
- *   - Device-detected conditions (a non-finite norm; a bounded wait of a bulk-copy kernel that
- *     gave up) are recorded in the workspace status word and read with gq_get_status.  On a
- *     non-finite norm every output is written as zeros.
+ *   - Device-detected conditions (a non-finite norm; a bounded wait of a bulk-copy kernel or of
+ *     the single-launch form's grid barrier that gave up) are recorded in the workspace status
+ *     word and read with gq_get_status.  On a non-finite norm every output is written as zeros.
  *   - Sizes: n >= 1, 1 <= d < 2^34 (the Philox counter holds j / 8 in 31 bits), n < 2^31.
  *   - Codes: int8 when the code needs more than 4 bits (s > 7), else int4 (two's-complement
  *     nibbles, element 2m in the low nibble of byte m).  Code rows have a pitch of
