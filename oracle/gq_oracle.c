@@ -143,6 +143,19 @@ uint32_t gqo_philox_word(uint64_t seed, uint64_t step, int64_t i, int64_t j)
     return (half16(a, h) << 16) | half16(b, h);
 }
 
+/* The words gqo_philox_word(seed, step, i, j) of worker i for the coordinates j = j0 .. j0 + w - 1,
+ * into out[0 .. w - 1] (a loop over the definition above, for callers that need many words). */
+int gqo_philox_words(uint64_t seed, uint64_t step, int64_t i, int64_t j0, int64_t w,
+                     uint32_t *out)
+{
+    int64_t j;
+    if (out == NULL || w < 0 || j0 < 0 || i < 0)
+        return GQO_ERR_INVALID;
+    for (j = 0; j < w; ++j)
+        out[j] = gqo_philox_word(seed, step, i, j0 + j);
+    return GQO_OK;
+}
+
 /* ------------------------------------------------------------------------------------------ */
 /* Input element access                                                                       */
 /* ------------------------------------------------------------------------------------------ */

@@ -57,6 +57,8 @@ def lib() -> ctypes.CDLL:
         L.gqo_philox4x32_10.restype = None
         L.gqo_philox_word.argtypes = [u64, u64, i64, i64]
         L.gqo_philox_word.restype = u32
+        L.gqo_philox_words.argtypes = [u64, u64, i64, i64, i64, vp]
+        L.gqo_philox_words.restype = ctypes.c_int
         L.gqo_global_norm.argtypes = [vp, ctypes.c_int, i64, i64, ctypes.c_int, ctypes.c_int]
         L.gqo_global_norm.restype = ctypes.c_double
         L.gqo_level_split.argtypes = [ctypes.c_float, ctypes.c_float, ctypes.c_int, ctypes.c_int,
@@ -122,6 +124,15 @@ def philox4x32_10(ctr, key) -> np.ndarray:
 
 def philox_word(seed: int, step: int, i: int, j: int) -> int:
     return int(lib().gqo_philox_word(seed, step, i, j))
+
+
+def philox_words(seed: int, step: int, i: int, j0: int, w: int) -> np.ndarray:
+    """The words philox_word(seed, step, i, j) for j = j0 .. j0 + w - 1 (uint32 array)."""
+    out = np.zeros(w, dtype=np.uint32)
+    rc = lib().gqo_philox_words(seed, step, i, j0, w, out.ctypes.data)
+    if rc != OK:
+        raise ValueError("gqo_philox_words returned %d" % rc)
+    return out
 
 
 def global_norm(x: np.ndarray, q: int, p: int) -> float:
