@@ -290,7 +290,9 @@ gq_status gq_allreduce_mean_to(const void* grads, int dtype, int64_t n, int64_t 
     const float* ws_norm = &reinterpret_cast<const gq::WsHeader*>(ws)->norm;
     gq::QuantArgs a = make_args(ws_norm, dtype, n, d, s, seed, step);
     a.out_dtype = out_dtype;
-    a.smallk = mode == gq::kL2L2;  // under the (2,2) norm Global-E levels above 1 are rare
+    // under the l2 norm over the coordinates ((2,2), (inf,2)) most |x| / N lie far below the
+    // first level: the quantise pass defers the few uncertain row-groups (compacting consumer)
+    a.smallk = mode == gq::kL2L2 || mode == gq::kMaxL2;
     if (!codes) {  // small problems: one launch, the matrix read once
         unsigned char* w = static_cast<unsigned char*>(ws);
         bool taken = false;

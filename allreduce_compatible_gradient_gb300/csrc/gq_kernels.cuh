@@ -1491,12 +1491,18 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_
 // One stage of RB rows (rows b*RB ..) of one chunk, for consumer thread tid (group g of its
 // problem): rows into registers SUB at a time, the stage released once its last rows are read,
 // then random words, decisions and sums.  a: the problem's arguments (d, n, step, row0, s, rk).
-template <typename T, int SCHEME, int CODE_BITS, bool TRUSTED, int SUB, bool SMALLK = false>
+// ZSKIP: while `probe` is set (from the start of a chunk, warp-uniform), every row pair is first
+// tested for being +-0 across the warp and skipped if so; the first pair with a non-zero element
+// clears `probe` for the rest of the chunk (zero blocks of sparse layers span whole columns, so a
+// chunk is either zero in every row or dense).
+template <typename T, int SCHEME, int CODE_BITS, bool TRUSTED, int SUB, bool SMALLK = false,
+          bool ZSKIP = false>
 __device__ __forceinline__ void tma_consume_stage(const unsigned char* stage, int lane, bool active,
                                                   int64_t b, int64_t g, const PhiloxGroup& pg,
                                                   const QuantArgs& a, const Decide& dc,
                                                   uint32_t empty_bar, float (&S)[kQCols],
-                                                  unsigned char* __restrict__ codes) {
+                                                  unsigned char* __restrict__ codes,
+                                                  bool* probe = nullptr) {
     using Cfg = TmaCfg<T>;
     constexpr int RB = Cfg::kRows;
     const uint32_t g32 = static_cast<uint32_t>(g);
@@ -1517,6 +1523,27 @@ __device__ __forceinline__ void tma_consume_stage(const unsigned char* stage, in
         if (u0 + SUB >= RB) {  // every row of the stage is in registers: release it
             __syncwarp();
             if (lane == 0) mbar_arrive(empty_bar);
+        }
+        if (ZSKIP && *probe) {
+            // a zero element has code 0 whatever its random word: rows that are +-0 for every
+            // lane of the warp need no random words or decisions
+            uint32_t o = 0u;
+            if (active && r0 < a.n) {
+#pragma unroll
+                for (int u = 0; u < SUB; ++u)
+#pragma unroll
+                    for (int c = 0; c < kQCols; ++c) o |= __float_as_uint(v[u][c]);
+            }
+            if (!__any_sync(0xFFFFFFFFu, (o & 0x7FFFFFFFu) != 0u)) {
+                if (CODE_BITS && active) {
+                    const int32_t zero[kQCols] = {0, 0, 0, 0, 0, 0, 0, 0};
+#pragma unroll
+                    for (int u = 0; u < SUB; ++u)
+                        if (r0 + u < a.n) store_codes<CODE_BITS>(codes, r0 + u, g, a.pitch, zero);
+                }
+                continue;
+            }
+            *probe = false;
         }
         if (!active || r0 >= a.n) continue;  // past the last worker: nothing to do
         uint32_t aw[SUB][4];
@@ -1543,6 +1570,232 @@ __device__ __forceinline__ void tma_consume_stage(const unsigned char* stage, in
                 accumulate_row<SCHEME>(v[u], yk[u], S, code);
             if (CODE_BITS) store_codes<CODE_BITS>(codes, r0 + u, g, a.pitch, code);
         }
+    }
+}
+
+// ---- deferred decisions (the compacting consumer) -------------------------------------------
+// Under an l2 norm of many elements most |x| / N are far below the first level, and most
+// row-groups (eight elements of one row) round every element down: when the smallest high half
+// H of their eight random words is at least the fast estimate P_c of the largest element's grid
+// position plus 3 units of 2^-16 (P_c is within 2 units of the exact position, so every T < r),
+// all eight codes are 0 and nothing is added.  That check costs one Philox call and a dozen
+// instructions per row-group.  The row-groups that fail it are queued per warp in shared memory
+// (raw values, random words, group and worker) and decided 32 at a time, one per lane, with the
+// full decision; their code values go into per-warp integer sums in shared memory (exact:
+// integers below 2^24), which each group's owner lane reads when its chunk is done.  So the
+// rare full decisions run on full warps instead of one lane at a time.
+constexpr int kQueue = 32;  // queued row-groups per warp
+
+template <typename T>
+struct CompactCfg {
+    static constexpr int kXVec = sizeof(T) == 4 ? 2 : 1;  // 16-byte pieces of a row-group
+    // per warp: raw values, random words, (group, worker), then the 8 x 32 integer sums
+    static constexpr int kWarpBytes = kQueue * (16 * kXVec + 16 + 8) + kQCols * 32 * 4;
+    static constexpr int kBytes = kTmaWarps * kWarpBytes;
+};
+
+template <typename T>
+struct WarpQueue {
+    uint4* qx;     // [kQueue][kXVec]
+    uint4* qw;     // [kQueue]
+    uint2* qm;     // [kQueue]: group, worker
+    int32_t* sum;  // [kQCols][32]: column c of the group owned by lane l at c * 32 + l
+};
+
+template <typename T>
+__device__ __forceinline__ WarpQueue<T> warp_queue(unsigned char* base, int warp) {
+    using C = CompactCfg<T>;
+    unsigned char* p = base + warp * C::kWarpBytes;
+    WarpQueue<T> q;
+    q.qx = reinterpret_cast<uint4*>(p);
+    q.qw = reinterpret_cast<uint4*>(p + kQueue * 16 * C::kXVec);
+    q.qm = reinterpret_cast<uint2*>(p + kQueue * (16 * C::kXVec + 16));
+    q.sum = reinterpret_cast<int32_t*>(p + kQueue * (16 * C::kXVec + 16 + 8));
+    return q;
+}
+
+// Largest magnitude of a row-group as an fp32 value (NaN stays NaN: integer maximum of the
+// magnitude bits; a trusted norm rules NaN out, so fp32 maxima of |x| are used there).
+template <typename T, bool TRUSTED>
+__device__ __forceinline__ float group_max_abs(const uint4 (&raw)[CompactCfg<T>::kXVec]) {
+    if (sizeof(T) == 2) {
+        const uint4 r = raw[0];
+        const uint32_t m = __vmaxu2(__vmaxu2(r.x & 0x7FFF7FFFu, r.y & 0x7FFF7FFFu),
+                                    __vmaxu2(r.z & 0x7FFF7FFFu, r.w & 0x7FFF7FFFu));
+        return __uint_as_float(max(m & 0xFFFFu, m >> 16) << 16);
+    } else if (TRUSTED) {
+        float m = 0.0f;
+#pragma unroll
+        for (int h = 0; h < CompactCfg<T>::kXVec; ++h) {
+            const uint4 r = raw[h];
+            m = fmaxf(m, fmaxf(fmaxf(fabsf(__uint_as_float(r.x)), fabsf(__uint_as_float(r.y))),
+                               fmaxf(fabsf(__uint_as_float(r.z)), fabsf(__uint_as_float(r.w)))));
+        }
+        return m;
+    } else {
+        uint32_t m = 0u;
+#pragma unroll
+        for (int h = 0; h < CompactCfg<T>::kXVec; ++h) {
+            const uint4 r = raw[h];
+            m = max(m, max(max(r.x & 0x7FFFFFFFu, r.y & 0x7FFFFFFFu),
+                           max(r.z & 0x7FFFFFFFu, r.w & 0x7FFFFFFFu)));
+        }
+        return __uint_as_float(m);
+    }
+}
+
+template <typename T>
+__device__ __forceinline__ void widen_raw(const uint4 (&raw)[CompactCfg<T>::kXVec],
+                                          float (&v)[kQCols]) {
+    if (sizeof(T) == 2) {
+        const uint32_t w[4] = {raw[0].x, raw[0].y, raw[0].z, raw[0].w};
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            v[2 * k] = __uint_as_float(w[k] << 16);
+            v[2 * k + 1] = __uint_as_float(w[k] & 0xFFFF0000u);
+        }
+    } else {
+        const uint32_t w[8] = {raw[0].x, raw[0].y, raw[0].z, raw[0].w,
+                               raw[CompactCfg<T>::kXVec - 1].x, raw[CompactCfg<T>::kXVec - 1].y,
+                               raw[CompactCfg<T>::kXVec - 1].z, raw[CompactCfg<T>::kXVec - 1].w};
+#pragma unroll
+        for (int c = 0; c < kQCols; ++c) v[c] = __uint_as_float(w[c]);
+    }
+}
+
+// Decide the first `cnt` queued row-groups, one per lane, and add their code values (Global-L:
+// the signed level index; Global-E: sign 2^(k-1), 0 for k = 0) to their owners' sums.
+template <typename T, int SCHEME, bool TRUSTED>
+__device__ __forceinline__ void flush_queue(const WarpQueue<T>& q, int cnt, int lane,
+                                            const QuantArgs& a, const Decide& dc) {
+    __syncwarp();
+    if (lane < cnt) {
+        uint4 raw[CompactCfg<T>::kXVec];
+#pragma unroll
+        for (int h = 0; h < CompactCfg<T>::kXVec; ++h) raw[h] = q.qx[lane * CompactCfg<T>::kXVec + h];
+        const uint4 w = q.qw[lane];
+        const uint2 m = q.qm[lane];
+        float v[1][kQCols];
+        widen_raw<T>(raw, v[0]);
+        const uint32_t aw[1][4] = {{w.x, w.y, w.z, w.w}};
+        uint32_t yk[1][kQCols];
+        decide_rows<SCHEME, TRUSTED, 1>(v, dc, a, m.x, m.y, aw, yk);
+        const int owner = static_cast<int>(m.x & 31u);
+#pragma unroll
+        for (int c = 0; c < kQCols; ++c) {
+            const int32_t k = static_cast<int32_t>(yk[0][c] >> 16) - 0x4300;
+            int32_t units = SCHEME == kLinear ? k : ((1 << k) >> 1);
+            if (__float_as_uint(v[0][c]) >> 31) units = -units;
+            if (units != 0) atomicAdd(&q.sum[c * 32 + owner], units);
+        }
+    }
+    __syncwarp();
+}
+
+// The rare flush when one stage alone queues more than a queue's worth of row-groups: kept out of
+// line so that the common path holds one inlined copy of the full decision.
+template <typename T, int SCHEME, bool TRUSTED>
+__device__ __noinline__ void flush_queue_cold(const WarpQueue<T>& q, int cnt, int lane,
+                                              const QuantArgs& a, const Decide& dc) {
+    flush_queue<T, SCHEME, TRUSTED>(q, cnt, lane, a, dc);
+}
+
+template <typename T>
+__device__ __forceinline__ void push_item(const WarpQueue<T>& q, int pos,
+                                          const uint4 (&raw)[CompactCfg<T>::kXVec], uint4 wd,
+                                          uint32_t g32, uint32_t worker) {
+#pragma unroll
+    for (int h = 0; h < CompactCfg<T>::kXVec; ++h) q.qx[pos * CompactCfg<T>::kXVec + h] = raw[h];
+    q.qw[pos] = wd;
+    q.qm[pos] = make_uint2(g32, worker);
+}
+
+// One stage (rows r0 .. r0 + nrows - 1 of this thread's group g32) through the compacting
+// consumer: every row-group's largest magnitude, the rows' random words (independent chains the
+// scheduler interleaves), the certainty test, then the row-groups that fail it are queued (one
+// ballot per row, one position each; the queue is flushed first if they would not fit).
+// count: queued row-groups of the warp (warp-uniform).
+template <typename T, int SCHEME, bool TRUSTED>
+__device__ __forceinline__ void tma_consume_compact(const unsigned char* stage, int lane,
+                                                    bool active, uint32_t r0, uint32_t nrows,
+                                                    uint32_t g32, const PhiloxGroup& pg,
+                                                    const QuantArgs& a, const Decide& dc,
+                                                    uint32_t empty_bar, const WarpQueue<T>& q,
+                                                    int& count) {
+    using Cfg = TmaCfg<T>;
+    using C = CompactCfg<T>;
+    constexpr int RB = Cfg::kRows;
+    uint4 raw[RB][C::kXVec];
+#pragma unroll
+    for (int u = 0; u < RB; ++u) {
+        const uint4* p = reinterpret_cast<const uint4*>(stage + u * Cfg::kRowBytes);
+#pragma unroll
+        for (int h = 0; h < C::kXVec; ++h) raw[u][h] = p[h];  // rows past nrows are ignored
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(empty_bar);  // every row of the stage is in registers
+    float mx[RB];
+    uint32_t any = 0u;
+#pragma unroll
+    for (int u = 0; u < RB; ++u) {
+        const float m = group_max_abs<T, TRUSTED>(raw[u]);
+        mx[u] = (active && static_cast<uint32_t>(u) < nrows) ? m : 0.0f;
+        any |= __float_as_uint(mx[u]);
+    }
+    // a stage that is zero across the warp (sparse layers) needs no random words at all
+    if (!__any_sync(0xFFFFFFFFu, any != 0u)) return;
+    const uint32_t w0 = r0 + a.row0;
+    uint4 wd[RB];
+    if (nrows == RB) {
+#pragma unroll
+        for (int u = 0; u < RB; ++u) wd[u] = philox_row(pg, w0 + u, a.step_lo, a.rk);
+    } else {
+#pragma unroll
+        for (int u = 0; u < RB; ++u)
+            wd[u] = static_cast<uint32_t>(u) < nrows ? philox_row(pg, w0 + u, a.step_lo, a.rk)
+                                                     : make_uint4(0u, 0u, 0u, 0u);
+    }
+    unsigned mk[RB];
+    int tot = 0;
+#pragma unroll
+    for (int u = 0; u < RB; ++u) {
+        const uint4 w = wd[u];
+        const uint32_t h2 = __vminu2(__vminu2(w.x, w.y), __vminu2(w.z, w.w));
+        const uint32_t minh = min(h2 & 0xFFFFu, h2 >> 16);
+        const uint32_t pbm = __float_as_uint(__fmaf_rn(mx[u], dc.c1, dc.c0));
+        // P_c + 3 > min H (unsigned: a NaN, infinite or P_c >= 1 estimate always queues)
+        const bool nd = __float_as_uint(mx[u]) != 0u && (!dc.fast || pbm - 0x4300FFFAu > minh);
+        mk[u] = __ballot_sync(0xFFFFFFFFu, nd);
+        tot += __popc(mk[u]);
+    }
+    if (tot == 0) return;
+    const unsigned lt = (1u << lane) - 1u;
+    if (count + tot > kQueue) {
+        flush_queue<T, SCHEME, TRUSTED>(q, count, lane, a, dc);
+        count = 0;
+    }
+    if (tot <= kQueue) {
+        int base = count;
+#pragma unroll
+        for (int u = 0; u < RB; ++u) {
+            if ((mk[u] >> lane) & 1u)
+                push_item<T>(q, base + __popc(mk[u] & lt), raw[u], wd[u], g32, w0 + u);
+            base += __popc(mk[u]);
+        }
+        count += tot;
+        return;
+    }
+    // more than a queue's worth in this one stage (rare): row by row
+#pragma unroll
+    for (int u = 0; u < RB; ++u) {
+        const int c = __popc(mk[u]);
+        if (count + c > kQueue) {
+            flush_queue_cold<T, SCHEME, TRUSTED>(q, count, lane, a, dc);
+            count = 0;
+        }
+        if ((mk[u] >> lane) & 1u)
+            push_item<T>(q, count + __popc(mk[u] & lt), raw[u], wd[u], g32, w0 + u);
+        count += c;
     }
 }
 
@@ -1610,8 +1863,11 @@ __device__ __forceinline__ bool tma_wait_full(uint32_t item, uint64_t (&full_bar
     return __all_sync(0xFFFFFFFFu, got && !*abort_flag);
 }
 
+// SMALLK: Global-E warps whose levels are all 0 or 1 take the Global-L accumulation.  ZSKIP:
+// rows that are zero across the whole warp skip their random words.  COMPACT (no codes): the
+// compacting consumer above; the dynamic shared memory then holds its queues after the ring.
 template <typename T, int SCHEME, int CODE_BITS, bool WRITE_OUT, bool TRUSTED, int SUB,
-          bool SMALLK = false>
+          bool SMALLK = false, bool ZSKIP = false, bool COMPACT = false>
 __global__ void __launch_bounds__(kTmaBlock, 1)
 quantize_tma_kernel(const T* __restrict__ x, QuantArgs a, int64_t groups,
                     unsigned char* __restrict__ codes, void* __restrict__ out,
@@ -1653,6 +1909,47 @@ quantize_tma_kernel(const T* __restrict__ x, QuantArgs a, int64_t groups,
             }
             tma_drain<NS>(ok, item, full_bar, &sh_abort, status);
         }
+    } else if (COMPACT && nchunks > 0) {  // consumers, compacting
+        static_assert(!COMPACT || CODE_BITS == 0, "the compacting consumer writes no codes");
+        const Decide dc = make_decide<SCHEME>(nrm, a.s);
+        const int lane = tid & 31;
+        const WarpQueue<T> wq = warp_queue<T>(tma_smem + Cfg::kSmemBytes, tid >> 5);
+#pragma unroll
+        for (int c = 0; c < kQCols; ++c) wq.sum[c * 32 + lane] = 0;
+        int count = 0;
+        uint32_t item = 0;
+        bool ok = true;
+        for (int64_t q = blockIdx.x; q < nchunks && ok; q += gridDim.x) {
+            const int64_t g = (nchunks - 1 - q) * kTmaConsumers + tid;
+            const bool active = g < full;
+            const PhiloxGroup pg = philox_group(static_cast<uint32_t>(g), a.step_lo, a.step_hi, a.rk);
+            for (int64_t b = 0; b < nbatch; ++b, ++item) {
+                if (!tma_wait_full<NS>(item, full_bar, &sh_abort)) {
+                    ok = false;
+                    break;
+                }
+                const unsigned char* stage =
+                    tma_smem + (item % NS) * Cfg::kStageBytes + tid * kQCols * sizeof(T);
+                tma_consume_compact<T, SCHEME, TRUSTED>(
+                    stage, lane, active, static_cast<uint32_t>(b * RB),
+                    static_cast<uint32_t>(min(static_cast<int64_t>(RB), a.n - b * RB)),
+                    static_cast<uint32_t>(g), pg, a, dc, smem_u32(&empty_bar[item % NS]), wq, count);
+            }
+            if (!ok) break;
+            flush_queue<T, SCHEME, TRUSTED>(wq, count, lane, a, dc);
+            count = 0;
+            float S[kQCols];
+#pragma unroll
+            for (int c = 0; c < kQCols; ++c) {
+                S[c] = static_cast<float>(wq.sum[c * 32 + lane]);  // exact: below 2^24
+                wq.sum[c * 32 + lane] = 0;
+            }
+            if (active && WRITE_OUT) store_out(out, a.sums, a.sums_i8, a.out_dtype, g, a.d, scale, S);
+        }
+        if (!ok) {
+            if (status) atomicCAS(status, 0u, kStatusTimeout);
+            sh_abort = 1;
+        }
     } else if (nchunks > 0) {  // consumers
         const Decide dc = make_decide<SCHEME>(nrm, a.s);
         const int lane = tid & 31;
@@ -1665,6 +1962,7 @@ quantize_tma_kernel(const T* __restrict__ x, QuantArgs a, int64_t groups,
             float S[kQCols];
 #pragma unroll
             for (int c = 0; c < kQCols; ++c) S[c] = 0.0f;
+            bool probe = true;
             for (int64_t b = 0; b < nbatch; ++b, ++item) {
                 if (!tma_wait_full<NS>(item, full_bar, &sh_abort)) {
                     ok = false;
@@ -1672,9 +1970,9 @@ quantize_tma_kernel(const T* __restrict__ x, QuantArgs a, int64_t groups,
                 }
                 const unsigned char* stage =
                     tma_smem + (item % NS) * Cfg::kStageBytes + tid * kQCols * sizeof(T);
-                tma_consume_stage<T, SCHEME, CODE_BITS, TRUSTED, SUB, SMALLK>(
+                tma_consume_stage<T, SCHEME, CODE_BITS, TRUSTED, SUB, SMALLK, ZSKIP>(
                     stage, lane, active, b, g, pg, a, dc, smem_u32(&empty_bar[item % NS]), S,
-                    codes);
+                    codes, &probe);
             }
             if (ok && active && WRITE_OUT)
                 store_out(out, a.sums, a.sums_i8, a.out_dtype, g, a.d, scale, S);

@@ -16,14 +16,19 @@ gq_status run_quant(const void* grads, const gq::QuantArgs& a, void* codes, void
     const int64_t groups = BITS ? a.pitch / gq::kQCols : (a.d + gq::kQCols - 1) / gq::kQCols;
     const int64_t chunks = (a.d / gq::kQCols) / gq::kTmaConsumers;
     if (status && a.vec_rows && chunks >= sm_count()) {
-        auto kt = gq::quantize_tma_kernel<T, SCHEME, BITS, OUT, TRUSTED, 2>;
+        auto kt = gq::quantize_tma_kernel<T, SCHEME, BITS, OUT, TRUSTED, 2, false, true>;
+        int tsmem = gq::TmaCfg<T>::kSmemBytes;
         if constexpr (BITS == 0 && OUT && !TRUSTED) {  // one rank's sums: often a single worker
-            if (a.n == 1) kt = gq::quantize_tma_kernel<T, SCHEME, BITS, OUT, TRUSTED, 1>;
+            if (a.n == 1) kt = gq::quantize_tma_kernel<T, SCHEME, BITS, OUT, TRUSTED, 1, false, true>;
         }
-        if constexpr (SCHEME == gq::kExp && BITS == 0 && OUT && TRUSTED) {
-            if (a.smallk) kt = gq::quantize_tma_kernel<T, SCHEME, BITS, OUT, TRUSTED, 2, true>;
+        if constexpr (BITS == 0 && OUT && TRUSTED) {
+            // under an l2 norm over all coordinates most elements round down: the compacting
+            // consumer
+            if (a.smallk) {
+                kt = gq::quantize_tma_kernel<T, SCHEME, BITS, OUT, TRUSTED, 2, false, false, true>;
+                tsmem += gq::CompactCfg<T>::kBytes;
+            }
         }
-        constexpr int tsmem = gq::TmaCfg<T>::kSmemBytes;
         if (blocks_per_sm(kt, tsmem, gq::kTmaBlock) < 1) return GQ_ERR_CUDA;
         const unsigned grid = static_cast<unsigned>(sm_count());
         kt<<<grid, gq::kTmaBlock, tsmem, st>>>(static_cast<const T*>(grads), a, groups,

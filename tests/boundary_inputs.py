@@ -161,19 +161,21 @@ def make_plan(R: np.ndarray, count: int, scheme: int, s: int, rng, small_norm: b
             "levels": np.array(levels), "signs": signs}
 
 
-def make_plan_l2(R: np.ndarray, count: int, s: int, rng, dtype: str = "f32",
+def make_plan_l2(R: np.ndarray, count: int, scheme: int, s: int, rng, dtype: str = "f32",
                  budget: float = 0.04):
-    """make_plan for Global-E under the (2, 2) norm, where every |x| / N counts towards N: the
-    placed elements keep sum (|x| / N)^2 below `budget`, so that they move the norm little.
-    Level-0 elements (v < 2^-(s-1), T = v 2^(s-1) 2^32) go to positions whose word is small
-    enough that v stays below sqrt(budget / 2 / count); a few elements go to levels 1 and 2
-    (v of 2^-(s-1) and more) as long as the budget allows."""
+    """make_plan for the (2, 2) norm, where every |x| / N counts towards N: the placed elements
+    keep sum (|x| / N)^2 below `budget`, so that they move the norm little.  Level-0 elements
+    (v below the first level, T = v u 2^32 with u = s for Global-L and 2^(s-1) for Global-E) go
+    to positions whose word is small enough that v stays below sqrt(budget / 2 / count); for
+    Global-E a few elements go to levels 1 and 2 (v of 2^-(s-1) and more) as long as the budget
+    allows (a Global-L level of 1 or more is v >= 1/s, too large for it)."""
     n, d = R.shape
     v0 = np.sqrt(budget / 2 / count)
-    rmax = min(2.0**32 - 1, v0 * 2.0 ** (s - 1) * 2.0**32)
+    unit = float(s) if scheme == LINEAR else 2.0 ** (s - 1)
+    rmax = min(2.0**32 - 1, v0 * unit * 2.0**32)
     flat = rng.permutation(n * d)
     small = flat[R.ravel()[flat] < rmax]
-    tdel = tie_offsets(R, EXP, s).ravel()
+    tdel = tie_offsets(R, scheme, s).ravel()
     if dtype == "bf16":
         positions = np.sort(small[: 24 * count])
         deltas = np.zeros(len(positions), dtype=np.int64)
@@ -184,7 +186,7 @@ def make_plan_l2(R: np.ndarray, count: int, s: int, rng, dtype: str = "f32",
                            for p in positions], dtype=np.int64)
     levels = np.zeros(len(positions), dtype=np.int64)
     left = budget / 2
-    for m in (1, 2):  # level m: v in [2^(m-s), 2^(m-s+1)), v^2 < 4^(m-s+1)
+    for m in ((1, 2) if scheme == EXP else ()):  # level m: v in [2^(m-s), 2^(m-s+1))
         k = int(left / 2 / 4.0 ** (m - s + 1))
         k = min(k, 64, len(positions) // 8)
         idx = rng.choice(len(positions), size=k, replace=False) if k else []
@@ -280,8 +282,8 @@ def l2_norm_matrix(n: int, d: int, scheme: int, s: int, seed: int, step: int, co
     until the norm no longer moves (or `rounds` iterations)."""
     base = background(n, d, rng, 1.0, dtype)
     R = words(n, d, seed, step)
-    if scheme == EXP and (q, p) == (2, 2):
-        plan = make_plan_l2(R, count, s, rng, dtype)
+    if (q, p) == (2, 2):
+        plan = make_plan_l2(R, count, scheme, s, rng, dtype)
     else:
         plan = make_plan(R, count, scheme, s, rng, dtype=dtype)
     N = np.float32(oracle.global_norm(to_dtype(base, dtype), q, p))

@@ -126,14 +126,14 @@ def test_fused_bulk_copy_max_norm(gq, oracle, dtype, scheme, s):
 
 
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
-@pytest.mark.parametrize("s", [8, 4])
-def test_fused_bulk_copy_l2_global_e(gq, oracle, dtype, s):
-    """Global-E under the (2, 2) norm: the kernel variant whose warps take the levels-0/1
-    accumulation when no element of theirs reaches level 2."""
+@pytest.mark.parametrize("scheme,s", [(EXP, 8), (EXP, 4), (LINEAR, 7), (LINEAR, 127)])
+def test_fused_bulk_copy_l2(gq, oracle, dtype, scheme, s):
+    """The (2, 2) norm: the compacting consumer (row-groups whose elements all round down are
+    settled by one comparison; the rest are queued and decided a warp at a time)."""
     n, d = 8, (1 << 20) if dtype == "f32" else (1 << 21)
-    rng = np.random.default_rng(40 + s)
-    xh, info = bi.l2_norm_matrix(n, d, EXP, s, SEED, STEP, 4096, rng, dtype)
-    _fused(gq, oracle, xh, 2, 2, EXP, s, 2)
+    rng = np.random.default_rng(40 + s + scheme)
+    xh, info = bi.l2_norm_matrix(n, d, scheme, s, SEED, STEP, 4096, rng, dtype)
+    _fused(gq, oracle, xh, 2, 2, scheme, s, 2)
 
 
 @pytest.mark.parametrize("scheme,s", SCHEMES)

@@ -110,3 +110,72 @@ def test_bulk_copy_path_l2_norm_and_zero(gq):
     assert torch.equal(out, ref)
     assert torch.count_nonzero(outz) == 0
     assert gq.gq_get_status(ws) == 0
+
+
+COMPACT_CASES = [
+    # n, d, dtype, scheme, s, (q, p)
+    (1, 700_000, "f32", EXP, 8, (2, 2)),       # one worker: three empty rows per stage
+    (3, 600_004, "f32", LINEAR, 7, (2, 2)),    # ragged last group
+    (5, 640_000, "bf16", EXP, 4, (2, 2)),
+    (8, 1_000_000, "f32", EXP, 21, (2, 2)),    # the largest s for 8 workers
+    (13, 655_360, "bf16", LINEAR, 127, (2, 2)),
+    (33, 600_000, "f32", EXP, 8, (INF, 2)),
+    (6, 1_200_008, "bf16", EXP, 8, (INF, 2)),
+]
+
+
+@pytest.mark.parametrize("n,d,dtype,scheme,s,qp", COMPACT_CASES)
+def test_compacting_consumer(gq, oracle_mod, n, d, dtype, scheme, s, qp):
+    """Norms with p = 2 take the compacting consumer (row-groups that certainly round down are
+    settled at once, the rest queued per warp and decided a warp at a time): its mean equals the
+    direct-load kernel's given the same norm bit for bit, and the oracle's on sampled windows.
+    Heavy-tailed inputs, so that some row-groups of most warps are queued."""
+    import torch
+    x = workloads.device_inputs("student_t3", n, d, seed=d + n, dtype=dtype)
+    q, p = qp
+    seed, step = 21, 6
+    ws = gq.gq_workspace()
+    norm = torch.empty(1, dtype=torch.float32, device="cuda")
+    out = gq.gq_allreduce_mean(x, q, p, scheme, s, seed, step, norm=norm, ws=ws)
+    ref = gq.gq_allreduce_mean_with_norm(x, norm, scheme, s, seed, step)
+    torch.cuda.synchronize()
+    assert gq.gq_get_status(ws) == 0
+    assert torch.equal(out, ref)
+    xh = to_host(x)
+    norm32 = float(norm.item())
+    assert norm32 == pytest.approx(oracle_mod.global_norm(xh, q, p), rel=1e-6)
+    out_h = out.cpu().numpy().astype(np.float64)
+    for j0, j1 in _windows(d, seed=d + 1):
+        ref_codes, rc = oracle_mod.quantize(xh, norm32, scheme, s, seed, step, j0, j1)
+        assert rc == 0
+        ref_out, rc = oracle_mod.dequantize(oracle_mod.reduce_codes(ref_codes, scheme, s), norm32,
+                                            scheme, s, n)
+        assert np.abs(out_h[j0:j1] - ref_out).max() <= 1e-6 * norm32
+
+
+@pytest.mark.parametrize("dtype,scheme,s,qp", [("f32", EXP, 4, (2, INF)), ("f32", LINEAR, 127, (INF, INF)),
+                                               ("bf16", EXP, 8, (INF, INF)), ("f32", EXP, 8, (2, 2))])
+def test_zero_blocks(gq, dtype, scheme, s, qp):
+    """Block-sparse inputs (half of the 4096-coordinate blocks zero for every worker, as in sparse
+    layers), with signed zeros, single non-zero elements in zero blocks and a worker whose rows
+    are zero in another pattern: rows that are zero across a warp skip their random words; the
+    result equals the direct-load kernel's bit for bit."""
+    import torch
+    n, d = 7, 1_048_576
+    x = workloads.device_inputs("laplace_block_sparse", n, d, seed=5, dtype=dtype)
+    flat = x.view(-1)
+    g = torch.Generator(device="cuda")
+    g.manual_seed(9)
+    idx = torch.randint(0, n * d, (64,), generator=g, device="cuda")
+    flat[idx[:32]] = -0.0
+    flat[idx[32:]] = 3e-3
+    x[3, : d // 2] = 0
+    q, p = qp
+    ws = gq.gq_workspace()
+    norm = torch.empty(1, dtype=torch.float32, device="cuda")
+    out = gq.gq_allreduce_mean(x, q, p, scheme, s, 4, 2, norm=norm, ws=ws)
+    ref = gq.gq_allreduce_mean_with_norm(x, norm, scheme, s, 4, 2)
+    torch.cuda.synchronize()
+    assert gq.gq_get_status(ws) == 0
+    assert torch.equal(out, ref)
+    assert torch.count_nonzero(out) > 0
