@@ -42,6 +42,8 @@ def lib() -> ctypes.CDLL:
         "gq_code_bits": (ci, [ci, ci]),
         "gq_code_pitch": (i64, [i64]),
         "gq_fused_launches": (ci, [ci, i64, i64, ci]),
+        "gq_norm_blocks": (i64, [ci, i64, i64, ci, ci]),
+        "gq_noalloc_max_blocks": (i64, []),
         "gq_code_bytes": (sz, [ci, ci, i64, i64]),
         "gq_global_norm": (ci, [vp, ci, i64, i64, ci, ci, vp, vp, sz, vp]),
         "gq_quantize": (ci, [vp, ci, i64, i64, vp, ci, ci, u64, u64, vp, vp]),
@@ -141,6 +143,17 @@ def gq_fused_launches(dtype, n: int, d: int, with_codes: bool = False) -> int:
     dtype: torch.float32 / torch.bfloat16 or F32 / BF16."""
     code = {torch.float32: F32, torch.bfloat16: BF16}.get(dtype, dtype)
     return lib().gq_fused_launches(int(code), n, d, 1 if with_codes else 0)
+
+
+def gq_norm_blocks(dtype, n: int, d: int, q: int, p: int) -> int:
+    """Blocks the norm step of an n x d problem launches on the current device (0 if invalid)."""
+    code = {torch.float32: F32, torch.bfloat16: BF16}.get(dtype, dtype)
+    return lib().gq_norm_blocks(int(code), n, d, q, p)
+
+
+def gq_noalloc_max_blocks() -> int:
+    """Most norm-step blocks gq_allreduce_mean_noalloc's fixed scratch holds."""
+    return lib().gq_noalloc_max_blocks()
 
 
 def gq_code_bytes(scheme: int, s: int, n: int, d: int) -> int:

@@ -122,6 +122,10 @@ class GlobalQSGDState:
         if self.reduce != "sum" and self.scheme != gq.EXP:
             raise ValueError("the re-rounding allreduce is Global-E's")
         n = self.world_size
+        if self.reduce == "ring" and n > 4096:
+            # ring step h of chunk c draws from stream 2^31 + 2^30 + h 2^12 + c: the chunk index
+            # has 12 bits, so more ranks would give two steps the same random words
+            raise ValueError("reduce='ring' supports at most 4096 ranks (world size %d)" % n)
         per_worker = self.s if self.scheme == gq.LINEAR else 1 << (self.s - 1)
         if n * per_worker >= 1 << 24:
             raise ValueError("world size %d x %d units per worker reaches 2^24: the integer sums "

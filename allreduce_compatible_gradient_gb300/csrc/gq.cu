@@ -436,6 +436,16 @@ int64_t norm_blocks_any(int dtype, int mode, int64_t n, int64_t d) {
 
 }  // namespace
 
+extern "C" int64_t gq_norm_blocks(int dtype, int64_t n, int64_t d, int q, int p) {
+    if ((dtype != GQ_F32 && dtype != GQ_BF16) || n < 1 || n >= (int64_t(1) << 31) || d < 1 ||
+        d >= kMaxD)
+        return 0;
+    const int mode = norm_mode(q, p);
+    return mode < 0 ? 0 : norm_blocks_any(dtype, mode, n, d);
+}
+
+extern "C" int64_t gq_noalloc_max_blocks(void) { return kNoAllocPartials; }
+
 extern "C" gq_status gq_allreduce_mean_noalloc(const void* grads, int dtype, int64_t n, int64_t d,
                                                int q, int p, int scheme, int s, uint64_t seed,
                                                uint64_t step, float* out_dev, float* norm_dev,
@@ -451,14 +461,28 @@ extern "C" gq_status gq_allreduce_mean_noalloc(const void* grads, int dtype, int
     unsigned char* ws = nullptr;
     if ((st = noalloc_scratch(&ws)) != GQ_OK) return st;
     cudaStream_t cs = static_cast<cudaStream_t>(stream);
-    // the array keeps the previous call's contents: the status word and the completion ticket
-    // must start at zero
+    // the array keeps the previous call's contents: the status word, the completion ticket and
+    // the single launch's barrier word must start at zero
     if (cudaMemsetAsync(ws, 0, gq::kHeaderBytes, cs) != cudaSuccess) return GQ_ERR_CUDA;
-    if ((st = norm_any(grads, dtype, mode, n, d, norm_dev, ws, cs)) != GQ_OK) return st;
     const float* ws_norm = &reinterpret_cast<const gq::WsHeader*>(ws)->norm;
-    const gq::QuantArgs a = make_args(ws_norm, dtype, n, d, s, seed, step);
+    gq::QuantArgs a = make_args(ws_norm, dtype, n, d, s, seed, step);
+    a.smallk = mode == gq::kL2L2 || mode == gq::kMaxL2;  // as gq_allreduce_mean chooses
+    if (!codes) {  // small problems: the single launch (its partials fit the scratch too)
+        bool taken = false;
+        if (dtype == GQ_F32)
+            st = scheme == GQ_LINEAR ? resident_f32_l(grads, a, mode, out_dev, norm_dev, ws, cs, &taken)
+                                     : resident_f32_e(grads, a, mode, out_dev, norm_dev, ws, cs, &taken);
+        else
+            st = scheme == GQ_LINEAR ? resident_bf16_l(grads, a, mode, out_dev, norm_dev, ws, cs, &taken)
+                                     : resident_bf16_e(grads, a, mode, out_dev, norm_dev, ws, cs, &taken);
+        if (taken) return st;
+    }
+    if ((st = norm_any(grads, dtype, mode, n, d, norm_dev, ws, cs)) != GQ_OK) return st;
+    // the scratch's status word lets large aligned problems take the bulk-copy kernel, as
+    // gq_allreduce_mean does (its bounded waits record a timeout there; nothing reads it back)
+    unsigned int* status = &reinterpret_cast<gq::WsHeader*>(ws)->status;
     return quant_any<true, true>(grads, dtype, a, scheme, gq_code_bits(scheme, s), codes, out_dev,
-                                 cs);
+                                 cs, status);
 }
 
 // ---- Global-E allreduce with re-rounding at every hop --------------------------------------

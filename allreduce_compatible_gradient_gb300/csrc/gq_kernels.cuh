@@ -1715,12 +1715,14 @@ __device__ __forceinline__ void push_item(const WarpQueue<T>& q, int pos,
 // scheduler interleaves), the certainty test, then the row-groups that fail it are queued (one
 // ballot per row, one position each; the queue is flushed first if they would not fit).
 // count: queued row-groups of the warp (warp-uniform).
-template <typename T, int SCHEME, bool TRUSTED>
+// ROW_BYTES: the stage's row pitch; release: run by lane 0 once every row of the stage is in
+// registers (frees the stage for the next copy).
+template <typename T, int SCHEME, bool TRUSTED, int ROW_BYTES, typename Release>
 __device__ __forceinline__ void tma_consume_compact(const unsigned char* stage, int lane,
                                                     bool active, uint32_t r0, uint32_t nrows,
                                                     uint32_t g32, const PhiloxGroup& pg,
                                                     const QuantArgs& a, const Decide& dc,
-                                                    uint32_t empty_bar, const WarpQueue<T>& q,
+                                                    const Release& release, const WarpQueue<T>& q,
                                                     int& count) {
     using Cfg = TmaCfg<T>;
     using C = CompactCfg<T>;
@@ -1728,12 +1730,12 @@ __device__ __forceinline__ void tma_consume_compact(const unsigned char* stage, 
     uint4 raw[RB][C::kXVec];
 #pragma unroll
     for (int u = 0; u < RB; ++u) {
-        const uint4* p = reinterpret_cast<const uint4*>(stage + u * Cfg::kRowBytes);
+        const uint4* p = reinterpret_cast<const uint4*>(stage + u * ROW_BYTES);
 #pragma unroll
         for (int h = 0; h < C::kXVec; ++h) raw[u][h] = p[h];  // rows past nrows are ignored
     }
     __syncwarp();
-    if (lane == 0) mbar_arrive(empty_bar);  // every row of the stage is in registers
+    if (lane == 0) release();  // every row of the stage is in registers
     float mx[RB];
     uint32_t any = 0u;
 #pragma unroll
@@ -1930,10 +1932,11 @@ quantize_tma_kernel(const T* __restrict__ x, QuantArgs a, int64_t groups,
                 }
                 const unsigned char* stage =
                     tma_smem + (item % NS) * Cfg::kStageBytes + tid * kQCols * sizeof(T);
-                tma_consume_compact<T, SCHEME, TRUSTED>(
+                const uint32_t eb = smem_u32(&empty_bar[item % NS]);
+                tma_consume_compact<T, SCHEME, TRUSTED, Cfg::kRowBytes>(
                     stage, lane, active, static_cast<uint32_t>(b * RB),
                     static_cast<uint32_t>(min(static_cast<int64_t>(RB), a.n - b * RB)),
-                    static_cast<uint32_t>(g), pg, a, dc, smem_u32(&empty_bar[item % NS]), wq, count);
+                    static_cast<uint32_t>(g), pg, a, dc, [eb] { mbar_arrive(eb); }, wq, count);
             }
             if (!ok) break;
             flush_queue<T, SCHEME, TRUSTED>(wq, count, lane, a, dc);

@@ -262,21 +262,31 @@ gq_status gq_exp_allreduce(const void *codes, int s, int64_t n, int64_t d, int o
  * whose device memory is planned in full ahead of time).  The paper has no counterpart to this
  * call; it exists for those callers only.
  *
- * Same arguments and results as gq_allreduce_mean minus ws / ws_bytes.  The norm step's scratch
- * (status word, completion ticket, norm and up to 1,024 per-block partials: 8,448 bytes) lives
- * in a fixed array in the library's device memory, which every GPU that loads the library holds
- * until the process exits.  Nothing is allocated: no cudaMalloc, cudaFree or allocating library
- * call.  The first call on a device looks up that array's device address (cudaGetSymbolAddress)
- * with the device current; make that first call before any stream capture.  A problem whose norm
- * step would launch more than 1,024 blocks is refused with GQ_ERR_WORKSPACE (on GB300 the norm
- * step launches at most 608).  Every call shares the one array: each call clears its status word
- * and ticket first, and calls that overlap on the GPU (other streams, other host threads) race,
- * so serialise them.  A non-finite norm gives all-zero outputs; there is no status word to read,
- * so test the norm written to norm_dev (nullable) instead.
+ * Same arguments, kernels and results as gq_allreduce_mean minus ws / ws_bytes (the single
+ * launch for small problems without codes, else the norm pass and the same quantise kernel).
+ * Its scratch (status word, completion ticket, norm, the single launch's barrier word and up to
+ * 1,024 per-block partials: 8,448 bytes) lives in a fixed array in the library's device memory,
+ * which every GPU that loads the library holds until the process exits.  Nothing is allocated:
+ * no cudaMalloc, cudaFree or allocating library call.  The first call on a device looks up that
+ * array's device address (cudaGetSymbolAddress) with the device current and keeps it for the
+ * process: make that first call before any stream capture, and do not call it again on a device
+ * after cudaDeviceReset (the address kept would be stale).  A problem whose norm step would
+ * launch more than gq_noalloc_max_blocks() = 1,024 blocks (gq_norm_blocks tells) is refused with
+ * GQ_ERR_WORKSPACE; on GB300 the norm step launches at most 608.  Every call shares the one array:
+ * each call clears its header first, and calls that overlap on the GPU (other streams, other host
+ * threads) race, so serialise them.  A non-finite norm gives all-zero outputs; there is no status
+ * word to read, so test the norm written to norm_dev (nullable) instead.
  */
 gq_status gq_allreduce_mean_noalloc(const void *grads, int dtype, int64_t n, int64_t d, int q,
                                     int p, int scheme, int s, uint64_t seed, uint64_t step,
                                     float *out_dev, float *norm_dev, void *codes, void *stream);
+
+/* Blocks the norm step launches for an n x d matrix of dtype under norm orders (q, p) on the
+ * current device (gq_global_norm, gq_allreduce_mean and its allocation-free form all use this
+ * count); 0 for invalid arguments.  And the most that gq_allreduce_mean_noalloc accepts (the
+ * partials its fixed scratch holds: 1,024).  No counterpart in the paper: sizing queries. */
+int64_t gq_norm_blocks(int dtype, int64_t n, int64_t d, int q, int p);
+int64_t gq_noalloc_max_blocks(void);
 
 /*
  * Segmented form (per layer or per gradient bucket, as the DDP hook of Global-QSGD's

@@ -255,6 +255,18 @@ def test_state_rejects_bad_configurations():
         assert st.bucket_step(5) == (3 << 16) | 5
         with pytest.raises(ValueError):
             st.bucket_step(1 << 16)
+        # the ring's random streams number chunks in 12 bits: at most 4096 ranks
+        cls = comm_hook.GlobalQSGDState
+        orig = cls.world_size
+        try:
+            cls.world_size = property(lambda self: 4097)
+            with pytest.raises(ValueError):
+                cls(scheme=1, s=2, reduce="ring", ops=object())
+            cls(scheme=1, s=2, reduce="tree", ops=object())
+            cls.world_size = property(lambda self: 4096)
+            cls(scheme=1, s=2, reduce="ring", ops=object())
+        finally:
+            cls.world_size = orig
     finally:
         dist.destroy_process_group()
 
