@@ -9,7 +9,8 @@ import os
 import torch
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
-_LIB_PATH = os.path.join(_PKG, "libgq.so")
+# GQ_LIBRARY selects another build of the same library (the debug build with bounds checks)
+_LIB_PATH = os.environ.get("GQ_LIBRARY") or os.path.join(_PKG, "libgq.so")
 
 F32, BF16, F16 = 0, 1, 2
 SUM_I32, SUM_I8 = 0, 1
@@ -73,6 +74,7 @@ def lib() -> ctypes.CDLL:
         "gq_quantize_codes": (ci, [vp, ci, i64, i64, i64, vp, ci, ci, u64, u64, vp, ci, vp, sz, vp]),
         "gq_exp_dequantize": (ci, [vp, i64, vp, ci, i64, vp, ci, vp]),
         "gq_status_string": (ctypes.c_char_p, [ci]),
+        "gq_debug_status": (ci, []),
     }
     for name, (res, args) in sig.items():
         fn = getattr(L, name)
@@ -143,6 +145,12 @@ def gq_fused_launches(dtype, n: int, d: int, with_codes: bool = False) -> int:
     dtype: torch.float32 / torch.bfloat16 or F32 / BF16."""
     code = {torch.float32: F32, torch.bfloat16: BF16}.get(dtype, dtype)
     return lib().gq_fused_launches(int(code), n, d, 1 if with_codes else 0)
+
+
+def gq_debug_status() -> int:
+    """The first failed bounds check of a debug build (its source line), 0 for none, -1 in a
+    normal build."""
+    return lib().gq_debug_status()
 
 
 def gq_norm_blocks(dtype, n: int, d: int, q: int, p: int) -> int:

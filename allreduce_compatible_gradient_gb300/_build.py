@@ -20,6 +20,8 @@ UNITS = ["gq.cu", "gq_quant_f32_l.cu", "gq_quant_f32_e.cu", "gq_quant_bf16_l.cu"
          "gq_quant_bf16_e.cu"]
 OBJ_DIR = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libgq.so")
+# the same library with the kernels' bounds checks compiled in (-DGQ_DEBUG)
+DEBUG_LIB = os.path.join(PKG, "libgq_debug.so")
 ARCH = "-gencode=arch=compute_103a,code=sm_103a"
 
 
@@ -45,30 +47,32 @@ def link_command(objs: list, out: str) -> list:
     return [nvcc(), ARCH, "-shared", "-o", out, *objs]
 
 
-def is_stale() -> bool:
-    if not os.path.exists(LIB):
+def is_stale(lib: str = LIB) -> bool:
+    if not os.path.exists(lib):
         return True
-    t = os.path.getmtime(LIB)
+    t = os.path.getmtime(lib)
     return any(os.path.getmtime(s) > t for s in sources())
 
 
-def build_library(force: bool = False, verbose: bool = False) -> str:
-    """Build libgq.so if missing or older than its sources; return its path."""
-    if force or is_stale():
+def build_library(force: bool = False, verbose: bool = False, debug: bool = False) -> str:
+    """Build libgq.so (debug: libgq_debug.so, with -DGQ_DEBUG) if missing or older than its
+    sources; return its path."""
+    lib = DEBUG_LIB if debug else LIB
+    if force or is_stale(lib):
         os.makedirs(OBJ_DIR, exist_ok=True)
-        extra = ("-Xptxas", "-v") if verbose else ()
-        tag = ".%d" % os.getpid()
+        extra = (("-Xptxas", "-v") if verbose else ()) + (("-DGQ_DEBUG",) if debug else ())
+        tag = ".%d%s" % (os.getpid(), ".dbg" if debug else "")
         objs = [os.path.join(OBJ_DIR, u[:-3] + tag + ".o") for u in UNITS]
-        tmp = LIB + ".tmp" + tag
+        tmp = lib + ".tmp" + tag
         try:
             procs = [subprocess.Popen(compile_command(u, o, extra)) for u, o in zip(UNITS, objs)]
             codes = [p.wait() for p in procs]
             if any(codes):
                 raise subprocess.CalledProcessError(next(c for c in codes if c), "nvcc")
             subprocess.run(link_command(objs, tmp), check=True)
-            os.replace(tmp, LIB)
+            os.replace(tmp, lib)
         finally:
             for f in objs + [tmp]:
                 if os.path.exists(f):
                     os.remove(f)
-    return LIB
+    return lib

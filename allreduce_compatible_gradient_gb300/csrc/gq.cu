@@ -366,6 +366,19 @@ gq_status gq_get_status(void* ws, void* stream) {
     return static_cast<gq_status>(v);
 }
 
+int gq_debug_status(void) {
+#ifdef GQ_DEBUG
+    if (cudaDeviceSynchronize() != cudaSuccess) return -2;
+    const unsigned int words[5] = {gq::debug_word_take(), debug_word_f32_l(), debug_word_f32_e(),
+                                   debug_word_bf16_l(), debug_word_bf16_e()};
+    for (unsigned int w : words)
+        if (w != 0u) return w == 0xFFFFFFFFu ? -2 : static_cast<int>(w);
+    return 0;
+#else
+    return -1;
+#endif
+}
+
 const char* gq_status_string(int status) {
     switch (status) {
         case GQ_OK: return "ok";

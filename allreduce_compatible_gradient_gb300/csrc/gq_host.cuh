@@ -131,7 +131,8 @@ inline bool resident_plan(int64_t n, int64_t d, int elt, int64_t* gpb, unsigned*
     gq_status quant_segments_##NAME(gq::SegLaunch& L, const int64_t* d, int64_t n,                \
                                     const gq::QuantArgs& base, unsigned char* ws, cudaStream_t st); \
     gq_status resident_##NAME(const void* grads, const gq::QuantArgs& a, int mode, void* out,       \
-                              float* norm_user, unsigned char* ws, cudaStream_t st, bool* taken);
+                              float* norm_user, unsigned char* ws, cudaStream_t st, bool* taken);  \
+    unsigned int debug_word_##NAME();
 GQH_QUANT_LAUNCHERS(f32_l)
 GQH_QUANT_LAUNCHERS(f32_e)
 GQH_QUANT_LAUNCHERS(bf16_l)

@@ -20,6 +20,37 @@
 
 namespace gq {
 
+// Debug builds (-DGQ_DEBUG; compute-sanitizer stands in for nothing here): logical bounds checks
+// at the kernels' stores and bulk copies.  A failed check records its source line in this
+// translation unit's debug word and the kernel goes on (no trap); gq_debug_status reads and
+// clears the words of all translation units.  Without GQ_DEBUG the checks compile to nothing.
+#ifdef GQ_DEBUG
+static __device__ unsigned int g_debug_word;
+#define GQ_BOUND(cond)                                                                      \
+    do {                                                                                    \
+        if (!(cond)) atomicCAS(&::gq::g_debug_word, 0u, static_cast<unsigned int>(__LINE__)); \
+    } while (0)
+#else
+#define GQ_BOUND(cond) \
+    do {               \
+    } while (0)
+#endif
+
+// This translation unit's debug word, read and cleared: 0 when no check failed (always 0 in a
+// build without GQ_DEBUG), 0xFFFFFFFF if it could not be read.
+static inline unsigned int debug_word_take() {
+#ifdef GQ_DEBUG
+    unsigned int v = 0u;
+    const unsigned int zero = 0u;
+    if (cudaMemcpyFromSymbol(&v, g_debug_word, sizeof v) != cudaSuccess) return 0xFFFFFFFFu;
+    if (v != 0u && cudaMemcpyToSymbol(g_debug_word, &zero, sizeof zero) != cudaSuccess)
+        return 0xFFFFFFFFu;
+    return v;
+#else
+    return 0u;
+#endif
+}
+
 constexpr int kThreads = 256;        // threads per block for every kernel
 // output element types of the dequantised mean (the values of gq_dtype)
 constexpr int kOutF32 = 0, kOutBF16 = 1, kOutF16 = 2;
@@ -410,6 +441,7 @@ __device__ __forceinline__ void norm_finalize(uint32_t maxbits, const ScaledSumS
 
     const uint64_t part_bits = block_partial<MODE>(maxbits, ssq, best_key, bad_col, sh_d, sh_u);
     if (threadIdx.x == 0) {
+        GQ_BOUND(vb >= 0 && vb < nblk && nblk <= kMaxPartials);
         partials[vb] = part_bits;
         __threadfence();
         const unsigned int t = atomicAdd(out.ticket, 1u);
@@ -793,6 +825,7 @@ template <int CODE_BITS>
 __device__ __forceinline__ void store_codes(unsigned char* __restrict__ codes, int64_t i,
                                             int64_t g, int64_t pitch,
                                             const int32_t (&c)[kQCols]) {
+    GQ_BOUND(i >= 0 && g >= 0 && (g + 1) * kQCols <= pitch);
     if (CODE_BITS == 8) {
         uint32_t w0 = 0, w1 = 0;
 #pragma unroll
@@ -1117,6 +1150,8 @@ __device__ __forceinline__ void store_out(void* __restrict__ out, void* __restri
                                           int sums_i8, int dt, int64_t g, int64_t d, float scale,
                                           const float (&S)[kQCols]) {
     const int64_t j0 = g * kQCols;
+    // callers pass every group of the code pitch (padding groups past d store nothing)
+    GQ_BOUND(g >= 0 && j0 < (d + 31) / 32 * 32);
     if (sums) {
         if (sums_i8) {
             int8_t* q = static_cast<int8_t*>(sums);
@@ -1903,6 +1938,8 @@ quantize_tma_kernel(const T* __restrict__ x, QuantArgs a, int64_t groups,
                 const uint32_t row_bytes = static_cast<uint32_t>(ng * kQCols * sizeof(T));
                 for (int64_t b = 0; b < nbatch; ++b) {
                     const int rows = static_cast<int>(min(static_cast<int64_t>(RB), a.n - b * RB));
+                    GQ_BOUND(rows >= 1 && b * RB + rows <= a.n && g0 >= 0 && ng >= 1 &&
+                             (g0 + ng) * kQCols <= a.d);
                     ok = tma_issue<T, NS>(item, x + b * RB * a.d + g0 * kQCols, a.d, rows,
                                           row_bytes, tma_smem, full_bar, empty_bar, &sh_abort);
                     if (!ok) break;
@@ -2049,6 +2086,8 @@ quantize_seg_tma_kernel(const __grid_constant__ SegLaunch L, QuantArgs base, int
                 const int64_t ng = min(static_cast<int64_t>(kTmaConsumers), sd.d / kQCols - g0);
                 const uint32_t row_bytes = static_cast<uint32_t>(ng * kQCols * sizeof(T));
                 const T* x = static_cast<const T*>(sd.x);
+                GQ_BOUND(k >= 0 && k < L.nseg && g0 >= 0 && ng >= 1 &&
+                         (g0 + ng) * kQCols <= sd.d);
                 for (int64_t b = 0; b < nbatch; ++b) {
                     const int rows = static_cast<int>(min(static_cast<int64_t>(RB), base.n - b * RB));
                     ok = tma_issue<T, NS>(item, x + b * RB * sd.d + g0 * kQCols, sd.d, rows,
@@ -2422,6 +2461,7 @@ resident_kernel(const T* __restrict__ x, QuantArgs a, int64_t gpb, void* __restr
     // 3. the partials of all blocks, the same norm in every block
     const uint64_t part =
         block_partial<MODE, kResThreads>(maxbits, ssq, best_key, bad_col, sh_d, sh_u);
+    GQ_BOUND(blockIdx.x < static_cast<unsigned>(kMaxPartials));
     if (tid == 0) partials[blockIdx.x] = part;
     if (!grid_barrier(hdr, gridDim.x, &sh_flag)) return;
     double comb = 0.0;
@@ -2560,6 +2600,7 @@ reduce_codes_kernel(const unsigned char* __restrict__ codes, int64_t n, int64_t 
             }
         }
         const int64_t j0 = q * K;
+        GQ_BOUND((q + 1) * 16 <= row_bytes);  // chunks of the code pitch (padding stores nothing)
         if (j0 + K <= d) {
 #pragma unroll
             for (int h = 0; h < K / 4; ++h)
@@ -2586,6 +2627,7 @@ dequantize_kernel(const void* __restrict__ sums_v, const float* __restrict__ nor
     for (int64_t q = static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x; q < quads;
          q += stride) {
         const int64_t j0 = q * 4;
+        GQ_BOUND(j0 < d);
         if (j0 + 4 <= d) {
             int4 t;
             if (SUM_I8) {
@@ -2755,6 +2797,7 @@ exp_combine_kernel(const int8_t* __restrict__ a, const int8_t* __restrict__ b, i
 #pragma unroll
             for (int c = 0; c < 8; ++c) ov[8 * h + c] = static_cast<int8_t>(code[c]);
         }
+        GQ_BOUND(j0 >= 0 && j0 < d);
         if (full) {
             *reinterpret_cast<uint4*>(out + j0) = *reinterpret_cast<const uint4*>(ov);
         } else {
@@ -2800,6 +2843,7 @@ exp_dequantize_kernel(const int8_t* __restrict__ codes, int64_t d,
     for (int64_t q = static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x; q < chunks;
          q += stride) {
         const int64_t j0 = q * 16;
+        GQ_BOUND(j0 < d);
         if (j0 + 16 <= d) {
             const uint4 w = __ldg(reinterpret_cast<const uint4*>(codes + j0));
             const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
@@ -2887,6 +2931,7 @@ exp_allreduce_kernel(const unsigned char* __restrict__ codes, int64_t n, int64_t
             }
             root = code;
         }
+        GQ_BOUND(j >= 0 && j < d);
         out[j] = scale * static_cast<float>(exp_units_dev(root));
         if (root_codes) root_codes[j] = static_cast<int8_t>(root);
     }

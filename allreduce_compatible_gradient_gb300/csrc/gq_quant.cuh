@@ -171,4 +171,5 @@ gq_status quant_entry(const void* grads, const gq::QuantArgs& a, int bits, bool 
                                    float* norm_user, unsigned char* ws, cudaStream_t st,           \
                                    bool* taken) {                                                  \
         return run_resident<T, SCHEME>(grads, a, mode, out, norm_user, ws, st, taken);             \
-    }
+    }                                                                                              \
+    unsigned int gqh::debug_word_##NAME() { return gq::debug_word_take(); }

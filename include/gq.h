@@ -354,6 +354,14 @@ gq_status gq_get_status(void *ws, void *stream);
 /* Static string naming a status value. */
 const char *gq_status_string(int status);
 
+/* Bounds checks of a debug build (the library compiled with -DGQ_DEBUG; the stand-in for a
+ * memory checker): every kernel store and bulk copy is checked against the logical extent of its
+ * buffer (d, the code pitch, the partials, the matrix), and a failed check records its source
+ * line instead of trapping.  Returns -1 in a normal build; in a debug build synchronises the
+ * device, returns and clears the first recorded line (0: none; -2: the word could not be read).
+ * No counterpart in the paper. */
+int gq_debug_status(void);
+
 /*
  * One rank's codes for a multi-GPU allreduce that moves codes rather than sums (the Global-E
  * re-rounding allreduce of Global-QSGD's performance-model paragraph): the m x d rows at grads,
