@@ -25,6 +25,9 @@
  *                          gqo_quantize on the window of the whole matrix
  *   gqo_reduce_codes       pinned: hand-decoded codes, exact level values
  *   gqo_dequantize         pinned: hand examples, Monte-Carlo mean
+ *   gqo_level_split_u16    pinned: the 16-bit-uniform mode's bias bound by brute force over
+ *                          all 2^16 uniforms, Monte-Carlo mean, agreement with the exact split
+ *   gqo_quantize_u16_cols  pinned: split + high half of the Philox word, ties H == F stay down
  *
  * Build: gcc -std=c99 -O2 -ffp-contract=off -fPIC -shared gq_oracle.c -lm
  * (-ffp-contract=off keeps every float operation a separately rounded IEEE operation on both
@@ -363,6 +366,139 @@ int gqo_quantize(const void *x, int dtype, int64_t n, int64_t d, int64_t j0, int
         return GQO_ERR_INVALID;
     return gqo_quantize_cols((const unsigned char *)x + (size_t)j0 * esize, dtype, n, d, j0,
                              j1 - j0, norm, scheme, s, seed, step, codes);
+}
+
+/* ------------------------------------------------------------------------------------------ */
+/* The 16-bit-uniform rounding mode (an option)                                               */
+/* ------------------------------------------------------------------------------------------ */
+
+/*
+ * Global-QSGD asks only for an unbiased random rounding between the two adjacent levels and fixes
+ * no random source.  Besides the exact mode above this project offers a cheaper one, whose
+ * decision uses a single 16-bit uniform per element, the high half H = r >> 16 of the element's
+ * word (so one Philox call serves eight elements), and a 16-bit fraction F of the element's
+ * position on the grid computed without a division:
+ *
+ *   Global-L_s: c1 = fp32(s / N) (one correctly rounded division for the whole matrix);
+ *               P16 = |x| c1 2^16 rounded to the nearest integer, ties to the odd one (the
+ *               product of two fp32 values is exact in fp64); P16 is clamped to s 2^16 (|x| > N
+ *               saturates); lower level lo = P16 >> 16, F = P16 & 0xFFFF.
+ *   Global-E_s: rcp = fp32(1 / N), w = min(fp32(|x| rcp), 1).  If w >= 2^-(s-1) (level 1 or
+ *               more): lo = s + e with 2^e <= w < 2^(e+1), and F = the top 16 of w's 23 fraction
+ *               bits (the rest truncated).  Else P16 = |x| rcp 2^(s-1) 2^16 rounded as for L
+ *               (at most 2^16), lo = P16 >> 16, F = P16 & 0xFFFF.
+ *
+ * The element rounds up iff H < F, so P(up) = F / 2^16.  E[level] differs from the exact position
+ * only through the 16-bit resolution of F and the rounding of c1 or rcp and w: by less than
+ * 2^-16 + 2^-22 of the level spacing.  A NaN element gets code 0.  For a norm outside
+ * [2^-100, 2^100] the decision is the exact mode's (gqo_level_split with the full word).
+ *
+ * Returns GQO_OK with (*lo, *F); 8 when the exact mode applies (norm out of range); errors as
+ * gqo_level_split.
+ */
+#define GQO_USE_EXACT 8
+
+/* Nearest integer to t >= 0, ties to the odd one. */
+static double round_half_odd(double t)
+{
+    double f = floor(t), r = t - f;
+    if (r > 0.5)
+        return f + 1.0;
+    if (r < 0.5)
+        return f;
+    return fmod(f, 2.0) == 1.0 ? f : f + 1.0;
+}
+
+int gqo_level_split_u16(float absx, float norm, int scheme, int s, int32_t *lo, uint32_t *F)
+{
+    float ax = fabsf(absx);
+    if (!(norm > 0.0f) || isinf(norm) || s < 1 || lo == NULL || F == NULL)
+        return GQO_ERR_INVALID;
+    if ((scheme == GQO_LINEAR && s > 127) || (scheme == GQO_EXP && s > 62))
+        return GQO_ERR_UNSUPPORTED;
+    if (scheme != GQO_LINEAR && scheme != GQO_EXP)
+        return GQO_ERR_INVALID;
+    if (!(norm >= ldexpf(1.0f, -100) && norm <= ldexpf(1.0f, 100)))
+        return GQO_USE_EXACT;
+    if (isnan(ax)) {
+        *lo = 0;
+        *F = 0;
+        return GQO_OK;
+    }
+    if (scheme == GQO_LINEAR) {
+        float c1 = (float)s / norm;                     /* one fp32 rounding */
+        double p16 = round_half_odd((double)ax * (double)c1 * 65536.0);
+        if (p16 > (double)s * 65536.0)
+            p16 = (double)s * 65536.0;
+        *lo = (int32_t)(p16 / 65536.0);
+        *F = (uint32_t)(p16 - (double)*lo * 65536.0);
+    } else {
+        float rcp = 1.0f / norm;                        /* one fp32 rounding */
+        float w = ax * rcp;                             /* one fp32 rounding */
+        if (w > 1.0f)
+            w = 1.0f;
+        if ((double)w >= ldexp(1.0, -(s - 1))) {
+            int ex;
+            uint32_t bits;
+            frexp((double)w, &ex);                      /* w = mant 2^ex, mant in [0.5, 1) */
+            memcpy(&bits, &w, sizeof bits);
+            *lo = s + (ex - 1);
+            *F = (bits & 0x7FFFFFu) >> 7;
+        } else {
+            double p16 = round_half_odd((double)ax * (double)rcp * ldexp(1.0, s - 1) * 65536.0);
+            *lo = (int32_t)(p16 / 65536.0);
+            *F = (uint32_t)(p16 - (double)*lo * 65536.0);
+        }
+    }
+    return GQO_OK;
+}
+
+/* gqo_quantize_cols in the 16-bit-uniform mode: code = sign(x) (lo + (H < F)) with
+ * H = gqo_philox_word(seed, step, i, j) >> 16; the exact mode's decision for norms outside
+ * [2^-100, 2^100]. */
+int gqo_quantize_u16_cols(const void *xw, int dtype, int64_t n, int64_t ld, int64_t j0,
+                          int64_t w, float norm, int scheme, int s, uint64_t seed, uint64_t step,
+                          int8_t *codes)
+{
+    int64_t i, j;
+    if (xw == NULL || codes == NULL || n < 1 || w < 0 || ld < w || j0 < 0)
+        return GQO_ERR_INVALID;
+    if (dtype != GQO_F32 && dtype != GQO_BF16)
+        return GQO_ERR_INVALID;
+    if (scheme != GQO_LINEAR && scheme != GQO_EXP)
+        return GQO_ERR_INVALID;
+    if (s < 1 || s > (scheme == GQO_LINEAR ? 127 : 62))
+        return GQO_ERR_UNSUPPORTED;
+    if (isnan(norm) || isinf(norm) || norm < 0.0f) {
+        memset(codes, 0, (size_t)(n * w));
+        return GQO_ERR_NONFINITE;
+    }
+    if (norm == 0.0f) {
+        memset(codes, 0, (size_t)(n * w));
+        return GQO_OK;
+    }
+    for (i = 0; i < n; ++i) {
+        for (j = 0; j < w; ++j) {
+            float xe = load_x(xw, dtype, i * ld + j);
+            uint32_t word = gqo_philox_word(seed, step, i, j0 + j);
+            int32_t lo, lvl;
+            uint32_t F;
+            int rc = gqo_level_split_u16(xe, norm, scheme, s, &lo, &F);
+            if (rc == GQO_USE_EXACT) {
+                uint32_t T;
+                rc = gqo_level_split(xe, norm, scheme, s, &lo, &T);
+                if (rc != GQO_OK)
+                    return rc;
+                lvl = lo + (int32_t)(word < T);
+            } else if (rc != GQO_OK) {
+                return rc;
+            } else {
+                lvl = lo + (int32_t)((word >> 16) < F); /* H < F: up with probability F / 2^16 */
+            }
+            codes[i * w + j] = (int8_t)(xe < 0.0f ? -lvl : lvl);
+        }
+    }
+    return GQO_OK;
 }
 
 /*

@@ -70,6 +70,12 @@ def lib() -> ctypes.CDLL:
         L.gqo_quantize_cols.argtypes = [vp, ctypes.c_int, i64, i64, i64, i64, ctypes.c_float,
                                         ctypes.c_int, ctypes.c_int, u64, u64, vp]
         L.gqo_quantize_cols.restype = ctypes.c_int
+        L.gqo_level_split_u16.argtypes = [ctypes.c_float, ctypes.c_float, ctypes.c_int,
+                                          ctypes.c_int, ctypes.POINTER(i32), ctypes.POINTER(u32)]
+        L.gqo_level_split_u16.restype = ctypes.c_int
+        L.gqo_quantize_u16_cols.argtypes = [vp, ctypes.c_int, i64, i64, i64, i64, ctypes.c_float,
+                                            ctypes.c_int, ctypes.c_int, u64, u64, vp]
+        L.gqo_quantize_u16_cols.restype = ctypes.c_int
         L.gqo_reduce_codes.argtypes = [vp, ctypes.c_int, ctypes.c_int, i64, i64, vp]
         L.gqo_reduce_codes.restype = ctypes.c_int
         L.gqo_dequantize.argtypes = [vp, ctypes.c_float, ctypes.c_int, ctypes.c_int, i64, i64, vp]
@@ -168,6 +174,43 @@ def quantize_cols(xw: np.ndarray, j0: int, norm32: float, scheme: int, s: int, s
     codes = np.zeros((n, w), dtype=np.int8)
     rc = lib().gqo_quantize_cols(ptr, code, n, w, j0, w, float(norm32), scheme, s, seed, step,
                                  codes.ctypes.data)
+    return codes, rc
+
+
+USE_EXACT = 8  # gqo_level_split_u16: the norm is out of the mode's range, the exact mode applies
+
+
+def level_split_u16(absx: float, norm: float, scheme: int, s: int):
+    """(lower level, F) of the 16-bit-uniform mode, or None where the exact mode applies."""
+    lo = ctypes.c_int32()
+    F = ctypes.c_uint32()
+    rc = lib().gqo_level_split_u16(absx, norm, scheme, s, ctypes.byref(lo), ctypes.byref(F))
+    if rc == USE_EXACT:
+        return None
+    if rc != OK:
+        raise ValueError("gqo_level_split_u16 returned %d" % rc)
+    return int(lo.value), int(F.value)
+
+
+def quantize_u16(x: np.ndarray, norm32: float, scheme: int, s: int, seed: int, step: int,
+                 j0: int = 0, j1: int | None = None):
+    """Codes of the 16-bit-uniform mode for the window [j0, j1) of x, and the return code."""
+    ptr, code, n, d = _grads(x)
+    j1 = d if j1 is None else j1
+    esize = 2 if code == BF16 else 4
+    codes = np.zeros((n, j1 - j0), dtype=np.int8)
+    rc = lib().gqo_quantize_u16_cols(ptr + j0 * esize, code, n, d, j0, j1 - j0, float(norm32),
+                                     scheme, s, seed, step, codes.ctypes.data)
+    return codes, rc
+
+
+def quantize_u16_cols(xw: np.ndarray, j0: int, norm32: float, scheme: int, s: int, seed: int,
+                      step: int):
+    """quantize_u16 on the columns j0 .. j0 + w - 1 of a larger matrix, given alone."""
+    ptr, code, n, w = _grads(xw)
+    codes = np.zeros((n, w), dtype=np.int8)
+    rc = lib().gqo_quantize_u16_cols(ptr, code, n, w, j0, w, float(norm32), scheme, s, seed,
+                                     step, codes.ctypes.data)
     return codes, rc
 
 

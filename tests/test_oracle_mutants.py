@@ -54,6 +54,17 @@ MUTANTS = [
     ("final square root dropped", "return p == 2 ? sqrt(outer) : outer;", "return outer;"),
     ("ring starts at worker c", "int code = codes[((c + 1) % n) * w + j];",
      "int code = codes[(c % n) * w + j];"),
+    ("16-bit mode: a tie rounds up", "lvl = lo + (int32_t)((word >> 16) < F);",
+     "lvl = lo + (int32_t)((word >> 16) <= F);"),
+    ("16-bit mode: low half of the word", "lvl = lo + (int32_t)((word >> 16) < F);",
+     "lvl = lo + (int32_t)((word & 0xFFFFu) < F);"),
+    ("16-bit mode: L truncates", "double p16 = round_half_odd((double)ax * (double)c1 * 65536.0);",
+     "double p16 = floor((double)ax * (double)c1 * 65536.0);"),
+    ("16-bit mode: E fraction from the low bits", "*F = (bits & 0x7FFFFFu) >> 7;",
+     "*F = bits & 0xFFFFu;"),
+    ("16-bit mode: no clamp at the top level",
+     "        if (p16 > (double)s * 65536.0)\n            p16 = (double)s * 65536.0;\n", ""),
+    ("16-bit mode: E level off by one", "*lo = s + (ex - 1);", "*lo = s + ex;"),
 ]
 
 
@@ -69,7 +80,7 @@ def test_pins_catch_mutant(tmp_path, name, old, new):
     env = dict(os.environ, GQ_ORACLE_LIB=str(so))
     pins = [os.path.join(ROOT, "tests", f) for f in
             ("test_oracle_philox.py", "test_oracle_norm.py", "test_oracle_quantize.py",
-             "test_oracle_exp_allreduce.py")]
+             "test_oracle_exp_allreduce.py", "test_oracle_u16.py")]
     r = subprocess.run([sys.executable, "-m", "pytest", "-x", "-q", "-p", "no:cacheprovider",
                         *pins], cwd=ROOT, env=env, capture_output=True, text=True, timeout=600)
     assert r.returncode != 0, "pins did not catch mutant %r" % name
