@@ -7,7 +7,8 @@ package is a thin ctypes binding with the same names.  PyTorch supplies device m
 streams only.  There is no CPU fallback: importing the package without a built libgq.so raises.
 """
 from ._binding import (  # noqa: F401
-    BF16, EXP, F16, F32, LINEAR, NORM_INF, NORM_L2, ORDER_RING, ORDER_TREE, SUM_I32, SUM_I8,
+    BF16, EXP, F16, F32, LINEAR, NORM_INF, NORM_L2, ORDER_RING, ORDER_TREE, ROUND_U16, SUM_I32,
+    SUM_I8,
     GQError, gq_abi_version, gq_allreduce_mean, gq_allreduce_mean_noalloc,
     gq_allreduce_mean_segments, gq_allreduce_mean_to, gq_allreduce_mean_with_norm, gq_code_bits,
     gq_code_bytes, gq_code_pitch, gq_debug_status, gq_dequantize, gq_dequantize_sums, gq_dequantize_to,

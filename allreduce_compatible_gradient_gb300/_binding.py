@@ -15,6 +15,7 @@ _LIB_PATH = os.environ.get("GQ_LIBRARY") or os.path.join(_PKG, "libgq.so")
 F32, BF16, F16 = 0, 1, 2
 SUM_I32, SUM_I8 = 0, 1
 LINEAR, EXP = 0, 1
+ROUND_U16 = 16  # added to a scheme: the 16-bit-uniform rounding mode
 NORM_INF, NORM_L2 = 0, 2
 ORDER_TREE, ORDER_RING = 0, 1
 

@@ -18,6 +18,10 @@ using namespace gqh;
 
 namespace {
 
+// The grid of a scheme argument (GQ_ROUND_U16 may be added to select the rounding mode).
+inline int grid_of(int scheme) { return scheme & ~GQ_ROUND_U16; }
+inline int u16_of(int scheme) { return (scheme & GQ_ROUND_U16) ? 1 : 0; }
+
 gq_status check_grads(const void* grads, int dtype, int64_t n, int64_t d) {
     if (!grads || !aligned16(grads)) return GQ_ERR_INVALID;
     if (dtype != GQ_F32 && dtype != GQ_BF16) return GQ_ERR_INVALID;
@@ -27,11 +31,12 @@ gq_status check_grads(const void* grads, int dtype, int64_t n, int64_t d) {
 
 // The sum of n workers' codes fits int8: n s <= 127 (L) or n 2^(s-1) <= 127 (E).
 bool fits_i8(int scheme, int s, int64_t n) {
-    const int64_t unit = scheme == GQ_LINEAR ? s : (int64_t(1) << (s - 1));
+    const int64_t unit = grid_of(scheme) == GQ_LINEAR ? s : (int64_t(1) << (s - 1));
     return n * unit <= 127;
 }
 
 gq_status check_scheme(int scheme, int s, int64_t n) {
+    scheme = grid_of(scheme);
     if (scheme != GQ_LINEAR && scheme != GQ_EXP) return GQ_ERR_INVALID;
     if (scheme == GQ_LINEAR) {
         if (s < 1 || s > 127) return GQ_ERR_UNSUPPORTED;
@@ -111,6 +116,7 @@ gq_status norm_any(const void* grads, int dtype, int mode, int64_t n, int64_t d,
 template <bool OUT, bool TRUSTED>
 gq_status quant_any(const void* grads, int dtype, const gq::QuantArgs& a, int scheme, int bits,
                     void* codes, void* out, cudaStream_t st, unsigned int* status = nullptr) {
+    scheme = grid_of(scheme);  // the rounding mode travels in a.u16
     if (dtype == GQ_F32)
         return scheme == GQ_LINEAR
                    ? quant_f32_l(grads, a, bits, OUT, TRUSTED, codes, out, st, status)
@@ -120,8 +126,9 @@ gq_status quant_any(const void* grads, int dtype, const gq::QuantArgs& a, int sc
 }
 
 gq::QuantArgs make_args(const float* norm_ptr, int dtype, int64_t n, int64_t d, int s,
-                        uint64_t seed, uint64_t step) {
+                        uint64_t seed, uint64_t step, int scheme) {
     gq::QuantArgs a;
+    a.u16 = u16_of(scheme);
     a.norm_ptr = norm_ptr;
     a.s = static_cast<uint32_t>(s);
     a.key0 = static_cast<uint32_t>(seed);
@@ -178,6 +185,7 @@ gq_status gq_workspace_init(void* ws, size_t ws_bytes, void* stream) {
 }
 
 int gq_code_bits(int scheme, int s) {
+    scheme = grid_of(scheme);
     if (scheme != GQ_LINEAR && scheme != GQ_EXP) return 0;
     if (s < 1 || s > (scheme == GQ_LINEAR ? 127 : 24)) return 0;
     return s <= 7 ? 4 : 8;
@@ -208,9 +216,9 @@ gq_status gq_quantize(const void* grads, int dtype, int64_t n, int64_t d, const 
     if (st != GQ_OK) return st;
     if ((st = check_scheme(scheme, s, n)) != GQ_OK) return st;
     if (!norm_dev || !codes || !aligned16(codes)) return GQ_ERR_INVALID;
-    const gq::QuantArgs a = make_args(norm_dev, dtype, n, d, s, seed, step);
-    return quant_any<false, false>(grads, dtype, a, scheme, gq_code_bits(scheme, s), codes,
-                                   nullptr, static_cast<cudaStream_t>(stream));
+    const gq::QuantArgs a = make_args(norm_dev, dtype, n, d, s, seed, step, scheme);
+    return quant_any<false, false>(grads, dtype, a, grid_of(scheme), gq_code_bits(scheme, s),
+                                   codes, nullptr, static_cast<cudaStream_t>(stream));
 }
 
 gq_status gq_reduce_codes(const void* codes, int scheme, int s, int64_t n, int64_t d,
@@ -222,6 +230,7 @@ gq_status gq_reduce_codes(const void* codes, int scheme, int s, int64_t n, int64
     const int bits = gq_code_bits(scheme, s);
     const int64_t row_bytes = gq_code_pitch(d) * bits / 8;
     const int64_t chunks = row_bytes / 16;
+    scheme = grid_of(scheme);  // the sum does not depend on the rounding mode
     cudaStream_t cs = static_cast<cudaStream_t>(stream);
     const unsigned char* c = static_cast<const unsigned char*>(codes);
 #define GQ_REDUCE(BITS, SCH)                                                     \
@@ -248,6 +257,7 @@ gq_status gq_dequantize_sums(const void* sum_dev, int sum_type, const float* nor
     if (n < 1 || n >= (int64_t(1) << 31) || d < 1 || d >= kMaxD) return GQ_ERR_INVALID;
     gq_status st = check_scheme(scheme, s, n);
     if (st != GQ_OK) return st;
+    scheme = grid_of(scheme);  // dequantisation does not depend on the rounding mode
     if (sum_type == GQ_SUM_I8 && !fits_i8(scheme, s, n)) return GQ_ERR_OVERFLOW;
     cudaStream_t cs = static_cast<cudaStream_t>(stream);
     const int64_t quads = (d + 3) / 4;
@@ -288,7 +298,7 @@ gq_status gq_allreduce_mean_to(const void* grads, int dtype, int64_t n, int64_t 
     if ((st = check_ws(ws, ws_bytes, n, d)) != GQ_OK) return st;
     cudaStream_t cs = static_cast<cudaStream_t>(stream);
     const float* ws_norm = &reinterpret_cast<const gq::WsHeader*>(ws)->norm;
-    gq::QuantArgs a = make_args(ws_norm, dtype, n, d, s, seed, step);
+    gq::QuantArgs a = make_args(ws_norm, dtype, n, d, s, seed, step, scheme);
     a.out_dtype = out_dtype;
     // under the l2 norm over the coordinates ((2,2), (inf,2)) most |x| / N lie far below the
     // first level: the quantise pass defers the few uncertain row-groups (compacting consumer)
@@ -297,11 +307,11 @@ gq_status gq_allreduce_mean_to(const void* grads, int dtype, int64_t n, int64_t 
         unsigned char* w = static_cast<unsigned char*>(ws);
         bool taken = false;
         if (dtype == GQ_F32)
-            st = scheme == GQ_LINEAR
+            st = grid_of(scheme) == GQ_LINEAR
                      ? resident_f32_l(grads, a, mode, out_dev, norm_dev, w, cs, &taken)
                      : resident_f32_e(grads, a, mode, out_dev, norm_dev, w, cs, &taken);
         else
-            st = scheme == GQ_LINEAR
+            st = grid_of(scheme) == GQ_LINEAR
                      ? resident_bf16_l(grads, a, mode, out_dev, norm_dev, w, cs, &taken)
                      : resident_bf16_e(grads, a, mode, out_dev, norm_dev, w, cs, &taken);
         if (taken) return st;
@@ -328,7 +338,7 @@ gq_status gq_allreduce_mean_with_norm(const void* grads, int dtype, int64_t n, i
     if ((st = check_scheme(scheme, s, n)) != GQ_OK) return st;
     if (!norm_dev || !out_dev || !aligned16(out_dev) || (codes && !aligned16(codes)))
         return GQ_ERR_INVALID;
-    const gq::QuantArgs a = make_args(norm_dev, dtype, n, d, s, seed, step);
+    const gq::QuantArgs a = make_args(norm_dev, dtype, n, d, s, seed, step, scheme);
     return quant_any<true, false>(grads, dtype, a, scheme, gq_code_bits(scheme, s), codes,
                                   out_dev, static_cast<cudaStream_t>(stream));
 }
@@ -478,15 +488,15 @@ extern "C" gq_status gq_allreduce_mean_noalloc(const void* grads, int dtype, int
     // the single launch's barrier word must start at zero
     if (cudaMemsetAsync(ws, 0, gq::kHeaderBytes, cs) != cudaSuccess) return GQ_ERR_CUDA;
     const float* ws_norm = &reinterpret_cast<const gq::WsHeader*>(ws)->norm;
-    gq::QuantArgs a = make_args(ws_norm, dtype, n, d, s, seed, step);
+    gq::QuantArgs a = make_args(ws_norm, dtype, n, d, s, seed, step, scheme);
     a.smallk = mode == gq::kL2L2 || mode == gq::kMaxL2;  // as gq_allreduce_mean chooses
     if (!codes) {  // small problems: the single launch (its partials fit the scratch too)
         bool taken = false;
         if (dtype == GQ_F32)
-            st = scheme == GQ_LINEAR ? resident_f32_l(grads, a, mode, out_dev, norm_dev, ws, cs, &taken)
+            st = grid_of(scheme) == GQ_LINEAR ? resident_f32_l(grads, a, mode, out_dev, norm_dev, ws, cs, &taken)
                                      : resident_f32_e(grads, a, mode, out_dev, norm_dev, ws, cs, &taken);
         else
-            st = scheme == GQ_LINEAR ? resident_bf16_l(grads, a, mode, out_dev, norm_dev, ws, cs, &taken)
+            st = grid_of(scheme) == GQ_LINEAR ? resident_bf16_l(grads, a, mode, out_dev, norm_dev, ws, cs, &taken)
                                      : resident_bf16_e(grads, a, mode, out_dev, norm_dev, ws, cs, &taken);
         if (taken) return st;
     }
@@ -615,7 +625,7 @@ extern "C" gq_status gq_quantize_sum(const void* grads, int dtype, int64_t m, in
     if (worker0 < 0 || worker0 + m > (int64_t(1) << 31)) return GQ_ERR_INVALID;
     if (sum_type == GQ_SUM_I8 && !fits_i8(scheme, s, m)) return GQ_ERR_OVERFLOW;
     if (ws && (st = check_ws(ws, ws_bytes, m, d)) != GQ_OK) return st;
-    gq::QuantArgs a = make_args(norm_dev, dtype, m, d, s, seed, step);
+    gq::QuantArgs a = make_args(norm_dev, dtype, m, d, s, seed, step, scheme);
     a.row0 = static_cast<uint32_t>(worker0);
     a.sums = sum_dev;
     a.sums_i8 = sum_type == GQ_SUM_I8;
@@ -678,7 +688,7 @@ extern "C" gq_status gq_allreduce_mean_segments(int64_t nseg, const void* const*
     if ((st = check_ws(ws, ws_bytes, n, 1)) != GQ_OK) return st;
     unsigned char* w = static_cast<unsigned char*>(ws);
     cudaStream_t cs = static_cast<cudaStream_t>(stream);
-    gq::QuantArgs base = make_args(nullptr, dtype, n, 1, s, seed, step << 16);
+    gq::QuantArgs base = make_args(nullptr, dtype, n, 1, s, seed, step << 16, scheme);
     base.out_dtype = out_dtype;
     gq::SegLaunch L;  // ~8 KB of kernel parameters per launch
     for (int64_t c0 = 0; c0 < nseg; c0 += gq::kSegChunk) {
@@ -691,14 +701,14 @@ extern "C" gq_status gq_allreduce_mean_segments(int64_t nseg, const void* const*
             L.seg[k].out = out[c0 + k];
         }
         st = dtype == GQ_F32
-                 ? norm_segments_any<float>(mode, L, d + c0, n, scheme, s, norms_dev, w, cs)
-                 : norm_segments_any<uint16_t>(mode, L, d + c0, n, scheme, s, norms_dev, w, cs);
+                 ? norm_segments_any<float>(mode, L, d + c0, n, grid_of(scheme), s, norms_dev, w, cs)
+                 : norm_segments_any<uint16_t>(mode, L, d + c0, n, grid_of(scheme), s, norms_dev, w, cs);
         if (st != GQ_OK) return st;
         if (dtype == GQ_F32)
-            st = scheme == GQ_LINEAR ? quant_segments_f32_l(L, d + c0, n, base, w, cs)
+            st = grid_of(scheme) == GQ_LINEAR ? quant_segments_f32_l(L, d + c0, n, base, w, cs)
                                      : quant_segments_f32_e(L, d + c0, n, base, w, cs);
         else
-            st = scheme == GQ_LINEAR ? quant_segments_bf16_l(L, d + c0, n, base, w, cs)
+            st = grid_of(scheme) == GQ_LINEAR ? quant_segments_bf16_l(L, d + c0, n, base, w, cs)
                                      : quant_segments_bf16_e(L, d + c0, n, base, w, cs);
         if (st != GQ_OK) return st;
     }
@@ -728,7 +738,7 @@ extern "C" gq_status gq_quantize_codes(const void* grads, int dtype, int64_t m, 
     if (code_bits != 8 && !(code_bits == 4 && s <= 7)) return GQ_ERR_INVALID;
     if (worker0 < 0 || worker0 + m > (int64_t(1) << 31)) return GQ_ERR_INVALID;
     if (ws && (st = check_ws(ws, ws_bytes, m, d)) != GQ_OK) return st;
-    gq::QuantArgs a = make_args(norm_dev, dtype, m, d, s, seed, step);
+    gq::QuantArgs a = make_args(norm_dev, dtype, m, d, s, seed, step, scheme);
     a.row0 = static_cast<uint32_t>(worker0);
     unsigned int* status = ws ? &reinterpret_cast<gq::WsHeader*>(ws)->status : nullptr;
     return quant_any<false, false>(grads, dtype, a, scheme, code_bits, codes, nullptr,

@@ -808,7 +808,8 @@ struct QuantArgs {
     void* sums;              // when set, the kernel writes the integer sums here instead of out
     int sums_i8;             // 1: the sums as int8 (they fit: |sum| <= 127), 0: as int32
     int out_dtype;           // kOutF32, kOutBF16 or kOutF16
-    int smallk;              // host hint: Global-E levels above 1 are rare (the (2,2) norm)
+    int smallk;              // host hint: most elements round down (an l2 norm over coordinates)
+    int u16;                 // 1: the 16-bit-uniform rounding mode (decide H < F, no exact path)
 };
 
 // Per-block fp32 dequantisation scale from the fp32 norm, computed in fp64 by one thread:
@@ -843,23 +844,35 @@ __device__ __forceinline__ void store_codes(unsigned char* __restrict__ codes, i
 }
 
 // Per-kernel constants of the rounding decision.
+// Exact mode: the addend c0 = 128 + 0xFFFD 2^-16 (so y = bits - H holds P_c + 0xFFFD - H), the
+// decision is certain when y's low half is at most 0xFFFB.  16-bit-uniform mode: c0 = 128 +
+// 0xFFFF 2^-16, so that y's high half is the level index plus [H < F]: every decision is final.
 struct Decide {
     float nrm;        // N
     float rcp;        // RN(1 / N)
     float c1;         // L: RN(s / N); E: 2^(s-1) RN(1 / N)
-    float c0;         // 128 + 0xFFFD 2^-16: the addend that places P in 16.16 fixed point
+    float c0;         // the addend that places P in 16.16 fixed point (see above)
     bool fast;        // 2^-100 <= N <= 2^100: the fast path's products stay normal and finite
     uint32_t bigmin;  // E: bits of 2^-(s-1)
     uint32_t cbig;    // E: ((s - 127) << 16) + bits of c0
+    uint32_t bigpb;   // bits of c0 + 2^16 units: P_c >= 1 from here on
+    uint32_t win;     // largest certain low half of y: 0xFFFB (exact), 0xFFFF (16-bit mode)
+    uint32_t lsub;    // (bits of fp32(P_c + c0)) - lsub = the compacting test's bound on F
 };
 
 template <int SCHEME>
-__device__ __forceinline__ Decide make_decide(float nrm, uint32_t s) {
+__device__ __forceinline__ Decide make_decide(float nrm, uint32_t s, int u16) {
     Decide dc;
+    const uint32_t c0b = u16 ? 0x4300FFFFu : 0x4300FFFDu;
     dc.nrm = nrm;
     dc.rcp = __frcp_rn(nrm);
     dc.fast = nrm >= 0x1p-100f && nrm <= 0x1p100f;
-    dc.c0 = __uint_as_float(0x4300FFFDu);
+    dc.c0 = __uint_as_float(c0b);
+    dc.bigpb = c0b + 0x10000u;
+    dc.win = u16 ? 0xFFFFu : 0xFFFBu;
+    // exact mode: certain down when min H >= P_c + 3, i.e. bits - (c0 bits - 3) <= min H;
+    // 16-bit mode: down when min H >= F = bits - c0 bits
+    dc.lsub = u16 ? c0b : c0b - 3u;
     if (SCHEME == kLinear) {
         dc.c1 = __fdiv_rn(static_cast<float>(s), nrm);
         dc.bigmin = 0u;
@@ -867,7 +880,7 @@ __device__ __forceinline__ Decide make_decide(float nrm, uint32_t s) {
     } else {
         dc.c1 = dc.rcp * exp2i(static_cast<int>(s) - 1);
         dc.bigmin = (128u - s) << 23;
-        dc.cbig = ((s - 127u) << 16) + 0x4300FFFDu;
+        dc.cbig = ((s - 127u) << 16) + c0b;
     }
     return dc;
 }
@@ -891,9 +904,12 @@ __device__ __forceinline__ uint32_t decide_rows(const float (&xv)[R][kQCols], co
     uint32_t worst[R];
     bool anybig = false;
     uint32_t pbs[R][kQCols];
+    // rows sent to the exact path whatever their estimates: all of them for a norm outside the
+    // fast path's range, and rows holding a NaN (in both rounding modes)
+    uint32_t force = dc.fast ? 0u : (1u << R) - 1u;
 #pragma unroll
     for (int u = 0; u < R; ++u) {
-        worst[u] = dc.fast ? 0u : 0xFFFFu;
+        worst[u] = 0u;
 #pragma unroll
         for (int c = 0; c < kQCols; ++c) {
             const float ax = fabsf(xv[u][c]);
@@ -906,9 +922,9 @@ __device__ __forceinline__ uint32_t decide_rows(const float (&xv)[R][kQCols], co
                 // below 2^-(s-1) (P < 1, the common case under l2 norms): P read as for L;
                 // at or above it the binade form is computed for the row (see below)
                 pb = __float_as_uint(__fmaf_rn(ax, dc.c1, dc.c0));
-                anybig |= pb >= 0x4301FFFDu;  // P_c >= 1
+                anybig |= pb >= dc.bigpb;  // P_c >= 1
             }
-            if (!TRUSTED && !(ax == ax)) worst[u] |= 0xFFFFu;  // NaN: decided on the exact path
+            if (!TRUSTED && !(ax == ax)) force |= 1u << u;  // NaN: decided on the exact path
             pbs[u][c] = pb;
         }
     }
@@ -942,19 +958,20 @@ __device__ __forceinline__ uint32_t decide_rows(const float (&xv)[R][kQCols], co
     uint32_t wall = worst[0];
 #pragma unroll
     for (int u = 1; u < R; ++u) wall = __vmaxu2(wall, worst[u]);
-    if ((wall & 0xFFFFu) <= 0xFFFBu && !(SCHEME == kLinear && (wall >> 16) > a.s + kOff))
+    if (force == 0u && (wall & 0xFFFFu) <= dc.win &&
+        !(SCHEME == kLinear && (wall >> 16) > a.s + kOff))
         return big;
 #pragma unroll
     for (int u = 0; u < R; ++u) {
         const bool over = SCHEME == kLinear && (worst[u] >> 16) > a.s + kOff;
-        if ((worst[u] & 0xFFFFu) > 0xFFFBu || over) {
+        if ((worst[u] & 0xFFFFu) > dc.win || over || ((force >> u) & 1u)) {
             const uint4 rb = philox4x32_10_rk(
                 make_uint4(g32 | 0x80000000u, row0 + u, a.step_lo, a.step_hi), a.rk);
             const uint32_t bw[4] = {rb.x, rb.y, rb.z, rb.w};
 #pragma unroll
             for (int c = 0; c < kQCols; ++c) {
                 const uint32_t y = yk[u][c];
-                const bool need = !dc.fast || (y & 0xFFFFu) > 0xFFFBu ||
+                const bool need = !dc.fast || (y & 0xFFFFu) > dc.win ||
                                   (SCHEME == kLinear && (y >> 16) > a.s + kOff) ||
                                   (!TRUSTED && !(xv[u][c] == xv[u][c]));
                 if (!need) continue;
@@ -1001,8 +1018,9 @@ __device__ __forceinline__ unsigned long long add2rz(unsigned long long a, unsig
 }
 // Accumulate one row-group's codes (k = (yk >> 16) - 0x4300) into the sums (fp32, exact:
 // integers below 2^24) and return the signed codes.  The level value is read off bit patterns:
-// L: yk read as a float is 128 + k + f, f = (low half) 2^-16 < 1 (at most 0xFFFB on the fast
-// path, 0 from the exact one), so adding 2^23 - 128 with rounding toward zero gives exactly
+// L: yk read as a float is 128 + k + f, f = (low half) 2^-16 < 1 (at most 0xFFFB on the exact
+// mode's fast path, 0xFFFF in the 16-bit mode, 0 from the exact path), so adding 2^23 - 128
+// with rounding toward zero gives exactly
 // 2^23 + k (floating-point adds, off the integer pipe); E: the float with exponent field k + 126
 // is 2^(k-1), and (v + 2^23) - 2^23 turns k = 0 (0.5) into 0 (the tie rounds to the even 2^23).
 // The subtractions and the signed accumulation run on column pairs.
@@ -1309,7 +1327,7 @@ __device__ __forceinline__ void quantize_body(const T* __restrict__ x, const Qua
     const float nrm = __ldg(a.norm_ptr);
     const float scale = block_scale<SCHEME>(nrm, a.n, a.s, &sh_scale);
     const bool live = nrm > 0.0f && nrm < __uint_as_float(kInfBits);
-    const Decide dc = make_decide<SCHEME>(nrm, a.s);
+    const Decide dc = make_decide<SCHEME>(nrm, a.s, a.u16);
     // groups [0, full) are staged through shared memory; the rest (the ragged last group, code
     // padding, or everything when rows are not 16-byte aligned) use direct loads
     int64_t full = 0;
@@ -1801,7 +1819,7 @@ __device__ __forceinline__ void tma_consume_compact(const unsigned char* stage, 
         const uint32_t minh = min(h2 & 0xFFFFu, h2 >> 16);
         const uint32_t pbm = __float_as_uint(__fmaf_rn(mx[u], dc.c1, dc.c0));
         // P_c + 3 > min H (unsigned: a NaN, infinite or P_c >= 1 estimate always queues)
-        const bool nd = __float_as_uint(mx[u]) != 0u && (!dc.fast || pbm - 0x4300FFFAu > minh);
+        const bool nd = __float_as_uint(mx[u]) != 0u && (!dc.fast || pbm - dc.lsub > minh);
         mk[u] = __ballot_sync(0xFFFFFFFFu, nd);
         tot += __popc(mk[u]);
     }
@@ -1950,7 +1968,7 @@ quantize_tma_kernel(const T* __restrict__ x, QuantArgs a, int64_t groups,
         }
     } else if (COMPACT && nchunks > 0) {  // consumers, compacting
         static_assert(!COMPACT || CODE_BITS == 0, "the compacting consumer writes no codes");
-        const Decide dc = make_decide<SCHEME>(nrm, a.s);
+        const Decide dc = make_decide<SCHEME>(nrm, a.s, a.u16);
         const int lane = tid & 31;
         const WarpQueue<T> wq = warp_queue<T>(tma_smem + Cfg::kSmemBytes, tid >> 5);
 #pragma unroll
@@ -1991,7 +2009,7 @@ quantize_tma_kernel(const T* __restrict__ x, QuantArgs a, int64_t groups,
             sh_abort = 1;
         }
     } else if (nchunks > 0) {  // consumers
-        const Decide dc = make_decide<SCHEME>(nrm, a.s);
+        const Decide dc = make_decide<SCHEME>(nrm, a.s, a.u16);
         const int lane = tid & 31;
         uint32_t item = 0;
         bool ok = true;
@@ -2026,7 +2044,7 @@ quantize_tma_kernel(const T* __restrict__ x, QuantArgs a, int64_t groups,
 
     // ---- the groups [full, groups): ragged last group, code padding, or all of them when the
     // norm is 0 or not finite; direct loads by the consumer threads
-    const Decide dc = make_decide<SCHEME>(nrm, a.s);
+    const Decide dc = make_decide<SCHEME>(nrm, a.s, a.u16);
     const int64_t rest = groups - full;
     const int64_t stride = static_cast<int64_t>(gridDim.x) * kTmaConsumers;
     for (int64_t it = static_cast<int64_t>(blockIdx.x) * kTmaConsumers + tid; it < rest;
@@ -2116,7 +2134,7 @@ quantize_seg_tma_kernel(const __grid_constant__ SegLaunch L, QuantArgs base, int
             k = find_segment(L, cg);
             a.d = L.seg[k].d;
             a.step_lo = base.step_lo | static_cast<uint32_t>(L.seg0 + k);
-            dc = make_decide<SCHEME>(norms[k], a.s);
+            dc = make_decide<SCHEME>(norms[k], a.s, a.u16);
             scale = scales[k];
         }
         const SegDesc& sd = L.seg[k];
@@ -2159,7 +2177,7 @@ quantize_seg_tma_kernel(const __grid_constant__ SegLaunch L, QuantArgs base, int
             a.vec_rows = sd.nb > 0;
             a.step_lo = base.step_lo | static_cast<uint32_t>(L.seg0 + k);
             a.norm_ptr = norms + k;
-            dc = make_decide<SCHEME>(norms[k], a.s);
+            dc = make_decide<SCHEME>(norms[k], a.s, a.u16);
             scale = scales[k];
         }
         const int64_t g = (sd.d + kQCols - 1) / kQCols - 1 - (it - sd.t0);
@@ -2470,7 +2488,7 @@ resident_kernel(const T* __restrict__ x, QuantArgs a, int64_t gpb, void* __restr
         const float n32 = norm_from_combined<MODE>(comb);
         sh_norm = n32;
         sh_scale = dequant_scale(SCHEME, n32, n, a.s);
-        sh_dc = make_decide<SCHEME>(n32, a.s);
+        sh_dc = make_decide<SCHEME>(n32, a.s, a.u16);
         if (blockIdx.x == 0) {
             hdr->norm = n32;
             if (norm_user) *norm_user = n32;

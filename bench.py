@@ -57,6 +57,8 @@ def _args():
                          "same kernels, e.g. for an ncu capture); named '<workload>_d<columns>'")
     ap.add_argument("--measure", default=None, choices=["exp-reduce", "segments", "sweep"],
                     help="extra measurement instead of the main bench line")
+    ap.add_argument("--rounding", default="exact", choices=["exact", "u16"],
+                    help="rounding mode: exact (default) or the 16-bit-uniform option")
     return ap.parse_args()
 
 
@@ -286,7 +288,9 @@ def run_reference(a, cfg):
 
 def _config_block(cfg, ngpus):
     return {"workload": cfg["name"], "n": cfg["n"], "d": cfg["d"], "input_dtype": cfg["dtype"],
-            "distribution": cfg["dist"], "scheme": "Global-L" if cfg["scheme"] == 0 else "Global-E",
+            "distribution": cfg["dist"],
+            "scheme": "Global-L" if cfg["scheme"] & 1 == 0 else "Global-E",
+            "rounding": "16-bit uniform" if cfg["scheme"] & 16 else "exact",
             "s": cfg["s"], "q": "inf" if cfg["q"] == 0 else 2, "p": "inf" if cfg["p"] == 0 else 2,
             "philox_seed": cfg["seed"], "parallelism": "replica x%d" % ngpus,
             "l2": "flushed between timed steps (512 MiB write, then 256 MiB read); input %.1f MB > 129 MB L2"
@@ -526,6 +530,9 @@ def main():
     from allreduce_compatible_gradient_gb300 import workloads
 
     cfg = dict(workloads.CONFIGS[a.config], name=a.config)
+    if a.rounding == "u16":
+        cfg["scheme"] |= 16  # GQ_ROUND_U16
+        cfg["name"] += "_u16"
     if a.columns is not None:
         if a.columns < 1:
             raise SystemExit("--columns must be positive")

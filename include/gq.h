@@ -79,6 +79,26 @@ typedef enum {
     GQ_EXP = 1     /* Global-E_s, exponential dithering */
 } gq_scheme;
 
+/*
+ * Rounding mode, added to the scheme argument of any call (GQ_LINEAR | GQ_ROUND_U16): the
+ * 16-bit-uniform mode.  The pages require an unbiased random rounding and fix no random source;
+ * by default the decision is exact (round up iff r < T, r the full 32-bit word).  In this mode
+ * element (i, j) rounds up iff H < F, where H is the high 16 bits of its word r and F a 16-bit
+ * fraction of its grid position computed without a division:
+ *   Global-L_s: P16 = |x| fp32(s / N) 2^16 rounded to the nearest integer, ties to the odd one,
+ *               at most s 2^16; lower level P16 >> 16, F = P16 & 0xFFFF;
+ *   Global-E_s: w = min(fp32(|x| fp32(1 / N)), 1); for w >= 2^-(s-1) lower level s + e with
+ *               2^e <= w < 2^(e+1) and F the top 16 of w's 23 fraction bits; below, P16 =
+ *               |x| fp32(1 / N) 2^(s-1) 2^16 rounded as for L, lower level P16 >> 16,
+ *               F = P16 & 0xFFFF.
+ * P(up) = F / 2^16, so the estimate's bias is below 2^-16 + 2^-22 of a level spacing per
+ * element.  A NaN element gets code 0; for a norm outside [2^-100, 2^100] the decision is the
+ * exact mode's.  Codes, sums and outputs have the same layout; gq_reduce_codes and the
+ * dequantising calls ignore the flag.  No counterpart in the paper beyond its unbiased rounding:
+ * an option of this library.
+ */
+#define GQ_ROUND_U16 16
+
 /* Norm orders for q and p. */
 #define GQ_NORM_INF 0
 #define GQ_NORM_L2 2
