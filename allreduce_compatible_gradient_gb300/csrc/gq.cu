@@ -148,6 +148,7 @@ gq::QuantArgs make_args(const float* norm_ptr, int dtype, int64_t n, int64_t d, 
     a.sums_i8 = 0;
     a.out_dtype = gq::kOutF32;
     a.smallk = 0;
+    a.pdl = 0;
     return a;
 }
 
@@ -318,6 +319,7 @@ gq_status gq_allreduce_mean_to(const void* grads, int dtype, int64_t n, int64_t 
     }
     if ((st = norm_any(grads, dtype, mode, n, d, norm_dev, ws, cs)) != GQ_OK) return st;
     unsigned int* status = &reinterpret_cast<gq::WsHeader*>(ws)->status;
+    a.pdl = 1;  // the quantise pass's launch overlaps the norm pass's tail
     return quant_any<true, true>(grads, dtype, a, scheme, gq_code_bits(scheme, s), codes, out_dev,
                                  cs, status);
 }
@@ -504,6 +506,7 @@ extern "C" gq_status gq_allreduce_mean_noalloc(const void* grads, int dtype, int
     // the scratch's status word lets large aligned problems take the bulk-copy kernel, as
     // gq_allreduce_mean does (its bounded waits record a timeout there; nothing reads it back)
     unsigned int* status = &reinterpret_cast<gq::WsHeader*>(ws)->status;
+    a.pdl = 1;
     return quant_any<true, true>(grads, dtype, a, scheme, gq_code_bits(scheme, s), codes, out_dev,
                                  cs, status);
 }

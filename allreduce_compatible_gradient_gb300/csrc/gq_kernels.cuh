@@ -87,6 +87,17 @@ __device__ __forceinline__ float dequant_scale(int scheme, float nrm, int64_t n,
                : static_cast<float>(ldexp(num, -static_cast<int>(s - 1)) / static_cast<double>(n));
 }
 
+// Programmatic dependent launch between the two passes of the fused call: the norm kernel lets
+// the launch of the kernel after it on the stream (the quantise pass) begin at once, and the
+// quantise kernel waits, before reading anything, until the norm kernel has completed and its
+// writes are visible.  Launched without the attribute, the wait returns at once.  Every norm
+// kernel's grid is one wave of resident blocks, so the dependent blocks, which can only be
+// placed where the norm blocks leave room, never hold back a norm block.
+__device__ __forceinline__ void pdl_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 // ------------------------------------------------------------------------------------------
 // Philox4x32-10 (Salmon, Moraes, Dror, Shaw, SC'11): ten rounds of the Philox-4x32 bijection.
 // Each round multiplies counter words 0 and 2 by the round multipliers (full 64-bit products),
@@ -634,6 +645,7 @@ __global__ void __launch_bounds__(kThreads, MODE == kL2Max ? 2 : (MODE == kMaxL2
 norm_kernel(const T* __restrict__ x, int64_t n, int64_t d, int64_t groups, bool vec_rows,
             float* __restrict__ norm_user, double* __restrict__ part_user,
             unsigned char* __restrict__ ws) {
+    pdl_launch_dependents();
     WsHeader* hdr = reinterpret_cast<WsHeader*>(ws);
     const NormSlots slots{reinterpret_cast<uint64_t*>(ws + kHeaderBytes), &hdr->ticket,
                           &hdr->status, &hdr->norm, norm_user, part_user};
@@ -650,6 +662,7 @@ norm_flat_kernel(const T* __restrict__ x, int64_t total, float* __restrict__ nor
     static_assert(MODE == kMaxMax || MODE == kL2L2, "flat norms: (inf, inf) and (2, 2)");
     constexpr int C = Elem<T>::kCols;
     constexpr int U = MODE == kMaxMax ? 16 : 8;  // 16-byte loads in flight per thread
+    pdl_launch_dependents();
     WsHeader* hdr = reinterpret_cast<WsHeader*>(ws);
     const NormSlots slots{reinterpret_cast<uint64_t*>(ws + kHeaderBytes), &hdr->ticket,
                           &hdr->status, &hdr->norm, norm_user, part_user};
@@ -810,6 +823,7 @@ struct QuantArgs {
     int out_dtype;           // kOutF32, kOutBF16 or kOutF16
     int smallk;              // host hint: most elements round down (an l2 norm over coordinates)
     int u16;                 // 1: the 16-bit-uniform rounding mode (decide H < F, no exact path)
+    int pdl;                 // host: launch the quantise pass dependent on the norm pass
 };
 
 // Per-block fp32 dequantisation scale from the fp32 norm, computed in fp64 by one thread:
@@ -1361,6 +1375,7 @@ __global__ void __launch_bounds__(kThreads, 2)
 quantize_kernel(const T* __restrict__ x, QuantArgs a, int64_t groups,
                 unsigned char* __restrict__ codes, void* __restrict__ out) {
     extern __shared__ uint4 stage[];
+    pdl_wait();  // the norm of the fused call's first pass
     quantize_body<T, SCHEME, CODE_BITS, WRITE_OUT, TRUSTED>(x, a, groups, codes, out, stage,
                                                             blockIdx.x, gridDim.x);
 }
@@ -1937,6 +1952,7 @@ quantize_tma_kernel(const T* __restrict__ x, QuantArgs a, int64_t groups,
     __shared__ volatile int sh_abort;
 
     const int tid = threadIdx.x;
+    pdl_wait();  // the norm of the fused call's first pass
     const float nrm = __ldg(a.norm_ptr);
     const float scale = block_scale<SCHEME>(nrm, a.n, a.s, &sh_scale);
     const bool live = nrm > 0.0f && nrm < __uint_as_float(kInfBits);

@@ -5,6 +5,29 @@
 
 namespace gqh {
 
+// A kernel launch, programmatically dependent on the previous kernel on the stream when pdl
+// (the quantise pass after the norm pass of the fused call: its launch overlaps the norm pass's
+// tail, and the kernel waits for the norm in griddepcontrol.wait).
+template <typename... P, typename... A>
+gq_status launch(void (*kernel)(P...), unsigned grid, unsigned block, size_t smem,
+                 cudaStream_t st, bool pdl, A... args) {
+    if (!pdl) {
+        kernel<<<grid, block, smem, st>>>(args...);
+        return launch_status();
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(block);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, args...) == cudaSuccess ? GQ_OK : GQ_ERR_CUDA;
+}
+
 // ---- quantize (+ sum + dequantize) ----------------------------------------------------------
 // TRUSTED: the norm comes from norm_kernel on the same gradients (fused path), so a finite norm
 // rules out NaN and infinite elements.
@@ -31,16 +54,14 @@ gq_status run_quant(const void* grads, const gq::QuantArgs& a, void* codes, void
         }
         if (blocks_per_sm(kt, tsmem, gq::kTmaBlock) < 1) return GQ_ERR_CUDA;
         const unsigned grid = static_cast<unsigned>(sm_count());
-        kt<<<grid, gq::kTmaBlock, tsmem, st>>>(static_cast<const T*>(grads), a, groups,
-                                               static_cast<unsigned char*>(codes), out, status);
-        return launch_status();
+        return launch(kt, grid, gq::kTmaBlock, tsmem, st, a.pdl != 0, static_cast<const T*>(grads),
+                      a, groups, static_cast<unsigned char*>(codes), out, status);
     }
     auto k = gq::quantize_kernel<T, SCHEME, BITS, OUT, TRUSTED>;
     constexpr int smem = gq::Staging<T>::kBytes;
     const unsigned grid = grid_for(k, groups, INT32_MAX, smem);
-    k<<<grid, kThreads, smem, st>>>(static_cast<const T*>(grads), a, groups,
-                                    static_cast<unsigned char*>(codes), out);
-    return launch_status();
+    return launch(k, grid, kThreads, smem, st, a.pdl != 0, static_cast<const T*>(grads), a, groups,
+                  static_cast<unsigned char*>(codes), out);
 }
 
 template <typename T, int SCHEME, bool OUT, bool TRUSTED>

@@ -222,7 +222,7 @@ def _oracle_window(cfg: dict, seconds: float):
     w = min(d, 1 << 14)
     x = workloads.host_inputs(cfg["dist"], cfg["n"], w, seed=cfg["input_seed"], dtype=cfg["dtype"])
     t0 = time.perf_counter()
-    gq_oracle.allreduce_mean(x, cfg["q"], cfg["p"], cfg["scheme"], cfg["s"], cfg["seed"],
+    gq_oracle.allreduce_mean(x, cfg["q"], cfg["p"], cfg["scheme"] & 1, cfg["s"], cfg["seed"],
                              cfg["step"])
     dt = time.perf_counter() - t0
     w = int(min(d, max(w, w * seconds / max(dt, 1e-6))))
@@ -236,7 +236,7 @@ def _time_oracle(cfg: dict, w: int, x) -> dict:
 
     elt = 2 if cfg["dtype"] == "bf16" else 4
     t0 = time.perf_counter()
-    gq_oracle.allreduce_mean(x, cfg["q"], cfg["p"], cfg["scheme"], cfg["s"], cfg["seed"],
+    gq_oracle.allreduce_mean(x, cfg["q"], cfg["p"], cfg["scheme"] & 1, cfg["s"], cfg["seed"],
                              cfg["step"])
     dt = time.perf_counter() - t0
     return {"value": round(cfg["n"] * w * elt / dt / 1e9, 6), "unit": UNIT, "cores": 1,
