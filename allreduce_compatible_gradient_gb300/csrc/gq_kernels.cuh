@@ -1563,8 +1563,7 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_
 // tested for being +-0 across the warp and skipped if so; the first pair with a non-zero element
 // clears `probe` for the rest of the chunk (zero blocks of sparse layers span whole columns, so a
 // chunk is either zero in every row or dense).
-template <typename T, int SCHEME, int CODE_BITS, bool TRUSTED, int SUB, bool SMALLK = false,
-          bool ZSKIP = false>
+template <typename T, int SCHEME, int CODE_BITS, bool TRUSTED, int SUB, bool ZSKIP = false>
 __device__ __forceinline__ void tma_consume_stage(const unsigned char* stage, int lane, bool active,
                                                   int64_t b, int64_t g, const PhiloxGroup& pg,
                                                   const QuantArgs& a, const Decide& dc,
@@ -1622,20 +1621,12 @@ __device__ __forceinline__ void tma_consume_stage(const unsigned char* stage, in
             aw[u][0] = ra.x; aw[u][1] = ra.y; aw[u][2] = ra.z; aw[u][3] = ra.w;
         }
         uint32_t yk[SUB][kQCols];
-        const uint32_t big = decide_rows<SCHEME, TRUSTED, SUB>(
-            v, dc, a, g32, static_cast<uint32_t>(r0) + a.row0, aw, yk);
-        // SMALLK (Global-E under the (2,2) norm, where levels above 1 are rare): when no row of
-        // the warp holds one, the level value 2^(k-1) [k >= 1] is k itself and the rows take the
-        // Global-L accumulation (decided per warp, so the warp does not diverge)
-        const bool small = SMALLK && SCHEME == kExp && !__any_sync(__activemask(), big != 0u);
+        decide_rows<SCHEME, TRUSTED, SUB>(v, dc, a, g32, static_cast<uint32_t>(r0) + a.row0, aw, yk);
 #pragma unroll
         for (int u = 0; u < SUB; ++u) {
             if (r0 + u >= a.n) break;
             int32_t code[kQCols];
-            if (small)
-                accumulate_row<kLinear>(v[u], yk[u], S, code);
-            else
-                accumulate_row<SCHEME>(v[u], yk[u], S, code);
+            accumulate_row<SCHEME>(v[u], yk[u], S, code);
             if (CODE_BITS) store_codes<CODE_BITS>(codes, r0 + u, g, a.pitch, code);
         }
     }
@@ -1933,11 +1924,10 @@ __device__ __forceinline__ bool tma_wait_full(uint32_t item, uint64_t (&full_bar
     return __all_sync(0xFFFFFFFFu, got && !*abort_flag);
 }
 
-// SMALLK: Global-E warps whose levels are all 0 or 1 take the Global-L accumulation.  ZSKIP:
-// rows that are zero across the whole warp skip their random words.  COMPACT (no codes): the
-// compacting consumer above; the dynamic shared memory then holds its queues after the ring.
+// ZSKIP: rows that are zero across the whole warp skip their random words.  COMPACT (no codes):
+// the compacting consumer above; the dynamic shared memory then holds its queues after the ring.
 template <typename T, int SCHEME, int CODE_BITS, bool WRITE_OUT, bool TRUSTED, int SUB,
-          bool SMALLK = false, bool ZSKIP = false, bool COMPACT = false>
+          bool ZSKIP = false, bool COMPACT = false>
 __global__ void __launch_bounds__(kTmaBlock, 1)
 quantize_tma_kernel(const T* __restrict__ x, QuantArgs a, int64_t groups,
                     unsigned char* __restrict__ codes, void* __restrict__ out,
@@ -2044,7 +2034,7 @@ quantize_tma_kernel(const T* __restrict__ x, QuantArgs a, int64_t groups,
                 }
                 const unsigned char* stage =
                     tma_smem + (item % NS) * Cfg::kStageBytes + tid * kQCols * sizeof(T);
-                tma_consume_stage<T, SCHEME, CODE_BITS, TRUSTED, SUB, SMALLK, ZSKIP>(
+                tma_consume_stage<T, SCHEME, CODE_BITS, TRUSTED, SUB, ZSKIP>(
                     stage, lane, active, b, g, pg, a, dc, smem_u32(&empty_bar[item % NS]), S,
                     codes, &probe);
             }

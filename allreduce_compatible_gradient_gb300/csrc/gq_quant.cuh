@@ -39,16 +39,16 @@ gq_status run_quant(const void* grads, const gq::QuantArgs& a, void* codes, void
     const int64_t groups = BITS ? a.pitch / gq::kQCols : (a.d + gq::kQCols - 1) / gq::kQCols;
     const int64_t chunks = (a.d / gq::kQCols) / gq::kTmaConsumers;
     if (status && a.vec_rows && chunks >= sm_count()) {
-        auto kt = gq::quantize_tma_kernel<T, SCHEME, BITS, OUT, TRUSTED, 2, false, true>;
+        auto kt = gq::quantize_tma_kernel<T, SCHEME, BITS, OUT, TRUSTED, 2, true>;
         int tsmem = gq::TmaCfg<T>::kSmemBytes;
         if constexpr (BITS == 0 && OUT && !TRUSTED) {  // one rank's sums: often a single worker
-            if (a.n == 1) kt = gq::quantize_tma_kernel<T, SCHEME, BITS, OUT, TRUSTED, 1, false, true>;
+            if (a.n == 1) kt = gq::quantize_tma_kernel<T, SCHEME, BITS, OUT, TRUSTED, 1, true>;
         }
         if constexpr (BITS == 0 && OUT && TRUSTED) {
             // under an l2 norm over all coordinates most elements round down: the compacting
             // consumer
             if (a.smallk) {
-                kt = gq::quantize_tma_kernel<T, SCHEME, BITS, OUT, TRUSTED, 2, false, false, true>;
+                kt = gq::quantize_tma_kernel<T, SCHEME, BITS, OUT, TRUSTED, 2, false, true>;
                 tsmem += gq::CompactCfg<T>::kBytes;
             }
         }
