@@ -1641,24 +1641,32 @@ __device__ __forceinline__ void tma_consume_stage(const unsigned char* stage, in
 // instructions per row-group.  The row-groups that fail it are queued per warp in shared memory
 // (raw values, random words, group and worker) and decided 32 at a time, one per lane, with the
 // full decision; their code values go into per-warp integer sums in shared memory (exact:
-// integers below 2^24), which each group's owner lane reads when its chunk is done.  So the
-// rare full decisions run on full warps instead of one lane at a time.
+// integers below 2^24), which each group's owner lane reads when its chunk's sums are complete.
+// So the rare full decisions run on full warps instead of one lane at a time.  With two sum
+// buffers (bf16, whose ring is small enough to leave room for them) a chunk's queue is not
+// decided at its end: the next chunk adds to the other buffer, and one flush completes both, so
+// flushes run on fuller queues and less often.  A queued item carries its buffer in bit 31 of
+// its group index (group indices stay below 2^31).
 constexpr int kQueue = 32;  // queued row-groups per warp
 
 template <typename T>
 struct CompactCfg {
     static constexpr int kXVec = sizeof(T) == 4 ? 2 : 1;  // 16-byte pieces of a row-group
-    // per warp: raw values, random words, (group, worker), then the 8 x 32 integer sums
-    static constexpr int kWarpBytes = kQueue * (16 * kXVec + 16 + 8) + kQCols * 32 * 4;
+    static constexpr int kSumBufs = sizeof(T) == 2 ? 2 : 1;
+    static constexpr int kStages = sizeof(T) == 2 ? 5 : TmaCfg<T>::kStages;  // ring stages
+    // per warp: raw values, random words, (group, worker), then the 8 x 32 integer sums per
+    // buffer
+    static constexpr int kWarpBytes = kQueue * (16 * kXVec + 16 + 8) + kSumBufs * kQCols * 32 * 4;
     static constexpr int kBytes = kTmaWarps * kWarpBytes;
+    static constexpr int kSmemBytes = kStages * TmaCfg<T>::kStageBytes + kBytes;  // ring + queues
 };
 
 template <typename T>
 struct WarpQueue {
     uint4* qx;     // [kQueue][kXVec]
     uint4* qw;     // [kQueue]
-    uint2* qm;     // [kQueue]: group, worker
-    int32_t* sum;  // [kQCols][32]: column c of the group owned by lane l at c * 32 + l
+    uint2* qm;     // [kQueue]: group (bit 31: sum buffer), worker
+    int32_t* sum;  // [kSumBufs][kQCols][32]: column c of the group owned by lane l at c * 32 + l
 };
 
 template <typename T>
@@ -1677,7 +1685,16 @@ __device__ __forceinline__ WarpQueue<T> warp_queue(unsigned char* base, int warp
 // magnitude bits; a trusted norm rules NaN out, so fp32 maxima of |x| are used there).
 template <typename T, bool TRUSTED>
 __device__ __forceinline__ float group_max_abs(const uint4 (&raw)[CompactCfg<T>::kXVec]) {
-    if (sizeof(T) == 2) {
+    if (sizeof(T) == 2 && TRUSTED) {
+        // bf16 pairs: max.xorsign.abs gives max(|a|, |b|) per half (its sign bit, the xor of
+        // the operands' signs, is dropped by the final fabsf)
+        const uint4 r = raw[0];
+        uint32_t m1, m2, m;
+        asm("max.xorsign.abs.bf16x2 %0, %1, %2;" : "=r"(m1) : "r"(r.x), "r"(r.y));
+        asm("max.xorsign.abs.bf16x2 %0, %1, %2;" : "=r"(m2) : "r"(r.z), "r"(r.w));
+        asm("max.xorsign.abs.bf16x2 %0, %1, %2;" : "=r"(m) : "r"(m1), "r"(m2));
+        return fmaxf(fabsf(__uint_as_float(m << 16)), fabsf(__uint_as_float(m & 0xFFFF0000u)));
+    } else if (sizeof(T) == 2) {
         const uint4 r = raw[0];
         const uint32_t m = __vmaxu2(__vmaxu2(r.x & 0x7FFF7FFFu, r.y & 0x7FFF7FFFu),
                                     __vmaxu2(r.z & 0x7FFF7FFFu, r.w & 0x7FFF7FFFu));
@@ -1738,14 +1755,14 @@ __device__ __forceinline__ void flush_queue(const WarpQueue<T>& q, int cnt, int 
         widen_raw<T>(raw, v[0]);
         const uint32_t aw[1][4] = {{w.x, w.y, w.z, w.w}};
         uint32_t yk[1][kQCols];
-        decide_rows<SCHEME, TRUSTED, 1>(v, dc, a, m.x, m.y, aw, yk);
-        const int owner = static_cast<int>(m.x & 31u);
+        decide_rows<SCHEME, TRUSTED, 1>(v, dc, a, m.x & 0x7FFFFFFFu, m.y, aw, yk);
+        int32_t* sum = q.sum + (m.x >> 31) * (kQCols * 32) + (m.x & 31u);
 #pragma unroll
         for (int c = 0; c < kQCols; ++c) {
             const int32_t k = static_cast<int32_t>(yk[0][c] >> 16) - 0x4300;
             int32_t units = SCHEME == kLinear ? k : ((1 << k) >> 1);
             if (__float_as_uint(v[0][c]) >> 31) units = -units;
-            if (units != 0) atomicAdd(&q.sum[c * 32 + owner], units);
+            if (units != 0) atomicAdd(&sum[c * 32], units);
         }
     }
     __syncwarp();
@@ -1769,10 +1786,11 @@ __device__ __forceinline__ void push_item(const WarpQueue<T>& q, int pos,
     q.qm[pos] = make_uint2(g32, worker);
 }
 
-// One stage (rows r0 .. r0 + nrows - 1 of this thread's group g32) through the compacting
+// One stage (rows r0 .. r0 + nrows - 1 of this thread's group) through the compacting
 // consumer: every row-group's largest magnitude, the rows' random words (independent chains the
 // scheduler interleaves), the certainty test, then the row-groups that fail it are queued (one
 // ballot per row, one position each; the queue is flushed first if they would not fit).
+// g32: the group index with the chunk's sum buffer in bit 31 (what a queued item records).
 // count: queued row-groups of the warp (warp-uniform).
 // ROW_BYTES: the stage's row pitch; release: run by lane 0 once every row of the stage is in
 // registers (frees the stage for the next copy).
@@ -1918,6 +1936,13 @@ __device__ __forceinline__ void tma_drain(bool ok, uint32_t item, uint64_t (&ful
 
 // Consumer wait for item `item`: bounded, and decided uniformly by the warp.
 template <int STAGES>
+__device__ __forceinline__ bool tma_wait_slot(uint32_t slot, uint32_t phase,
+                                              uint64_t (&full_bar)[STAGES],
+                                              volatile int* abort_flag) {
+    const bool got = mbar_wait(smem_u32(&full_bar[slot]), phase);
+    return __all_sync(0xFFFFFFFFu, got && !*abort_flag);
+}
+template <int STAGES>
 __device__ __forceinline__ bool tma_wait_full(uint32_t item, uint64_t (&full_bar)[STAGES],
                                               volatile int* abort_flag) {
     const bool got = mbar_wait(smem_u32(&full_bar[item % STAGES]), (item / STAGES) & 1u);
@@ -1934,7 +1959,7 @@ quantize_tma_kernel(const T* __restrict__ x, QuantArgs a, int64_t groups,
                     unsigned int* __restrict__ status) {
     using Cfg = TmaCfg<T>;
     constexpr int RB = Cfg::kRows;
-    constexpr int NS = Cfg::kStages;
+    constexpr int NS = COMPACT ? CompactCfg<T>::kStages : Cfg::kStages;
     extern __shared__ __align__(128) unsigned char tma_smem[];
     __shared__ __align__(8) uint64_t full_bar[NS];
     __shared__ __align__(8) uint64_t empty_bar[NS];
@@ -1974,41 +1999,69 @@ quantize_tma_kernel(const T* __restrict__ x, QuantArgs a, int64_t groups,
         }
     } else if (COMPACT && nchunks > 0) {  // consumers, compacting
         static_assert(!COMPACT || CODE_BITS == 0, "the compacting consumer writes no codes");
+        using C = CompactCfg<T>;
         const Decide dc = make_decide<SCHEME>(nrm, a.s, a.u16);
         const int lane = tid & 31;
-        const WarpQueue<T> wq = warp_queue<T>(tma_smem + Cfg::kSmemBytes, tid >> 5);
+        const WarpQueue<T> wq = warp_queue<T>(tma_smem + NS * Cfg::kStageBytes, tid >> 5);
 #pragma unroll
-        for (int c = 0; c < kQCols; ++c) wq.sum[c * 32 + lane] = 0;
+        for (int c = 0; c < C::kSumBufs * kQCols; ++c) wq.sum[c * 32 + lane] = 0;
+        // a chunk's output: its sums (complete after a flush) scaled, and the buffer cleared
+        const auto emit = [&](int64_t gg, bool act, uint32_t buf) {
+            float S[kQCols];
+#pragma unroll
+            for (int c = 0; c < kQCols; ++c) {
+                int32_t* p = wq.sum + (buf * kQCols + c) * 32 + lane;
+                S[c] = static_cast<float>(*p);  // exact: below 2^24
+                *p = 0;
+            }
+            if (act && WRITE_OUT) store_out(out, a.sums, a.sums_i8, a.out_dtype, gg, a.d, scale, S);
+        };
         int count = 0;
-        uint32_t item = 0;
+        uint32_t slot = 0, phase = 0;  // ring position of the next stage
+        uint32_t buf = 0;              // sum buffer of the current chunk
+        bool pending = false;          // the previous chunk's output waits for the next flush
+        int64_t pend_g = 0;
+        bool pend_act = false;
         bool ok = true;
-        for (int64_t q = blockIdx.x; q < nchunks && ok; q += gridDim.x) {
+        for (int64_t q = blockIdx.x; q < nchunks; q += gridDim.x) {
             const int64_t g = (nchunks - 1 - q) * kTmaConsumers + tid;
             const bool active = g < full;
             const PhiloxGroup pg = philox_group(static_cast<uint32_t>(g), a.step_lo, a.step_hi, a.rk);
-            for (int64_t b = 0; b < nbatch; ++b, ++item) {
-                if (!tma_wait_full<NS>(item, full_bar, &sh_abort)) {
+            const uint32_t tag = static_cast<uint32_t>(g) | (buf << 31);
+            for (int64_t b = 0; b < nbatch; ++b) {
+                if (!tma_wait_slot<NS>(slot, phase, full_bar, &sh_abort)) {
                     ok = false;
                     break;
                 }
                 const unsigned char* stage =
-                    tma_smem + (item % NS) * Cfg::kStageBytes + tid * kQCols * sizeof(T);
-                const uint32_t eb = smem_u32(&empty_bar[item % NS]);
+                    tma_smem + slot * Cfg::kStageBytes + tid * kQCols * sizeof(T);
+                const uint32_t eb = smem_u32(&empty_bar[slot]);
                 tma_consume_compact<T, SCHEME, TRUSTED, Cfg::kRowBytes>(
                     stage, lane, active, static_cast<uint32_t>(b * RB),
-                    static_cast<uint32_t>(min(static_cast<int64_t>(RB), a.n - b * RB)),
-                    static_cast<uint32_t>(g), pg, a, dc, [eb] { mbar_arrive(eb); }, wq, count);
+                    static_cast<uint32_t>(min(static_cast<int64_t>(RB), a.n - b * RB)), tag, pg,
+                    a, dc, [eb] { mbar_arrive(eb); }, wq, count);
+                if (++slot == NS) {
+                    slot = 0;
+                    phase ^= 1u;
+                }
             }
             if (!ok) break;
-            flush_queue<T, SCHEME, TRUSTED>(wq, count, lane, a, dc);
-            count = 0;
-            float S[kQCols];
-#pragma unroll
-            for (int c = 0; c < kQCols; ++c) {
-                S[c] = static_cast<float>(wq.sum[c * 32 + lane]);  // exact: below 2^24
-                wq.sum[c * 32 + lane] = 0;
+            if (C::kSumBufs == 1 || pending) {  // one flush completes this chunk (and the previous)
+                flush_queue<T, SCHEME, TRUSTED>(wq, count, lane, a, dc);
+                count = 0;
+                if (pending) emit(pend_g, pend_act, buf ^ 1u);
+                emit(g, active, buf);
+                pending = false;
+            } else {
+                pending = true;
+                pend_g = g;
+                pend_act = active;
             }
-            if (active && WRITE_OUT) store_out(out, a.sums, a.sums_i8, a.out_dtype, g, a.d, scale, S);
+            buf ^= static_cast<uint32_t>(C::kSumBufs - 1);
+        }
+        if (ok && pending) {
+            flush_queue<T, SCHEME, TRUSTED>(wq, count, lane, a, dc);
+            emit(pend_g, pend_act, buf ^ 1u);
         }
         if (!ok) {
             if (status) atomicCAS(status, 0u, kStatusTimeout);

@@ -49,7 +49,7 @@ gq_status run_quant(const void* grads, const gq::QuantArgs& a, void* codes, void
             // consumer
             if (a.smallk) {
                 kt = gq::quantize_tma_kernel<T, SCHEME, BITS, OUT, TRUSTED, 2, false, true>;
-                tsmem += gq::CompactCfg<T>::kBytes;
+                tsmem = gq::CompactCfg<T>::kSmemBytes;
             }
         }
         if (blocks_per_sm(kt, tsmem, gq::kTmaBlock) < 1) return GQ_ERR_CUDA;

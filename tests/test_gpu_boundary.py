@@ -11,7 +11,7 @@ more than one unit low (the window's margin).  Every kernel's codes must equal t
 for bit, its code sums (read back exactly from the dequantised mean) too, and its mean within
 1e-6 N:
   * the fused call, two passes, bulk-copy quantise kernel (fp32 and bf16; max norm; and the
-    (2, 2) norm under Global-E, which takes the levels-0/1 accumulation), with and without codes;
+    (2, 2) norm under Global-E, which takes the compacting consumer), with and without codes;
   * the fused call on unaligned rows (direct-load kernel);
   * the single launch (matrix held in shared memory);
   * a supplied norm (gq_allreduce_mean_with_norm, gq_quantize): also |x| equal to and above N;
