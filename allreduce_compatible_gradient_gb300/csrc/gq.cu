@@ -147,7 +147,7 @@ gq::QuantArgs make_args(const float* norm_ptr, int dtype, int64_t n, int64_t d, 
     a.sums = nullptr;
     a.sums_i8 = 0;
     a.out_dtype = gq::kOutF32;
-    a.smallk = 0;
+    a.compact = 0;
     a.pdl = 0;
     return a;
 }
@@ -303,7 +303,7 @@ gq_status gq_allreduce_mean_to(const void* grads, int dtype, int64_t n, int64_t 
     a.out_dtype = out_dtype;
     // under the l2 norm over the coordinates ((2,2), (inf,2)) most |x| / N lie far below the
     // first level: the quantise pass defers the few uncertain row-groups (compacting consumer)
-    a.smallk = mode == gq::kL2L2 || mode == gq::kMaxL2;
+    a.compact = mode == gq::kL2L2 || mode == gq::kMaxL2;
     if (!codes) {  // small problems: one launch, the matrix read once
         unsigned char* w = static_cast<unsigned char*>(ws);
         bool taken = false;
@@ -491,7 +491,7 @@ extern "C" gq_status gq_allreduce_mean_noalloc(const void* grads, int dtype, int
     if (cudaMemsetAsync(ws, 0, gq::kHeaderBytes, cs) != cudaSuccess) return GQ_ERR_CUDA;
     const float* ws_norm = &reinterpret_cast<const gq::WsHeader*>(ws)->norm;
     gq::QuantArgs a = make_args(ws_norm, dtype, n, d, s, seed, step, scheme);
-    a.smallk = mode == gq::kL2L2 || mode == gq::kMaxL2;  // as gq_allreduce_mean chooses
+    a.compact = mode == gq::kL2L2 || mode == gq::kMaxL2;  // as gq_allreduce_mean chooses
     if (!codes) {  // small problems: the single launch (its partials fit the scratch too)
         bool taken = false;
         if (dtype == GQ_F32)

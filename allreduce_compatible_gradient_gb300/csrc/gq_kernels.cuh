@@ -821,7 +821,8 @@ struct QuantArgs {
     void* sums;              // when set, the kernel writes the integer sums here instead of out
     int sums_i8;             // 1: the sums as int8 (they fit: |sum| <= 127), 0: as int32
     int out_dtype;           // kOutF32, kOutBF16 or kOutF16
-    int smallk;              // host hint: most elements round down (an l2 norm over coordinates)
+    int compact;             // host hint: most elements round down (an l2 norm over coordinates):
+                             // the compacting consumer
     int u16;                 // 1: the 16-bit-uniform rounding mode (decide H < F, no exact path)
     int pdl;                 // host: launch the quantise pass dependent on the norm pass
 };

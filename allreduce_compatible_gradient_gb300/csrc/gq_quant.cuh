@@ -47,7 +47,7 @@ gq_status run_quant(const void* grads, const gq::QuantArgs& a, void* codes, void
         if constexpr (BITS == 0 && OUT && TRUSTED) {
             // under an l2 norm over all coordinates most elements round down: the compacting
             // consumer
-            if (a.smallk) {
+            if (a.compact) {
                 kt = gq::quantize_tma_kernel<T, SCHEME, BITS, OUT, TRUSTED, 2, false, true>;
                 tsmem = gq::CompactCfg<T>::kSmemBytes;
             }
