@@ -1795,16 +1795,16 @@ __device__ __forceinline__ void push_item(const WarpQueue<T>& q, int pos,
 // count: queued row-groups of the warp (warp-uniform).
 // ROW_BYTES: the stage's row pitch; release: run by lane 0 once every row of the stage is in
 // registers (frees the stage for the next copy).
-template <typename T, int SCHEME, bool TRUSTED, int ROW_BYTES, typename Release>
-__device__ __forceinline__ void tma_consume_compact(const unsigned char* stage, int lane,
-                                                    bool active, uint32_t r0, uint32_t nrows,
-                                                    uint32_t g32, const PhiloxGroup& pg,
-                                                    const QuantArgs& a, const Decide& dc,
-                                                    const Release& release, const WarpQueue<T>& q,
-                                                    int& count) {
-    using Cfg = TmaCfg<T>;
+// RB: the rows this copy handles (nrows <= RB); COLD: decide an overflowing queue out of line.
+template <typename T, int SCHEME, bool TRUSTED, int ROW_BYTES, int RB, bool COLD,
+          typename Release>
+__device__ __forceinline__ void tma_consume_compact_rows(const unsigned char* stage, int lane,
+                                                         bool active, uint32_t r0, uint32_t nrows,
+                                                         uint32_t g32, const PhiloxGroup& pg,
+                                                         const QuantArgs& a, const Decide& dc,
+                                                         const Release& release,
+                                                         const WarpQueue<T>& q, int& count) {
     using C = CompactCfg<T>;
-    constexpr int RB = Cfg::kRows;
     uint4 raw[RB][C::kXVec];
 #pragma unroll
     for (int u = 0; u < RB; ++u) {
@@ -1851,7 +1851,10 @@ __device__ __forceinline__ void tma_consume_compact(const unsigned char* stage, 
     if (tot == 0) return;
     const unsigned lt = (1u << lane) - 1u;
     if (count + tot > kQueue) {
-        flush_queue<T, SCHEME, TRUSTED>(q, count, lane, a, dc);
+        if (COLD)
+            flush_queue_cold<T, SCHEME, TRUSTED>(q, count, lane, a, dc);
+        else
+            flush_queue<T, SCHEME, TRUSTED>(q, count, lane, a, dc);
         count = 0;
     }
     if (tot <= kQueue) {
@@ -1899,21 +1902,22 @@ __device__ __forceinline__ void tma_init_barriers(uint64_t (&full_bar)[STAGES],
 
 // Producer, item `item` of the block: wait (bounded) until its stage is free, then copy `rows`
 // rows of row_bytes starting at src (row stride ld elements) into it.  False if the wait gave up
-// or the consumers stopped.
+// or the consumers stopped.  nst stages of stage_bytes each (at most STAGES).
 template <typename T, int STAGES>
 __device__ __forceinline__ bool tma_issue(uint32_t item, const T* src, int64_t ld, int rows,
                                           uint32_t row_bytes, unsigned char* smem,
                                           uint64_t (&full_bar)[STAGES],
                                           uint64_t (&empty_bar)[STAGES],
-                                          volatile int* abort_flag) {
+                                          volatile int* abort_flag, uint32_t nst = STAGES,
+                                          uint32_t stage_bytes = TmaCfg<T>::kStageBytes) {
     using Cfg = TmaCfg<T>;
-    const int st = static_cast<int>(item % STAGES);
-    if (item >= STAGES && !mbar_wait(smem_u32(&empty_bar[st]), ((item / STAGES) - 1u) & 1u))
+    const uint32_t st = item % nst;
+    if (item >= nst && !mbar_wait(smem_u32(&empty_bar[st]), ((item / nst) - 1u) & 1u))
         return false;
     if (*abort_flag) return false;
     const uint32_t fb = smem_u32(&full_bar[st]);
     mbar_arrive_expect_tx(fb, static_cast<uint32_t>(rows) * row_bytes);
-    const uint32_t dst = smem_u32(smem + st * Cfg::kStageBytes);
+    const uint32_t dst = smem_u32(smem + st * stage_bytes);
     for (int u = 0; u < rows; ++u) bulk_load(dst + u * Cfg::kRowBytes, src + u * ld, row_bytes, fb);
     return true;
 }
@@ -1923,15 +1927,16 @@ __device__ __forceinline__ bool tma_issue(uint32_t item, const T* src, int64_t l
 template <int STAGES>
 __device__ __forceinline__ void tma_drain(bool ok, uint32_t item, uint64_t (&full_bar)[STAGES],
                                           volatile int* abort_flag,
-                                          unsigned int* __restrict__ status) {
+                                          unsigned int* __restrict__ status,
+                                          uint32_t nst = STAGES) {
     if (!ok) {
         if (status) atomicCAS(status, 0u, kStatusTimeout);
         *abort_flag = 1;
     }
-    const uint32_t inflight = item < STAGES ? item : STAGES;
+    const uint32_t inflight = item < nst ? item : nst;
     for (uint32_t k = 0; k < inflight; ++k) {
         const uint32_t it = item - 1 - k;
-        mbar_wait(smem_u32(&full_bar[it % STAGES]), (it / STAGES) & 1u);
+        mbar_wait(smem_u32(&full_bar[it % nst]), (it / nst) & 1u);
     }
 }
 
@@ -1952,18 +1957,24 @@ __device__ __forceinline__ bool tma_wait_full(uint32_t item, uint64_t (&full_bar
 
 // ZSKIP: rows that are zero across the whole warp skip their random words.  COMPACT (no codes):
 // the compacting consumer above; the dynamic shared memory then holds its queues after the ring.
+// RS: rows per ring stage (TmaCfg<T>::kRows; 2 for one or two workers: as many stages of two
+// rows as the ring holds, so that as many bytes stay in flight as with full stages and the
+// compacting consumer spends no work on empty row slots).
 template <typename T, int SCHEME, int CODE_BITS, bool WRITE_OUT, bool TRUSTED, int SUB,
-          bool ZSKIP = false, bool COMPACT = false>
+          bool ZSKIP = false, bool COMPACT = false, int RS = TmaCfg<T>::kRows>
 __global__ void __launch_bounds__(kTmaBlock, 1)
 quantize_tma_kernel(const T* __restrict__ x, QuantArgs a, int64_t groups,
                     unsigned char* __restrict__ codes, void* __restrict__ out,
                     unsigned int* __restrict__ status) {
     using Cfg = TmaCfg<T>;
     constexpr int RB = Cfg::kRows;
-    constexpr int NS = COMPACT ? CompactCfg<T>::kStages : Cfg::kStages;
+    constexpr int NS = COMPACT ? CompactCfg<T>::kStages : Cfg::kStages;  // stages of RB rows
+    static_assert(RS == RB || RS == 2, "stages of kRows rows, or of two rows");
+    constexpr uint32_t NST = static_cast<uint32_t>(NS * RB / RS);  // stages of RS rows
+    constexpr uint32_t kStageB = static_cast<uint32_t>(RS * Cfg::kRowBytes);
     extern __shared__ __align__(128) unsigned char tma_smem[];
-    __shared__ __align__(8) uint64_t full_bar[NS];
-    __shared__ __align__(8) uint64_t empty_bar[NS];
+    __shared__ __align__(8) uint64_t full_bar[NST];
+    __shared__ __align__(8) uint64_t empty_bar[NST];
     __shared__ float sh_scale;
     __shared__ volatile int sh_abort;
 
@@ -1972,11 +1983,12 @@ quantize_tma_kernel(const T* __restrict__ x, QuantArgs a, int64_t groups,
     const float nrm = __ldg(a.norm_ptr);
     const float scale = block_scale<SCHEME>(nrm, a.n, a.s, &sh_scale);
     const bool live = nrm > 0.0f && nrm < __uint_as_float(kInfBits);
-    tma_init_barriers<NS>(full_bar, empty_bar, &sh_abort);
+    tma_init_barriers<NST>(full_bar, empty_bar, &sh_abort);
 
     const int64_t full = live ? a.d / kQCols : 0;  // groups taken through shared memory
     const int64_t nchunks = (full + kTmaConsumers - 1) / kTmaConsumers;
-    const int64_t nbatch = (a.n + RB - 1) / RB;
+    const int64_t nbatch = (a.n + RS - 1) / RS;
+    GQ_BOUND(RS == RB || a.n <= RS);  // two-row stages hold every worker of a chunk
 
     if (tid >= kTmaConsumers) {
         if (tid == kTmaConsumers) {  // producer: lane 0 of the last warp
@@ -1987,16 +1999,17 @@ quantize_tma_kernel(const T* __restrict__ x, QuantArgs a, int64_t groups,
                 const int64_t ng = min(static_cast<int64_t>(kTmaConsumers), full - g0);
                 const uint32_t row_bytes = static_cast<uint32_t>(ng * kQCols * sizeof(T));
                 for (int64_t b = 0; b < nbatch; ++b) {
-                    const int rows = static_cast<int>(min(static_cast<int64_t>(RB), a.n - b * RB));
-                    GQ_BOUND(rows >= 1 && b * RB + rows <= a.n && g0 >= 0 && ng >= 1 &&
+                    const int rows = static_cast<int>(min(static_cast<int64_t>(RS), a.n - b * RS));
+                    GQ_BOUND(rows >= 1 && b * RS + rows <= a.n && g0 >= 0 && ng >= 1 &&
                              (g0 + ng) * kQCols <= a.d);
-                    ok = tma_issue<T, NS>(item, x + b * RB * a.d + g0 * kQCols, a.d, rows,
-                                          row_bytes, tma_smem, full_bar, empty_bar, &sh_abort);
+                    ok = tma_issue<T, NST>(item, x + b * RS * a.d + g0 * kQCols, a.d, rows,
+                                           row_bytes, tma_smem, full_bar, empty_bar, &sh_abort,
+                                           NST, kStageB);
                     if (!ok) break;
                     ++item;  // counts the stages actually issued
                 }
             }
-            tma_drain<NS>(ok, item, full_bar, &sh_abort, status);
+            tma_drain<NST>(ok, item, full_bar, &sh_abort, status);
         }
     } else if (COMPACT && nchunks > 0) {  // consumers, compacting
         static_assert(!COMPACT || CODE_BITS == 0, "the compacting consumer writes no codes");
@@ -2030,18 +2043,17 @@ quantize_tma_kernel(const T* __restrict__ x, QuantArgs a, int64_t groups,
             const PhiloxGroup pg = philox_group(static_cast<uint32_t>(g), a.step_lo, a.step_hi, a.rk);
             const uint32_t tag = static_cast<uint32_t>(g) | (buf << 31);
             for (int64_t b = 0; b < nbatch; ++b) {
-                if (!tma_wait_slot<NS>(slot, phase, full_bar, &sh_abort)) {
+                if (!tma_wait_slot<NST>(slot, phase, full_bar, &sh_abort)) {
                     ok = false;
                     break;
                 }
-                const unsigned char* stage =
-                    tma_smem + slot * Cfg::kStageBytes + tid * kQCols * sizeof(T);
+                const unsigned char* stage = tma_smem + slot * kStageB + tid * kQCols * sizeof(T);
                 const uint32_t eb = smem_u32(&empty_bar[slot]);
-                tma_consume_compact<T, SCHEME, TRUSTED, Cfg::kRowBytes>(
-                    stage, lane, active, static_cast<uint32_t>(b * RB),
-                    static_cast<uint32_t>(min(static_cast<int64_t>(RB), a.n - b * RB)), tag, pg,
+                tma_consume_compact_rows<T, SCHEME, TRUSTED, Cfg::kRowBytes, RS, (RS < RB)>(
+                    stage, lane, active, static_cast<uint32_t>(b * RS),
+                    static_cast<uint32_t>(min(static_cast<int64_t>(RS), a.n - b * RS)), tag, pg,
                     a, dc, [eb] { mbar_arrive(eb); }, wq, count);
-                if (++slot == NS) {
+                if (++slot == NST) {
                     slot = 0;
                     phase ^= 1u;
                 }
@@ -2071,7 +2083,7 @@ quantize_tma_kernel(const T* __restrict__ x, QuantArgs a, int64_t groups,
     } else if (nchunks > 0) {  // consumers
         const Decide dc = make_decide<SCHEME>(nrm, a.s, a.u16);
         const int lane = tid & 31;
-        uint32_t item = 0;
+        uint32_t slot = 0, phase = 0;  // ring position of the next stage
         bool ok = true;
         for (int64_t q = blockIdx.x; q < nchunks && ok; q += gridDim.x) {
             const int64_t g = (nchunks - 1 - q) * kTmaConsumers + tid;
@@ -2081,16 +2093,20 @@ quantize_tma_kernel(const T* __restrict__ x, QuantArgs a, int64_t groups,
 #pragma unroll
             for (int c = 0; c < kQCols; ++c) S[c] = 0.0f;
             bool probe = true;
-            for (int64_t b = 0; b < nbatch; ++b, ++item) {
-                if (!tma_wait_full<NS>(item, full_bar, &sh_abort)) {
+            // (stage b holds rows b RB ..; two-row stages hold all the workers: b = 0)
+            for (int64_t b = 0; b < nbatch; ++b) {
+                if (!tma_wait_slot<NST>(slot, phase, full_bar, &sh_abort)) {
                     ok = false;
                     break;
                 }
-                const unsigned char* stage =
-                    tma_smem + (item % NS) * Cfg::kStageBytes + tid * kQCols * sizeof(T);
+                const unsigned char* stage = tma_smem + slot * kStageB + tid * kQCols * sizeof(T);
                 tma_consume_stage<T, SCHEME, CODE_BITS, TRUSTED, SUB, ZSKIP>(
-                    stage, lane, active, b, g, pg, a, dc, smem_u32(&empty_bar[item % NS]), S,
-                    codes, &probe);
+                    stage, lane, active, b, g, pg, a, dc, smem_u32(&empty_bar[slot]), S, codes,
+                    &probe);
+                if (++slot == NST) {
+                    slot = 0;
+                    phase ^= 1u;
+                }
             }
             if (ok && active && WRITE_OUT)
                 store_out(out, a.sums, a.sums_i8, a.out_dtype, g, a.d, scale, S);

@@ -45,10 +45,16 @@ gq_status run_quant(const void* grads, const gq::QuantArgs& a, void* codes, void
             if (a.n == 1) kt = gq::quantize_tma_kernel<T, SCHEME, BITS, OUT, TRUSTED, 1, true>;
         }
         if constexpr (BITS == 0 && OUT && TRUSTED) {
+            // one or two workers: stages of two rows
+            if (a.n <= 2)
+                kt = gq::quantize_tma_kernel<T, SCHEME, BITS, OUT, TRUSTED, 2, true, false, 2>;
             // under an l2 norm over all coordinates most elements round down: the compacting
             // consumer
             if (a.compact) {
-                kt = gq::quantize_tma_kernel<T, SCHEME, BITS, OUT, TRUSTED, 2, false, true>;
+                kt = a.n <= 2 ? gq::quantize_tma_kernel<T, SCHEME, BITS, OUT, TRUSTED, 2, false,
+                                                        true, 2>
+                              : gq::quantize_tma_kernel<T, SCHEME, BITS, OUT, TRUSTED, 2, false,
+                                                        true>;
                 tsmem = gq::CompactCfg<T>::kSmemBytes;
             }
         }

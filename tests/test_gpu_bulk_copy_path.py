@@ -21,7 +21,9 @@ CASES = [
     (5, 600_004, "f32", LINEAR, 7, True),     # d % 8 = 4: the last group is half full
     (5, 600_004, "f32", EXP, 8, False),
     (8, 1_000_000, "f32", LINEAR, 127, True),
-    (1, 700_000, "f32", EXP, 4, True),        # one worker: a half-empty row batch
+    (1, 700_000, "f32", EXP, 4, True),        # one worker: stages of one row
+    (2, 800_000, "f32", LINEAR, 7, True),     # two workers: stages of two rows, twice as many
+    (2, 1_310_720, "bf16", EXP, 8, False),
     (7, 640_000, "f32", LINEAR, 15, False),
     (3, 600_000, "bf16", EXP, 4, True),
     (8, 655_360, "bf16", LINEAR, 15, False),
@@ -114,7 +116,9 @@ def test_bulk_copy_path_l2_norm_and_zero(gq):
 
 COMPACT_CASES = [
     # n, d, dtype, scheme, s, (q, p)
-    (1, 700_000, "f32", EXP, 8, (2, 2)),       # one worker: three empty rows per stage
+    (1, 700_000, "f32", EXP, 8, (2, 2)),       # one worker: stages of one row
+    (2, 900_000, "bf16", EXP, 8, (2, 2)),      # two workers: stages of two rows
+    (2, 800_004, "f32", LINEAR, 15, (2, 2)),
     (3, 600_004, "f32", LINEAR, 7, (2, 2)),    # ragged last group
     (5, 640_000, "bf16", EXP, 4, (2, 2)),
     (8, 1_000_000, "f32", EXP, 21, (2, 2)),    # the largest s for 8 workers

@@ -90,6 +90,8 @@ FUSED = [
     (1, 700_003, "f32", 2, 0, 1, 4, "f32", True),       # one worker, unaligned rows
     (6, 1_200_008, "bf16", 0, 2, 0, 7, "f16", False),   # compacting consumer, bf16
     (5, 1_048_576, "f32", 2, 0, 1, 4, "f32", True),     # zero blocks: rows skipped
+    (2, 1_048_576, "f32", 2, 2, 0, 7, "f32", False),    # two workers: stages of two rows
+    (2, 800_000, "bf16", 0, 0, 1, 4, "bf16", True),     # two workers, codes
 ]
 
 
