@@ -1667,7 +1667,8 @@ struct WarpQueue {
     uint4* qx;     // [kQueue][kXVec]
     uint4* qw;     // [kQueue]
     uint2* qm;     // [kQueue]: group (bit 31: sum buffer), worker
-    int32_t* sum;  // [kSumBufs][kQCols][32]: column c of the group owned by lane l at c * 32 + l
+    int32_t* sum;  // [kSumBufs][2][32][4]: column c of the group owned by lane l at
+                   // (c / 4) * 128 + l * 4 + c % 4 (a lane's four columns in 16 bytes)
 };
 
 template <typename T>
@@ -1757,13 +1758,13 @@ __device__ __forceinline__ void flush_queue(const WarpQueue<T>& q, int cnt, int 
         const uint32_t aw[1][4] = {{w.x, w.y, w.z, w.w}};
         uint32_t yk[1][kQCols];
         decide_rows<SCHEME, TRUSTED, 1>(v, dc, a, m.x & 0x7FFFFFFFu, m.y, aw, yk);
-        int32_t* sum = q.sum + (m.x >> 31) * (kQCols * 32) + (m.x & 31u);
+        int32_t* sum = q.sum + (m.x >> 31) * (kQCols * 32) + (m.x & 31u) * 4;
 #pragma unroll
         for (int c = 0; c < kQCols; ++c) {
             const int32_t k = static_cast<int32_t>(yk[0][c] >> 16) - 0x4300;
             int32_t units = SCHEME == kLinear ? k : ((1 << k) >> 1);
             if (__float_as_uint(v[0][c]) >> 31) units = -units;
-            if (units != 0) atomicAdd(&sum[c * 32], units);
+            if (units != 0) atomicAdd(&sum[(c >> 2) * 128 + (c & 3)], units);
         }
     }
     __syncwarp();
@@ -2017,17 +2018,19 @@ quantize_tma_kernel(const T* __restrict__ x, QuantArgs a, int64_t groups,
         const Decide dc = make_decide<SCHEME>(nrm, a.s, a.u16);
         const int lane = tid & 31;
         const WarpQueue<T> wq = warp_queue<T>(tma_smem + NS * Cfg::kStageBytes, tid >> 5);
+        int4* const lsum = reinterpret_cast<int4*>(wq.sum) + lane;  // this lane's 16-byte pieces
 #pragma unroll
-        for (int c = 0; c < C::kSumBufs * kQCols; ++c) wq.sum[c * 32 + lane] = 0;
+        for (int h = 0; h < C::kSumBufs * 2; ++h) lsum[h * 32] = make_int4(0, 0, 0, 0);
         // a chunk's output: its sums (complete after a flush) scaled, and the buffer cleared
         const auto emit = [&](int64_t gg, bool act, uint32_t buf) {
-            float S[kQCols];
-#pragma unroll
-            for (int c = 0; c < kQCols; ++c) {
-                int32_t* p = wq.sum + (buf * kQCols + c) * 32 + lane;
-                S[c] = static_cast<float>(*p);  // exact: below 2^24
-                *p = 0;
-            }
+            const int4 lo = lsum[buf * 64], hi = lsum[buf * 64 + 32];
+            lsum[buf * 64] = make_int4(0, 0, 0, 0);
+            lsum[buf * 64 + 32] = make_int4(0, 0, 0, 0);
+            // exact: integers below 2^24
+            float S[kQCols] = {static_cast<float>(lo.x), static_cast<float>(lo.y),
+                               static_cast<float>(lo.z), static_cast<float>(lo.w),
+                               static_cast<float>(hi.x), static_cast<float>(hi.y),
+                               static_cast<float>(hi.z), static_cast<float>(hi.w)};
             if (act && WRITE_OUT) store_out(out, a.sums, a.sums_i8, a.out_dtype, gg, a.d, scale, S);
         };
         int count = 0;
