@@ -905,7 +905,7 @@ __device__ __forceinline__ Decide make_decide(float nrm, uint32_t s, int u16) {
 // scratch).  The rare exact path runs for a row only if one of its elements needs it, and then
 // only for those elements (one extra Philox call for the row).
 template <int SCHEME, bool TRUSTED, int R>
-__device__ __forceinline__ uint32_t decide_rows(const float (&xv)[R][kQCols], const Decide& dc,
+__device__ __forceinline__ void decide_rows(const float (&xv)[R][kQCols], const Decide& dc,
                                             const QuantArgs& a, uint32_t g32, uint32_t row0,
                                             const uint32_t (&aw)[R][4],
                                             uint32_t (&yk)[R][kQCols]) {
@@ -965,17 +965,12 @@ __device__ __forceinline__ uint32_t decide_rows(const float (&xv)[R][kQCols], co
     // exact path (the correctly rounded quotient and the full word) for an uncertain element,
     // a Global-L level index above s, a NaN, or every element when the norm is out of the fast
     // path's range; one test for all R rows first (almost always none needs it)
-    uint32_t big = 0;  // returned: Global-E rows that may hold a level index of 2 or more
-    if (SCHEME == kExp) {
-#pragma unroll
-        for (int u = 0; u < R; ++u) big |= (worst[u] >= ((kOff + 2u) << 16) ? 1u : 0u) << u;
-    }
     uint32_t wall = worst[0];
 #pragma unroll
     for (int u = 1; u < R; ++u) wall = __vmaxu2(wall, worst[u]);
     if (force == 0u && (wall & 0xFFFFu) <= dc.win &&
         !(SCHEME == kLinear && (wall >> 16) > a.s + kOff))
-        return big;
+        return;
 #pragma unroll
     for (int u = 0; u < R; ++u) {
         const bool over = SCHEME == kLinear && (worst[u] >> 16) > a.s + kOff;
@@ -997,11 +992,9 @@ __device__ __forceinline__ uint32_t decide_rows(const float (&xv)[R][kQCols], co
                 const uint32_t r = (half16(aw[u], c) << 16) | half16(bw, c);
                 const uint32_t k = hi + (r < lo ? 1u : 0u);
                 yk[u][c] = (k + kOff) << 16;
-                if (k >= 2u) big |= 1u << u;
             }
         }
     }
-    return big;
 }
 
 // Packed fp32 pairs for the paired arithmetic of sm_100-class GPUs (add.f32x2, fma.f32x2: two
