@@ -1951,8 +1951,8 @@ __device__ __forceinline__ bool tma_wait_full(uint32_t item, uint64_t (&full_bar
 
 // ZSKIP: rows that are zero across the whole warp skip their random words.  COMPACT (no codes):
 // the compacting consumer above; the dynamic shared memory then holds its queues after the ring.
-// RS: rows per ring stage (TmaCfg<T>::kRows; 2 for one or two workers: as many stages of two
-// rows as the ring holds, so that as many bytes stay in flight as with full stages and the
+// RS: rows per ring stage (TmaCfg<T>::kRows; 1 or 2 for one or two workers: as many stages
+// as the ring holds, so that as many bytes stay in flight as with full stages and the
 // compacting consumer spends no work on empty row slots).
 template <typename T, int SCHEME, int CODE_BITS, bool WRITE_OUT, bool TRUSTED, int SUB,
           bool ZSKIP = false, bool COMPACT = false, int RS = TmaCfg<T>::kRows>
@@ -1963,7 +1963,7 @@ quantize_tma_kernel(const T* __restrict__ x, QuantArgs a, int64_t groups,
     using Cfg = TmaCfg<T>;
     constexpr int RB = Cfg::kRows;
     constexpr int NS = COMPACT ? CompactCfg<T>::kStages : Cfg::kStages;  // stages of RB rows
-    static_assert(RS == RB || RS == 2, "stages of kRows rows, or of two rows");
+    static_assert(RS == RB || RS == 2 || RS == 1, "stages of kRows rows, or of two or one");
     constexpr uint32_t NST = static_cast<uint32_t>(NS * RB / RS);  // stages of RS rows
     constexpr uint32_t kStageB = static_cast<uint32_t>(RS * Cfg::kRowBytes);
     extern __shared__ __align__(128) unsigned char tma_smem[];
@@ -1982,7 +1982,7 @@ quantize_tma_kernel(const T* __restrict__ x, QuantArgs a, int64_t groups,
     const int64_t full = live ? a.d / kQCols : 0;  // groups taken through shared memory
     const int64_t nchunks = (full + kTmaConsumers - 1) / kTmaConsumers;
     const int64_t nbatch = (a.n + RS - 1) / RS;
-    GQ_BOUND(RS == RB || a.n <= RS);  // two-row stages hold every worker of a chunk
+    GQ_BOUND(RS == RB || a.n <= RS);  // short stages hold every worker of a chunk
 
     if (tid >= kTmaConsumers) {
         if (tid == kTmaConsumers) {  // producer: lane 0 of the last warp
@@ -2089,7 +2089,7 @@ quantize_tma_kernel(const T* __restrict__ x, QuantArgs a, int64_t groups,
 #pragma unroll
             for (int c = 0; c < kQCols; ++c) S[c] = 0.0f;
             bool probe = true;
-            // (stage b holds rows b RB ..; two-row stages hold all the workers: b = 0)
+            // (stage b holds rows b RB ..; short stages hold all the workers: b = 0)
             for (int64_t b = 0; b < nbatch; ++b) {
                 if (!tma_wait_slot<NST>(slot, phase, full_bar, &sh_abort)) {
                     ok = false;

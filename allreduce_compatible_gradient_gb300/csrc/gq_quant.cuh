@@ -41,20 +41,25 @@ gq_status run_quant(const void* grads, const gq::QuantArgs& a, void* codes, void
     if (status && a.vec_rows && chunks >= sm_count()) {
         auto kt = gq::quantize_tma_kernel<T, SCHEME, BITS, OUT, TRUSTED, 2, true>;
         int tsmem = gq::TmaCfg<T>::kSmemBytes;
-        if constexpr (BITS == 0 && OUT && !TRUSTED) {  // one rank's sums: often a single worker
-            if (a.n == 1) kt = gq::quantize_tma_kernel<T, SCHEME, BITS, OUT, TRUSTED, 1, true>;
+        // One or two workers (one rank's share of a multi-GPU call; small fused calls): ring
+        // stages of one or two rows, as many as the ring holds, so that as many bytes stay in
+        // flight as with four-row stages.
+        if constexpr ((BITS == 0 && OUT) || (BITS != 0 && !OUT && !TRUSTED)) {
+            if (a.n == 1)
+                kt = gq::quantize_tma_kernel<T, SCHEME, BITS, OUT, TRUSTED, 1, true, false, 1>;
         }
         if constexpr (BITS == 0 && OUT && TRUSTED) {
-            // one or two workers: stages of two rows
-            if (a.n <= 2)
+            if (a.n == 2)
                 kt = gq::quantize_tma_kernel<T, SCHEME, BITS, OUT, TRUSTED, 2, true, false, 2>;
             // under an l2 norm over all coordinates most elements round down: the compacting
             // consumer
             if (a.compact) {
-                kt = a.n <= 2 ? gq::quantize_tma_kernel<T, SCHEME, BITS, OUT, TRUSTED, 2, false,
-                                                        true, 2>
-                              : gq::quantize_tma_kernel<T, SCHEME, BITS, OUT, TRUSTED, 2, false,
-                                                        true>;
+                kt = a.n == 1   ? gq::quantize_tma_kernel<T, SCHEME, BITS, OUT, TRUSTED, 2, false,
+                                                          true, 1>
+                     : a.n == 2 ? gq::quantize_tma_kernel<T, SCHEME, BITS, OUT, TRUSTED, 2, false,
+                                                          true, 2>
+                                : gq::quantize_tma_kernel<T, SCHEME, BITS, OUT, TRUSTED, 2, false,
+                                                          true>;
                 tsmem = gq::CompactCfg<T>::kSmemBytes;
             }
         }
