@@ -2838,12 +2838,54 @@ __device__ __forceinline__ void exp_reround8(const TI (&t)[8], uint32_t g8, uint
         if (t[c] < 0) code[c] = -code[c];
 }
 
+// Codes with |k| <= kExpTab (every code a quantiser writes, s <= 24) combine through a table in
+// shared memory: entry (ka + kExpTab) kExpTabN + (kb + kExpTab) holds the split of the exact sum
+// t = units(ka) + units(kb) (|t| <= 2^24): the lower level index, the sign of t (bit 8) and the
+// threshold T, computed in the block's prologue with the same integer arithmetic as the split.
+constexpr int kExpTab = 24;
+constexpr int kExpTabN = 2 * kExpTab + 1;
+
+// Re-rounded signed codes of eight coordinates from their table entries (as exp_reround8).
+__device__ __forceinline__ void exp_reround8_tab(const uint2 (&e)[8], uint32_t g8, uint32_t sid,
+                                                 const ExpArgs& ea, int32_t (&code)[8]) {
+    const uint4 ra = philox4x32_10_rk(make_uint4(g8, sid, ea.step_lo, ea.step_hi), ea.rk);
+    const uint32_t aw[4] = {ra.x, ra.y, ra.z, ra.w};
+    bool tie = false;
+#pragma unroll
+    for (int c = 0; c < 8; ++c) {
+        const uint32_t h = half16(aw, c);
+        tie |= h == (e[c].y >> 16);
+        code[c] = static_cast<int32_t>((e[c].x & 0xFFu) + (h < (e[c].y >> 16) ? 1u : 0u));
+    }
+    if (tie) {  // the high half equals the threshold's: the low half decides (rare)
+        const uint4 rb = philox4x32_10_rk(make_uint4(g8 | 0x80000000u, sid, ea.step_lo, ea.step_hi),
+                                          ea.rk);
+        const uint32_t bw[4] = {rb.x, rb.y, rb.z, rb.w};
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+            const uint32_t r = (half16(aw, c) << 16) | half16(bw, c);
+            code[c] = static_cast<int32_t>((e[c].x & 0xFFu) + (r < e[c].y ? 1u : 0u));
+        }
+    }
+#pragma unroll
+    for (int c = 0; c < 8; ++c)
+        if (e[c].x >> 8) code[c] = -code[c];
+}
+
 // One step on d coordinates: out = re-round(decode(a) + decode(b)); coordinate j of the buffers
 // is coordinate jbase + j of the whole vector (jbase a multiple of 8), which keys its random
 // word.  Each thread owns 16 coordinates (one 16-byte load of a and of b, one 16-byte store).
 static __global__ void __launch_bounds__(kThreads, 3)
 exp_combine_kernel(const int8_t* __restrict__ a, const int8_t* __restrict__ b, int64_t d,
                    int64_t jbase, uint32_t sid, ExpArgs ea, int8_t* __restrict__ out) {
+    __shared__ uint2 tab[kExpTabN * kExpTabN];
+    for (int i = threadIdx.x; i < kExpTabN * kExpTabN; i += kThreads) {
+        const int32_t t = exp_units32(i / kExpTabN - kExpTab) + exp_units32(i % kExpTabN - kExpTab);
+        uint32_t lo, T;
+        exp_split32(static_cast<uint32_t>(t < 0 ? -t : t), lo, T);
+        tab[i] = make_uint2(lo | (t < 0 ? 0x100u : 0u), T);
+    }
+    __syncthreads();
     const int64_t chunks = (d + 15) / 16;
     const int64_t stride = static_cast<int64_t>(gridDim.x) * kThreads;
     for (int64_t q = static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x; q < chunks;
@@ -2861,17 +2903,26 @@ exp_combine_kernel(const int8_t* __restrict__ a, const int8_t* __restrict__ b, i
                 bv[c] = j0 + c < d ? b[j0 + c] : 0;
             }
         }
-        // codes up to |k| = 30 (every code a quantiser writes, s <= 24) sum in 32 bits
-        uint32_t wide = 0;  // largest c + 30 as unsigned: above 60 iff some |c| > 30
+        // codes up to |k| = 24 take the table, up to 30 sum in 32 bits, larger in 64 bits
+        int32_t mag = 0;  // largest |c| of the 32 codes
 #pragma unroll
-        for (int c = 0; c < 16; ++c)
-            wide = max(wide, max(static_cast<uint32_t>(av[c] + 30), static_cast<uint32_t>(bv[c] + 30)));
-        const bool big = wide > 60u;
+        for (int c = 0; c < 16; ++c) mag = max(mag, max(abs(int32_t{av[c]}), abs(int32_t{bv[c]})));
+        const bool big = mag > 30;
+        const bool tabled = mag <= kExpTab;
         int8_t ov[16];
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
             int32_t code[8];
-            if (!big) {
+            if (tabled) {
+                uint2 e[8];
+#pragma unroll
+                for (int c = 0; c < 8; ++c) {
+                    const int i = (av[8 * h + c] + kExpTab) * kExpTabN + (bv[8 * h + c] + kExpTab);
+                    GQ_BOUND(i >= 0 && i < kExpTabN * kExpTabN);
+                    e[c] = tab[i];
+                }
+                exp_reround8_tab(e, static_cast<uint32_t>((jbase + j0) / 8 + h), sid, ea, code);
+            } else if (!big) {
                 int32_t t[8];
 #pragma unroll
                 for (int c = 0; c < 8; ++c)

@@ -39,6 +39,26 @@ def test_combine_matches_oracle(gq, oracle_mod, d):
         np.testing.assert_array_equal(got, oracle_mod.exp_combine(a, b, 0xABCDEF0123, 17, sid))
 
 
+@pytest.mark.parametrize("lim", [24, 25, 30, 31, 62])
+def test_combine_code_ranges(gq, oracle_mod, lim):
+    """The three arithmetic paths of the combine kernel: codes up to |k| = 24 through the table of
+    splits, up to 30 in 32 bits, larger (extended codes of earlier hops) in 64 bits; a thread's 16
+    coordinates take the table only if all of them fit, so groups of each kind sit side by side."""
+    import torch
+    d = 70_003
+    rng = np.random.default_rng(lim)
+    a = rng.integers(-12, 13, d).astype(np.int8)
+    b = rng.integers(-12, 13, d).astype(np.int8)
+    big = rng.random(d) < 0.02  # about a quarter of the 16-coordinate groups hold a large code
+    a[big] = rng.integers(-lim, lim + 1, int(big.sum())).astype(np.int8)
+    b[: 64] = lim  # the largest magnitude at both signs in the first groups
+    b[64: 128] = -lim
+    sid = oracle_mod.exp_ring_stream(2, 5)
+    got = gq.gq_exp_combine(torch.from_numpy(a).cuda(), torch.from_numpy(b).cuda(), 77, 3,
+                            sid).cpu().numpy()
+    np.testing.assert_array_equal(got, oracle_mod.exp_combine(a, b, 77, 3, sid))
+
+
 @pytest.mark.parametrize("order", [0, 1])
 @pytest.mark.parametrize("s", [4, 8])
 @pytest.mark.parametrize("n,d", [(1, 100), (2, 1001), (3, 4099), (5, 333), (8, 20000), (16, 777)])
