@@ -705,6 +705,29 @@ def main():
     if gq.gq_get_status(ws) != 0:
         raise RuntimeError("device status not ok after the timed steps")
 
+    # compression error of one step (outside every timed region): the relative l2 distance of the
+    # dequantised mean from the exact mean of the n rows, both in fp64
+    step(0)
+    torch.cuda.synchronize()
+    exact = x.mean(0, dtype=torch.float64)
+    mnorm = float(exact.norm())
+    rel = float((out.double() - exact).norm()) / mnorm if mnorm > 0 else 0.0
+    del exact
+    # the variance bound of the quantiser over the whole matrix, E||Q - X||_F^2 <= min(n d N^2 /
+    # (4 s^2), N ||X||_1 / s) (Global-L) or ||X||_F^2 / 8 + 2^-(s-1) N ||X||_1 (Global-E), divided
+    # by n^2 for the mean of n independently rounded rows
+    l1 = sum(float(x[i].abs().sum(dtype=torch.float64)) for i in range(n))
+    l2sq = sum(float(x[i].double().square().sum()) for i in range(n))
+    N = float(norm.item())
+    if sc & 1 == 0:
+        bound = min(n * d * N * N / (4.0 * s * s), N * l1 / s)
+    else:
+        bound = l2sq / 8.0 + 2.0 ** -(s - 1) * N * l1
+    rel_bound = (bound ** 0.5) / n / mnorm if mnorm > 0 else 0.0
+    compression = {"rel_l2": round(rel, 6), "rel_l2_bound": round(rel_bound, 6),
+                   "of": "||out - mean(x)||_2 / ||mean(x)||_2 for one step; bound: the square root "
+                         "of the quantiser's variance bound over n^2, over ||mean(x)||_2"}
+
     cpu = None
     if rank == 0 and not a.no_cpu_baseline:
         cpu = cpu_baseline(cfg, a.cpu_seconds)
@@ -717,7 +740,7 @@ def main():
                 "dtype": cfg["dtype"], "data": "synthetic",
                 "config": _config_block(cfg, world), "roofline": roofline,
                 "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches * a.steps,
-                "clocks": clk, "impl": "ours"}
+                "clocks": clk, "compression_error": compression, "impl": "ours"}
         print(json.dumps(line), flush=True)
     if world > 1:
         import torch.distributed as dist
