@@ -10,7 +10,8 @@ from ._binding import (  # noqa: F401
     BF16, EXP, F16, F32, LINEAR, NORM_INF, NORM_L2, ORDER_RING, ORDER_TREE, ROUND_U16, SUM_I32,
     SUM_I8,
     GQError, gq_abi_version, gq_allreduce_mean, gq_allreduce_mean_noalloc,
-    gq_allreduce_mean_segments, gq_allreduce_mean_to, gq_allreduce_mean_with_norm, gq_code_bits,
+    gq_allreduce_mean_segments, gq_allreduce_mean_to, gq_allreduce_mean_with_norm,
+    gq_allreduce_mean_with_norm_ws, gq_code_bits,
     gq_code_bytes, gq_code_pitch, gq_debug_status, gq_dequantize, gq_dequantize_sums, gq_dequantize_to,
     gq_exp_allreduce, gq_exp_combine, gq_exp_dequantize, gq_exp_ring_stream, gq_exp_tree_stream,
     gq_fused_launches, gq_get_status, gq_global_norm, gq_noalloc_max_blocks, gq_norm_blocks,

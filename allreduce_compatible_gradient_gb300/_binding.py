@@ -54,6 +54,8 @@ def lib() -> ctypes.CDLL:
         "gq_allreduce_mean": (ci, [vp, ci, i64, i64, ci, ci, ci, ci, u64, u64, vp, vp, vp, vp, sz,
                                    vp]),
         "gq_allreduce_mean_with_norm": (ci, [vp, ci, i64, i64, vp, ci, ci, u64, u64, vp, vp, vp]),
+        "gq_allreduce_mean_with_norm_ws": (ci, [vp, ci, i64, i64, vp, ci, ci, u64, u64, vp, vp, vp,
+                                                sz, vp]),
         "gq_allreduce_mean_noalloc": (ci, [vp, ci, i64, i64, ci, ci, ci, ci, u64, u64, vp, vp, vp,
                                            vp]),
         "gq_philox4x32_10": (ci, [vp, vp, i64, vp]),
@@ -254,14 +256,29 @@ def gq_allreduce_mean_to(grads, q, p, scheme, s, seed, step, out=None, out_dtype
 
 
 def gq_allreduce_mean_with_norm(grads, norm, scheme, s, seed, step, out=None, codes=None,
-                                stream=None) -> torch.Tensor:
+                                ws=None, stream=None) -> torch.Tensor:
+    """Steps 2-4 with a supplied device norm; a workspace (ws) lets large problems take the
+    bulk-copy kernel (gq_allreduce_mean_with_norm_ws)."""
     dt, n, d = _grads(grads)
     if out is None:
         out = torch.empty(d, dtype=torch.float32, device=grads.device)
-    _check(lib().gq_allreduce_mean_with_norm(_p(grads), dt, n, d, _p(norm), scheme, s, seed, step,
-                                             _p(out), _p(codes), _stream(stream)),
-           "gq_allreduce_mean_with_norm")
+    if ws is None:
+        _check(lib().gq_allreduce_mean_with_norm(_p(grads), dt, n, d, _p(norm), scheme, s, seed,
+                                                 step, _p(out), _p(codes), _stream(stream)),
+               "gq_allreduce_mean_with_norm")
+    else:
+        _check(lib().gq_allreduce_mean_with_norm_ws(_p(grads), dt, n, d, _p(norm), scheme, s,
+                                                    seed, step, _p(out), _p(codes), _p(ws),
+                                                    ws.numel(), _stream(stream)),
+               "gq_allreduce_mean_with_norm_ws")
     return out
+
+
+def gq_allreduce_mean_with_norm_ws(grads, norm, scheme, s, seed, step, ws, out=None, codes=None,
+                                   stream=None) -> torch.Tensor:
+    """gq_allreduce_mean_with_norm with a workspace (the bulk-copy kernel for large problems)."""
+    return gq_allreduce_mean_with_norm(grads, norm, scheme, s, seed, step, out=out, codes=codes,
+                                       ws=ws, stream=stream)
 
 
 def gq_allreduce_mean_segments(grads, q, p, scheme, s, seed, step, outs=None, norms=None,

@@ -332,17 +332,27 @@ gq_status gq_allreduce_mean(const void* grads, int dtype, int64_t n, int64_t d, 
                                 norm_dev, codes, ws, ws_bytes, stream);
 }
 
-gq_status gq_allreduce_mean_with_norm(const void* grads, int dtype, int64_t n, int64_t d,
-                                      const float* norm_dev, int scheme, int s, uint64_t seed,
-                                      uint64_t step, float* out_dev, void* codes, void* stream) {
+gq_status gq_allreduce_mean_with_norm_ws(const void* grads, int dtype, int64_t n, int64_t d,
+                                         const float* norm_dev, int scheme, int s, uint64_t seed,
+                                         uint64_t step, float* out_dev, void* codes, void* ws,
+                                         size_t ws_bytes, void* stream) {
     gq_status st = check_grads(grads, dtype, n, d);
     if (st != GQ_OK) return st;
     if ((st = check_scheme(scheme, s, n)) != GQ_OK) return st;
     if (!norm_dev || !out_dev || !aligned16(out_dev) || (codes && !aligned16(codes)))
         return GQ_ERR_INVALID;
+    if (ws && (st = check_ws(ws, ws_bytes, n, d)) != GQ_OK) return st;
     const gq::QuantArgs a = make_args(norm_dev, dtype, n, d, s, seed, step, scheme);
+    unsigned int* status = ws ? &reinterpret_cast<gq::WsHeader*>(ws)->status : nullptr;
     return quant_any<true, false>(grads, dtype, a, scheme, gq_code_bits(scheme, s), codes,
-                                  out_dev, static_cast<cudaStream_t>(stream));
+                                  out_dev, static_cast<cudaStream_t>(stream), status);
+}
+
+gq_status gq_allreduce_mean_with_norm(const void* grads, int dtype, int64_t n, int64_t d,
+                                      const float* norm_dev, int scheme, int s, uint64_t seed,
+                                      uint64_t step, float* out_dev, void* codes, void* stream) {
+    return gq_allreduce_mean_with_norm_ws(grads, dtype, n, d, norm_dev, scheme, s, seed, step,
+                                          out_dev, codes, nullptr, 0, stream);
 }
 
 gq_status gq_philox4x32_10(const uint32_t* ctr_key_dev, uint32_t* out_dev, int64_t count,

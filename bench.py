@@ -492,7 +492,8 @@ def _two_pass_roofline(gq, x, q, p, sc, s, seed, a, cfg, stream, flush_l2, norm,
         ev_k[k][0].record(stream)
         gq.gq_global_norm(x, q, p, norm=norm, ws=ws, stream=stream)
         ev_k[k][1].record(stream)
-        gq.gq_allreduce_mean_with_norm(x, norm, sc, s, seed, a.warmup + k, out=out, stream=stream)
+        gq.gq_allreduce_mean_with_norm(x, norm, sc, s, seed, a.warmup + k, out=out, ws=ws,
+                                       stream=stream)
         ev_k[k][2].record(stream)
     torch.cuda.synchronize()
     t_norm = statistics.mean(e[0].elapsed_time(e[1]) for e in ev_k)

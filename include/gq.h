@@ -232,6 +232,20 @@ gq_status gq_allreduce_mean_with_norm(const void *grads, int dtype, int64_t n, i
                                       uint64_t step, float *out_dev, void *codes, void *stream);
 
 /*
+ * gq_allreduce_mean_with_norm with a workspace (ws, ws_bytes as for gq_allreduce_mean; the
+ * caller owns it; 16-byte aligned, at least gq_workspace_bytes(n, d) bytes, else
+ * GQ_ERR_WORKSPACE): large problems with 16-byte aligned rows then take the bulk-copy quantise
+ * kernel, whose bounded waits report GQ_ERR_TIMEOUT in the workspace's status word (read by
+ * gq_get_status).  ws NULL is gq_allreduce_mean_with_norm.  Outputs are bit-identical to it:
+ * the norm is not trusted (|x| above it saturates, a NaN element gives code 0).  Calls that
+ * share a workspace must not overlap on the GPU.
+ */
+gq_status gq_allreduce_mean_with_norm_ws(const void *grads, int dtype, int64_t n, int64_t d,
+                                         const float *norm_dev, int scheme, int s, uint64_t seed,
+                                         uint64_t step, float *out_dev, void *codes, void *ws,
+                                         size_t ws_bytes, void *stream);
+
+/*
  * Global-E allreduce with re-rounding at every hop (Global-QSGD: the custom reduction the
  * implementation paragraph uses for exponential dithering; the extra variance of "stochastic
  * rounding during AllReduce" counted in the theta worked example; the tree allreduce of the

@@ -114,6 +114,44 @@ def test_bulk_copy_path_l2_norm_and_zero(gq):
     assert gq.gq_get_status(ws) == 0
 
 
+@pytest.mark.parametrize("dtype,scheme,s,with_codes", [("f32", EXP, 8, True), ("f32", LINEAR, 127, False),
+                                                    ("bf16", EXP, 4, False), ("bf16", LINEAR, 15, True)])
+def test_with_norm_workspace(gq, oracle_mod, dtype, scheme, s, with_codes):
+    """gq_allreduce_mean_with_norm_ws (the bulk-copy kernel under a supplied, untrusted norm)
+    equals gq_allreduce_mean_with_norm (direct loads) bit for bit, codes too, on values above the
+    norm, a NaN and zero blocks; and the oracle on windows."""
+    import torch
+    from gpu_common import to_host, unpack_codes
+    n, d = 5, 1_048_576
+    x = workloads.device_inputs("laplace_block_sparse", n, d, seed=11, dtype=dtype)
+    x[1, 5] = float("nan")
+    norm = gq.gq_global_norm(x[2:], 0, 0) * 0.5  # half the maximum of rows 2..: many |x| above N
+    ws = gq.gq_workspace()
+    cb = gq.gq_code_bytes(scheme, s, n, d)
+    c1 = torch.empty(cb, dtype=torch.uint8, device="cuda") if with_codes else None
+    c2 = torch.empty(cb, dtype=torch.uint8, device="cuda") if with_codes else None
+    got = gq.gq_allreduce_mean_with_norm_ws(x, norm, scheme, s, 6, 7, ws, codes=c1)
+    ref = gq.gq_allreduce_mean_with_norm(x, norm, scheme, s, 6, 7, codes=c2)
+    torch.cuda.synchronize()
+    assert gq.gq_get_status(ws) == 0
+    assert torch.equal(got, ref)
+    if with_codes:
+        assert torch.equal(c1, c2)
+    xh = to_host(x)
+    N32 = np.float32(norm.item())
+    out_h = got.cpu().numpy().astype(np.float64)
+    allc = unpack_codes(c1.cpu().numpy(), scheme, s, n, d) if with_codes else None
+    for j0, j1 in _windows(d, 3):
+        xw = np.ascontiguousarray(xh[:, j0:j1])
+        codes, rc = oracle_mod.quantize_cols(xw, j0, N32, scheme, s, 6, 7)
+        assert rc == 0
+        sums = oracle_mod.reduce_codes(codes, scheme, s)
+        want, _ = oracle_mod.dequantize(sums, N32, scheme, s, n)
+        assert np.abs(out_h[j0:j1] - want).max() <= 1e-6 * float(N32)
+        if with_codes:
+            np.testing.assert_array_equal(allc[:, j0:j1], codes)
+
+
 COMPACT_CASES = [
     # n, d, dtype, scheme, s, (q, p)
     (1, 700_000, "f32", EXP, 8, (2, 2)),       # one worker: stages of one row
