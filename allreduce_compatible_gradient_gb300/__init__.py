@@ -16,5 +16,5 @@ from ._binding import (  # noqa: F401
     gq_exp_allreduce, gq_exp_combine, gq_exp_dequantize, gq_exp_ring_stream, gq_exp_tree_stream,
     gq_fused_launches, gq_get_status, gq_global_norm, gq_noalloc_max_blocks, gq_norm_blocks,
     gq_norm_finish, gq_norm_partial, gq_philox4x32_10, gq_quantize,
-    gq_quantize_codes, gq_quantize_sum, gq_reduce_codes, gq_selftest_wait_timeout,
+    gq_quantize_codes, gq_quantize_sum, gq_quantize_ws, gq_reduce_codes, gq_selftest_wait_timeout,
     gq_status_string, gq_workspace, gq_workspace_bytes, lib, library_path)

@@ -49,6 +49,7 @@ def lib() -> ctypes.CDLL:
         "gq_code_bytes": (sz, [ci, ci, i64, i64]),
         "gq_global_norm": (ci, [vp, ci, i64, i64, ci, ci, vp, vp, sz, vp]),
         "gq_quantize": (ci, [vp, ci, i64, i64, vp, ci, ci, u64, u64, vp, vp]),
+        "gq_quantize_ws": (ci, [vp, ci, i64, i64, vp, ci, ci, u64, u64, vp, vp, sz, vp]),
         "gq_reduce_codes": (ci, [vp, ci, ci, i64, i64, vp, vp]),
         "gq_dequantize": (ci, [vp, vp, ci, ci, i64, i64, vp, vp]),
         "gq_allreduce_mean": (ci, [vp, ci, i64, i64, ci, ci, ci, ci, u64, u64, vp, vp, vp, vp, sz,
@@ -190,13 +191,27 @@ def gq_global_norm(grads, q, p, norm=None, ws=None, stream=None) -> torch.Tensor
     return norm
 
 
-def gq_quantize(grads, norm, scheme, s, seed, step, codes=None, stream=None) -> torch.Tensor:
+def gq_quantize(grads, norm, scheme, s, seed, step, codes=None, ws=None,
+                stream=None) -> torch.Tensor:
+    """Step 2 with a supplied device norm; a workspace (ws) lets large problems take the
+    bulk-copy kernel (gq_quantize_ws)."""
     dt, n, d = _grads(grads)
     if codes is None:
         codes = torch.empty(gq_code_bytes(scheme, s, n, d), dtype=torch.uint8, device=grads.device)
-    _check(lib().gq_quantize(_p(grads), dt, n, d, _p(norm), scheme, s, seed, step, _p(codes),
-                             _stream(stream)), "gq_quantize")
+    if ws is None:
+        _check(lib().gq_quantize(_p(grads), dt, n, d, _p(norm), scheme, s, seed, step, _p(codes),
+                                 _stream(stream)), "gq_quantize")
+    else:
+        _check(lib().gq_quantize_ws(_p(grads), dt, n, d, _p(norm), scheme, s, seed, step,
+                                    _p(codes), _p(ws), ws.numel(), _stream(stream)),
+               "gq_quantize_ws")
     return codes
+
+
+def gq_quantize_ws(grads, norm, scheme, s, seed, step, ws, codes=None,
+                   stream=None) -> torch.Tensor:
+    """gq_quantize with a workspace (the bulk-copy kernel for large problems)."""
+    return gq_quantize(grads, norm, scheme, s, seed, step, codes=codes, ws=ws, stream=stream)
 
 
 def gq_reduce_codes(codes, scheme, s, n, d, sums=None, stream=None) -> torch.Tensor:

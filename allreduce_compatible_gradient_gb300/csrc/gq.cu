@@ -210,16 +210,25 @@ gq_status gq_global_norm(const void* grads, int dtype, int64_t n, int64_t d, int
     return norm_any(grads, dtype, mode, n, d, norm_dev, ws, static_cast<cudaStream_t>(stream));
 }
 
-gq_status gq_quantize(const void* grads, int dtype, int64_t n, int64_t d, const float* norm_dev,
-                      int scheme, int s, uint64_t seed, uint64_t step, void* codes,
-                      void* stream) {
+gq_status gq_quantize_ws(const void* grads, int dtype, int64_t n, int64_t d,
+                         const float* norm_dev, int scheme, int s, uint64_t seed, uint64_t step,
+                         void* codes, void* ws, size_t ws_bytes, void* stream) {
     gq_status st = check_grads(grads, dtype, n, d);
     if (st != GQ_OK) return st;
     if ((st = check_scheme(scheme, s, n)) != GQ_OK) return st;
     if (!norm_dev || !codes || !aligned16(codes)) return GQ_ERR_INVALID;
+    if (ws && (st = check_ws(ws, ws_bytes, n, d)) != GQ_OK) return st;
     const gq::QuantArgs a = make_args(norm_dev, dtype, n, d, s, seed, step, scheme);
+    unsigned int* status = ws ? &reinterpret_cast<gq::WsHeader*>(ws)->status : nullptr;
     return quant_any<false, false>(grads, dtype, a, grid_of(scheme), gq_code_bits(scheme, s),
-                                   codes, nullptr, static_cast<cudaStream_t>(stream));
+                                   codes, nullptr, static_cast<cudaStream_t>(stream), status);
+}
+
+gq_status gq_quantize(const void* grads, int dtype, int64_t n, int64_t d, const float* norm_dev,
+                      int scheme, int s, uint64_t seed, uint64_t step, void* codes,
+                      void* stream) {
+    return gq_quantize_ws(grads, dtype, n, d, norm_dev, scheme, s, seed, step, codes, nullptr, 0,
+                          stream);
 }
 
 gq_status gq_reduce_codes(const void* codes, int scheme, int s, int64_t n, int64_t d,

@@ -156,6 +156,17 @@ gq_status gq_quantize(const void *grads, int dtype, int64_t n, int64_t d, const 
                       void *stream);
 
 /*
+ * gq_quantize with a workspace (ws, ws_bytes as for gq_allreduce_mean; caller-owned, 16-byte
+ * aligned, at least gq_workspace_bytes(n, d) bytes, else GQ_ERR_WORKSPACE): large problems with
+ * 16-byte aligned rows take the bulk-copy kernel, whose bounded waits report GQ_ERR_TIMEOUT in
+ * the workspace's status word.  ws NULL is gq_quantize; the codes are bit-identical either way.
+ * Calls that share a workspace must not overlap on the GPU.
+ */
+gq_status gq_quantize_ws(const void *grads, int dtype, int64_t n, int64_t d,
+                         const float *norm_dev, int scheme, int s, uint64_t seed, uint64_t step,
+                         void *codes, void *ws, size_t ws_bytes, void *stream);
+
+/*
  * Step 3: sum the code matrix over the n workers into int32 sums[d] (the allreduce reduction
  * of the communication hook: the native integer sum for Global-L; for Global-E each level index
  * k is summed as 2^(k-1) units of 2^-(s-1)).  Exact.

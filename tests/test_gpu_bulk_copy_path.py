@@ -117,9 +117,9 @@ def test_bulk_copy_path_l2_norm_and_zero(gq):
 @pytest.mark.parametrize("dtype,scheme,s,with_codes", [("f32", EXP, 8, True), ("f32", LINEAR, 127, False),
                                                     ("bf16", EXP, 4, False), ("bf16", LINEAR, 15, True)])
 def test_with_norm_workspace(gq, oracle_mod, dtype, scheme, s, with_codes):
-    """gq_allreduce_mean_with_norm_ws (the bulk-copy kernel under a supplied, untrusted norm)
-    equals gq_allreduce_mean_with_norm (direct loads) bit for bit, codes too, on values above the
-    norm, a NaN and zero blocks; and the oracle on windows."""
+    """gq_allreduce_mean_with_norm_ws and gq_quantize_ws (the bulk-copy kernel under a supplied,
+    untrusted norm) equal gq_allreduce_mean_with_norm and gq_quantize (direct loads) bit for bit,
+    codes too, on values above the norm, a NaN and zero blocks; and the oracle on windows."""
     import torch
     from gpu_common import to_host, unpack_codes
     n, d = 5, 1_048_576
@@ -132,11 +132,15 @@ def test_with_norm_workspace(gq, oracle_mod, dtype, scheme, s, with_codes):
     c2 = torch.empty(cb, dtype=torch.uint8, device="cuda") if with_codes else None
     got = gq.gq_allreduce_mean_with_norm_ws(x, norm, scheme, s, 6, 7, ws, codes=c1)
     ref = gq.gq_allreduce_mean_with_norm(x, norm, scheme, s, 6, 7, codes=c2)
+    q1 = gq.gq_quantize_ws(x, norm, scheme, s, 6, 7, ws)   # codes alone, both kernels
+    q2 = gq.gq_quantize(x, norm, scheme, s, 6, 7)
     torch.cuda.synchronize()
     assert gq.gq_get_status(ws) == 0
     assert torch.equal(got, ref)
+    assert torch.equal(q1, q2)
     if with_codes:
         assert torch.equal(c1, c2)
+        assert torch.equal(q1, c1)
     xh = to_host(x)
     N32 = np.float32(norm.item())
     out_h = got.cpu().numpy().astype(np.float64)
